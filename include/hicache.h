@@ -1,0 +1,246 @@
+/*
+ * hicache.h -- C ABI of libhicache: paged KV movement between GPU HBM (L1) and
+ * pinned host DRAM (L2) for a tiered prefix-KV cache, on GB300 (sm_103a).
+ *
+ * The two operations come from the pages' description of HiCache:
+ *   - backup (write-back, L1 -> L2): gather every layer of the given device pages
+ *     into the given host pages.  "Tuning SGLang HiCache L2 on Kunlunxin
+ *     P800/P900", sections 2.1-2.2 (transfer_kv_all_layer, a D2H backup
+ *     submitted on its own stream by a backup thread);
+ *   - load (L2 -> L1): scatter host pages back into device pages, either all
+ *     layers at once or one layer per call (transfer_kv_per_layer) so that
+ *     attention on layer i overlaps the load of layer i+1.  Same page, section 2.1;
+ *     "HiCache 시스템 설계와 최적화", section "CPU→GPU 전송 최적화" (layer overlap:
+ *     layer N computes while layer N+1 loads); "Rethinking the SGLang HiCache
+ *     Boundary", section "Why compute, H2D, and D2H should stay in one GPU
+ *     execution domain" (an H2D stream, a KV_READY event, the compute stream
+ *     waiting on it).
+ *
+ * Memory layouts.  The device pool is layer-first: for each buffer b (K then V
+ * for MHA/GQA; one latent buffer for MLA) and layer l, one caller-owned device
+ * allocation of (device_num_pages * page_size) rows of row_elems elements; the
+ * row of token t of device page d is row d*page_size + t ("different layers are
+ * different buffers", Tuning ... section 2.1).  The host pool is one pinned
+ * allocation in one of three layouts, each with a leading buffer dim:
+ *   HICACHE_LAYER_FIRST        (B, layer, size, kv_dim)               [Tuning ... 2.1]
+ *   HICACHE_PAGE_FIRST         (B, size, layer, kv_dim)               [HiCache 설계, 데이터 전송 최적화]
+ *   HICACHE_PAGE_FIRST_DIRECT  (B, page_num, layer_num, page_size, kv_dim) [Tuning ... 2.1]
+ * where size = host_num_pages * page_size.  Indices are page indices (int64);
+ * the i-th device page pairs with the i-th host page.  Bytes are copied as-is:
+ * no dtype conversion, elem_bytes only sizes the rows.
+ *
+ * Conventions for every call below.
+ *   - Streams and events are CUDA handles (cudaStream_t / cudaEvent_t) passed
+ *     as void*; NULL is the legacy default stream.
+ *   - Index arrays are HOST memory, read during the call only: the caller may
+ *     free or reuse them as soon as the call returns.
+ *   - Transfers only enqueue work on the given stream and return; ordering
+ *     against the caller's compute is the caller's (record an event before a
+ *     backup; use hicache_wait_layer for loads).
+ *   - Every argument is validated BEFORE anything is enqueued: a call that
+ *     returns an error has enqueued nothing.  n == 0 is valid and launches no
+ *     kernel (hicache_load_layer still records its layer event).
+ *   - Return value: HICACHE_OK (0) or a negative hicache_status; the text of
+ *     the last error of the calling thread is in hicache_last_error().
+ *   - Thread safety: a pool may be used from several host threads at once
+ *     (e.g. a backup thread and a load thread), each on its own stream.
+ */
+#ifndef HICACHE_H_
+#define HICACHE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HICACHE_OK = 0,
+  HICACHE_ERR_INVALID_ARG = -1,     /* null pointer, bad size, bad layout/layer/direction */
+  HICACHE_ERR_INDEX_RANGE = -2,     /* a page index outside its pool */
+  HICACHE_ERR_DUPLICATE_INDEX = -3, /* a destination page named twice in one call */
+  HICACHE_ERR_ALIGNMENT = -4,       /* pointer or row size not a multiple of 16 bytes */
+  HICACHE_ERR_NOT_PINNED = -5,      /* host pool not page-locked / not device-mapped */
+  HICACHE_ERR_CUDA = -6,            /* a CUDA runtime call failed (text in last_error) */
+  HICACHE_ERR_TIMEOUT = -7,         /* hicache_wait ran out of time */
+  HICACHE_ERR_NOMEM = -8,           /* host allocation failed */
+  HICACHE_ERR_DEVICE_CHECK = -9     /* checked mode: a kernel saw an out-of-range offset */
+} hicache_status;
+
+typedef enum {
+  HICACHE_LAYOUT_POOL = -1,         /* the pool's own layout (desc.layout) */
+  HICACHE_LAYER_FIRST = 0,
+  HICACHE_PAGE_FIRST = 1,
+  HICACHE_PAGE_FIRST_DIRECT = 2
+} hicache_layout;
+
+typedef enum {
+  HICACHE_DIR_BACKUP = 0,           /* device -> host (L1 -> L2) */
+  HICACHE_DIR_LOAD = 1              /* host -> device (L2 -> L1) */
+} hicache_direction;
+
+/* Pool flags. */
+#define HICACHE_POOL_CHECKED 0x1    /* kernels bounds-check every offset against the
+                                       pool and buffer sizes and report, instead of
+                                       touching, anything outside (debug; slower) */
+
+/* Host allocation flags for hicache_host_alloc. */
+#define HICACHE_HOST_THP 0x1        /* anonymous mmap + madvise(MADV_HUGEPAGE) before
+                                       page-locking ("Tuning ... section 2.4": huge pages
+                                       cut translation entries ~512x; madvise must come
+                                       before registration) */
+
+typedef struct {
+  int32_t num_layers;       /* L >= 1 */
+  int32_t num_buffers;      /* B: 2 = K,V (MHA/GQA), 1 = MLA latent; B*L <= 512 */
+  int32_t page_size;        /* P >= 1 tokens per page */
+  int32_t elem_bytes;       /* bytes per element (2 for bf16) */
+  int64_t row_elems;        /* R: kv_heads*head_dim, or kv_dim (e.g. 576) */
+  int64_t host_num_pages;   /* Hp: pages in the host pool */
+  int32_t layout;           /* hicache_layout of the host pool (not POOL) */
+  int32_t launch_ctas;      /* CTAs per transfer launch; 0 = automatic */
+  int32_t flags;            /* HICACHE_POOL_* */
+  int32_t reserved;         /* must be 0 */
+} hicache_pool_desc;
+
+/* Borrowed device KV, passed to each call.  buf_ptrs: host array of B*L device
+ * pointers, buffer-major (K layer 0..L-1, then V layer 0..L-1); each points to
+ * device_num_pages*page_size rows of row_elems elements, contiguous, 16-byte
+ * aligned.  The library does not keep the pointers after the call returns. */
+typedef struct {
+  void *const *buf_ptrs;
+  int64_t device_num_pages;
+} hicache_device_kv;
+
+typedef struct hicache_pool hicache_pool; /* opaque */
+typedef struct hicache_plan hicache_plan; /* opaque: a validated, pre-passed index set */
+
+/* ---- version / diagnostics ------------------------------------------------ */
+
+/* Library version as 10000*major + 100*minor + patch. */
+int32_t hicache_version(void);
+
+/* Text of the calling thread's most recent error ("" if none).  The pointer
+ * stays valid until the thread's next hicache call. */
+const char *hicache_last_error(void);
+
+/* Number of kernels the library has launched in this process (all threads). */
+int64_t hicache_launch_count(void);
+
+/* ---- pinned host memory --------------------------------------------------- */
+
+/* Allocate `bytes` of page-locked host memory that the current device can
+ * address, for use as a host pool.  flags: HICACHE_HOST_THP or 0 (plain
+ * cudaHostAlloc).  *out receives the host pointer; free with hicache_host_free.
+ * Errors: INVALID_ARG (bytes == 0, out NULL), NOMEM, CUDA. */
+int hicache_host_alloc(size_t bytes, int32_t flags, void **out);
+int hicache_host_free(void *ptr);
+
+/* ---- pool ----------------------------------------------------------------- */
+
+/* Create a pool over a caller-owned pinned host buffer of host_bytes bytes
+ * (borrowed: it must outlive the pool).  The buffer must be page-locked and
+ * mapped for the current device (hicache_host_alloc, cudaHostAlloc, or a
+ * torch pin_memory tensor), 16-byte aligned, and at least
+ * B*L*host_num_pages*page_size*row_elems*elem_bytes bytes.  The pool binds to
+ * the current device and creates one CUDA event per layer (timing disabled).
+ * Errors: INVALID_ARG, ALIGNMENT (row bytes or pointer not 16-byte multiples),
+ * NOT_PINNED, CUDA. */
+int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t host_bytes,
+                        hicache_pool **out);
+int hicache_pool_destroy(hicache_pool *pool);
+
+/* ---- transfers -------------------------------------------------------------
+ * device_pages / host_pages: n page indices each (host memory).  Validation:
+ * 0 <= device_pages[i] < kv->device_num_pages, 0 <= host_pages[i] <
+ * host_num_pages (INDEX_RANGE); a backup may not name a host page twice and a
+ * load may not name a device page twice (DUPLICATE_INDEX: the result would
+ * depend on execution order); a source page may repeat.
+ * Each call enqueues ceil(runs / 1536) kernel launches, where runs is the number
+ * of maximal page runs contiguous on both sides; calls of up to 1536 pages are
+ * exactly one launch. */
+
+/* L1 -> L2: every layer and buffer of the given device pages into the given
+ * host pages. */
+int hicache_backup(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
+                   const int64_t *host_pages, int64_t n, int32_t layout, void *stream);
+
+/* L2 -> L1: every layer and buffer of the given host pages into the given
+ * device pages. */
+int hicache_load(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
+                 const int64_t *host_pages, int64_t n, int32_t layout, void *stream);
+
+/* L2 -> L1 for one layer (every buffer of layer_id), then records the pool's
+ * event for that layer on `stream`. */
+int hicache_load_layer(hicache_pool *pool, const hicache_device_kv *kv,
+                       const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                       int32_t layout, int32_t layer_id, void *stream);
+
+/* ---- plans: pre-pass once, execute many times -------------------------------
+ * A plan holds the validated, sorted, run-merged index set of one transfer, so
+ * that the L per-layer loads of one request pay for validation and the pre-pass
+ * once (the prepare-ahead idea of "Rethinking the SGLang HiCache Boundary",
+ * section "PrepareBatch / ExecuteBatch").  device_num_pages bounds the device
+ * indices.  A plan is immutable and may be executed from several threads. */
+int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,
+                        int64_t n, int64_t device_num_pages, int32_t direction,
+                        hicache_plan **out);
+/* Execute a plan: every layer (layer_id < 0) or one layer (a load plan only;
+ * records that layer's event).  kv->device_num_pages must be >= the plan's. */
+int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                         int32_t layer_id, void *stream);
+/* Number of pages and of merged runs in a plan. */
+int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs);
+int hicache_plan_destroy(hicache_plan *plan);
+
+/* ---- per-layer events (KV_READY) ---------------------------------------------- */
+
+/* The pool-owned event recorded by the last load of `layer` (*event_out is a
+ * cudaEvent_t; do not destroy it). */
+int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
+/* Make `compute_stream` wait (on the device; the host does not block) for the
+ * last load of `layer` enqueued before this call. */
+int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
+
+/* Block the calling host thread until all work on `stream` is done, polling at
+ * most every 50 us, for at most timeout_us microseconds (< 0 = no limit).
+ * Returns OK, TIMEOUT (work still pending; nothing is cancelled) or CUDA. */
+int hicache_wait(void *stream, int64_t timeout_us);
+
+/* ---- host-only helpers (no CUDA call; usable without a GPU) ------------------ */
+
+/* Validate a transfer and run the pre-pass without a pool: the checks that a
+ * transfer call makes on its indices.  direction: hicache_direction.  On OK,
+ * *num_runs receives the number of maximal runs (pairs sorted by host page,
+ * merged while device and host page both step by one), and if runs_out is not
+ * NULL and runs_capacity >= *num_runs, runs_out receives 3 int64 per run:
+ * first host page, first device page, page count. */
+int hicache_prepass(int64_t host_num_pages, int64_t device_num_pages, const int64_t *device_pages,
+                    const int64_t *host_pages, int64_t n, int32_t direction, int64_t *num_runs,
+                    int64_t *runs_out, int64_t runs_capacity);
+
+/* Number of byte ranges contiguous on both sides that the transfer consists of
+ * (the DMA-descriptor count of a copy engine; "Tuning ... section 2.1": 39,936
+ * for page_first_direct vs 78 for layer_first at 512 pages x 78 layers, per
+ * buffer), for every layer (layer_id < 0) or one layer.  Returns the count, or
+ * a negative hicache_status. */
+int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *device_pages,
+                              const int64_t *host_pages, int64_t n, int32_t layout,
+                              int32_t layer_id);
+
+/* ---- measurement helper ------------------------------------------------------ */
+
+/* A stand-in for attention on one layer: reads the given pages of every buffer
+ * of `layer` `reps` times and adds the 32-bit words of one pass into
+ * *out_sum_dev (a device uint64, mod 2^64).  Used to show that a compute stream
+ * that waited on a layer event sees that layer loaded, and to measure overlap. */
+int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc *desc,
+                           const int64_t *device_pages, int64_t n, int32_t layer_id,
+                           int32_t reps, uint64_t *out_sum_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HICACHE_H_ */

@@ -158,17 +158,19 @@ int oracle_load(void *const *dev_bufs, const void *host, int64_t B, int64_t L,
  * A segment is a maximal byte range that is contiguous on BOTH sides of the
  * copy: one DMA descriptor in the pages' terms.  [T21 2.1][B-L2 "DMA Segment
  * Explosion"].  Counted by brute force over token rows: a row (b, l, pair i,
- * token t) is always contiguous on both sides (R elements).  Rows are visited in
- * device order -- buffer (b, l), then device slot d_i*P + t ascending -- and a
- * new segment starts at every row that does not continue the previous one on
- * both the device side (same buffer, next slot) and the host side (next R
- * elements).  layer < 0 counts every layer; otherwise only that layer. */
+ * token t) is always contiguous on both sides (R elements).  Rows are visited
+ * buffer (b, l) by buffer, pairs in ascending (host page, device page) order,
+ * tokens ascending -- a fixed order, so that the count depends on the set of
+ * pairs and not on the order of the arguments -- and a new segment starts at
+ * every row that does not continue the previous one on both the device side
+ * (same buffer, next slot) and the host side (next R elements).  layer < 0
+ * counts every layer; otherwise only that layer. */
 
-static const int64_t *g_sort_keys;  /* qsort has no context argument in C89 */
-static int cmp_by_key(const void *a, const void *b) {
+static const int64_t *g_host_keys, *g_dev_keys;  /* qsort has no context argument */
+static int cmp_by_host_then_dev(const void *a, const void *b) {
   const int64_t ia = *(const int64_t *)a, ib = *(const int64_t *)b;
-  if (g_sort_keys[ia] < g_sort_keys[ib]) return -1;
-  if (g_sort_keys[ia] > g_sort_keys[ib]) return 1;
+  if (g_host_keys[ia] != g_host_keys[ib]) return g_host_keys[ia] < g_host_keys[ib] ? -1 : 1;
+  if (g_dev_keys[ia] != g_dev_keys[ib]) return g_dev_keys[ia] < g_dev_keys[ib] ? -1 : 1;
   return (ia > ib) - (ia < ib);
 }
 
@@ -183,8 +185,9 @@ int64_t oracle_segment_count(int64_t B, int64_t L, int64_t P, int64_t R, int64_t
   order = (int64_t *)malloc((size_t)n * sizeof(int64_t));
   if (!order) return -1;
   for (i = 0; i < n; ++i) order[i] = i;
-  g_sort_keys = dev_pages;
-  qsort(order, (size_t)n, sizeof(int64_t), cmp_by_key);
+  g_host_keys = host_pages;
+  g_dev_keys = dev_pages;
+  qsort(order, (size_t)n, sizeof(int64_t), cmp_by_host_then_dev);
   for (b = 0; b < B; ++b)
     for (l = l_begin; l < l_end; ++l) {
       int have_prev = 0;

@@ -236,8 +236,8 @@ def pin_roundtrip_and_untouched(o):
 
 def _runs(dp, hp):
     """Maximal runs of pairs where the device AND the host page both step by
-    one, counted on the pairs sorted by device page."""
-    order = np.argsort(dp, kind="stable")
+    one, counted on the pairs sorted by (host page, device page)."""
+    order = np.lexsort((np.asarray(dp), np.asarray(hp)))
     d, h = np.asarray(dp)[order], np.asarray(hp)[order]
     if len(d) == 0:
         return 0
@@ -283,6 +283,12 @@ def pin_segment_count_closed_forms(o):
             # one layer: page_first rows of one layer are L*R apart on the host
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["page_first"], 1) == B * n * P
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["layer_first"], 0) == B * runs
+        # a repeated source page (a backup may copy one device page twice): the
+        # count does not depend on the order of the arguments
+        dp2 = np.array([1, 2, 2, 7]); hp2 = np.array([3, 9, 4, 5])
+        for perm in ([0, 1, 2, 3], [2, 0, 3, 1], [3, 2, 1, 0]):
+            assert o.segment_count(B, L, P, R, Hp, dp2[perm], hp2[perm], LAYOUT_IDS["layer_first"]) \
+                == B * L * _runs(dp2, hp2) == B * L * 3
         # a single layer pool: every layout degenerates to layer_first's count
         dp, hp = rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False)
         for lay in LAYOUT_IDS.values():

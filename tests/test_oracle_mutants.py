@@ -29,7 +29,7 @@ MUTANTS = [
      "if (layer >= 0) { l_begin = 0; l_end = layer + 1; }\n  for (i = 0; i < n; ++i)\n    if (host_pages[i] < 0 || host_pages[i] >= Hp || dev_pages[i] < 0) return -1;\n  for (i = 0; i < n; ++i) {\n    const int64_t d = dev_pages[i], h = host_pages[i];\n    for (b = 0; b < B; ++b)\n      for (l = l_begin; l < l_end; ++l) {\n        uint8_t"),
     ("segment_host_step", "host == prev_host + R", "host == prev_host + 1"),
     ("segment_slot_step", "slot == prev_slot + 1", "slot == prev_slot + P"),
-    ("segment_unsorted", "qsort(order, (size_t)n, sizeof(int64_t), cmp_by_key);", ""),
+    ("segment_unsorted", "qsort(order, (size_t)n, sizeof(int64_t), cmp_by_host_then_dev);", ""),
     ("load_reads_wrong_pair", "const int64_t d = dev_pages[i], h = host_pages[i];\n    for (b = 0; b < B; ++b)\n      for (l = l_begin",
      "const int64_t d = dev_pages[i], h = host_pages[n - 1 - i];\n    for (b = 0; b < B; ++b)\n      for (l = l_begin"),
 ]
