@@ -1,0 +1,437 @@
+"""Benchmark: L1 <-> L2 KV movement GB/s at 32K tokens on GB300.
+
+A step is one pass of the hot path over the Llama-3-8B-shaped workload (32
+layers, K and V, 8 KV heads x 128, page 64; 512 pages = 32,768 tokens; device
+pages from a fragmented allocator, host pages contiguous), in each host layout
+(layer_first, page_first, page_first_direct):
+    backup   512 pages L1 -> L2                      (4 GiB)
+    load     512 pages L2 -> L1                      (4 GiB)
+    bidir    backup of request A while request B loads on a second stream
+             (4 GiB each way)
+so 48 GiB move per step.  Every transfer is one kernel launch of libhicache.
+
+Reported: whole-step GB/s (`value`), per layout/operation GB/s and their
+fraction of the host-link peak measured in the same run (pinned
+cudaMemcpyAsync of 1 GiB: H2D, D2H, both at once), the roofline of the
+dominant kernel, the device-side HBM fraction, clocks during the timed
+region, an end-to-end number through the Python API with host wall-clock,
+and the oracle's rate on the host cores (``cpu_baseline``).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+path has no exchange step); value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "L1↔L2 KV GB/s (load, backup, bidir) at 32K tokens; % of measured host-link peak"
+LAYOUT_NAMES = ["layer_first", "page_first", "page_first_direct"]
+NOMINAL = {"pcie_gen5_x16_per_dir_gbs": 63.0, "nvlink_c2c_per_dir_gbs": 450.0}
+GB = 1e9
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "MEASURED_PEAKS.json"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------- workload
+def build_workload(device):
+    import torch
+    import tiered_kv_cache_gb300 as hc
+    from tiered_kv_cache_gb300 import workloads as wl
+
+    s = wl.LLAMA3_8B
+    vals = [v.view(torch.int16) for v in wl.kv_values(s, device=device)]
+    t = wl.llama_transfer(s, 512)
+    a_dev = t.device_pages
+    rng = wl.index_rng(s.seed + 1)
+    b_dev = wl.fragmented_pages(rng, s.device_pages, 512, exclude=a_dev)
+    a_host = wl.contiguous_pages(512, 0)
+    b_host = wl.contiguous_pages(512, 512)
+    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first")
+    kv = hc.DeviceKV(vals, s.device_pages)
+    return dict(shape=s, vals=vals, kv=kv, pool=pool, a_dev=a_dev, b_dev=b_dev, a_host=a_host,
+                b_host=b_host, bytes_per_xfer=512 * s.page_bytes)
+
+
+def link_peaks(torch, nbytes=1 << 30, reps=5):
+    """Pinned cudaMemcpyAsync of 1 GiB: H2D, D2H, and both at once."""
+    host_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host_b = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dev_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            s2.wait_event(e0)
+            fn()
+            done = torch.cuda.Event()
+            done.record(s2)
+            s1.wait_event(done)
+            e1.record(s1)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) / 1e3)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            dev_a.copy_(host_a, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            host_b.copy_(dev_b, non_blocking=True)
+
+    def both():
+        with torch.cuda.stream(s1):
+            dev_a.copy_(host_a, non_blocking=True)
+        with torch.cuda.stream(s2):
+            host_b.copy_(dev_b, non_blocking=True)
+
+    t_h2d, t_d2h, t_bi = timed(h2d), timed(d2h), timed(both)
+    res = {"h2d_gbs": nbytes / t_h2d / GB, "d2h_gbs": nbytes / t_d2h / GB,
+           "bidir_gbs": 2 * nbytes / t_bi / GB, "bytes": nbytes, "how": "pinned cudaMemcpyAsync, best of 5"}
+    dev_d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    t_dd = timed(lambda: dev_d.copy_(dev_a))
+    res["d2d_gbs"] = 2 * nbytes / t_dd / GB
+    del host_a, host_b, dev_a, dev_b, dev_d
+    return res
+
+
+def run_step(torch, w, s1, s2, ev=None):
+    """One step; if `ev` is a list, (name, start, end) event triples are appended."""
+    pool, kv = w["pool"], w["kv"]
+    for lay in LAYOUT_NAMES:
+        lid = {"layer_first": 0, "page_first": 1, "page_first_direct": 2}[lay]
+
+        def mark():
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(s1)
+            return e
+        e0 = mark() if ev is not None else None
+        pool.backup(kv, w["a_dev"], w["a_host"], lid, stream=s1)
+        e1 = mark() if ev is not None else None
+        pool.load(kv, w["a_dev"], w["a_host"], lid, stream=s1)
+        e2 = mark() if ev is not None else None
+        if ev is None:
+            e2 = torch.cuda.Event()
+            e2.record(s1)
+        s2.wait_event(e2)
+        pool.backup(kv, w["a_dev"], w["a_host"], lid, stream=s1)
+        pool.load(kv, w["b_dev"], w["b_host"], lid, stream=s2)
+        j = torch.cuda.Event(enable_timing=ev is not None)
+        j.record(s2)
+        s1.wait_event(j)
+        e3 = mark() if ev is not None else None
+        if ev is not None:
+            ev += [(f"{lay}/backup", e0, e1), (f"{lay}/load", e1, e2), (f"{lay}/bidir", e2, e3)]
+
+
+def cpu_baseline(seconds_target=12.0, pages=24):
+    """The oracle (single-threaded C, as written) on a bounded sample of the
+    same workload: `pages` pages per transfer, each layout, backup and load."""
+    import oracle
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B
+    o = oracle.Oracle()
+    rng = np.random.default_rng(0)
+    Dp = Hp = pages * 2
+    B, L, P, R = s.num_buffers, s.num_layers, s.page_size, s.row_elems
+    dev = [rng.integers(0, 65535, (Dp * P, R), dtype=np.uint16) for _ in range(B * L)]
+    host = np.zeros(B * L * Hp * P * R, np.uint16)
+    dp = wl.fragmented_pages(rng, Dp, pages)
+    hp = np.arange(pages)
+    moved = 0
+    t0 = time.perf_counter()
+    ops = 0
+    while True:
+        for lid in (0, 1, 2):
+            o.backup(dev, host, B, L, P, R, Hp, dp, hp, lid)
+            o.load(dev, host, B, L, P, R, Hp, dp, hp, lid)
+            moved += 2 * pages * s.page_bytes
+            ops += 2
+        el = time.perf_counter() - t0
+        if el >= seconds_target or ops >= 60:
+            break
+    return {"value": moved / el / GB, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{ops} transfers of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB each) of the "
+                      f"same shape, backup+load in all three layouts, host arrays, {el:.1f} s"}
+
+
+def reference_arm(args):
+    """`--impl reference`: the oracle on the host cores, timed on the same
+    workload shape, a bounded sample per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B
+    o = oracle.Oracle()
+    pages = 4
+    rng = np.random.default_rng(0)
+    Dp = Hp = 16
+    B, L, P, R = s.num_buffers, s.num_layers, s.page_size, s.row_elems
+    dev = [rng.integers(0, 65535, (Dp * P, R), dtype=np.uint16) for _ in range(B * L)]
+    host = np.zeros(B * L * Hp * P * R, np.uint16)
+    dp = wl.fragmented_pages(rng, Dp, pages)
+    hp = np.arange(pages)
+
+    def step():
+        for lid in (0, 1, 2):
+            o.backup(dev, host, B, L, P, R, Hp, dp, hp, lid)
+            o.load(dev, host, B, L, P, R, Hp, dp, hp, lid)
+        return 6 * pages * s.page_bytes
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    moved = sum(step() for _ in range(args.steps))
+    el = time.perf_counter() - t0
+    v = moved / el / GB
+    sample = f"per step: backup+load of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB) in each layout"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "llama3_8b_32k (oracle sample)", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ctas", type=int, default=0, help="CTAs per transfer launch (0 = automatic)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import tiered_kv_cache_gb300 as hc
+    from tiered_kv_cache_gb300 import build as hc_build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    hc_build.build()
+    peaks, peaks_src = measured_peaks()
+
+    link = link_peaks(torch)
+    w = build_workload("cuda")
+    if args.ctas:
+        w["pool"].close()
+        s = w["shape"]
+        w["pool"] = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
+                            "layer_first", launch_ctas=args.ctas)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(max(args.warmup, 3)):
+        run_step(torch, w, s1, s2)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region (device clock) --------------------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    launches0 = hc.launch_count()
+    ev = []
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(s1)
+    for _ in range(args.steps):
+        run_step(torch, w, s1, s2, ev)
+    t_end.record(s1)
+    barrier()
+    launches = hc.launch_count() - launches0
+    clk = clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    bpx = w["bytes_per_xfer"]
+    step_bytes = len(LAYOUT_NAMES) * 4 * bpx
+    value = world * args.steps * step_bytes / elapsed / GB
+
+    per = {}
+    for name, a, b in ev:
+        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    breakdown = {}
+    for lay in LAYOUT_NAMES:
+        bk = bpx / statistics.mean(per[f"{lay}/backup"]) / GB
+        ld = bpx / statistics.mean(per[f"{lay}/load"]) / GB
+        bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
+        breakdown[lay] = {
+            "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1), "bidir_gbs": round(bi, 1),
+            "backup_frac_of_link": round(bk / link["d2h_gbs"], 3),
+            "load_frac_of_link": round(ld / link["h2d_gbs"], 3),
+            "bidir_frac_of_link": round(bi / link["bidir_gbs"], 3),
+        }
+    # dominant single-direction kernel: the largest total time
+    singles = {k: sum(v) for k, v in per.items() if not k.endswith("bidir")}
+    dom = max(singles, key=singles.get)
+    dom_avg = statistics.mean(per[dom])
+    achieved = bpx / dom_avg / GB
+    dom_peak = link["d2h_gbs"] if dom.endswith("backup") else link["h2d_gbs"]
+    roofline = {"bound": "host_link", "kernel": f"xfer_kernel ({dom})", "achieved": round(achieved, 1),
+                "peak": round(dom_peak, 1), "unit": "GB/s", "frac": round(achieved / dom_peak, 3),
+                "traffic": None,
+                "peak_source": "in-run pinned cudaMemcpyAsync of 1 GiB, same direction (no host-link "
+                               "figure in MEASURED_PEAKS.json)",
+                "bytes_per_launch": bpx, "avg_launch_ms": round(dom_avg * 1e3, 3)}
+    # device side of the same kernel: the payload crosses HBM once
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    roofline_hbm = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4),
+                    "peak_source": f"{peaks_src} hbm_gbs (of measured)" if peaks_src != "fallback" else "fallback"}
+
+    # ---- end to end through the public API, host wall clock -----------------
+    torch.cuda.synchronize()
+    e2e_steps = max(2, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        run_step(torch, w, s1, s2)
+        hc.wait(s1)
+    e2e_t = time.perf_counter() - t0
+    e2e = {"value": round(world * e2e_steps * step_bytes / e2e_t / GB, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx + len(LAYOUT_NAMES) * 4 * 512 * 16,
+           "d2h_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx,
+           "how": "host wall clock around the Python API calls (validation, pre-pass, launch) and a "
+                  "host wait on the stream each step; host-index bytes counted as H2D"}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "llama3_8b_32k: 32 layers, K+V, 8 kv heads x 128, bf16, page 64, "
+                               "512 pages = 32768 tokens per transfer, fragmented device pages, "
+                               "contiguous host pages",
+                   "step": "per layout (layer_first, page_first, page_first_direct): backup, load, "
+                           "concurrent backup+load on two streams; 48 GiB per step",
+                   "l2": "inputs larger than L2 (4 GiB per transfer)",
+                   "launch_ctas": args.ctas or "auto"},
+        "roofline": roofline,
+        "roofline_hbm": roofline_hbm,
+        "link_peak": {**{k: round(v, 1) if isinstance(v, float) else v for k, v in link.items()}, **NOMINAL},
+        "breakdown": breakdown,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline()
+    w["pool"].close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -64,8 +64,7 @@ typedef enum {
   HICACHE_ERR_NOT_PINNED = -5,      /* host pool not page-locked / not device-mapped */
   HICACHE_ERR_CUDA = -6,            /* a CUDA runtime call failed (text in last_error) */
   HICACHE_ERR_TIMEOUT = -7,         /* hicache_wait ran out of time */
-  HICACHE_ERR_NOMEM = -8,           /* host allocation failed */
-  HICACHE_ERR_DEVICE_CHECK = -9     /* checked mode: a kernel saw an out-of-range offset */
+  HICACHE_ERR_NOMEM = -8            /* host allocation failed */
 } hicache_status;
 
 typedef enum {
@@ -79,11 +78,6 @@ typedef enum {
   HICACHE_DIR_BACKUP = 0,           /* device -> host (L1 -> L2) */
   HICACHE_DIR_LOAD = 1              /* host -> device (L2 -> L1) */
 } hicache_direction;
-
-/* Pool flags. */
-#define HICACHE_POOL_CHECKED 0x1    /* kernels bounds-check every offset against the
-                                       pool and buffer sizes and report, instead of
-                                       touching, anything outside (debug; slower) */
 
 /* Host allocation flags for hicache_host_alloc. */
 #define HICACHE_HOST_THP 0x1        /* anonymous mmap + madvise(MADV_HUGEPAGE) before
@@ -100,7 +94,7 @@ typedef struct {
   int64_t host_num_pages;   /* Hp: pages in the host pool */
   int32_t layout;           /* hicache_layout of the host pool (not POOL) */
   int32_t launch_ctas;      /* CTAs per transfer launch; 0 = automatic */
-  int32_t flags;            /* HICACHE_POOL_* */
+  int32_t flags;            /* must be 0 */
   int32_t reserved;         /* must be 0 */
 } hicache_pool_desc;
 
@@ -232,9 +226,12 @@ int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *devi
 /* ---- measurement helper ------------------------------------------------------ */
 
 /* A stand-in for attention on one layer: reads the given pages of every buffer
- * of `layer` `reps` times and adds the 32-bit words of one pass into
- * *out_sum_dev (a device uint64, mod 2^64).  Used to show that a compute stream
- * that waited on a layer event sees that layer loaded, and to measure overlap. */
+ * of `layer` `reps` times and adds every 32-bit word it reads into *out_sum_dev
+ * (a device uint64, mod 2^64; reps times the one-pass sum).  Used to show that a
+ * compute stream that waited on a layer event sees that layer loaded, and to
+ * measure compute/transfer overlap.  desc gives the shape (its host_num_pages
+ * and layout are not used); device_pages are host memory, n <= any size (one
+ * launch per 6144 pages).  Errors: INVALID_ARG, INDEX_RANGE, ALIGNMENT, CUDA. */
 int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc *desc,
                            const int64_t *device_pages, int64_t n, int32_t layer_id,
                            int32_t reps, uint64_t *out_sum_dev, void *stream);

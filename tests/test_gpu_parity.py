@@ -1,0 +1,281 @@
+"""GPU path vs the oracle, element by element, through the C ABI (GB300).
+
+Small shapes compare whole pools; they span several 16 KiB tiles with ragged
+tails, rows of 16 B to 2 KiB, 1-, 2- and 4-byte elements, one to three buffers,
+every layout, backup / load / per-layer load / plans.  The five workload shapes
+are checked at their full sizes in test_gpu_workloads.py."""
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gb300 as hc
+from tiered_kv_cache_gb300 import build as hc_build
+from tiered_kv_cache_gb300 import workloads as wl
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = list(hc.LAYOUTS.values())
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    hc_build.build()
+    torch.cuda.init()
+
+
+# (name, B, L, P, R, es, Dp, Hp, n, pattern)
+SHAPES = [
+    ("gqa_p16", 2, 2, 16, 128, 2, 64, 128, 12, "random"),
+    ("mla_like", 1, 5, 8, 576, 2, 40, 48, 17, "runs"),
+    ("row16B_3buf", 3, 3, 3, 8, 2, 30, 31, 11, "random"),
+    ("fp8_rows48B", 2, 4, 5, 48, 1, 24, 24, 9, "runs"),
+    ("fp32_rows48B", 2, 3, 4, 12, 4, 24, 26, 8, "random"),
+    ("ragged_tiles", 2, 2, 64, 72, 2, 60, 64, 40, "contiguous"),
+    ("one_layer", 2, 1, 16, 64, 2, 32, 32, 10, "runs"),
+    ("one_token_pages", 1, 6, 1, 256, 2, 64, 80, 33, "random"),
+]
+
+
+def indices(pattern, Dp, Hp, n, seed):
+    rng = np.random.default_rng(seed)
+    if pattern == "random":
+        return rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False)
+    if pattern == "contiguous":
+        return np.arange(n) + (Dp - n) // 2, np.arange(n) + 1
+    dp = wl.fragmented_pages(rng, Dp, n, max_run=4)
+    hp = np.sort(rng.choice(Hp, n, replace=False))
+    hp[: n // 2] = np.arange(n // 2) + 2      # half of it contiguous on the host too
+    hp = np.unique(hp)
+    while len(hp) < n:
+        extra = rng.choice(Hp, n - len(hp), replace=False)
+        hp = np.unique(np.concatenate([hp, extra]))
+    return dp, hp[:n]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_backup_load_parity(shape, layout):
+    name, B, L, P, R, es, Dp, Hp, n, pattern = shape
+    dp, hp = indices(pattern, Dp, Hp, n, seed=len(name) + layout)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, es, seed=7 + layout)
+    with hc.Pool(L, B, P, R, Hp, layout, elem_bytes=es) as pool:
+        gh.check_backup(pool, bufs, dp, hp, layout, B, L, P, R, Hp, es)
+        gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, es)
+        for layer in sorted({0, L - 1, L // 2}):
+            gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, es, layer=layer, seed=layer + 3)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_tiny_gqa_backup_then_load(layout):
+    """The tiny GQA pool: back up 12 random device pages into 12 random host
+    pages, sentinel-fill the device, load into 12 fresh random device pages."""
+    s = wl.TINY_GQA
+    B, L, P, R, Dp, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.device_pages, s.host_pages
+    rng = wl.index_rng(s.seed)
+    src = wl.distinct_pages(rng, Dp, 12)
+    hp = wl.distinct_pages(rng, Hp, 12)
+    dst = wl.distinct_pages(rng, Dp, 12)
+    vals = [t.view(torch.int16) for t in wl.kv_values(s, device="cuda")]
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        gh.check_backup(pool, vals, src, hp, layout, B, L, P, R, Hp, 2)
+        host_before = pool.host_array().copy()
+        orig = gh.to_np(vals, 2)
+        gh.sentinel_fill(vals, 0xFF)
+        kv = hc.DeviceKV(vals, Dp)
+        pool.load(kv, dst, hp, layout)
+        torch.cuda.synchronize()
+        want = [np.full((Dp * P, R), 0xFFFF, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host_before, B, L, P, R, Hp, dst, hp, layout)
+        got = gh.to_np(vals, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k])
+            for s_, d_ in zip(src, dst):   # round trip: the pages came back
+                assert np.array_equal(got[k][d_ * P:(d_ + 1) * P], orig[k][s_ * P:(s_ + 1) * P])
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_plan_execute_matches_direct_calls(layout):
+    B, L, P, R, Dp, Hp, n = 2, 4, 16, 128, 48, 64, 20
+    dp, hp = indices("runs", Dp, Hp, n, seed=5)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=11)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        plan = pool.plan(dp, hp, Dp, hc.BACKUP)
+        pn, pr = plan.info()
+        assert pn == n and pr == len(hc.prepass(Hp, Dp, dp, hp, hc.BACKUP))
+        host = pool.host_array(np.uint8)
+        host[:] = 0x11
+        kv = hc.DeviceKV(bufs, Dp)
+        plan.execute(kv)
+        torch.cuda.synchronize()
+        want = np.full(host.size, 0x11, np.uint8).view(np.uint16)
+        gh.orc().backup(gh.to_np(bufs, 2), want, B, L, P, R, Hp, dp, hp, layout)
+        assert np.array_equal(host.view(np.uint16), want)
+        # a load plan executed layer by layer equals one all-layer load
+        lplan = pool.plan(dp, hp, Dp, hc.LOAD)
+        host[:] = np.random.default_rng(2).integers(0, 256, host.size, dtype=np.uint8)
+        gh.sentinel_fill(bufs)
+        s = torch.cuda.Stream()
+        for layer in range(L):
+            lplan.execute(kv, layer=layer, stream=s)
+        s.synchronize()
+        want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, layout)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k])
+        with pytest.raises(hc.HiCacheError):      # per-layer execution of a backup plan
+            plan.execute(kv, layer=0)
+        plan.close()
+        lplan.close()
+
+
+def test_one_launch_per_call_and_errors_enqueue_nothing():
+    B, L, P, R, Dp, Hp = 2, 32, 16, 1024, 64, 64
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    kv = hc.DeviceKV(bufs, Dp)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        for n in (1, 2, 3, 4, 37, 64):
+            rng = np.random.default_rng(n)
+            c0 = hc.launch_count()
+            pool.load(kv, rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False))
+            assert hc.launch_count() - c0 == 1
+        c0 = hc.launch_count()
+        pool.backup(kv, [], [])                     # n == 0: nothing launched
+        assert hc.launch_count() == c0
+        bad = [
+            (([0, Dp], [0, 1]), "INDEX_RANGE"),
+            (([0, 1], [Hp, 1]), "INDEX_RANGE"),
+            (([-1], [0]), "INDEX_RANGE"),
+            (([3, 3], [0, 1]), "DUPLICATE_INDEX"),  # load writes device page 3 twice
+        ]
+        for (dp, hp), status in bad:
+            with pytest.raises(hc.HiCacheError) as e:
+                pool.load(kv, dp, hp)
+            assert e.value.status == status
+        with pytest.raises(hc.HiCacheError) as e:   # backup writes host page 5 twice
+            pool.backup(kv, [0, 1], [5, 5])
+        assert e.value.status == "DUPLICATE_INDEX"
+        with pytest.raises(hc.HiCacheError) as e:
+            pool.load_layer(kv, [0], [0], L)
+        assert e.value.status == "INVALID_ARG"
+        with pytest.raises(hc.HiCacheError) as e:
+            pool.load(kv, [0], [0], layout=9)
+        assert e.value.status == "INVALID_ARG"
+        misaligned = hc.DeviceKV([bufs[0].data_ptr() + 8] + [b.data_ptr() for b in bufs[1:]], Dp)
+        with pytest.raises(hc.HiCacheError) as e:
+            pool.load(misaligned, [0], [0])
+        assert e.value.status == "ALIGNMENT"
+        assert hc.launch_count() == c0
+        # the failed calls changed nothing
+        torch.cuda.synchronize()
+        assert all(int(b.abs().sum()) == 0 for b in bufs[:2])
+
+
+def test_zero_page_layer_load_still_records_event():
+    B, L, P, R, Dp, Hp = 1, 3, 4, 64, 8, 8
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        s = torch.cuda.Stream()
+        pool.load_layer(hc.DeviceKV(bufs, Dp), [], [], 1, stream=s)
+        assert pool.layer_event(1) != 0
+        pool.wait_layer(1, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+
+
+def test_pool_rejects_pageable_and_accepts_torch_pinned():
+    B, L, P, R, Hp = 1, 2, 4, 64, 4
+    nbytes = B * L * Hp * P * R * 2
+    pageable = np.zeros(nbytes // 2 + 64, np.uint16)
+    addr = (pageable.ctypes.data + 15) // 16 * 16
+    with pytest.raises(hc.HiCacheError) as e:
+        hc.Pool(L, B, P, R, Hp, "layer_first", host_ptr=addr, host_bytes=nbytes)
+    assert e.value.status == "NOT_PINNED"
+    pinned = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    bufs = gh.random_device_bufs(B, L, P, R, 6, seed=3)
+    with hc.Pool(L, B, P, R, Hp, "page_first", host_ptr=pinned.data_ptr(), host_bytes=nbytes) as pool:
+        gh.check_backup(pool, bufs, [5, 0, 2], [1, 3, 0], 1, B, L, P, R, Hp, 2)
+
+
+def test_thp_host_pool():
+    B, L, P, R, Dp, Hp = 2, 4, 16, 256, 32, 40
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=9)
+    dp, hp = indices("runs", Dp, Hp, 24, seed=9)
+    with hc.Pool(L, B, P, R, Hp, "page_first_direct", thp=True) as pool:
+        gh.check_backup(pool, bufs, dp, hp, 2, B, L, P, R, Hp, 2)
+        gh.check_load(pool, bufs, dp, hp, 2, B, L, P, R, Hp, 2)
+
+
+def test_wait_times_out_without_cancelling():
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(int(1.5e9))               # a kernel that spins ~1 s, then ends
+    with pytest.raises(hc.HiCacheError) as e:
+        hc.wait(s, timeout_us=2000)
+    assert e.value.status == "TIMEOUT"
+    hc.wait(s, timeout_us=-1)                       # still completes
+    hc.wait(s, timeout_us=0)
+
+
+def test_layer_events_gate_compute():
+    """Per-layer loads on a transfer stream, each followed by the stand-in
+    attention on a compute stream that waited on that layer's event: every
+    checksum must see its layer fully loaded."""
+    B, L, P, R, Dp, Hp, n = 1, 8, 64, 576, 96, 96, 80
+    rng = np.random.default_rng(4)
+    dp = wl.fragmented_pages(rng, Dp, n)
+    hp = np.arange(n)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=4)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        gh.sentinel_fill(bufs, 0)
+        torch.cuda.synchronize()
+        kv = hc.DeviceKV(bufs, Dp)
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        for layer in range(L):
+            plan.execute(kv, layer=layer, stream=xfer)
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, reps=1, stream=comp)
+        comp.synchronize()
+        want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+        got = sums.cpu().numpy().view(np.uint64)
+        for layer in range(L):
+            words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+                                    for b in range(B)])
+            assert int(got[layer]) == int(words.astype(np.uint64).sum() % (1 << 64)), layer
+
+
+def test_bidirectional_streams():
+    """Backup of request A on one stream while request B loads on another."""
+    B, L, P, R, Dp, Hp, n = 2, 6, 16, 512, 64, 64, 24
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(Dp)
+    a_dev, b_dev = perm[:n], perm[n:2 * n]
+    a_host, b_host = np.arange(n), np.arange(n, 2 * n)
+    for layout in LAYOUTS:
+        bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=20 + layout)
+        with hc.Pool(L, B, P, R, Hp, layout) as pool:
+            host = pool.host_array(np.uint8)
+            host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+            host0 = host.copy()
+            dev0 = gh.to_np(bufs, 2)
+            kv = hc.DeviceKV(bufs, Dp)
+            s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+            pool.backup(kv, a_dev, a_host, stream=s1)
+            pool.load(kv, b_dev, b_host, stream=s2)
+            torch.cuda.synchronize()
+            want_host = host0.view(np.uint16).copy()
+            gh.orc().backup(dev0, want_host, B, L, P, R, Hp, a_dev, a_host, layout)
+            want_dev = [x.copy() for x in dev0]
+            gh.orc().load(want_dev, host0.view(np.uint16), B, L, P, R, Hp, b_dev, b_host, layout)
+            assert np.array_equal(host.view(np.uint16), want_host)
+            got = gh.to_np(bufs, 2)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want_dev[k])

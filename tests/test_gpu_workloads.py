@@ -1,0 +1,206 @@
+"""The four large workload shapes at their full sizes, on the GPU, in the launch
+configuration the benchmark times (automatic grid).
+
+Full pools are too large for the oracle to redo in seconds, so each transfer is
+checked on sampled elements whose host and device offsets come from the oracle
+one by one, plus properties that hold at any size: untouched pages keep their
+sentinel, a backup followed by a load is the identity, every call of up to
+1536 pages is one launch."""
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gb300 as hc
+from tiered_kv_cache_gb300 import build as hc_build
+from tiered_kv_cache_gb300 import workloads as wl
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+SENT16 = 0xC3C3          # never a normal(0,1) bf16 (it is about -390)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    hc_build.build()
+    torch.cuda.init()
+    yield
+    torch.cuda.empty_cache()
+
+
+def position_fill(words: np.ndarray, chunk=1 << 26):
+    """Host pool words = their own index: any misplaced copy is visible."""
+    for off in range(0, words.size, chunk):
+        m = min(chunk, words.size - off)
+        words[off:off + m] = np.arange(off, off + m, dtype=np.uint32)
+
+
+def count_equal(a: np.ndarray, value, chunk=1 << 27) -> int:
+    return sum(int(np.count_nonzero(a[o:o + chunk] == value)) for o in range(0, a.size, chunk))
+
+
+def device_pool(shape: wl.KVShape):
+    vals = wl.kv_values(shape, device="cuda")
+    return [v.view(torch.int16) for v in vals]
+
+
+def untouched_pages_ok(bufs, P, moved, sentinel16):
+    Dp = bufs[0].shape[0] // P
+    mask = torch.ones(Dp, dtype=torch.bool, device="cuda")
+    mask[torch.as_tensor(np.asarray(moved), device="cuda")] = False
+    s = torch.tensor(sentinel16, dtype=torch.int32).to(torch.int16).item()
+    for b in bufs:
+        rows = b.view(Dp, -1)[mask]
+        if rows.numel() and not bool((rows == s).all()):
+            return False
+    return True
+
+
+def run_backup_load(pool, bufs, shape, dp, hp, layout, samples=20000, seed=0):
+    B, L, P, R, Hp = shape.num_buffers, shape.num_layers, shape.page_size, shape.row_elems, shape.host_pages
+    Dp = bufs[0].shape[0] // P
+    kv = hc.DeviceKV(bufs, Dp)
+    host = pool.host_array(np.uint16)
+    # backup
+    host.view(np.uint8)[:] = 0xC3
+    c0 = hc.launch_count()
+    pool.backup(kv, dp, hp, layout)
+    torch.cuda.synchronize()
+    assert hc.launch_count() - c0 == 1
+    assert gh.sampled_host_check(host, bufs, dp, hp, layout, B, L, P, R, Hp, samples, seed)
+    moved_words = len(dp) * B * L * P * R
+    assert count_equal(host, SENT16) == host.size - moved_words
+    # load into sentinel-filled device pages from a position-coded host pool
+    keep = [b.clone() for b in bufs]
+    position_fill(host.view(np.uint32))
+    gh.sentinel_fill(bufs, 0xC3)
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    pool.load(kv, dp, hp, layout)
+    torch.cuda.synchronize()
+    assert hc.launch_count() - c0 == 1
+    assert gh.sampled_host_check(host, bufs, dp, hp, layout, B, L, P, R, Hp, samples, seed + 1)
+    assert untouched_pages_ok(bufs, P, dp, SENT16)
+    for b, k in zip(bufs, keep):
+        b.copy_(k)
+    del keep
+
+
+@pytest.mark.parametrize("shuffled_host", [False, True], ids=["host_contiguous", "host_shuffled"])
+def test_llama3_8b_32k_all_layouts(shuffled_host):
+    s = wl.LLAMA3_8B
+    t = wl.llama_transfer(s, 512, shuffled_host=shuffled_host)
+    bufs = device_pool(s)
+    with hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
+                 "layer_first") as pool:
+        for layout in hc.LAYOUTS.values():
+            run_backup_load(pool, bufs, s, t.device_pages, t.host_pages, layout, seed=layout)
+        # round trip through the host into other device pages is the identity
+        src = t.device_pages
+        rest = np.setdiff1d(np.arange(s.device_pages), src)[: len(src)]
+        kv = hc.DeviceKV(bufs, s.device_pages)
+        for layout in hc.LAYOUTS.values():
+            pool.backup(kv, src, t.host_pages, layout)
+            pool.load(kv, rest, t.host_pages, layout)
+            torch.cuda.synchronize()
+            P = s.page_size
+            si = torch.as_tensor(src, device="cuda")
+            di = torch.as_tensor(rest, device="cuda")
+            for b in bufs:
+                v = b.view(s.device_pages, -1)
+                assert torch.equal(v[si], v[di])
+    del bufs
+    torch.cuda.empty_cache()
+
+
+def test_deep78_32k_bidirectional():
+    s = wl.DEEP_STRESS
+    a, b_req = wl.deep_bidir_transfers(s, 512)
+    bufs = device_pool(s)
+    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    kv = hc.DeviceKV(bufs, s.device_pages)
+    with hc.Pool(L, B, P, R, Hp, "page_first_direct") as pool:
+        host = pool.host_array(np.uint16)
+        for layout in hc.LAYOUTS.values():
+            position_fill(host.view(np.uint32))
+            s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+            c0 = hc.launch_count()
+            pool.backup(kv, a.device_pages, a.host_pages, layout, stream=s1)
+            pool.load(kv, b_req.device_pages, b_req.host_pages, layout, stream=s2)
+            torch.cuda.synchronize()
+            assert hc.launch_count() - c0 == 2
+            assert gh.sampled_host_check(host, bufs, a.device_pages, a.host_pages, layout, B, L, P, R, Hp,
+                                         20000, 10 + layout)
+            assert gh.sampled_host_check(host, bufs, b_req.device_pages, b_req.host_pages, layout, B, L, P,
+                                         R, Hp, 20000, 20 + layout)
+    del bufs, kv
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tokens", [4096, 16384, 65536])
+def test_mla61_per_layer_load_with_events(tokens):
+    s = wl.MLA_LATENT
+    t = wl.mla_transfer(s, tokens)
+    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    bufs = device_pool(s)
+    kv = hc.DeviceKV(bufs, s.device_pages)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint16)
+        position_fill(host.view(np.uint32))
+        gh.sentinel_fill(bufs, 0xC3)
+        torch.cuda.synchronize()
+        xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        plan = pool.plan(t.device_pages, t.host_pages, s.device_pages, hc.LOAD)
+        c0 = hc.launch_count()
+        for layer in range(L):
+            plan.execute(kv, layer=layer, stream=xfer)
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 == 2 * L
+        assert gh.sampled_host_check(host, bufs, t.device_pages, t.host_pages, 1, B, L, P, R, Hp, 30000, 4)
+        assert untouched_pages_ok(bufs, P, t.device_pages, SENT16)
+        # the checksums taken behind each layer event equal those taken after
+        # everything finished
+        after = torch.zeros(L, dtype=torch.int64, device="cuda")
+        for layer in range(L):
+            hc.layer_checksum(kv, pool, t.device_pages, layer, after.data_ptr() + 8 * layer)
+        torch.cuda.synchronize()
+        assert torch.equal(sums, after)
+        if tokens <= 16384:
+            # and both equal the sums of what the oracle loads
+            n = len(t.device_pages)
+            want = [np.zeros((n * P, R), np.uint16) for _ in range(L)]
+            gh.orc().load(want, host, B, L, P, R, Hp, np.arange(n), t.host_pages, 1)
+            exp = np.array([w.view(np.uint32).astype(np.uint64).sum() for w in want], np.uint64)
+            assert np.array_equal(after.cpu().numpy().view(np.uint64), exp)
+        plan.close()
+    del bufs, kv
+    torch.cuda.empty_cache()
+
+
+def test_small_mix_one_launch_per_call():
+    s = wl.SMALL_MIX
+    reqs = wl.small_mix_requests(s)[:300]
+    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    bufs = device_pool(s)
+    kv = hc.DeviceKV(bufs, s.device_pages)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        host = pool.host_array(np.uint16)
+        position_fill(host.view(np.uint32))
+        for k, r in enumerate(reqs):
+            c0 = hc.launch_count()
+            if r.direction == "backup":
+                pool.backup(kv, r.device_pages, r.host_pages)
+            else:
+                pool.load(kv, r.device_pages, r.host_pages)
+            torch.cuda.synchronize()
+            assert hc.launch_count() - c0 == 1
+            assert gh.sampled_host_check(host, bufs, r.device_pages, r.host_pages, 0, B, L, P, R, Hp,
+                                         1000, k), k
+    del bufs, kv
+    torch.cuda.empty_cache()

@@ -1,0 +1,342 @@
+"""tiered_kv_cache_gb300: L1 (GPU HBM) <-> L2 (pinned host DRAM) paged KV movement
+for GB300, as a thin ctypes binding over ``libhicache.so``.
+
+The binding only marshals arguments: every step of a transfer (validation,
+pre-pass, kernels) runs in the C/CUDA library.  There is no fallback: if the
+library is not built, importing works but every call raises.
+
+Names follow the C ABI in ``include/hicache.h``:
+    Pool.backup / Pool.load / Pool.load_layer / Pool.wait_layer
+    Pool.plan(...) -> Plan.execute(...)
+    host_alloc / host_free, wait, prepass, segment_count, layer_checksum
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+__all__ = [
+    "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
+    "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan",
+    "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum",
+    "launch_count", "version",
+]
+
+LAYOUT_POOL = -1
+LAYER_FIRST = 0
+PAGE_FIRST = 1
+PAGE_FIRST_DIRECT = 2
+LAYOUTS = {"layer_first": LAYER_FIRST, "page_first": PAGE_FIRST,
+           "page_first_direct": PAGE_FIRST_DIRECT}
+BACKUP = 0
+LOAD = 1
+HOST_THP = 0x1
+
+STATUS = {0: "OK", -1: "INVALID_ARG", -2: "INDEX_RANGE", -3: "DUPLICATE_INDEX", -4: "ALIGNMENT",
+          -5: "NOT_PINNED", -6: "CUDA", -7: "TIMEOUT", -8: "NOMEM"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libhicache.so")
+
+
+class HiCacheError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS.get(code, code)}: {message}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("num_buffers", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
+                ("row_elems", ctypes.c_int64), ("host_num_pages", ctypes.c_int64),
+                ("layout", ctypes.c_int32), ("launch_ctas", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class _DeviceKVStruct(ctypes.Structure):
+    _fields_ = [("buf_ptrs", ctypes.POINTER(ctypes.c_void_p)), ("device_num_pages", ctypes.c_int64)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+_P = ctypes.POINTER
+
+
+def _bind(lib):
+    sigs = {
+        "hicache_version": (_i32, []),
+        "hicache_last_error": (ctypes.c_char_p, []),
+        "hicache_launch_count": (_i64, []),
+        "hicache_host_alloc": (ctypes.c_int, [_sz, _i32, _P(_vp)]),
+        "hicache_host_free": (ctypes.c_int, [_vp]),
+        "hicache_pool_create": (ctypes.c_int, [_P(PoolDesc), _vp, _sz, _P(_vp)]),
+        "hicache_pool_destroy": (ctypes.c_int, [_vp]),
+        "hicache_backup": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
+        "hicache_load": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
+        "hicache_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _i32, _vp]),
+        "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
+        "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
+        "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
+        "hicache_plan_destroy": (ctypes.c_int, [_vp]),
+        "hicache_layer_event": (ctypes.c_int, [_vp, _i32, _P(_vp)]),
+        "hicache_wait_layer": (ctypes.c_int, [_vp, _i32, _vp]),
+        "hicache_wait": (ctypes.c_int, [_vp, _i64]),
+        "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
+        "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
+        "hicache_layer_checksum": (ctypes.c_int, [_P(_DeviceKVStruct), _P(PoolDesc), _vp, _i64, _i32,
+                                                  _i32, _vp, _vp]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+def library():
+    """The loaded libhicache (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lib_lock:
+            if _lib is None:
+                path = library_path()
+                if not os.path.exists(path):
+                    raise RuntimeError(
+                        f"{path} is missing: build it with tiered_kv_cache_gb300.build.build() "
+                        "(there is no fallback path)")
+                _lib = _bind(ctypes.CDLL(path))
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        msg = library().hicache_last_error().decode(errors="replace")
+        raise HiCacheError(rc, msg)
+
+
+def _stream(stream) -> int:
+    """cudaStream_t handle from None (legacy default), an int, or a torch stream."""
+    if stream is None:
+        return 0
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _idx(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64).reshape(-1))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data if a.size else None
+
+
+def version() -> int:
+    return library().hicache_version()
+
+
+def launch_count() -> int:
+    return library().hicache_launch_count()
+
+
+def host_alloc(nbytes: int, thp: bool = False) -> int:
+    """Page-locked, device-mapped host memory (HICACHE_HOST_THP: mmap + huge
+    pages before locking).  Returns the host address."""
+    out = ctypes.c_void_p()
+    _check(library().hicache_host_alloc(nbytes, HOST_THP if thp else 0, ctypes.byref(out)))
+    return out.value
+
+
+def host_free(ptr: int):
+    _check(library().hicache_host_free(ptr))
+
+
+def wait(stream=None, timeout_us: int = -1):
+    """Block until `stream` is idle, for at most timeout_us (raises TIMEOUT)."""
+    _check(library().hicache_wait(_stream(stream), timeout_us))
+
+
+class DeviceKV:
+    """B*L device buffer pointers (buffer-major) plus the device pool size in
+    pages.  ``tensors`` may be torch tensors (their data_ptr is taken) or raw
+    integer addresses; the caller keeps the memory alive."""
+
+    def __init__(self, tensors, device_num_pages: int):
+        ptrs = [t if isinstance(t, int) else t.data_ptr() for t in tensors]
+        self._arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        self._tensors = tensors
+        self.struct = _DeviceKVStruct(ctypes.cast(self._arr, ctypes.POINTER(ctypes.c_void_p)),
+                                      device_num_pages)
+        self.device_num_pages = device_num_pages
+        self.num_buffers_total = len(ptrs)
+
+
+def _desc(num_layers, num_buffers, page_size, row_elems, host_num_pages, layout,
+          elem_bytes=2, launch_ctas=0) -> PoolDesc:
+    if isinstance(layout, str):
+        layout = LAYOUTS[layout]
+    return PoolDesc(num_layers, num_buffers, page_size, elem_bytes, row_elems, host_num_pages,
+                    layout, launch_ctas, 0, 0)
+
+
+def prepass(host_num_pages: int, device_num_pages: int, device_pages, host_pages, direction: int):
+    """Validate a transfer and return its runs as an (r, 3) int64 array of
+    (first host page, first device page, page count)."""
+    dp, hp = _idx(device_pages), _idx(host_pages)
+    if dp.size != hp.size:
+        raise ValueError("device_pages and host_pages differ in length")
+    nr = ctypes.c_int64()
+    out = np.zeros((max(1, dp.size), 3), np.int64)
+    _check(library().hicache_prepass(host_num_pages, device_num_pages, _ptr(dp), _ptr(hp), dp.size,
+                                     direction, ctypes.byref(nr), out.ctypes.data, out.shape[0]))
+    return out[: nr.value].copy()
+
+
+def segment_count(num_layers, num_buffers, page_size, row_elems, host_num_pages, layout,
+                  device_pages, host_pages, layer: int = -1, elem_bytes: int = 2) -> int:
+    d = _desc(num_layers, num_buffers, page_size, row_elems, host_num_pages, layout, elem_bytes)
+    dp, hp = _idx(device_pages), _idx(host_pages)
+    r = library().hicache_segment_count(ctypes.byref(d), _ptr(dp), _ptr(hp), dp.size, d.layout, layer)
+    if r < 0:
+        _check(int(r))
+    return int(r)
+
+
+def layer_checksum(kv: DeviceKV, pool_or_desc, device_pages, layer: int, out_ptr: int,
+                   reps: int = 1, stream=None):
+    """Stand-in attention: adds the 32-bit words of `layer` of the given device
+    pages (every buffer, `reps` passes) into the device uint64 at out_ptr."""
+    desc = pool_or_desc.desc if isinstance(pool_or_desc, Pool) else pool_or_desc
+    dp = _idx(device_pages)
+    _check(library().hicache_layer_checksum(ctypes.byref(kv.struct), ctypes.byref(desc), _ptr(dp),
+                                            dp.size, layer, reps, out_ptr, _stream(stream)))
+
+
+class Pool:
+    """A host L2 pool of ``host_num_pages`` pages in one layout.
+
+    If ``host_ptr`` is None the pool allocates its pinned memory with
+    host_alloc (``thp`` selects the huge-page path) and frees it on close()."""
+
+    def __init__(self, num_layers: int, num_buffers: int, page_size: int, row_elems: int,
+                 host_num_pages: int, layout="layer_first", elem_bytes: int = 2,
+                 host_ptr: int | None = None, host_bytes: int | None = None,
+                 launch_ctas: int = 0, thp: bool = False):
+        self.desc = _desc(num_layers, num_buffers, page_size, row_elems, host_num_pages, layout,
+                          elem_bytes, launch_ctas)
+        self.num_layers, self.num_buffers, self.page_size = num_layers, num_buffers, page_size
+        self.row_elems, self.host_num_pages, self.elem_bytes = row_elems, host_num_pages, elem_bytes
+        self.layout = self.desc.layout
+        self.nbytes = num_buffers * num_layers * host_num_pages * page_size * row_elems * elem_bytes
+        self._owned = host_ptr is None
+        self.host_ptr = host_alloc(self.nbytes, thp) if host_ptr is None else host_ptr
+        self.host_bytes = self.nbytes if host_bytes is None else host_bytes
+        h = ctypes.c_void_p()
+        try:
+            _check(library().hicache_pool_create(ctypes.byref(self.desc), self.host_ptr,
+                                                 self.host_bytes, ctypes.byref(h)))
+        except Exception:
+            if self._owned:
+                host_free(self.host_ptr)
+            raise
+        self.handle = h.value
+
+    # numpy view of the host pool (no copy)
+    def host_array(self, dtype=np.uint16) -> np.ndarray:
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self.host_ptr)
+        return np.frombuffer(buf, dtype=np.uint8).view(dtype)
+
+    def _xfer(self, fn, kv: DeviceKV, device_pages, host_pages, layout, stream, *extra):
+        dp, hp = _idx(device_pages), _idx(host_pages)
+        if dp.size != hp.size:
+            raise ValueError("device_pages and host_pages differ in length")
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        args = [self.handle, ctypes.byref(kv.struct), _ptr(dp), _ptr(hp), dp.size, layout]
+        _check(fn(*args, *extra, _stream(stream)))
+
+    def backup(self, kv: DeviceKV, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
+        self._xfer(library().hicache_backup, kv, device_pages, host_pages, layout, stream)
+
+    def load(self, kv: DeviceKV, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
+        self._xfer(library().hicache_load, kv, device_pages, host_pages, layout, stream)
+
+    def load_layer(self, kv: DeviceKV, device_pages, host_pages, layer: int, layout=LAYOUT_POOL,
+                   stream=None):
+        self._xfer(library().hicache_load_layer, kv, device_pages, host_pages, layout, stream, layer)
+
+    def wait_layer(self, layer: int, compute_stream=None):
+        _check(library().hicache_wait_layer(self.handle, layer, _stream(compute_stream)))
+
+    def layer_event(self, layer: int) -> int:
+        ev = ctypes.c_void_p()
+        _check(library().hicache_layer_event(self.handle, layer, ctypes.byref(ev)))
+        return ev.value
+
+    def plan(self, device_pages, host_pages, device_num_pages: int, direction: int) -> "Plan":
+        return Plan(self, device_pages, host_pages, device_num_pages, direction)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check(library().hicache_pool_destroy(self.handle))
+            self.handle = None
+            if self._owned and self.host_ptr:
+                host_free(self.host_ptr)
+                self.host_ptr = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Plan:
+    """A validated, pre-passed transfer that can be executed many times (e.g.
+    once per layer)."""
+
+    def __init__(self, pool: Pool, device_pages, host_pages, device_num_pages: int, direction: int):
+        dp, hp = _idx(device_pages), _idx(host_pages)
+        if dp.size != hp.size:
+            raise ValueError("device_pages and host_pages differ in length")
+        h = ctypes.c_void_p()
+        _check(library().hicache_plan_create(pool.handle, _ptr(dp), _ptr(hp), dp.size,
+                                             device_num_pages, direction, ctypes.byref(h)))
+        self.pool = pool
+        self.handle = h.value
+
+    def execute(self, kv: DeviceKV, layer: int = -1, layout=LAYOUT_POOL, stream=None):
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_plan_execute(self.handle, ctypes.byref(kv.struct), layout, layer,
+                                              _stream(stream)))
+
+    def info(self):
+        n, r = ctypes.c_int64(), ctypes.c_int64()
+        _check(library().hicache_plan_info(self.handle, ctypes.byref(n), ctypes.byref(r)))
+        return n.value, r.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            library().hicache_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

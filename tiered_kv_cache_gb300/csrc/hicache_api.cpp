@@ -1,0 +1,681 @@
+// hicache_api.cpp -- host side of libhicache: argument validation, the index
+// sort / run-length pre-pass, pools, plans, per-layer events and launches.
+//
+// Every transfer call validates everything BEFORE it enqueues anything, so a
+// call that fails has no effect.  Kernels are launched through
+// hicache::launch_xfer (hicache_kernels.cu).
+
+#include "hicache.h"
+
+#include <cuda_runtime.h>
+#include <sys/mman.h>
+#include <unistd.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <thread>
+#include <unordered_map>
+#include <vector>
+
+#include "hicache_internal.h"
+
+using hicache::RunRec;
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<int64_t> g_launches{0};
+
+int set_error(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_error(cudaError_t e, const char *what) {
+  return set_error(HICACHE_ERR_CUDA, "%s: %s (%d)", what, cudaGetErrorString(e), int(e));
+}
+
+// ---- pinned host allocations -------------------------------------------------
+struct HostAlloc {
+  size_t bytes;   // mapped length (THP allocations are rounded up to 2 MiB)
+  bool thp;
+};
+std::mutex g_alloc_mu;
+std::unordered_map<void *, HostAlloc> g_allocs;
+
+// ---- shape checks ------------------------------------------------------------
+struct Shape {
+  int64_t L, B, P, R, es, Hp;
+  int64_t row_bytes, V, PV, LPV;
+  int32_t layout;
+};
+
+int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
+  if (!d) return set_error(HICACHE_ERR_INVALID_ARG, "pool descriptor is NULL");
+  if (d->num_layers < 1 || d->num_buffers < 1 || d->page_size < 1 || d->elem_bytes < 1 ||
+      d->row_elems < 1 || d->host_num_pages < 1)
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "pool descriptor sizes must be >= 1 (layers %d, buffers %d, page_size %d, "
+                     "elem_bytes %d, row_elems %lld, host pages %lld)",
+                     d->num_layers, d->num_buffers, d->page_size, d->elem_bytes,
+                     (long long)d->row_elems, (long long)d->host_num_pages);
+  if (int64_t(d->num_layers) * d->num_buffers > hicache::kMaxBufs)
+    return set_error(HICACHE_ERR_INVALID_ARG, "num_buffers * num_layers = %lld exceeds %d",
+                     (long long)d->num_layers * d->num_buffers, hicache::kMaxBufs);
+  if (d->layout < HICACHE_LAYER_FIRST || d->layout > HICACHE_PAGE_FIRST_DIRECT)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown pool layout %d", d->layout);
+  if (d->launch_ctas < 0 || d->flags != 0 || d->reserved != 0)
+    return set_error(HICACHE_ERR_INVALID_ARG, "launch_ctas must be >= 0; flags and reserved must be 0");
+  if (d->host_num_pages >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "host_num_pages must be < 2^31");
+  s->L = d->num_layers;
+  s->B = d->num_buffers;
+  s->P = d->page_size;
+  s->R = d->row_elems;
+  s->es = d->elem_bytes;
+  s->Hp = d->host_num_pages;
+  s->layout = d->layout;
+  if (s->R > (int64_t(1) << 40) / s->es)
+    return set_error(HICACHE_ERR_INVALID_ARG, "row of %lld elements is too large", (long long)s->R);
+  s->row_bytes = s->R * s->es;
+  s->V = s->row_bytes / 16;
+  s->PV = s->P * s->V;
+  s->LPV = s->L * s->PV;
+  if (need_alignment) {
+    if (s->row_bytes % 16 != 0)
+      return set_error(HICACHE_ERR_ALIGNMENT, "row of %lld bytes is not a multiple of 16",
+                       (long long)s->row_bytes);
+    if (s->LPV >= INT32_MAX)
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "one page of every layer (%lld x 16 bytes) must be < 32 GiB",
+                       (long long)s->LPV);
+  }
+  return HICACHE_OK;
+}
+
+int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out) {
+  if (layout == HICACHE_LAYOUT_POOL) layout = pool_layout;
+  if (layout < HICACHE_LAYER_FIRST || layout > HICACHE_PAGE_FIRST_DIRECT)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown layout %d", layout);
+  *out = layout;
+  return HICACHE_OK;
+}
+
+// ---- the pre-pass ------------------------------------------------------------
+struct Pair {
+  int64_t h, d;
+};
+inline bool pair_less(const Pair &a, const Pair &b) {
+  return a.h < b.h || (a.h == b.h && a.d < b.d);
+}
+
+// Validate n index pairs and reduce them to runs: pairs sorted by (host page,
+// device page), merged while both pages step by one (at most max_run pages per
+// run).  On error nothing is changed but the last-error text.
+int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+            int32_t direction, int64_t max_run, std::vector<RunRec> *runs) {
+  if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n = %lld is negative", (long long)n);
+  if (direction != HICACHE_DIR_BACKUP && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown direction %d", direction);
+  if (Dp < 1 || Dp >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "device_num_pages = %lld must be in [1, 2^31)",
+                     (long long)Dp);
+  runs->clear();
+  if (n == 0) return HICACHE_OK;
+  if (!dev || !host) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
+  thread_local std::vector<Pair> pairs;
+  pairs.resize(size_t(n));
+  bool sorted = true;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t d = dev[i], h = host[i];
+    if (d < 0 || d >= Dp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] = %lld outside [0, %lld)",
+                       (long long)i, (long long)d, (long long)Dp);
+    if (h < 0 || h >= Hp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "host_pages[%lld] = %lld outside [0, %lld)",
+                       (long long)i, (long long)h, (long long)Hp);
+    pairs[size_t(i)] = Pair{h, d};
+    if (i > 0 && pair_less(pairs[size_t(i)], pairs[size_t(i - 1)])) sorted = false;
+  }
+  if (!sorted) std::sort(pairs.begin(), pairs.end(), pair_less);
+  if (direction == HICACHE_DIR_BACKUP) {
+    for (int64_t i = 1; i < n; ++i)
+      if (pairs[size_t(i)].h == pairs[size_t(i - 1)].h)
+        return set_error(HICACHE_ERR_DUPLICATE_INDEX,
+                         "host page %lld is a backup destination twice",
+                         (long long)pairs[size_t(i)].h);
+  } else if (n <= 32) {
+    for (int64_t i = 0; i < n; ++i)
+      for (int64_t k = i + 1; k < n; ++k)
+        if (dev[i] == dev[k])
+          return set_error(HICACHE_ERR_DUPLICATE_INDEX,
+                           "device page %lld is a load destination twice", (long long)dev[i]);
+  } else {
+    thread_local std::vector<int64_t> ds;
+    ds.assign(dev, dev + n);
+    std::sort(ds.begin(), ds.end());
+    for (int64_t i = 1; i < n; ++i)
+      if (ds[size_t(i)] == ds[size_t(i - 1)])
+        return set_error(HICACHE_ERR_DUPLICATE_INDEX,
+                         "device page %lld is a load destination twice", (long long)ds[size_t(i)]);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const Pair &p = pairs[size_t(i)];
+    if (!runs->empty()) {
+      RunRec &r = runs->back();
+      if (p.h == r.h0 + r.len && p.d == r.d0 + r.len && r.len < max_run) {
+        ++r.len;
+        continue;
+      }
+    }
+    runs->push_back(RunRec{p.h, p.d, 1});
+  }
+  return HICACHE_OK;
+}
+
+constexpr int64_t kMaxTiles = int64_t(1) << 30;
+
+int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX - 1) / s.LPV); }
+
+}  // namespace
+
+// ---- pool and plan objects -----------------------------------------------------
+struct hicache_pool {
+  hicache_pool_desc desc;
+  Shape shape;
+  void *host = nullptr;       // host pointer of the pool
+  void *host_dev = nullptr;   // device-visible alias
+  size_t host_bytes = 0;
+  int device = 0;
+  int ctas = 0;
+  std::vector<cudaEvent_t> events;  // one per layer
+};
+
+struct hicache_plan {
+  hicache_pool *pool = nullptr;
+  int32_t direction = 0;
+  int64_t n = 0;
+  int64_t device_num_pages = 0;
+  std::vector<RunRec> runs;
+};
+
+namespace {
+
+int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_pages) {
+  if (!kv || !kv->buf_ptrs) return set_error(HICACHE_ERR_INVALID_ARG, "device KV is NULL");
+  if (kv->device_num_pages < 1 || kv->device_num_pages >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "device_num_pages = %lld must be in [1, 2^31)",
+                     (long long)kv->device_num_pages);
+  if (kv->device_num_pages < min_pages)
+    return set_error(HICACHE_ERR_INVALID_ARG, "device_num_pages = %lld is below the plan's %lld",
+                     (long long)kv->device_num_pages, (long long)min_pages);
+  const int64_t nb = pool->shape.B * pool->shape.L;
+  for (int64_t i = 0; i < nb; ++i) {
+    const void *p = kv->buf_ptrs[i];
+    if (!p) return set_error(HICACHE_ERR_INVALID_ARG, "device buffer %lld is NULL", (long long)i);
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+      return set_error(HICACHE_ERR_ALIGNMENT, "device buffer %lld is not 16-byte aligned",
+                       (long long)i);
+  }
+  return HICACHE_OK;
+}
+
+// Enqueue the transfer of `runs` (already validated).  layer < 0: all layers.
+int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
+            int32_t layout, int32_t layer, bool to_host, void *stream) {
+  if (runs.empty()) return HICACHE_OK;
+  const Shape &s = pool->shape;
+  const bool all = layer < 0;
+  const int32_t nb = int32_t(s.B * s.L);
+  const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
+  const int64_t outers = lf_all ? s.B * s.L : s.B;
+  const int64_t upp = (all && layout != HICACHE_LAYER_FIRST) ? s.LPV : s.PV;
+  const int64_t max_runs = (hicache::kBlobWords - nb) / 2;
+
+  thread_local hicache::XferParams params;
+  hicache::XferHeader &h = params.h;
+  h.host = pool->host_dev;
+  h.L = int32_t(s.L);
+  h.P = int32_t(s.P);
+  h.V = int32_t(s.V);
+  h.num_bufs = nb;
+  h.layer = all ? 0 : layer;
+  h.Hp = int32_t(s.Hp);
+  h.unit_per_page = uint32_t(upp);
+  h.PV = uint32_t(s.PV);
+  h.LV = uint32_t(s.L * s.V);
+  h.LPV = uint32_t(s.LPV);
+  h.fd_V = hicache::make_fastdiv(uint32_t(s.V));
+  h.fd_PV = hicache::make_fastdiv(uint32_t(s.PV));
+  h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
+  h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
+  for (int32_t i = 0; i < nb; ++i)
+    params.blob[i] = uint64_t(reinterpret_cast<uintptr_t>(kv->buf_ptrs[i]));
+  hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[nb]);
+
+  size_t next = 0;
+  while (next < runs.size()) {
+    // greedy chunk: at most max_runs runs and kMaxTiles tiles per launch (the
+    // kernel's 32-bit grid-stride index then never overflows)
+    int64_t tiles = 0;
+    int32_t count = 0;
+    while (next + size_t(count) < runs.size() && count < max_runs) {
+      const RunRec &r = runs[next + size_t(count)];
+      const int64_t t = (r.len * upp + hicache::kTileVecs - 1) / hicache::kTileVecs;
+      if (count > 0 && (tiles + t) * outers > kMaxTiles) break;
+      table[count] = hicache::Run{int32_t(r.h0), int32_t(r.d0), int32_t(r.len), int32_t(tiles)};
+      tiles += t;
+      ++count;
+    }
+    if (tiles * outers > kMaxTiles)
+      return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+    h.n_runs = count;
+    h.tiles_per_outer = int32_t(tiles);
+    h.total_tiles = int32_t(tiles * outers);
+    hicache::XferLaunch x;
+    x.params = &params;
+    x.layout = layout;
+    x.all_layers = all;
+    x.to_host = to_host;
+    x.grid = int(std::min<int64_t>(h.total_tiles, pool->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_xfer(x);
+    if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    next += size_t(count);
+  }
+  return HICACHE_OK;
+}
+
+int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev,
+             const int64_t *host, int64_t n, int32_t layout, int32_t layer, int32_t direction,
+             void *stream) {
+  g_last_error.clear();
+  if (!pool) return set_error(HICACHE_ERR_INVALID_ARG, "pool is NULL");
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if (layer >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer,
+                     (long long)pool->shape.L);
+  if ((rc = check_kv(pool, kv, 0))) return rc;
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction,
+                    max_run_pages(pool->shape), &runs)))
+    return rc;
+  if ((rc = enqueue(pool, kv, runs, lay, layer, direction == HICACHE_DIR_BACKUP, stream))) return rc;
+  if (layer >= 0) {
+    const cudaError_t e = cudaEventRecord(pool->events[size_t(layer)], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+  }
+  return HICACHE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hicache_version(void) { return 100; }
+
+const char *hicache_last_error(void) { return g_last_error.c_str(); }
+
+int64_t hicache_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int hicache_host_alloc(size_t bytes, int32_t flags, void **out) {
+  g_last_error.clear();
+  if (!out || bytes == 0) return set_error(HICACHE_ERR_INVALID_ARG, "bytes must be > 0 and out non-NULL");
+  if (flags & ~int32_t(HICACHE_HOST_THP)) return set_error(HICACHE_ERR_INVALID_ARG, "unknown flags");
+  *out = nullptr;
+  void *p = nullptr;
+  size_t mapped = bytes;
+  const bool thp = (flags & HICACHE_HOST_THP) != 0;
+  if (thp) {
+    const size_t huge = size_t(2) << 20;
+    mapped = (bytes + huge - 1) / huge * huge;
+    p = mmap(nullptr, mapped, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (p == MAP_FAILED) return set_error(HICACHE_ERR_NOMEM, "mmap of %zu bytes failed", mapped);
+    // huge pages must be requested before the pages are locked
+    (void)madvise(p, mapped, MADV_HUGEPAGE);
+    const cudaError_t e =
+        cudaHostRegister(p, mapped, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+      munmap(p, mapped);
+      return cuda_error(e, "cudaHostRegister");
+    }
+  } else {
+    const cudaError_t e = cudaHostAlloc(&p, bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_error(e, "cudaHostAlloc");
+  }
+  {
+    std::lock_guard<std::mutex> g(g_alloc_mu);
+    g_allocs[p] = HostAlloc{mapped, thp};
+  }
+  *out = p;
+  return HICACHE_OK;
+}
+
+int hicache_host_free(void *ptr) {
+  g_last_error.clear();
+  if (!ptr) return HICACHE_OK;
+  HostAlloc a;
+  {
+    std::lock_guard<std::mutex> g(g_alloc_mu);
+    auto it = g_allocs.find(ptr);
+    if (it == g_allocs.end())
+      return set_error(HICACHE_ERR_INVALID_ARG, "pointer was not allocated by hicache_host_alloc");
+    a = it->second;
+    g_allocs.erase(it);
+  }
+  if (a.thp) {
+    const cudaError_t e = cudaHostUnregister(ptr);
+    munmap(ptr, a.bytes);
+    if (e != cudaSuccess) return cuda_error(e, "cudaHostUnregister");
+  } else {
+    const cudaError_t e = cudaFreeHost(ptr);
+    if (e != cudaSuccess) return cuda_error(e, "cudaFreeHost");
+  }
+  return HICACHE_OK;
+}
+
+int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t host_bytes,
+                        hicache_pool **out) {
+  g_last_error.clear();
+  if (!out) return set_error(HICACHE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Shape s{};
+  int rc = check_desc(desc, &s, true);
+  if (rc) return rc;
+  if (!host_pool) return set_error(HICACHE_ERR_INVALID_ARG, "host pool pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(host_pool) % 16 != 0)
+    return set_error(HICACHE_ERR_ALIGNMENT, "host pool is not 16-byte aligned");
+  const int64_t need = s.B * s.Hp * s.LPV * 16;
+  if (int64_t(host_bytes) < need)
+    return set_error(HICACHE_ERR_INVALID_ARG, "host pool of %zu bytes is below the %lld needed",
+                     host_bytes, (long long)need);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  cudaPointerAttributes attr;
+  e = cudaPointerGetAttributes(&attr, host_pool);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return set_error(HICACHE_ERR_NOT_PINNED, "host pool is not CUDA host memory: %s",
+                     cudaGetErrorString(e));
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+    return set_error(HICACHE_ERR_NOT_PINNED, "host pool is not page-locked, device-mapped memory");
+  // the whole range must be one pinned allocation: check its last byte as well
+  cudaPointerAttributes attr_end;
+  e = cudaPointerGetAttributes(&attr_end, static_cast<char *>(host_pool) + need - 1);
+  if (e != cudaSuccess || attr_end.type != cudaMemoryTypeHost) {
+    (void)cudaGetLastError();
+    return set_error(HICACHE_ERR_NOT_PINNED, "host pool is not pinned up to its last byte");
+  }
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute");
+
+  hicache_pool *p = new (std::nothrow) hicache_pool();
+  if (!p) return set_error(HICACHE_ERR_NOMEM, "out of host memory");
+  p->desc = *desc;
+  p->shape = s;
+  p->host = host_pool;
+  p->host_dev = attr.devicePointer;
+  p->host_bytes = host_bytes;
+  p->device = dev;
+  p->ctas = desc->launch_ctas > 0 ? desc->launch_ctas : sms * hicache::kDefaultCtasPerSm;
+  p->events.resize(size_t(s.L), nullptr);
+  for (auto &ev : p->events) {
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      hicache_pool_destroy(p);
+      return cuda_error(e, "cudaEventCreateWithFlags");
+    }
+  }
+  *out = p;
+  return HICACHE_OK;
+}
+
+int hicache_pool_destroy(hicache_pool *pool) {
+  if (!pool) return HICACHE_OK;
+  for (auto ev : pool->events)
+    if (ev) cudaEventDestroy(ev);
+  delete pool;
+  return HICACHE_OK;
+}
+
+int hicache_backup(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
+                   const int64_t *host_pages, int64_t n, int32_t layout, void *stream) {
+  return transfer(pool, kv, device_pages, host_pages, n, layout, -1, HICACHE_DIR_BACKUP, stream);
+}
+
+int hicache_load(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
+                 const int64_t *host_pages, int64_t n, int32_t layout, void *stream) {
+  return transfer(pool, kv, device_pages, host_pages, n, layout, -1, HICACHE_DIR_LOAD, stream);
+}
+
+int hicache_load_layer(hicache_pool *pool, const hicache_device_kv *kv,
+                       const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                       int32_t layout, int32_t layer_id, void *stream) {
+  if (layer_id < 0) {
+    g_last_error.clear();
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d is negative", layer_id);
+  }
+  return transfer(pool, kv, device_pages, host_pages, n, layout, layer_id, HICACHE_DIR_LOAD, stream);
+}
+
+int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,
+                        int64_t n, int64_t device_num_pages, int32_t direction,
+                        hicache_plan **out) {
+  g_last_error.clear();
+  if (!pool || !out) return set_error(HICACHE_ERR_INVALID_ARG, "pool or out is NULL");
+  *out = nullptr;
+  std::vector<RunRec> runs;
+  int rc = prepass(pool->shape.Hp, device_num_pages, device_pages, host_pages, n, direction,
+                   max_run_pages(pool->shape), &runs);
+  if (rc) return rc;
+  hicache_plan *p = new (std::nothrow) hicache_plan();
+  if (!p) return set_error(HICACHE_ERR_NOMEM, "out of host memory");
+  p->pool = pool;
+  p->direction = direction;
+  p->n = n;
+  p->device_num_pages = device_num_pages;
+  p->runs = std::move(runs);
+  *out = p;
+  return HICACHE_OK;
+}
+
+int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                         int32_t layer_id, void *stream) {
+  g_last_error.clear();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  hicache_pool *pool = plan->pool;
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if (layer_id >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)pool->shape.L);
+  if (layer_id >= 0 && plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
+  if ((rc = enqueue(pool, kv, plan->runs, lay, layer_id < 0 ? -1 : layer_id,
+                    plan->direction == HICACHE_DIR_BACKUP, stream)))
+    return rc;
+  if (layer_id >= 0) {
+    const cudaError_t e =
+        cudaEventRecord(pool->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+  }
+  return HICACHE_OK;
+}
+
+int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs) {
+  g_last_error.clear();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (num_pages) *num_pages = plan->n;
+  if (num_runs) *num_runs = int64_t(plan->runs.size());
+  return HICACHE_OK;
+}
+
+int hicache_plan_destroy(hicache_plan *plan) {
+  delete plan;
+  return HICACHE_OK;
+}
+
+int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out) {
+  g_last_error.clear();
+  if (!pool || !event_out) return set_error(HICACHE_ERR_INVALID_ARG, "pool or event_out is NULL");
+  if (layer < 0 || layer >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
+                     (long long)pool->shape.L);
+  *event_out = pool->events[size_t(layer)];
+  return HICACHE_OK;
+}
+
+int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream) {
+  g_last_error.clear();
+  if (!pool) return set_error(HICACHE_ERR_INVALID_ARG, "pool is NULL");
+  if (layer < 0 || layer >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
+                     (long long)pool->shape.L);
+  const cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream),
+                                            pool->events[size_t(layer)], 0);
+  if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent");
+  return HICACHE_OK;
+}
+
+int hicache_wait(void *stream, int64_t timeout_us) {
+  g_last_error.clear();
+  const auto start = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) return HICACHE_OK;
+    if (e != cudaErrorNotReady) return cuda_error(e, "cudaStreamQuery");
+    const int64_t waited = std::chrono::duration_cast<std::chrono::microseconds>(
+                               std::chrono::steady_clock::now() - start)
+                               .count();
+    if (timeout_us >= 0 && waited >= timeout_us)
+      return set_error(HICACHE_ERR_TIMEOUT, "stream still busy after %lld us", (long long)waited);
+    int64_t nap = 50;
+    if (timeout_us >= 0) nap = std::min<int64_t>(nap, std::max<int64_t>(1, timeout_us - waited));
+    std::this_thread::sleep_for(std::chrono::microseconds(nap));
+  }
+}
+
+int hicache_prepass(int64_t host_num_pages, int64_t device_num_pages, const int64_t *device_pages,
+                    const int64_t *host_pages, int64_t n, int32_t direction, int64_t *num_runs,
+                    int64_t *runs_out, int64_t runs_capacity) {
+  g_last_error.clear();
+  if (!num_runs) return set_error(HICACHE_ERR_INVALID_ARG, "num_runs is NULL");
+  if (host_num_pages < 1 || host_num_pages >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "host_num_pages must be in [1, 2^31)");
+  std::vector<RunRec> runs;
+  const int rc = prepass(host_num_pages, device_num_pages, device_pages, host_pages, n, direction,
+                         INT32_MAX, &runs);
+  if (rc) return rc;
+  *num_runs = int64_t(runs.size());
+  if (runs_out && runs_capacity >= int64_t(runs.size())) {
+    for (size_t i = 0; i < runs.size(); ++i) {
+      runs_out[3 * i] = runs[i].h0;
+      runs_out[3 * i + 1] = runs[i].d0;
+      runs_out[3 * i + 2] = runs[i].len;
+    }
+  }
+  return HICACHE_OK;
+}
+
+int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *device_pages,
+                              const int64_t *host_pages, int64_t n, int32_t layout,
+                              int32_t layer_id) {
+  g_last_error.clear();
+  Shape s{};
+  int rc = check_desc(desc, &s, false);
+  if (rc) return rc;
+  int32_t lay = 0;
+  if ((rc = resolve_layout(layout, s.layout, &lay))) return rc;
+  if (layer_id >= s.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)s.L);
+  if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n is negative");
+  if (n == 0) return 0;
+  if (!device_pages || !host_pages) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
+  // runs over the set of pairs; repeated sources are fine for a count
+  std::vector<Pair> pairs(static_cast<size_t>(n));
+  for (int64_t i = 0; i < n; ++i) {
+    if (device_pages[i] < 0 || host_pages[i] < 0 || host_pages[i] >= s.Hp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "page index out of range at %lld", (long long)i);
+    pairs[size_t(i)] = Pair{host_pages[i], device_pages[i]};
+  }
+  std::sort(pairs.begin(), pairs.end(), pair_less);
+  int64_t nruns = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const bool cont = i > 0 && pairs[size_t(i)].h == pairs[size_t(i - 1)].h + 1 &&
+                      pairs[size_t(i)].d == pairs[size_t(i - 1)].d + 1;
+    if (!cont) ++nruns;
+  }
+  const int64_t layers = layer_id < 0 ? s.L : 1;
+  // with one layer in the pool, every layout stores a buffer's pages back to back
+  if (lay == HICACHE_LAYER_FIRST || s.L == 1) return s.B * layers * nruns;
+  // one segment per (buffer, layer, page): the same layer of the next page is
+  // L*P rows further on the host
+  if (lay == HICACHE_PAGE_FIRST_DIRECT) return s.B * layers * n;
+  return s.B * layers * n * s.P;  // page_first: one row per (buffer, layer, token)
+}
+
+int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc *desc,
+                           const int64_t *device_pages, int64_t n, int32_t layer_id,
+                           int32_t reps, uint64_t *out_sum_dev, void *stream) {
+  g_last_error.clear();
+  Shape s{};
+  int rc = check_desc(desc, &s, true);
+  if (rc) return rc;
+  if (!kv || !kv->buf_ptrs || !out_sum_dev)
+    return set_error(HICACHE_ERR_INVALID_ARG, "kv or out_sum_dev is NULL");
+  if (layer_id < 0 || layer_id >= s.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)s.L);
+  if (s.B > 8) return set_error(HICACHE_ERR_INVALID_ARG, "at most 8 buffers");
+  if (reps < 1 || n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "reps must be >= 1, n >= 0");
+  if (n > 0 && !device_pages) return set_error(HICACHE_ERR_INVALID_ARG, "device_pages is NULL");
+  if (int64_t(n) * s.PV >= INT32_MAX) return set_error(HICACHE_ERR_INVALID_ARG, "too many pages");
+  for (int64_t i = 0; i < n; ++i)
+    if (device_pages[i] < 0 || device_pages[i] >= kv->device_num_pages)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] out of range", (long long)i);
+  thread_local hicache::ChecksumParams p;
+  for (int64_t b = 0; b < s.B; ++b) {
+    p.bufs[b] = kv->buf_ptrs[b * s.L + layer_id];
+    if (!p.bufs[b] || reinterpret_cast<uintptr_t>(p.bufs[b]) % 16)
+      return set_error(HICACHE_ERR_ALIGNMENT, "buffer NULL or not 16-byte aligned");
+  }
+  p.B = int32_t(s.B);
+  p.reps = reps;
+  p.PV = uint32_t(s.PV);
+  p.out = reinterpret_cast<unsigned long long *>(out_sum_dev);
+  for (int64_t first = 0; first < n; first += hicache::kChecksumMaxPages) {
+    const int64_t cnt = std::min<int64_t>(hicache::kChecksumMaxPages, n - first);
+    p.n = int32_t(cnt);
+    for (int64_t i = 0; i < cnt; ++i) p.pages[i] = int32_t(device_pages[first + i]);
+    const int64_t vecs = cnt * s.PV * s.B;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(1024, (vecs + hicache::kThreads - 1) / hicache::kThreads)));
+    const int e = hicache::launch_checksum(p, grid, stream);
+    if (e != 0) return cuda_error(cudaError_t(e), "checksum kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  return HICACHE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// hicache_internal.h -- types shared by the host API (hicache_api.cpp) and the
+// transfer kernels (hicache_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define HC_HD __host__ __device__ __forceinline__
+#else
+#define HC_HD inline
+#endif
+
+namespace hicache {
+
+// ---- launch geometry ------------------------------------------------------
+constexpr int kThreads = 256;                    // threads per CTA
+constexpr int kUnroll = 4;                       // 16-byte vectors in flight per thread
+constexpr int kTileVecs = kThreads * kUnroll;    // vectors per tile: 16 KiB
+constexpr int kMaxBufs = 512;                    // B * L device buffers per call
+constexpr int kBlobWords = 3584;                 // 28 KiB of kernel parameters: buffer
+                                                 // pointers, then the run table
+constexpr int kDefaultCtasPerSm = 2;
+
+// ---- division by a run-time constant ---------------------------------------
+// q = floor(n / d) for 0 <= n < 2^31 by one multiply-high, an add and a shift:
+// the round-up method of Granlund & Montgomery, "Division by invariant integers
+// using multiplication" (PLDI 1994): with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, floor(n / d) = (mulhi(m, n) + n) >> s.
+// (mulhi(m, n) <= n, so the sum fits 32 bits while n < 2^31.)
+struct FastDiv {
+  uint32_t d;
+  uint32_t m;
+  uint32_t s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{d, 1u, 0u};
+  uint32_t s = 0;
+  while ((uint64_t(1) << s) < d) ++s;
+  f.s = s;
+  f.m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1);
+  return f;
+}
+
+HC_HD uint32_t fast_div(uint32_t n, const FastDiv &f) {
+#if defined(__CUDA_ARCH__)
+  const uint32_t hi = __umulhi(n, f.m);
+#else
+  const uint32_t hi = uint32_t((uint64_t(n) * f.m) >> 32);
+#endif
+  return (hi + n) >> f.s;
+}
+
+// ---- run table -------------------------------------------------------------
+// A run: `len` pages whose host pages h0.. and device pages d0.. both step by
+// one.  tile0 = tiles of the runs before it within one "outer" unit.
+struct Run {
+  int32_t h0;
+  int32_t d0;
+  int32_t len;
+  int32_t tile0;
+};
+
+// Host-side run record (before tiling).
+struct RunRec {
+  int64_t h0;
+  int64_t d0;
+  int64_t len;
+};
+
+enum Layout : int32_t { kLayerFirst = 0, kPageFirst = 1, kPageFirstDirect = 2 };
+
+// Everything a transfer launch needs, in vectors of 16 bytes.
+struct XferHeader {
+  void *host;                 // device-visible alias of the host pool
+  int32_t L, P, V, num_bufs;  // layers, page size, vectors per row, B*L
+  int32_t layer;              // the layer of a single-layer transfer
+  int32_t Hp;                 // host pool pages
+  int32_t n_runs;
+  int32_t tiles_per_outer;    // tiles of one outer unit (a buffer, or a buffer-layer)
+  int32_t total_tiles;
+  uint32_t unit_per_page;     // vectors one page contributes to a unit
+  uint32_t PV, LV, LPV;       // P*V, L*V, L*P*V
+  FastDiv fd_V, fd_PV, fd_LV, fd_LPV;
+};
+
+struct XferParams {
+  XferHeader h;
+  // blob[0 .. num_bufs): device buffer pointers (buffer-major b*L + l);
+  // then n_runs Run records (two words each).
+  uint64_t blob[kBlobWords];
+};
+static_assert(sizeof(XferParams) <= 32764, "kernel parameter limit");
+
+// Stand-in compute: pages are passed in the parameters.
+constexpr int kChecksumMaxPages = 6144;
+struct ChecksumParams {
+  void *bufs[8];              // the B buffers of one layer
+  int32_t B, n, reps, pad;
+  uint32_t PV;                // vectors per page of one buffer
+  unsigned long long *out;
+  int32_t pages[kChecksumMaxPages];
+};
+static_assert(sizeof(ChecksumParams) <= 32764, "kernel parameter limit");
+
+// Launch entry points (hicache_kernels.cu).  Return a cudaError_t value.
+struct XferLaunch {
+  XferParams *params;         // filled header + blob; the launcher completes it
+  int layout;
+  bool all_layers;
+  bool to_host;
+  int grid;
+  void *stream;
+};
+int launch_xfer(const XferLaunch &x);
+int launch_checksum(const ChecksumParams &p, int grid, void *stream);
+
+}  // namespace hicache

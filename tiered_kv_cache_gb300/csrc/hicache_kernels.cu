@@ -1,0 +1,194 @@
+// hicache_kernels.cu -- sm_103a transfer kernels for the L1 <-> L2 KV movement.
+//
+// One kernel body serves backup (device -> host) and load (host -> device) for
+// the three host layouts, for every layer at once or for one layer:
+//
+//   * The pre-pass (host side) sorts the index pairs by host page and merges
+//     pages that are consecutive on BOTH sides into runs.  The run table and
+//     the B*L device-buffer pointers travel in the kernel parameters, so a
+//     call of up to 1536 runs is exactly one launch and no descriptor or
+//     per-segment submission ever reaches the GPU.  (The pages trace the
+//     cost of page_first_direct to one DMA descriptor per page x layer
+//     segment: "Tuning SGLang HiCache L2 on Kunlunxin P800/P900", sections
+//     2.1 and 2.3; "Baidu's KVCache Overhaul", section "DMA Segment Explosion
+//     & Batched Gather/Scatter".  Here every segment boundary is just address
+//     arithmetic inside a warp.)
+//   * The work is cut into "units" that are contiguous on the HOST side:
+//       layer_first, any layer count      unit = (buffer, layer, run)
+//       page_first(_direct), all layers   unit = (buffer, run): all layers of
+//                                         the run's pages are one host range
+//       page_first(_direct), one layer    unit = (buffer, run), host strided
+//     and every unit into tiles of 16 KiB (1024 vectors of 16 bytes).  CTAs
+//     take tiles in host-address order (grid-stride), so the host link sees
+//     long sequential streams of whole 128-byte lines in every layout.
+//   * Each thread of a tile moves 4 independent 16-byte vectors: 4 loads in
+//     flight before the first store.  The device-side address of every vector
+//     is decoded on the fly (a multiply-high division per dimension), which
+//     performs the layout transpose without a shared-memory pass: rows are
+//     >= 16 bytes, so each warp's device accesses stay whole 32-byte sectors,
+//     and the host side is touched strictly in order.
+//
+// No tensor cores: nothing here is a contraction.  No TMA multicast, no
+// cross-CTA waits, no spin loops: a kernel always runs to completion.
+
+#include <cuda_runtime.h>
+
+#include "hicache_internal.h"
+
+namespace hicache {
+namespace {
+
+// Streaming (evict-first) 16-byte accesses: every byte is touched once.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// Address of vector w of the current unit.  `dev` and `host` receive vector
+// pointers; b, l, run describe the unit (l is ignored where the unit spans all
+// layers).
+template <int LAYOUT, bool ALL>
+__device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bufs, int b, int l,
+                                           const Run &r, uint32_t w, uint4 *&dev, uint4 *&host) {
+  uint4 *const hbase = static_cast<uint4 *>(h.host);
+  if (LAYOUT == kLayerFirst) {
+    // host (B, L, size, R): unit (b, l, run) is contiguous on both sides
+    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
+    host = hbase + (int64_t(b * h.L + l) * h.Hp + r.h0) * h.PV + w;
+  } else if (LAYOUT == kPageFirstDirect && ALL) {
+    // host (B, Hp, L, P, R): the unit is [page j][layer ll][token, elem]
+    const uint32_t j = fast_div(w, h.fd_LPV);
+    const uint32_t rem = w - j * h.LPV;
+    const uint32_t ll = fast_div(rem, h.fd_PV);
+    const uint32_t q = rem - ll * h.PV;
+    dev = bufs[b * h.L + ll] + int64_t(r.d0 + int32_t(j)) * h.PV + q;
+    host = hbase + (int64_t(b) * h.Hp + r.h0) * h.LPV + w;
+  } else if (LAYOUT == kPageFirst && ALL) {
+    // host (B, size, L, R): the unit is [token][layer ll][elem]
+    const uint32_t tok = fast_div(w, h.fd_LV);
+    const uint32_t rem = w - tok * h.LV;
+    const uint32_t ll = fast_div(rem, h.fd_V);
+    const uint32_t v = rem - ll * h.V;
+    dev = bufs[b * h.L + ll] + (int64_t(r.d0) * h.P + tok) * h.V + v;
+    host = hbase + (int64_t(b) * h.Hp + r.h0) * h.P * h.LV + w;
+  } else if (LAYOUT == kPageFirstDirect) {
+    // one layer: device contiguous over the run, host one P*R block per page
+    const uint32_t j = fast_div(w, h.fd_PV);
+    const uint32_t q = w - j * h.PV;
+    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
+    host = hbase + ((int64_t(b) * h.Hp + r.h0 + j) * h.L + l) * h.PV + q;
+  } else {
+    // page_first, one layer: device contiguous over the run, host one row per token
+    const uint32_t tok = fast_div(w, h.fd_V);
+    const uint32_t v = w - tok * h.V;
+    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
+    host = hbase + (((int64_t(b) * h.Hp + r.h0) * h.P + tok) * h.L + l) * h.V + v;
+  }
+}
+
+template <int LAYOUT, bool ALL, bool TO_HOST>
+__global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ XferParams p) {
+  __shared__ uint4 *s_bufs[kMaxBufs];
+  const XferHeader &h = p.h;
+  for (int i = threadIdx.x; i < h.num_bufs; i += kThreads)
+    s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
+  __syncthreads();
+  const Run *runs = reinterpret_cast<const Run *>(&p.blob[h.num_bufs]);
+  const bool lf_all = (LAYOUT == kLayerFirst) && ALL;
+
+  for (int32_t g = blockIdx.x; g < h.total_tiles; g += gridDim.x) {
+    const int32_t outer = g / h.tiles_per_outer;
+    const int32_t inner = g - outer * h.tiles_per_outer;
+    int b, l;
+    if (lf_all) {
+      b = outer / h.L;
+      l = outer - b * h.L;
+    } else {
+      b = outer;
+      l = h.layer;
+    }
+    // the run holding tile `inner`: last run with tile0 <= inner
+    int lo = 0, hi = h.n_runs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (runs[mid].tile0 <= inner) lo = mid; else hi = mid - 1;
+    }
+    const Run r = runs[lo];
+    const uint32_t w0 = uint32_t(inner - r.tile0) * kTileVecs + threadIdx.x;
+    const uint32_t unit = uint32_t(r.len) * h.unit_per_page;
+
+    uint4 v[kUnroll];
+    uint4 *dst[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const uint32_t w = w0 + k * kThreads;
+      dst[k] = nullptr;
+      if (w < unit) {
+        uint4 *dev, *host;
+        map_vector<LAYOUT, ALL>(h, s_bufs, b, l, r, w, dev, host);
+        if (TO_HOST) {
+          v[k] = ld_stream(dev);
+          dst[k] = host;
+        } else {
+          v[k] = ld_stream(host);
+          dst[k] = dev;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k)
+      if (dst[k] != nullptr) st_stream(dst[k], v[k]);
+  }
+}
+
+// Stand-in for attention on one layer: read every vector of the given pages of
+// the layer's buffers `reps` times and add up their 32-bit words.
+__global__ void __launch_bounds__(kThreads) checksum_kernel(const __grid_constant__ ChecksumParams p) {
+  const uint32_t per_buf = uint32_t(p.n) * p.PV;
+  const uint64_t total = uint64_t(per_buf) * p.B;
+  unsigned long long acc = 0;
+  for (int rep = 0; rep < p.reps; ++rep) {
+    for (uint64_t i = uint64_t(blockIdx.x) * kThreads + threadIdx.x; i < total;
+         i += uint64_t(gridDim.x) * kThreads) {
+      const uint32_t b = uint32_t(i / per_buf);
+      const uint32_t w = uint32_t(i - uint64_t(b) * per_buf);
+      const uint32_t j = w / p.PV;
+      const uint32_t q = w - j * p.PV;
+      const uint4 x = __ldcg(static_cast<const uint4 *>(p.bufs[b]) + int64_t(p.pages[j]) * p.PV + q);
+      acc += (unsigned long long)x.x + x.y + x.z + x.w;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, off);
+  if ((threadIdx.x & 31) == 0 && acc != 0) atomicAdd(p.out, acc);
+}
+
+template <int LAYOUT, bool ALL, bool TO_HOST>
+cudaError_t launch_one(const XferLaunch &x) {
+  xfer_kernel<LAYOUT, ALL, TO_HOST>
+      <<<x.grid, kThreads, 0, static_cast<cudaStream_t>(x.stream)>>>(*x.params);
+  return cudaGetLastError();
+}
+
+template <int LAYOUT>
+cudaError_t launch_layout(const XferLaunch &x) {
+  if (x.all_layers)
+    return x.to_host ? launch_one<LAYOUT, true, true>(x) : launch_one<LAYOUT, true, false>(x);
+  return x.to_host ? launch_one<LAYOUT, false, true>(x) : launch_one<LAYOUT, false, false>(x);
+}
+
+}  // namespace
+
+int launch_xfer(const XferLaunch &x) {
+  switch (x.layout) {
+    case kLayerFirst: return int(launch_layout<kLayerFirst>(x));
+    case kPageFirst: return int(launch_layout<kPageFirst>(x));
+    case kPageFirstDirect: return int(launch_layout<kPageFirstDirect>(x));
+    default: return int(cudaErrorInvalidValue);
+  }
+}
+
+int launch_checksum(const ChecksumParams &p, int grid, void *stream) {
+  checksum_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  return int(cudaGetLastError());
+}
+
+}  // namespace hicache
