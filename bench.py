@@ -44,6 +44,10 @@ NOMINAL = {"pcie_gen5_x16_per_dir_gbs": 63.0, "nvlink_c2c_per_dir_gbs": 450.0}
 GB = 1e9
 
 
+def frac(a, b, nd=3):
+    return round(a / b, nd) if b else None
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -121,23 +125,29 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
-def build_workload(device):
+def build_workload(device, pages=512, launch_ctas=0):
+    """The Llama-3-8B-shaped pools (1024 device and 1024 host pages at 512
+    pages per transfer; 2x `pages` each for a scaled-down case)."""
+    import dataclasses
     import torch
     import tiered_kv_cache_gb300 as hc
     from tiered_kv_cache_gb300 import workloads as wl
 
     s = wl.LLAMA3_8B
+    if pages != 512:
+        s = dataclasses.replace(s, device_pages=2 * pages, host_pages=2 * pages)
     vals = [v.view(torch.int16) for v in wl.kv_values(s, device=device)]
-    t = wl.llama_transfer(s, 512)
+    t = wl.llama_transfer(s, pages)
     a_dev = t.device_pages
     rng = wl.index_rng(s.seed + 1)
-    b_dev = wl.fragmented_pages(rng, s.device_pages, 512, exclude=a_dev)
-    a_host = wl.contiguous_pages(512, 0)
-    b_host = wl.contiguous_pages(512, 512)
-    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first")
+    b_dev = wl.fragmented_pages(rng, s.device_pages, pages, exclude=a_dev)
+    a_host = wl.contiguous_pages(pages, 0)
+    b_host = wl.contiguous_pages(pages, pages)
+    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first",
+                   launch_ctas=launch_ctas)
     kv = hc.DeviceKV(vals, s.device_pages)
     return dict(shape=s, vals=vals, kv=kv, pool=pool, a_dev=a_dev, b_dev=b_dev, a_host=a_host,
-                b_host=b_host, bytes_per_xfer=512 * s.page_bytes)
+                b_host=b_host, bytes_per_xfer=pages * s.page_bytes, pages=pages)
 
 
 def link_peaks(torch, nbytes=1 << 30, reps=5):
@@ -300,6 +310,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctas", type=int, default=0, help="CTAs per transfer launch (0 = automatic)")
+    ap.add_argument("--pages", type=int, default=512,
+                    help="pages per transfer (512 = the 32K-token workload; smaller for profiling)")
+    ap.add_argument("--no-link-probe", action="store_true",
+                    help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -316,13 +330,11 @@ def main():
     hc_build.build()
     peaks, peaks_src = measured_peaks()
 
-    link = link_peaks(torch)
-    w = build_workload("cuda")
-    if args.ctas:
-        w["pool"].close()
-        s = w["shape"]
-        w["pool"] = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
-                            "layer_first", launch_ctas=args.ctas)
+    if args.no_link_probe:
+        link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
+    else:
+        link = link_peaks(torch)
+    w = build_workload("cuda", args.pages, args.ctas)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     for _ in range(max(args.warmup, 3)):
         run_step(torch, w, s1, s2)
@@ -356,6 +368,7 @@ def main():
         elapsed = float(t.item())
     bpx = w["bytes_per_xfer"]
     step_bytes = len(LAYOUT_NAMES) * 4 * bpx
+    npages = w["pages"]
     value = world * args.steps * step_bytes / elapsed / GB
 
     per = {}
@@ -368,9 +381,9 @@ def main():
         bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
         breakdown[lay] = {
             "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1), "bidir_gbs": round(bi, 1),
-            "backup_frac_of_link": round(bk / link["d2h_gbs"], 3),
-            "load_frac_of_link": round(ld / link["h2d_gbs"], 3),
-            "bidir_frac_of_link": round(bi / link["bidir_gbs"], 3),
+            "backup_frac_of_link": frac(bk, link["d2h_gbs"]),
+            "load_frac_of_link": frac(ld, link["h2d_gbs"]),
+            "bidir_frac_of_link": frac(bi, link["bidir_gbs"]),
         }
     # dominant single-direction kernel: the largest total time
     singles = {k: sum(v) for k, v in per.items() if not k.endswith("bidir")}
@@ -379,7 +392,8 @@ def main():
     achieved = bpx / dom_avg / GB
     dom_peak = link["d2h_gbs"] if dom.endswith("backup") else link["h2d_gbs"]
     roofline = {"bound": "host_link", "kernel": f"xfer_kernel ({dom})", "achieved": round(achieved, 1),
-                "peak": round(dom_peak, 1), "unit": "GB/s", "frac": round(achieved / dom_peak, 3),
+                "peak": round(dom_peak, 1) if dom_peak else None, "unit": "GB/s",
+                "frac": frac(achieved, dom_peak),
                 "traffic": None,
                 "peak_source": "in-run pinned cudaMemcpyAsync of 1 GiB, same direction (no host-link "
                                "figure in MEASURED_PEAKS.json)",
@@ -399,7 +413,7 @@ def main():
         hc.wait(s1)
     e2e_t = time.perf_counter() - t0
     e2e = {"value": round(world * e2e_steps * step_bytes / e2e_t / GB, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx + len(LAYOUT_NAMES) * 4 * 512 * 16,
+           "h2d_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx + len(LAYOUT_NAMES) * 4 * npages * 16,
            "d2h_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx,
            "how": "host wall clock around the Python API calls (validation, pre-pass, launch) and a "
                   "host wait on the stream each step; host-index bytes counted as H2D"}
@@ -409,12 +423,12 @@ def main():
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "llama3_8b_32k: 32 layers, K+V, 8 kv heads x 128, bf16, page 64, "
-                               "512 pages = 32768 tokens per transfer, fragmented device pages, "
-                               "contiguous host pages",
+        "config": {"workload": f"llama3_8b_{npages * 64 // 1024}k: 32 layers, K+V, 8 kv heads x 128, "
+                               f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
+                               "fragmented device pages, contiguous host pages",
                    "step": "per layout (layer_first, page_first, page_first_direct): backup, load, "
-                           "concurrent backup+load on two streams; 48 GiB per step",
-                   "l2": "inputs larger than L2 (4 GiB per transfer)",
+                           f"concurrent backup+load on two streams; {step_bytes / 2**30:.0f} GiB per step",
+                   "l2": f"inputs larger than L2 ({bpx / 2**20:.0f} MiB per transfer)",
                    "launch_ctas": args.ctas or "auto"},
         "roofline": roofline,
         "roofline_hbm": roofline_hbm,

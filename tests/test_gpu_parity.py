@@ -249,7 +249,7 @@ def test_layer_events_gate_compute():
         for layer in range(L):
             words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
                                     for b in range(B)])
-            assert int(got[layer]) == int(words.astype(np.uint64).sum() % (1 << 64)), layer
+            assert int(got[layer]) == int(words.astype(np.uint64).sum(dtype=np.uint64)), layer
 
 
 def test_bidirectional_streams():

@@ -32,10 +32,10 @@ def gpu():
 
 
 def position_fill(words: np.ndarray, chunk=1 << 26):
-    """Host pool words = their own index: any misplaced copy is visible."""
+    """Host pool words = their own index mod 2^32: a misplaced copy is visible."""
     for off in range(0, words.size, chunk):
         m = min(chunk, words.size - off)
-        words[off:off + m] = np.arange(off, off + m, dtype=np.uint32)
+        words[off:off + m] = np.arange(off, off + m, dtype=np.uint64).astype(np.uint32)
 
 
 def count_equal(a: np.ndarray, value, chunk=1 << 27) -> int:

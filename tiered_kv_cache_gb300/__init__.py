@@ -20,7 +20,7 @@ import numpy as np
 
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
-    "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan",
+    "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum",
     "launch_count", "version",
 ]
@@ -220,11 +220,32 @@ def layer_checksum(kv: DeviceKV, pool_or_desc, device_pages, layer: int, out_ptr
                                             dp.size, layer, reps, out_ptr, _stream(stream)))
 
 
+class PinnedHost:
+    """Pinned host memory from host_alloc, freed when the last reference (the
+    pool, or any numpy view of it) goes away."""
+
+    def __init__(self, nbytes: int, thp: bool = False):
+        self.nbytes = nbytes
+        self.ptr = host_alloc(nbytes, thp)
+
+    def free(self):
+        if self.ptr:
+            ptr, self.ptr = self.ptr, None
+            host_free(ptr)
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
 class Pool:
     """A host L2 pool of ``host_num_pages`` pages in one layout.
 
     If ``host_ptr`` is None the pool allocates its pinned memory with
-    host_alloc (``thp`` selects the huge-page path) and frees it on close()."""
+    host_alloc (``thp`` selects the huge-page path); that memory lives as long
+    as the pool or any array returned by host_array()."""
 
     def __init__(self, num_layers: int, num_buffers: int, page_size: int, row_elems: int,
                  host_num_pages: int, layout="layer_first", elem_bytes: int = 2,
@@ -236,22 +257,18 @@ class Pool:
         self.row_elems, self.host_num_pages, self.elem_bytes = row_elems, host_num_pages, elem_bytes
         self.layout = self.desc.layout
         self.nbytes = num_buffers * num_layers * host_num_pages * page_size * row_elems * elem_bytes
-        self._owned = host_ptr is None
-        self.host_ptr = host_alloc(self.nbytes, thp) if host_ptr is None else host_ptr
+        self._mem = PinnedHost(self.nbytes, thp) if host_ptr is None else None
+        self.host_ptr = self._mem.ptr if host_ptr is None else host_ptr
         self.host_bytes = self.nbytes if host_bytes is None else host_bytes
         h = ctypes.c_void_p()
-        try:
-            _check(library().hicache_pool_create(ctypes.byref(self.desc), self.host_ptr,
-                                                 self.host_bytes, ctypes.byref(h)))
-        except Exception:
-            if self._owned:
-                host_free(self.host_ptr)
-            raise
+        _check(library().hicache_pool_create(ctypes.byref(self.desc), self.host_ptr,
+                                             self.host_bytes, ctypes.byref(h)))
         self.handle = h.value
 
-    # numpy view of the host pool (no copy)
     def host_array(self, dtype=np.uint16) -> np.ndarray:
+        """numpy view of the host pool (no copy); keeps the memory alive."""
         buf = (ctypes.c_uint8 * self.nbytes).from_address(self.host_ptr)
+        buf._owner = self._mem
         return np.frombuffer(buf, dtype=np.uint8).view(dtype)
 
     def _xfer(self, fn, kv: DeviceKV, device_pages, host_pages, layout, stream, *extra):
@@ -288,9 +305,7 @@ class Pool:
         if getattr(self, "handle", None):
             _check(library().hicache_pool_destroy(self.handle))
             self.handle = None
-            if self._owned and self.host_ptr:
-                host_free(self.host_ptr)
-                self.host_ptr = None
+        self._mem = None   # freed once no host_array view is left
 
     def __enter__(self):
         return self
