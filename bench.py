@@ -7,8 +7,9 @@ pages from a fragmented allocator, host pages contiguous), in each host layout
     backup   512 pages L1 -> L2                      (4 GiB)
     load     512 pages L2 -> L1                      (4 GiB)
     bidir    backup of request A while request B loads on a second stream
-             (4 GiB each way)
-so 48 GiB move per step.  Every transfer is one kernel launch of libhicache.
+             (4 GiB each way, two launches)
+    fused    the same pair as one launch (hicache_backup_load)
+so 72 GiB move per step.  Every transfer is one kernel launch of libhicache.
 
 Reported: whole-step GB/s (`value`), per layout/operation GB/s and their
 fraction of the host-link peak measured in the same run (pinned
@@ -42,6 +43,33 @@ METRIC = "L1↔L2 KV GB/s (load, backup, bidir) at 32K tokens; % of measured hos
 LAYOUT_NAMES = ["layer_first", "page_first", "page_first_direct"]
 NOMINAL = {"pcie_gen5_x16_per_dir_gbs": 63.0, "nvlink_c2c_per_dir_gbs": 450.0}
 GB = 1e9
+
+
+def kernel_fingerprint() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("hicache_kernels.cu", "hicache_internal.h"):
+        with open(os.path.join(ROOT, "tiered_kv_cache_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-page DRAM and C2C bytes of each (layout/op) kernel from the last ncu
+    capture, if the kernel source has not changed since."""
+    path = os.path.join(ROOT, "profiles", "xfer_kernel_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if "=" in line:
+                k, v = (x.strip() for x in line.split("=", 1))
+                out[k] = v
+    if out.get("kernel_source_sha256_16") != kernel_fingerprint():
+        return {}
+    return out
 
 
 def frac(a, b, nd=3):
@@ -224,8 +252,11 @@ def run_step(torch, w, s1, s2, ev=None):
         j.record(s2)
         s1.wait_event(j)
         e3 = mark() if ev is not None else None
+        pool.backup_load(kv, w["a_dev"], w["a_host"], w["b_dev"], w["b_host"], lid, stream=s1)
+        e4 = mark() if ev is not None else None
         if ev is not None:
-            ev += [(f"{lay}/backup", e0, e1), (f"{lay}/load", e1, e2), (f"{lay}/bidir", e2, e3)]
+            ev += [(f"{lay}/backup", e0, e1), (f"{lay}/load", e1, e2), (f"{lay}/bidir", e2, e3),
+                   (f"{lay}/bidir_fused", e3, e4)]
 
 
 def cpu_baseline(seconds_target=12.0, pages=24):
@@ -367,7 +398,7 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed = float(t.item())
     bpx = w["bytes_per_xfer"]
-    step_bytes = len(LAYOUT_NAMES) * 4 * bpx
+    step_bytes = len(LAYOUT_NAMES) * 6 * bpx
     npages = w["pages"]
     value = world * args.steps * step_bytes / elapsed / GB
 
@@ -379,22 +410,32 @@ def main():
         bk = bpx / statistics.mean(per[f"{lay}/backup"]) / GB
         ld = bpx / statistics.mean(per[f"{lay}/load"]) / GB
         bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
+        bf = 2 * bpx / statistics.mean(per[f"{lay}/bidir_fused"]) / GB
         breakdown[lay] = {
-            "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1), "bidir_gbs": round(bi, 1),
+            "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1),
+            "bidir_streams_gbs": round(bi, 1), "bidir_fused_gbs": round(bf, 1),
             "backup_frac_of_link": frac(bk, link["d2h_gbs"]),
             "load_frac_of_link": frac(ld, link["h2d_gbs"]),
-            "bidir_frac_of_link": frac(bi, link["bidir_gbs"]),
+            "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
+            "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
         }
     # dominant single-direction kernel: the largest total time
-    singles = {k: sum(v) for k, v in per.items() if not k.endswith("bidir")}
+    singles = {k: sum(v) for k, v in per.items() if "bidir" not in k}
     dom = max(singles, key=singles.get)
     dom_avg = statistics.mean(per[dom])
     achieved = bpx / dom_avg / GB
     dom_peak = link["d2h_gbs"] if dom.endswith("backup") else link["h2d_gbs"]
+    rec = recorded_traffic()
+    traffic = rec.get(f"{dom} dram_bytes_per_page")
+    link_traffic = rec.get(f"{dom} c2c_bytes_per_page")
     roofline = {"bound": "host_link", "kernel": f"xfer_kernel ({dom})", "achieved": round(achieved, 1),
                 "peak": round(dom_peak, 1) if dom_peak else None, "unit": "GB/s",
                 "frac": frac(achieved, dom_peak),
-                "traffic": None,
+                "traffic": int(traffic) * npages if traffic else None,
+                "traffic_c2c": int(link_traffic) * npages if link_traffic else None,
+                "traffic_source": "ncu dram__bytes_read+write (and ctc__*_bytes_data_user) of a 64-page "
+                                  "capture, scaled per page; null when that kernel was not captured or "
+                                  "its source changed since" ,
                 "peak_source": "in-run pinned cudaMemcpyAsync of 1 GiB, same direction (no host-link "
                                "figure in MEASURED_PEAKS.json)",
                 "bytes_per_launch": bpx, "avg_launch_ms": round(dom_avg * 1e3, 3)}
@@ -413,8 +454,8 @@ def main():
         hc.wait(s1)
     e2e_t = time.perf_counter() - t0
     e2e = {"value": round(world * e2e_steps * step_bytes / e2e_t / GB, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx + len(LAYOUT_NAMES) * 4 * npages * 16,
-           "d2h_bytes_per_step": len(LAYOUT_NAMES) * 2 * bpx,
+           "h2d_bytes_per_step": len(LAYOUT_NAMES) * 3 * bpx + len(LAYOUT_NAMES) * 6 * npages * 16,
+           "d2h_bytes_per_step": len(LAYOUT_NAMES) * 3 * bpx,
            "how": "host wall clock around the Python API calls (validation, pre-pass, launch) and a "
                   "host wait on the stream each step; host-index bytes counted as H2D"}
 
@@ -427,7 +468,8 @@ def main():
                                f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
                                "fragmented device pages, contiguous host pages",
                    "step": "per layout (layer_first, page_first, page_first_direct): backup, load, "
-                           f"concurrent backup+load on two streams; {step_bytes / 2**30:.0f} GiB per step",
+                           "concurrent backup+load of two requests on two streams, and the same pair "
+                           f"as one fused launch; {step_bytes / 2**30:.0f} GiB per step",
                    "l2": f"inputs larger than L2 ({bpx / 2**20:.0f} MiB per transfer)",
                    "launch_ctas": args.ctas or "auto"},
         "roofline": roofline,

@@ -171,6 +171,25 @@ int hicache_load_layer(hicache_pool *pool, const hicache_device_kv *kv,
                        const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                        int32_t layout, int32_t layer_id, void *stream);
 
+/* Both directions in one launch: a backup of n_backup pages and a load of
+ * n_load pages, every layer.  Every CTA alternates a backup tile and a load
+ * tile, so both directions of the host link stay busy until both finish (two
+ * launches on two streams let one direction finish early and the other run
+ * alone).  The concurrent backup of one request and load of another is the
+ * pages' bidirectional transfer ("Tuning ... section 2.1": layer_first +
+ * bidirectional async; "Baidu's KVCache Overhaul", section "Bidirectional
+ * Async Transfer"), here fused into one submission.  Validation is that of
+ * hicache_backup for the first set and hicache_load for the second, plus:
+ * no device page may be both read by the backup and written by the load, and
+ * no host page both written by the backup and read by the load (INVALID_ARG),
+ * so the result does not depend on how the two interleave.  Either count may
+ * be 0 (then this is a plain backup or load). */
+int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
+                        const int64_t *backup_device_pages, const int64_t *backup_host_pages,
+                        int64_t n_backup, const int64_t *load_device_pages,
+                        const int64_t *load_host_pages, int64_t n_load, int32_t layout,
+                        void *stream);
+
 /* ---- plans: pre-pass once, execute many times -------------------------------
  * A plan holds the validated, sorted, run-merged index set of one transfer, so
  * that the L per-layer loads of one request pay for validation and the pre-pass

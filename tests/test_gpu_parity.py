@@ -279,3 +279,54 @@ def test_bidirectional_streams():
             got = gh.to_np(bufs, 2)
             for k in range(B * L):
                 assert np.array_equal(got[k], want_dev[k])
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+@pytest.mark.parametrize("sizes", [(24, 24), (30, 7), (5, 40), (0, 12), (12, 0)], ids=str)
+def test_backup_load_fused(layout, sizes):
+    """One launch that backs up request A and loads request B equals the
+    oracle's backup of A followed by its load of B (they touch disjoint pages)."""
+    nb_, nl_ = sizes
+    B, L, P, R, Dp, Hp = 2, 5, 16, 256, 96, 96
+    rng = np.random.default_rng(31 + layout + nb_)
+    perm = rng.permutation(Dp)
+    a_dev, b_dev = perm[:nb_], perm[nb_:nb_ + nl_]
+    hperm = rng.permutation(Hp)
+    a_host, b_host = np.sort(hperm[:nb_]), hperm[nb_:nb_ + nl_]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=40 + layout)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0 = host.copy()
+        dev0 = gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        c0 = hc.launch_count()
+        pool.backup_load(kv, a_dev, a_host, b_dev, b_host)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 == (1 if nb_ + nl_ else 0)
+        want_host = host0.view(np.uint16).copy()
+        gh.orc().backup(dev0, want_host, B, L, P, R, Hp, a_dev, a_host, layout)
+        want_dev = [x.copy() for x in dev0]
+        gh.orc().load(want_dev, host0.view(np.uint16), B, L, P, R, Hp, b_dev, b_host, layout)
+        assert np.array_equal(host.view(np.uint16), want_host)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want_dev[k])
+
+
+def test_backup_load_rejects_hazards():
+    B, L, P, R, Dp, Hp = 1, 2, 4, 64, 16, 16
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    kv = hc.DeviceKV(bufs, Dp)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        c0 = hc.launch_count()
+        with pytest.raises(hc.HiCacheError) as e:     # the load overwrites a page the backup reads
+            pool.backup_load(kv, [1, 2], [0, 1], [5, 2], [8, 9])
+        assert e.value.status == "INVALID_ARG" and "device page 2" in str(e.value)
+        with pytest.raises(hc.HiCacheError) as e:     # the load reads a host page the backup writes
+            pool.backup_load(kv, [1, 2], [0, 1], [5, 6], [1, 9])
+        assert e.value.status == "INVALID_ARG" and "host page 1" in str(e.value)
+        with pytest.raises(hc.HiCacheError) as e:     # the usual checks still apply to each side
+            pool.backup_load(kv, [1, 2], [3, 3], [5, 6], [8, 9])
+        assert e.value.status == "DUPLICATE_INDEX"
+        assert hc.launch_count() == c0

@@ -136,6 +136,16 @@ def test_deep78_32k_bidirectional():
                                          20000, 10 + layout)
             assert gh.sampled_host_check(host, bufs, b_req.device_pages, b_req.host_pages, layout, B, L, P,
                                          R, Hp, 20000, 20 + layout)
+            # the same two requests as one fused launch
+            position_fill(host.view(np.uint32))
+            c0 = hc.launch_count()
+            pool.backup_load(kv, a.device_pages, a.host_pages, b_req.device_pages, b_req.host_pages, layout)
+            torch.cuda.synchronize()
+            assert hc.launch_count() - c0 == 1
+            assert gh.sampled_host_check(host, bufs, a.device_pages, a.host_pages, layout, B, L, P, R, Hp,
+                                         20000, 30 + layout)
+            assert gh.sampled_host_check(host, bufs, b_req.device_pages, b_req.host_pages, layout, B, L, P,
+                                         R, Hp, 20000, 40 + layout)
     del bufs, kv
     torch.cuda.empty_cache()
 

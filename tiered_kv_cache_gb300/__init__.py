@@ -82,6 +82,8 @@ def _bind(lib):
         "hicache_backup": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
         "hicache_load": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
         "hicache_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _i32, _vp]),
+        "hicache_backup_load": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _vp, _vp, _i64,
+                                               _i32, _vp]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
@@ -289,6 +291,18 @@ class Pool:
     def load_layer(self, kv: DeviceKV, device_pages, host_pages, layer: int, layout=LAYOUT_POOL,
                    stream=None):
         self._xfer(library().hicache_load_layer, kv, device_pages, host_pages, layout, stream, layer)
+
+    def backup_load(self, kv: DeviceKV, backup_device_pages, backup_host_pages, load_device_pages,
+                    load_host_pages, layout=LAYOUT_POOL, stream=None):
+        """A backup and a load in one launch (both directions of the link at once)."""
+        bd, bh = _idx(backup_device_pages), _idx(backup_host_pages)
+        ld, lh = _idx(load_device_pages), _idx(load_host_pages)
+        if bd.size != bh.size or ld.size != lh.size:
+            raise ValueError("device and host page lists differ in length")
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_backup_load(self.handle, ctypes.byref(kv.struct), _ptr(bd), _ptr(bh), bd.size,
+                                             _ptr(ld), _ptr(lh), ld.size, layout, _stream(stream)))
 
     def wait_layer(self, layer: int, compute_stream=None):
         _check(library().hicache_wait_layer(self.handle, layer, _stream(compute_stream)))

@@ -233,17 +233,50 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
   return HICACHE_OK;
 }
 
-// Enqueue the transfer of `runs` (already validated).  layer < 0: all layers.
+// Copy runs[next..] into job `j` of the parameters, starting at blob word
+// `word`: at most max_runs runs and kMaxTiles tiles (so the kernel's 32-bit
+// grid-stride index never overflows).  Returns the number of runs taken, or -1
+// if even one run is too large.
+int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
+                 int64_t max_runs, hicache::XferParams &params, int32_t word, int j) {
+  hicache::Job &job = params.h.job[j];
+  hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
+  int64_t tiles = 0;
+  int32_t count = 0;
+  while (next + size_t(count) < runs.size() && count < max_runs) {
+    const RunRec &r = runs[next + size_t(count)];
+    const int64_t t = (r.len * upp + hicache::kTileVecs - 1) / hicache::kTileVecs;
+    if ((tiles + t) * outers > kMaxTiles) {
+      if (count == 0) return -1;
+      break;
+    }
+    table[count] = hicache::Run{int32_t(r.h0), int32_t(r.d0), int32_t(r.len), int32_t(tiles)};
+    tiles += t;
+    ++count;
+  }
+  job.n_runs = count;
+  job.runs_word = word;
+  job.tiles_per_outer = int32_t(tiles);
+  job.total_tiles = int32_t(tiles * outers);
+  return count;
+}
+
+// Enqueue validated runs.  One direction: `runs` moves towards the host if
+// to_host; layer < 0 means every layer.  Both directions (`load_runs` not
+// NULL): `runs` is a backup and `load_runs` a load, every layer, one kernel
+// per chunk so the two directions share every CTA.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
-            int32_t layout, int32_t layer, bool to_host, void *stream) {
-  if (runs.empty()) return HICACHE_OK;
+            const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
+            void *stream) {
+  const bool bidir = load_runs != nullptr;
+  if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
   const Shape &s = pool->shape;
   const bool all = layer < 0;
   const int32_t nb = int32_t(s.B * s.L);
   const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
   const int64_t outers = lf_all ? s.B * s.L : s.B;
   const int64_t upp = (all && layout != HICACHE_LAYER_FIRST) ? s.LPV : s.PV;
-  const int64_t max_runs = (hicache::kBlobWords - nb) / 2;
+  const int64_t capacity = (hicache::kBlobWords - nb) / 2;  // runs per launch
 
   thread_local hicache::XferParams params;
   hicache::XferHeader &h = params.h;
@@ -262,42 +295,53 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   h.fd_PV = hicache::make_fastdiv(uint32_t(s.PV));
   h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
   h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
+  h.job[1] = hicache::Job{0, nb, 0, 0};
   for (int32_t i = 0; i < nb; ++i)
     params.blob[i] = uint64_t(reinterpret_cast<uintptr_t>(kv->buf_ptrs[i]));
-  hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[nb]);
 
-  size_t next = 0;
-  while (next < runs.size()) {
-    // greedy chunk: at most max_runs runs and kMaxTiles tiles per launch (the
-    // kernel's 32-bit grid-stride index then never overflows)
-    int64_t tiles = 0;
-    int32_t count = 0;
-    while (next + size_t(count) < runs.size() && count < max_runs) {
-      const RunRec &r = runs[next + size_t(count)];
-      const int64_t t = (r.len * upp + hicache::kTileVecs - 1) / hicache::kTileVecs;
-      if (count > 0 && (tiles + t) * outers > kMaxTiles) break;
-      table[count] = hicache::Run{int32_t(r.h0), int32_t(r.d0), int32_t(r.len), int32_t(tiles)};
-      tiles += t;
-      ++count;
+  size_t next0 = 0, next1 = 0;
+  const size_t n1 = bidir ? load_runs->size() : 0;
+  while (next0 < runs.size() || next1 < n1) {
+    const bool more0 = next0 < runs.size(), more1 = next1 < n1;
+    const int64_t cap0 = more1 ? capacity / 2 : capacity;
+    const int32_t c0 = fill_job(runs, next0, upp, outers, more0 ? cap0 : 0, params, nb, 0);
+    if (c0 < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+    int32_t c1 = 0;
+    if (bidir) {
+      c1 = fill_job(*load_runs, next1, upp, outers, more1 ? capacity - c0 : 0, params, nb + 2 * c0, 1);
+      if (c1 < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
     }
-    if (tiles * outers > kMaxTiles)
-      return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
-    h.n_runs = count;
-    h.tiles_per_outer = int32_t(tiles);
-    h.total_tiles = int32_t(tiles * outers);
     hicache::XferLaunch x;
     x.params = &params;
     x.layout = layout;
     x.all_layers = all;
     x.to_host = to_host;
-    x.grid = int(std::min<int64_t>(h.total_tiles, pool->ctas));
+    x.bidir = bidir;
+    const int64_t tiles = int64_t(h.job[0].total_tiles) + (bidir ? h.job[1].total_tiles : 0);
+    x.grid = int(std::min<int64_t>(tiles, pool->ctas));
     x.stream = stream;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    next += size_t(count);
+    next0 += size_t(c0);
+    next1 += size_t(c1);
   }
   return HICACHE_OK;
+}
+
+// Sorted-merge test: do two page sets share a page?
+bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common) {
+  std::sort(a.begin(), a.end());
+  std::sort(b.begin(), b.end());
+  size_t i = 0, k = 0;
+  while (i < a.size() && k < b.size()) {
+    if (a[i] == b[k]) {
+      *common = a[i];
+      return true;
+    }
+    if (a[i] < b[k]) ++i; else ++k;
+  }
+  return false;
 }
 
 int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev,
@@ -316,7 +360,8 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
   if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction,
                     max_run_pages(pool->shape), &runs)))
     return rc;
-  if ((rc = enqueue(pool, kv, runs, lay, layer, direction == HICACHE_DIR_BACKUP, stream))) return rc;
+  if ((rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream)))
+    return rc;
   if (layer >= 0) {
     const cudaError_t e = cudaEventRecord(pool->events[size_t(layer)], static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
@@ -477,6 +522,43 @@ int hicache_load_layer(hicache_pool *pool, const hicache_device_kv *kv,
   return transfer(pool, kv, device_pages, host_pages, n, layout, layer_id, HICACHE_DIR_LOAD, stream);
 }
 
+int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
+                        const int64_t *backup_device_pages, const int64_t *backup_host_pages,
+                        int64_t n_backup, const int64_t *load_device_pages,
+                        const int64_t *load_host_pages, int64_t n_load, int32_t layout,
+                        void *stream) {
+  g_last_error.clear();
+  if (!pool) return set_error(HICACHE_ERR_INVALID_ARG, "pool is NULL");
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, 0))) return rc;
+  thread_local std::vector<RunRec> brun, lrun;
+  if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, backup_device_pages, backup_host_pages,
+                    n_backup, HICACHE_DIR_BACKUP, max_run_pages(pool->shape), &brun)))
+    return rc;
+  if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, load_device_pages, load_host_pages, n_load,
+                    HICACHE_DIR_LOAD, max_run_pages(pool->shape), &lrun)))
+    return rc;
+  if (n_backup > 0 && n_load > 0) {
+    // the result must not depend on the order of the two directions
+    int64_t page = 0;
+    if (intersects(std::vector<int64_t>(backup_device_pages, backup_device_pages + n_backup),
+                   std::vector<int64_t>(load_device_pages, load_device_pages + n_load), &page))
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "device page %lld is read by the backup and written by the load",
+                       (long long)page);
+    if (intersects(std::vector<int64_t>(backup_host_pages, backup_host_pages + n_backup),
+                   std::vector<int64_t>(load_host_pages, load_host_pages + n_load), &page))
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "host page %lld is written by the backup and read by the load",
+                       (long long)page);
+  }
+  if (lrun.empty()) return enqueue(pool, kv, brun, nullptr, lay, -1, true, stream);
+  if (brun.empty()) return enqueue(pool, kv, lrun, nullptr, lay, -1, false, stream);
+  return enqueue(pool, kv, brun, &lrun, lay, -1, true, stream);
+}
+
 int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,
                         int64_t n, int64_t device_num_pages, int32_t direction,
                         hicache_plan **out) {
@@ -512,7 +594,7 @@ int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, 
   if (layer_id >= 0 && plan->direction != HICACHE_DIR_LOAD)
     return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
   if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
-  if ((rc = enqueue(pool, kv, plan->runs, lay, layer_id < 0 ? -1 : layer_id,
+  if ((rc = enqueue(pool, kv, plan->runs, nullptr, lay, layer_id < 0 ? -1 : layer_id,
                     plan->direction == HICACHE_DIR_BACKUP, stream)))
     return rc;
   if (layer_id >= 0) {

@@ -70,24 +70,31 @@ struct RunRec {
 
 enum Layout : int32_t { kLayerFirst = 0, kPageFirst = 1, kPageFirstDirect = 2 };
 
+// One direction of a launch: its run table and tile counts.
+struct Job {
+  int32_t n_runs;
+  int32_t runs_word;          // first word of the job's run table in XferParams::blob
+  int32_t tiles_per_outer;    // tiles of one outer unit (a buffer, or a buffer-layer)
+  int32_t total_tiles;
+};
+
 // Everything a transfer launch needs, in vectors of 16 bytes.
 struct XferHeader {
   void *host;                 // device-visible alias of the host pool
   int32_t L, P, V, num_bufs;  // layers, page size, vectors per row, B*L
   int32_t layer;              // the layer of a single-layer transfer
   int32_t Hp;                 // host pool pages
-  int32_t n_runs;
-  int32_t tiles_per_outer;    // tiles of one outer unit (a buffer, or a buffer-layer)
-  int32_t total_tiles;
   uint32_t unit_per_page;     // vectors one page contributes to a unit
   uint32_t PV, LV, LPV;       // P*V, L*V, L*P*V
   FastDiv fd_V, fd_PV, fd_LV, fd_LPV;
+  Job job[2];                 // [0]: the transfer (the backup of a bidirectional
+                              // launch); [1]: the load of a bidirectional launch
 };
 
 struct XferParams {
   XferHeader h;
   // blob[0 .. num_bufs): device buffer pointers (buffer-major b*L + l);
-  // then n_runs Run records (two words each).
+  // then the run tables of the jobs (two words per Run).
   uint64_t blob[kBlobWords];
 };
 static_assert(sizeof(XferParams) <= 32764, "kernel parameter limit");
@@ -105,10 +112,11 @@ static_assert(sizeof(ChecksumParams) <= 32764, "kernel parameter limit");
 
 // Launch entry points (hicache_kernels.cu).  Return a cudaError_t value.
 struct XferLaunch {
-  XferParams *params;         // filled header + blob; the launcher completes it
+  XferParams *params;         // filled header + blob
   int layout;
   bool all_layers;
   bool to_host;
+  bool bidir;                 // job[0] backup and job[1] load, all layers, one launch
   int grid;
   void *stream;
 };

@@ -84,58 +84,99 @@ __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bu
   }
 }
 
+// Move tile `g` of one job: 16 KiB of one unit, 4 vectors per thread, all
+// loads issued before the first store.
+template <int LAYOUT, bool ALL, bool TO_HOST>
+__device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, const Run *runs,
+                                          uint4 *const *bufs, int32_t g) {
+  const int32_t outer = g / job.tiles_per_outer;
+  const int32_t inner = g - outer * job.tiles_per_outer;
+  int b, l;
+  if (LAYOUT == kLayerFirst && ALL) {
+    b = outer / h.L;
+    l = outer - b * h.L;
+  } else {
+    b = outer;
+    l = h.layer;
+  }
+  // the run holding tile `inner`: the last run with tile0 <= inner
+  int lo = 0, hi = job.n_runs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (runs[mid].tile0 <= inner) lo = mid; else hi = mid - 1;
+  }
+  const Run r = runs[lo];
+  const uint32_t w0 = uint32_t(inner - r.tile0) * kTileVecs + threadIdx.x;
+  const uint32_t unit = uint32_t(r.len) * h.unit_per_page;
+
+  uint4 v[kUnroll];
+  uint4 *dst[kUnroll];
+#pragma unroll
+  for (int k = 0; k < kUnroll; ++k) {
+    const uint32_t w = w0 + k * kThreads;
+    dst[k] = nullptr;
+    if (w < unit) {
+      uint4 *dev, *host;
+      map_vector<LAYOUT, ALL>(h, bufs, b, l, r, w, dev, host);
+      if (TO_HOST) {
+        v[k] = ld_stream(dev);
+        dst[k] = host;
+      } else {
+        v[k] = ld_stream(host);
+        dst[k] = dev;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kUnroll; ++k)
+    if (dst[k] != nullptr) st_stream(dst[k], v[k]);
+}
+
+__device__ __forceinline__ const Run *job_runs(const XferParams &p, int j) {
+  return reinterpret_cast<const Run *>(&p.blob[p.h.job[j].runs_word]);
+}
+
+__device__ __forceinline__ void load_buffer_table(const XferParams &p, uint4 **s_bufs) {
+  for (int i = threadIdx.x; i < p.h.num_bufs; i += kThreads)
+    s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
+  __syncthreads();
+}
+
+// One direction: CTAs take tiles grid-stride in host-address order.
 template <int LAYOUT, bool ALL, bool TO_HOST>
 __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ XferParams p) {
   __shared__ uint4 *s_bufs[kMaxBufs];
-  const XferHeader &h = p.h;
-  for (int i = threadIdx.x; i < h.num_bufs; i += kThreads)
-    s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
-  __syncthreads();
-  const Run *runs = reinterpret_cast<const Run *>(&p.blob[h.num_bufs]);
-  const bool lf_all = (LAYOUT == kLayerFirst) && ALL;
+  load_buffer_table(p, s_bufs);
+  const Job &job = p.h.job[0];
+  const Run *runs = job_runs(p, 0);
+  for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x)
+    move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g);
+}
 
-  for (int32_t g = blockIdx.x; g < h.total_tiles; g += gridDim.x) {
-    const int32_t outer = g / h.tiles_per_outer;
-    const int32_t inner = g - outer * h.tiles_per_outer;
-    int b, l;
-    if (lf_all) {
-      b = outer / h.L;
-      l = outer - b * h.L;
+// Both directions in one launch: job 0 is a backup, job 1 a load, every layer.
+// Each CTA alternates a backup tile and a load tile, so the two directions of
+// the host link advance together and neither finishes early, leaving the
+// other to run alone; once one job runs out the CTA finishes the other.
+template <int LAYOUT>
+__global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__ XferParams p) {
+  __shared__ uint4 *s_bufs[kMaxBufs];
+  load_buffer_table(p, s_bufs);
+  const Job &jb = p.h.job[0];
+  const Job &jl = p.h.job[1];
+  const Run *rb = job_runs(p, 0);
+  const Run *rl = job_runs(p, 1);
+  int32_t ib = blockIdx.x, il = blockIdx.x;
+  bool backup_turn = true;
+  while (ib < jb.total_tiles || il < jl.total_tiles) {
+    const bool do_backup = il >= jl.total_tiles || (backup_turn && ib < jb.total_tiles);
+    if (do_backup) {
+      move_tile<LAYOUT, true, true>(p.h, jb, rb, s_bufs, ib);
+      ib += gridDim.x;
     } else {
-      b = outer;
-      l = h.layer;
+      move_tile<LAYOUT, true, false>(p.h, jl, rl, s_bufs, il);
+      il += gridDim.x;
     }
-    // the run holding tile `inner`: last run with tile0 <= inner
-    int lo = 0, hi = h.n_runs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (runs[mid].tile0 <= inner) lo = mid; else hi = mid - 1;
-    }
-    const Run r = runs[lo];
-    const uint32_t w0 = uint32_t(inner - r.tile0) * kTileVecs + threadIdx.x;
-    const uint32_t unit = uint32_t(r.len) * h.unit_per_page;
-
-    uint4 v[kUnroll];
-    uint4 *dst[kUnroll];
-#pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      const uint32_t w = w0 + k * kThreads;
-      dst[k] = nullptr;
-      if (w < unit) {
-        uint4 *dev, *host;
-        map_vector<LAYOUT, ALL>(h, s_bufs, b, l, r, w, dev, host);
-        if (TO_HOST) {
-          v[k] = ld_stream(dev);
-          dst[k] = host;
-        } else {
-          v[k] = ld_stream(host);
-          dst[k] = dev;
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kUnroll; ++k)
-      if (dst[k] != nullptr) st_stream(dst[k], v[k]);
+    backup_turn = !backup_turn;
   }
 }
 
@@ -170,6 +211,10 @@ cudaError_t launch_one(const XferLaunch &x) {
 
 template <int LAYOUT>
 cudaError_t launch_layout(const XferLaunch &x) {
+  if (x.bidir) {
+    bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, static_cast<cudaStream_t>(x.stream)>>>(*x.params);
+    return cudaGetLastError();
+  }
   if (x.all_layers)
     return x.to_host ? launch_one<LAYOUT, true, true>(x) : launch_one<LAYOUT, true, false>(x);
   return x.to_host ? launch_one<LAYOUT, false, true>(x) : launch_one<LAYOUT, false, false>(x);
