@@ -153,22 +153,29 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
-def build_workload(device, pages=512, launch_ctas=0):
-    """The Llama-3-8B-shaped pools (1024 device and 1024 host pages at 512
-    pages per transfer; 2x `pages` each for a scaled-down case)."""
+def build_workload(device, pages=512, launch_ctas=0, name="llama3_8b_32k"):
+    """Two requests A and B of `pages` pages each over the workload's pools:
+    llama3_8b_32k -- fragmented device pages (runs of 1-8), contiguous host;
+    deep78_32k    -- 78 layers, fully scattered device pages, contiguous host.
+    (1024 device and 1024 host pages at 512 pages per transfer; 2x `pages`
+    each for a scaled-down case.)"""
     import dataclasses
     import torch
     import tiered_kv_cache_gb300 as hc
     from tiered_kv_cache_gb300 import workloads as wl
 
-    s = wl.LLAMA3_8B
+    s = wl.LLAMA3_8B if name == "llama3_8b_32k" else wl.DEEP_STRESS
     if pages != 512:
         s = dataclasses.replace(s, device_pages=2 * pages, host_pages=2 * pages)
     vals = [v.view(torch.int16) for v in wl.kv_values(s, device=device)]
-    t = wl.llama_transfer(s, pages)
-    a_dev = t.device_pages
-    rng = wl.index_rng(s.seed + 1)
-    b_dev = wl.fragmented_pages(rng, s.device_pages, pages, exclude=a_dev)
+    if name == "llama3_8b_32k":
+        t = wl.llama_transfer(s, pages)
+        a_dev = t.device_pages
+        rng = wl.index_rng(s.seed + 1)
+        b_dev = wl.fragmented_pages(rng, s.device_pages, pages, exclude=a_dev)
+    else:
+        a, b = wl.deep_bidir_transfers(s, pages)
+        a_dev, b_dev = a.device_pages, b.device_pages
     a_host = wl.contiguous_pages(pages, 0)
     b_host = wl.contiguous_pages(pages, pages)
     pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first",
@@ -333,6 +340,161 @@ def reference_arm(args):
     }), flush=True)
 
 
+def _elapsed(torch, e0, e1):
+    return e0.elapsed_time(e1) / 1e3
+
+
+def bench_mla_overlap(torch, hc, args):
+    """MLA latent (61 layers, kv_dim 576, page 64), page_first host pool:
+    per-layer loads on a transfer stream, each recording its layer event; a
+    stand-in attention kernel per layer on a compute stream that waits on that
+    event.  Reports (a) the 61 per-layer loads alone, (b) the compute alone,
+    (c) both overlapped, and the overlap efficiency (a + b - c) / min(a, b)."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.MLA_LATENT
+    vals = [v.view(torch.int16) for v in wl.kv_values(s, device="cuda")]
+    kv = hc.DeviceKV(vals, s.device_pages)
+    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "page_first",
+                   launch_ctas=args.ctas)
+    L = s.num_layers
+    sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+    out = {}
+    launches0 = hc.launch_count()
+    for tokens, prio in ((4096, 0), (16384, 0), (65536, 0), (4096, -1), (16384, -1), (65536, -1)):
+        # prio -1: the transfer stream outranks the compute stream, so the block
+        # scheduler places the transfer's CTAs first as compute CTAs retire
+        xfer = torch.cuda.Stream(priority=prio)
+        comp = torch.cuda.Stream()
+        t = wl.mla_transfer(s, tokens)
+        n = len(t.device_pages)
+        plan = pool.plan(t.device_pages, t.host_pages, s.device_pages, hc.LOAD)
+        nbytes = n * s.page_bytes
+
+        def timed(fn, reps=args.steps):
+            best = []
+            for _ in range(max(args.warmup, 3)):
+                fn()
+            torch.cuda.synchronize()
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(xfer)
+                comp.wait_event(e0)
+                fn()
+                j = torch.cuda.Event()
+                j.record(comp)
+                xfer.wait_event(j)
+                e1.record(xfer)
+                torch.cuda.synchronize()
+                best.append(_elapsed(torch, e0, e1))
+            return statistics.median(best)
+
+        def loads():
+            for layer in range(L):
+                plan.execute(kv, layer=layer, stream=xfer)
+
+        def one_load():
+            plan.execute(kv, layer=-1, stream=xfer)
+
+        def computes(reps):
+            for layer in range(L):
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
+        def overlapped(reps):
+            for layer in range(L):
+                plan.execute(kv, layer=layer, stream=xfer)
+                pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
+        a = timed(loads)
+        whole = timed(one_load)
+        c1 = timed(lambda: computes(1))
+        reps = max(1, int(round(a / c1)))          # stand-in attention about as long as the loads
+        b = timed(lambda: computes(reps))
+        c = timed(lambda: overlapped(reps))
+        out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
+            "pages": n, "bytes": nbytes,
+            "per_layer_loads_ms": round(a * 1e3, 3), "per_layer_load_gbs": round(nbytes / a / GB, 1),
+            "one_launch_load_ms": round(whole * 1e3, 3), "one_launch_load_gbs": round(nbytes / whole / GB, 1),
+            "compute_ms": round(b * 1e3, 3), "compute_reps": reps,
+            "overlapped_ms": round(c * 1e3, 3),
+            "overlap_efficiency": round((a + b - c) / min(a, b), 3),
+        }
+        plan.close()
+    launches = hc.launch_count() - launches0
+    pool.close()
+    return out, launches
+
+
+def bench_small_mix(torch, hc, args):
+    """10,000 seeded requests, 1-256 pages log-uniform, 30% backup / 70% load,
+    random pages, layer_first.  Per-call latency = host wall clock from the API
+    call until the stream is idle; aggregate GB/s without per-call waits."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.SMALL_MIX
+    vals = [v.view(torch.int16) for v in wl.kv_values(s, device="cuda")]
+    kv = hc.DeviceKV(vals, s.device_pages)
+    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first",
+                   launch_ctas=args.ctas)
+    reqs = wl.small_mix_requests(s)
+    st = torch.cuda.Stream()
+    handle = st.cuda_stream
+
+    def call(r):
+        if r.direction == "backup":
+            pool.backup(kv, r.device_pages, r.host_pages, stream=handle)
+        else:
+            pool.load(kv, r.device_pages, r.host_pages, stream=handle)
+
+    for r in reqs[:200]:
+        call(r)
+    hc.wait(handle)
+    lat, submit = [], []
+    launches0 = hc.launch_count()
+    for r in reqs:
+        t0 = time.perf_counter()
+        call(r)
+        t1 = time.perf_counter()
+        hc.wait(handle)
+        t2 = time.perf_counter()
+        submit.append(t1 - t0)
+        lat.append(t2 - t0)
+    per_call_launches = (hc.launch_count() - launches0) / len(reqs)
+    total = sum(len(r.device_pages) for r in reqs) * s.page_bytes
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0.record(st)
+    for r in reqs:
+        call(r)
+    e1.record(st)
+    hc.wait(handle)
+    wall = time.perf_counter() - t0
+    dev = _elapsed(torch, e0, e1)
+    lat_us = np.array(lat) * 1e6
+    sub_us = np.array(submit) * 1e6
+    sizes = np.array([len(r.device_pages) for r in reqs])
+
+    def pct(a, q):
+        return round(float(np.percentile(a, q)), 1)
+    by_size = {}
+    for lo, hi in ((1, 4), (5, 64), (65, 256)):
+        m = (sizes >= lo) & (sizes <= hi)
+        by_size[f"{lo}-{hi}_pages"] = {"calls": int(m.sum()), "p50_us": pct(lat_us[m], 50),
+                                       "p99_us": pct(lat_us[m], 99)}
+    out = {"requests": len(reqs), "bytes": total,
+           "latency_p50_us": pct(lat_us, 50), "latency_p99_us": pct(lat_us, 99),
+           "submit_p50_us": pct(sub_us, 50), "submit_p99_us": pct(sub_us, 99),
+           "latency_by_size": by_size, "launches_per_call": per_call_launches,
+           "aggregate_gbs_device": round(total / dev / GB, 1),
+           "aggregate_gbs_wall": round(total / wall / GB, 1)}
+    pool.close()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -345,6 +507,10 @@ def main():
                     help="pages per transfer (512 = the 32K-token workload; smaller for profiling)")
     ap.add_argument("--no-link-probe", action="store_true",
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
+    ap.add_argument("--workload", default="llama3_8b_32k",
+                    choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix"],
+                    help="llama3_8b_32k is the headline step; the others measure the remaining "
+                         "workload shapes")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -365,7 +531,31 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch)
-    w = build_workload("cuda", args.pages, args.ctas)
+    if args.workload in ("mla61_overlap", "small_mix"):
+        t0 = time.perf_counter()
+        if args.workload == "mla61_overlap":
+            res, launches = bench_mla_overlap(torch, hc, args)
+            value = res["64k"]["per_layer_load_gbs"]
+            what = {"workload": "mla61: 61 layers, one latent buffer, kv_dim 576, bf16, page 64, "
+                                "page_first host pool; 4K/16K/64K-token per-layer loads with an "
+                                "event per layer and a stand-in attention kernel on a second stream",
+                    "value": "GB/s of the 61 per-layer loads at 64K tokens"}
+        else:
+            res = bench_small_mix(torch, hc, args)
+            launches = int(res["launches_per_call"] * res["requests"])
+            value = res["aggregate_gbs_device"]
+            what = {"workload": "small_mix: 32 layers, K+V, 8 kv heads x 128, page 16, 10,000 requests "
+                                "of 1-256 pages (log-uniform), 30% backup, layer_first",
+                    "value": "aggregate GB/s without per-call waits"}
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                              "config": what, "results": res, "gpu_launches": launches,
+                              "link_peak": link, "wall_s": round(time.perf_counter() - t0, 1)}),
+                  flush=True)
+        return
+    w = build_workload("cuda", args.pages, args.ctas, args.workload)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     for _ in range(max(args.warmup, 3)):
         run_step(torch, w, s1, s2)
@@ -464,9 +654,12 @@ def main():
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"llama3_8b_{npages * 64 // 1024}k: 32 layers, K+V, 8 kv heads x 128, "
-                               f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
-                               "fragmented device pages, contiguous host pages",
+        "config": {"workload": (f"llama3_8b_{npages * 64 // 1024}k: 32 layers, K+V, 8 kv heads x 128, "
+                                f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
+                                "fragmented device pages, contiguous host pages")
+                   if args.workload == "llama3_8b_32k" else
+                   (f"deep78_{npages * 64 // 1024}k: 78 layers, K+V, 8 kv heads x 128, bf16, page 64, "
+                    f"{npages} pages per transfer, fully scattered device pages, contiguous host pages"),
                    "step": "per layout (layer_first, page_first, page_first_direct): backup, load, "
                            "concurrent backup+load of two requests on two streams, and the same pair "
                            f"as one fused launch; {step_bytes / 2**30:.0f} GiB per step",

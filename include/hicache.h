@@ -93,7 +93,8 @@ typedef struct {
   int64_t row_elems;        /* R: kv_heads*head_dim, or kv_dim (e.g. 576) */
   int64_t host_num_pages;   /* Hp: pages in the host pool */
   int32_t layout;           /* hicache_layout of the host pool (not POOL) */
-  int32_t launch_ctas;      /* CTAs per transfer launch; 0 = automatic */
+  int32_t launch_ctas;      /* CTAs per direction of a transfer launch (a fused
+                               backup+load gets twice as many); 0 = one per SM */
   int32_t flags;            /* must be 0 */
   int32_t reserved;         /* must be 0 */
 } hicache_pool_desc;
@@ -216,9 +217,10 @@ int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
  * last load of `layer` enqueued before this call. */
 int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
 
-/* Block the calling host thread until all work on `stream` is done, polling at
- * most every 50 us, for at most timeout_us microseconds (< 0 = no limit).
- * Returns OK, TIMEOUT (work still pending; nothing is cancelled) or CUDA. */
+/* Block the calling host thread until all work on `stream` is done, for at
+ * most timeout_us microseconds (< 0 = no limit).  Polls back to back for the
+ * first 500 us, then every 50 us.  Returns OK, TIMEOUT (work still pending;
+ * nothing is cancelled) or CUDA. */
 int hicache_wait(void *stream, int64_t timeout_us);
 
 /* ---- host-only helpers (no CUDA call; usable without a GPU) ------------------ */

@@ -313,12 +313,14 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     }
     hicache::XferLaunch x;
     x.params = &params;
+    x.words = nb + 2 * (c0 + c1);
     x.layout = layout;
     x.all_layers = all;
     x.to_host = to_host;
     x.bidir = bidir;
     const int64_t tiles = int64_t(h.job[0].total_tiles) + (bidir ? h.job[1].total_tiles : 0);
-    x.grid = int(std::min<int64_t>(tiles, pool->ctas));
+    // a fused launch carries both directions: one share of CTAs for each
+    x.grid = int(std::min<int64_t>(tiles, (bidir ? 2 : 1) * int64_t(pool->ctas)));
     x.stream = stream;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
@@ -652,9 +654,16 @@ int hicache_wait(void *stream, int64_t timeout_us) {
                                .count();
     if (timeout_us >= 0 && waited >= timeout_us)
       return set_error(HICACHE_ERR_TIMEOUT, "stream still busy after %lld us", (long long)waited);
-    int64_t nap = 50;
-    if (timeout_us >= 0) nap = std::min<int64_t>(nap, std::max<int64_t>(1, timeout_us - waited));
-    std::this_thread::sleep_for(std::chrono::microseconds(nap));
+    // Poll back to back for the first 500 us (small transfers finish within
+    // tens of microseconds and a sleep overshoots by the timer slack), then
+    // sleep 50 us between polls.
+    if (waited < 500) {
+      std::this_thread::yield();
+    } else {
+      int64_t nap = 50;
+      if (timeout_us >= 0) nap = std::min<int64_t>(nap, std::max<int64_t>(1, timeout_us - waited));
+      std::this_thread::sleep_for(std::chrono::microseconds(nap));
+    }
   }
 }
 

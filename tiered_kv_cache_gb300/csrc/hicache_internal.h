@@ -14,12 +14,19 @@ namespace hicache {
 
 // ---- launch geometry ------------------------------------------------------
 constexpr int kThreads = 256;                    // threads per CTA
-constexpr int kUnroll = 4;                       // 16-byte vectors in flight per thread
-constexpr int kTileVecs = kThreads * kUnroll;    // vectors per tile: 16 KiB
+#ifndef HICACHE_UNROLL
+#define HICACHE_UNROLL 4
+#endif
+constexpr int kUnroll = HICACHE_UNROLL;          // 16-byte vectors in flight per thread
+constexpr int kTileVecs = kThreads * kUnroll;    // vectors per tile (16 KiB at unroll 4)
 constexpr int kMaxBufs = 512;                    // B * L device buffers per call
 constexpr int kBlobWords = 3584;                 // 28 KiB of kernel parameters: buffer
                                                  // pointers, then the run table
-constexpr int kDefaultCtasPerSm = 2;
+constexpr int kBlobWordsSmall = 480;             // the same in under 4 KiB, for calls
+                                                 // whose table fits (cheaper to launch)
+// One CTA per SM and direction saturates the host link (16 KiB in flight per
+// CTA) and leaves the rest of each SM to the compute the transfer overlaps.
+constexpr int kDefaultCtasPerSm = 1;
 
 // ---- division by a run-time constant ---------------------------------------
 // q = floor(n / d) for 0 <= n < 2^31 by one multiply-high, an add and a shift:
@@ -91,13 +98,17 @@ struct XferHeader {
                               // launch); [1]: the load of a bidirectional launch
 };
 
-struct XferParams {
+template <int WORDS>
+struct XferParamsT {
   XferHeader h;
   // blob[0 .. num_bufs): device buffer pointers (buffer-major b*L + l);
   // then the run tables of the jobs (two words per Run).
-  uint64_t blob[kBlobWords];
+  uint64_t blob[WORDS];
 };
+using XferParams = XferParamsT<kBlobWords>;
+using XferParamsSmall = XferParamsT<kBlobWordsSmall>;
 static_assert(sizeof(XferParams) <= 32764, "kernel parameter limit");
+static_assert(sizeof(XferParamsSmall) <= 4096, "small parameter block");
 
 // Stand-in compute: pages are passed in the parameters.
 constexpr int kChecksumMaxPages = 6144;
@@ -113,6 +124,7 @@ static_assert(sizeof(ChecksumParams) <= 32764, "kernel parameter limit");
 // Launch entry points (hicache_kernels.cu).  Return a cudaError_t value.
 struct XferLaunch {
   XferParams *params;         // filled header + blob
+  int words;                  // blob words in use (selects the small parameter block)
   int layout;
   bool all_layers;
   bool to_host;

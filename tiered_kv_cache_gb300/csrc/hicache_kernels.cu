@@ -132,19 +132,21 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
     if (dst[k] != nullptr) st_stream(dst[k], v[k]);
 }
 
-__device__ __forceinline__ const Run *job_runs(const XferParams &p, int j) {
+template <class Params>
+__device__ __forceinline__ const Run *job_runs(const Params &p, int j) {
   return reinterpret_cast<const Run *>(&p.blob[p.h.job[j].runs_word]);
 }
 
-__device__ __forceinline__ void load_buffer_table(const XferParams &p, uint4 **s_bufs) {
+template <class Params>
+__device__ __forceinline__ void load_buffer_table(const Params &p, uint4 **s_bufs) {
   for (int i = threadIdx.x; i < p.h.num_bufs; i += kThreads)
     s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
   __syncthreads();
 }
 
 // One direction: CTAs take tiles grid-stride in host-address order.
-template <int LAYOUT, bool ALL, bool TO_HOST>
-__global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ XferParams p) {
+template <int LAYOUT, bool ALL, bool TO_HOST, class Params>
+__global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ Params p) {
   __shared__ uint4 *s_bufs[kMaxBufs];
   load_buffer_table(p, s_bufs);
   const Job &job = p.h.job[0];
@@ -157,8 +159,8 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
 // Each CTA alternates a backup tile and a load tile, so the two directions of
 // the host link advance together and neither finishes early, leaving the
 // other to run alone; once one job runs out the CTA finishes the other.
-template <int LAYOUT>
-__global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__ XferParams p) {
+template <int LAYOUT, class Params>
+__global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__ Params p) {
   __shared__ uint4 *s_bufs[kMaxBufs];
   load_buffer_table(p, s_bufs);
   const Job &jb = p.h.job[0];
@@ -202,17 +204,35 @@ __global__ void __launch_bounds__(kThreads) checksum_kernel(const __grid_constan
   if ((threadIdx.x & 31) == 0 && acc != 0) atomicAdd(p.out, acc);
 }
 
+template <class Params>
+const Params &params_for(const XferLaunch &x, Params &small) {
+  small.h = x.params->h;
+  for (int i = 0; i < x.words; ++i) small.blob[i] = x.params->blob[i];
+  return small;
+}
+
 template <int LAYOUT, bool ALL, bool TO_HOST>
 cudaError_t launch_one(const XferLaunch &x) {
-  xfer_kernel<LAYOUT, ALL, TO_HOST>
-      <<<x.grid, kThreads, 0, static_cast<cudaStream_t>(x.stream)>>>(*x.params);
+  const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  if (x.words <= kBlobWordsSmall) {
+    XferParamsSmall small;
+    xfer_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(params_for(x, small));
+  } else {
+    xfer_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(*x.params);
+  }
   return cudaGetLastError();
 }
 
 template <int LAYOUT>
 cudaError_t launch_layout(const XferLaunch &x) {
   if (x.bidir) {
-    bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, static_cast<cudaStream_t>(x.stream)>>>(*x.params);
+    const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+    if (x.words <= kBlobWordsSmall) {
+      XferParamsSmall small;
+      bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small));
+    } else {
+      bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params);
+    }
     return cudaGetLastError();
   }
   if (x.all_layers)
