@@ -21,8 +21,9 @@ import numpy as np
 LAYER_FIRST = 0
 PAGE_FIRST = 1
 PAGE_FIRST_DIRECT = 2
+PAGE_FIRST_DIRECT_KV = 3
 LAYOUTS = {"layer_first": LAYER_FIRST, "page_first": PAGE_FIRST,
-           "page_first_direct": PAGE_FIRST_DIRECT}
+           "page_first_direct": PAGE_FIRST_DIRECT, "page_first_direct_kv": PAGE_FIRST_DIRECT_KV}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "hicache_oracle.c")

@@ -39,7 +39,15 @@
  *    printed per-buffer dims (K sub-pool, then V sub-pool); MLA has B = 1;
  *  - the i-th device page pairs with the i-th host page; elements are copied as
  *    raw bytes (no dtype conversion, NaN payloads and signed zeros survive);
- *  - a load_layer call moves every buffer of that one layer.
+ *  - a load_layer call moves every buffer of that one layer;
+ *  - page_first_direct_kv (an L3-ready variant): dims (page_num, B, layer_num,
+ *    page_size, 1, kv_dim), so that ALL the KV of one page -- K and V, every
+ *    layer -- is one contiguous block that can go to L3 as a single object.
+ *    [B-L2] "L2 Layout Choice": L3 needs page-first, contiguous per page, for
+ *    large sequential I/O and zero-copy; "DMA Segment Explosion & Batched
+ *    Gather/Scatter": write-back gathers all layers into a contiguous page.
+ *    [H-DT] "배치 지향 데이터 구성": all KV of a page in contiguous memory,
+ *    handed to L3 as a single object without copies.
  *
  * Notation (matches the pages' dims):
  *   B  buffers (2 = K,V ; 1 = MLA latent)      L  layers (layer_num)
@@ -54,6 +62,7 @@
 #define ORACLE_LAYER_FIRST 0
 #define ORACLE_PAGE_FIRST 1
 #define ORACLE_PAGE_FIRST_DIRECT 2
+#define ORACLE_PAGE_FIRST_DIRECT_KV 3
 
 /* Offset, in elements, of element (b, l, h, t, e) inside the host pool.
  * Returns -1 for an unknown layout. */
@@ -61,7 +70,6 @@ int64_t oracle_host_elem_offset(int32_t layout, int64_t B, int64_t L, int64_t P,
                                 int64_t R, int64_t Hp, int64_t b, int64_t l,
                                 int64_t h, int64_t t, int64_t e) {
   const int64_t S = Hp * P;   /* "size": tokens in the host pool, per buffer */
-  (void)B;
   switch (layout) {
     case ORACLE_LAYER_FIRST:
       /* dims (B, layer, size, 1, kv_dim)                                  [T21] */
@@ -72,6 +80,9 @@ int64_t oracle_host_elem_offset(int32_t layout, int64_t B, int64_t L, int64_t P,
     case ORACLE_PAGE_FIRST_DIRECT:
       /* dims (B, page_num, layer_num, page_size, 1, kv_dim)               [T21] */
       return ((((b * Hp + h) * L + l) * P) + t) * R + e;
+    case ORACLE_PAGE_FIRST_DIRECT_KV:
+      /* dims (page_num, B, layer_num, page_size, 1, kv_dim)        [B-L2][H-DT] */
+      return ((((h * B + b) * L + l) * P) + t) * R + e;
     default:
       return -1;
   }
@@ -91,7 +102,7 @@ static void copy_elem(uint8_t *dst, const uint8_t *src, int64_t es) {
 static int check_dims(int64_t B, int64_t L, int64_t P, int64_t R, int64_t Hp,
                       int64_t es, int32_t layout) {
   if (B <= 0 || L <= 0 || P <= 0 || R <= 0 || Hp <= 0 || es <= 0) return -1;
-  if (layout < ORACLE_LAYER_FIRST || layout > ORACLE_PAGE_FIRST_DIRECT) return -1;
+  if (layout < ORACLE_LAYER_FIRST || layout > ORACLE_PAGE_FIRST_DIRECT_KV) return -1;
   return 0;
 }
 

@@ -159,6 +159,8 @@ def _numpy_layout(D, P, lay):
     if lay == "page_first":           # (B, size, layer, kv_dim)
         return D.transpose(0, 2, 1, 3).reshape(-1)
     Hp = S // P
+    if lay == "page_first_direct_kv":  # (page_num, B, layer_num, page_size, kv_dim)
+        return D.reshape(B, L, Hp, P, R).transpose(2, 0, 1, 3, 4).reshape(-1)
     # (B, page_num, layer_num, page_size, kv_dim)
     return D.reshape(B, L, Hp, P, R).transpose(0, 2, 1, 3, 4).reshape(-1)
 
@@ -276,9 +278,10 @@ def pin_segment_count_closed_forms(o):
                 hp = np.arange(n) * 1 + 2
             runs = _runs(dp, hp)
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["layer_first"]) == B * L * runs
-            # more than one layer: page_first_direct never merges two pages of a
+            # more than one layer: page_first_direct(_kv) never merges two pages of a
             # layer, page_first never merges two tokens of a layer
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["page_first_direct"]) == B * L * n
+            assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["page_first_direct_kv"]) == B * L * n
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["page_first"]) == B * L * n * P
             # one layer: page_first rows of one layer are L*R apart on the host
             assert o.segment_count(B, L, P, R, Hp, dp, hp, LAYOUT_IDS["page_first"], 1) == B * n * P
@@ -289,10 +292,13 @@ def pin_segment_count_closed_forms(o):
         for perm in ([0, 1, 2, 3], [2, 0, 3, 1], [3, 2, 1, 0]):
             assert o.segment_count(B, L, P, R, Hp, dp2[perm], hp2[perm], LAYOUT_IDS["layer_first"]) \
                 == B * L * _runs(dp2, hp2) == B * L * 3
-        # a single layer pool: every layout degenerates to layer_first's count
+        # a single layer pool: every layout but page_first_direct_kv degenerates to
+        # layer_first's count; page_first_direct_kv still interleaves the buffers
+        # inside each page, so only a one-buffer pool merges pages
         dp, hp = rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False)
-        for lay in LAYOUT_IDS.values():
-            assert o.segment_count(B, 1, P, R, Hp, dp, hp, lay) == B * _runs(dp, hp)
+        for name, lay in LAYOUT_IDS.items():
+            want = B * _runs(dp, hp) if (name != "page_first_direct_kv" or B == 1) else B * n
+            assert o.segment_count(B, 1, P, R, Hp, dp, hp, lay) == want, name
 
 
 ALL_PINS = [pin_hand_worked_backup, pin_hand_worked_load, pin_load_layer_touches_one_layer,

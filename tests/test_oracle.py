@@ -19,7 +19,8 @@ def test_golden_files_parse():
     cases = oracle_pins.parse_hand_worked()
     assert {c["name"] for c in cases} == {"swap", "kv_rows", "middle"}
     for c in cases:
-        assert set(c["layouts"]) == {"layer_first", "page_first", "page_first_direct"}
+        assert set(c["layouts"]) == {"layer_first", "page_first", "page_first_direct",
+                                     "page_first_direct_kv"}
     rows = oracle_pins.parse_segment_counts()
     assert {r["expected"] for r in rows} == {39936, 78}
 

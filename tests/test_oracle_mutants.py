@@ -21,6 +21,8 @@ MUTANTS = [
     ("pf_token_layer_swapped", "(((b * S) + h * P + t) * L + l) * R + e", "(((b * S) + h * P + l) * L + t) * R + e"),
     ("pf_buffer_stride_pages", "(((b * S) + h * P + t) * L + l) * R + e", "(((b * Hp) + h * P + t) * L + l) * R + e"),
     ("pfd_page_layer_swapped", "((((b * Hp + h) * L + l) * P) + t) * R + e", "((((b * L + l) * Hp + h) * P) + t) * R + e"),
+    ("pfd_kv_buffer_outside_page", "((((h * B + b) * L + l) * P) + t) * R + e", "((((b * Hp + h) * L + l) * P) + t) * R + e"),
+    ("pfd_kv_layer_buffer_swapped", "((((h * B + b) * L + l) * P) + t) * R + e", "((((h * L + l) * B + b) * P) + t) * R + e"),
     ("size_without_page_size", "const int64_t S = Hp * P;", "const int64_t S = Hp;"),
     ("dev_slot_transposed", "return (d * P + t) * R + e;", "return (t * P + d) * R + e;"),
     ("backup_buffer_index", "const uint8_t *src = (const uint8_t *)dev_bufs[b * L + l];",
