@@ -40,7 +40,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "L1↔L2 KV GB/s (load, backup, bidir) at 32K tokens; % of measured host-link peak"
-LAYOUT_NAMES = ["layer_first", "page_first", "page_first_direct"]
+LAYOUT_NAMES = ["layer_first", "page_first", "page_first_direct"]   # the pages' three layouts
+LAYOUT_IDS = {"layer_first": 0, "page_first": 1, "page_first_direct": 2, "page_first_direct_kv": 3}
 NOMINAL = {"pcie_gen5_x16_per_dir_gbs": 63.0, "nvlink_c2c_per_dir_gbs": 450.0}
 GB = 1e9
 
@@ -70,6 +71,24 @@ def recorded_traffic():
     if out.get("kernel_source_sha256_16") != kernel_fingerprint():
         return {}
     return out
+
+
+def max_over_ranks(seconds: float, world: int) -> float:
+    """The slowest rank's time: every rank replicates the same transfers on its
+    own GPU and host link, so the job ends when the last rank does."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: float, max_seconds: float, world: int) -> float:
+    """Bytes moved by all ranks / the slowest rank's time (weak scaling)."""
+    return world * bytes_per_rank / max_seconds / GB
 
 
 def frac(a, b, nd=3):
@@ -238,7 +257,7 @@ def run_step(torch, w, s1, s2, ev=None):
     """One step; if `ev` is a list, (name, start, end) event triples are appended."""
     pool, kv = w["pool"], w["kv"]
     for lay in LAYOUT_NAMES:
-        lid = {"layer_first": 0, "page_first": 1, "page_first_direct": 2}[lay]
+        lid = LAYOUT_IDS[lay]
 
         def mark():
             e = torch.cuda.Event(enable_timing=True)
@@ -266,35 +285,68 @@ def run_step(torch, w, s1, s2, ev=None):
                    (f"{lay}/bidir_fused", e3, e4)]
 
 
-def cpu_baseline(seconds_target=12.0, pages=24):
-    """The oracle (single-threaded C, as written) on a bounded sample of the
-    same workload: `pages` pages per transfer, each layout, backup and load."""
+def _oracle_rate(shape, pages, seconds, threads=1, layouts=(0, 1, 2)):
+    """GB/s of the oracle (single-threaded C, as written) doing backup + load of
+    `pages` pages of `shape` per layout, on host arrays.  With threads > 1 the
+    pairs are split into `threads` disjoint groups, each handled by one oracle
+    call on its own thread (ctypes drops the GIL during the call)."""
+    import threading
     import oracle
     from tiered_kv_cache_gb300 import workloads as wl
-    s = wl.LLAMA3_8B
     o = oracle.Oracle()
     rng = np.random.default_rng(0)
     Dp = Hp = pages * 2
-    B, L, P, R = s.num_buffers, s.num_layers, s.page_size, s.row_elems
+    B, L, P, R = shape.num_buffers, shape.num_layers, shape.page_size, shape.row_elems
     dev = [rng.integers(0, 65535, (Dp * P, R), dtype=np.uint16) for _ in range(B * L)]
     host = np.zeros(B * L * Hp * P * R, np.uint16)
     dp = wl.fragmented_pages(rng, Dp, pages)
     hp = np.arange(pages)
-    moved = 0
+    groups = [(dp[k::threads], hp[k::threads]) for k in range(threads)]
+
+    def run(fn):
+        if threads == 1:
+            fn(dp, hp)
+            return
+        ts = [threading.Thread(target=fn, args=g) for g in groups]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+
+    moved, ops = 0, 0
     t0 = time.perf_counter()
-    ops = 0
     while True:
-        for lid in (0, 1, 2):
-            o.backup(dev, host, B, L, P, R, Hp, dp, hp, lid)
-            o.load(dev, host, B, L, P, R, Hp, dp, hp, lid)
-            moved += 2 * pages * s.page_bytes
+        for lid in layouts:
+            run(lambda d, h: o.backup(dev, host, B, L, P, R, Hp, d, h, lid))
+            run(lambda d, h: o.load(dev, host, B, L, P, R, Hp, d, h, lid))
+            moved += 2 * pages * shape.page_bytes
             ops += 2
         el = time.perf_counter() - t0
-        if el >= seconds_target or ops >= 60:
+        if el >= seconds or ops >= 60:
             break
-    return {"value": moved / el / GB, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return moved / el / GB, ops, el
+
+
+def cpu_baseline(seconds_target=10.0, pages=24):
+    """The oracle on the host cores, on bounded samples of the workloads: the
+    headline is one core on the Llama-3-8B shape; the deep-78 and MLA shapes
+    and an all-cores run of the same loop split over the pairs are reported
+    beside it."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B
+    v, ops, el = _oracle_rate(s, pages, seconds_target)
+    ncores = os.cpu_count() or 1
+    va, opsa, ela = _oracle_rate(s, 8 * ncores, 4.0, threads=ncores)
+    vd, _, eld = _oracle_rate(wl.DEEP_STRESS, 8, 3.0)
+    vm, _, elm = _oracle_rate(wl.MLA_LATENT, 32, 3.0, layouts=(1,))
+    return {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{ops} transfers of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB each) of the "
-                      f"same shape, backup+load in all three layouts, host arrays, {el:.1f} s"}
+                      f"llama3_8b shape, backup+load in all three layouts, host arrays, {el:.1f} s",
+            "all_cores": {"value": round(va, 2), "cores": ncores,
+                          "sample": f"{opsa} transfers of {8 * ncores} pages split over {ncores} threads, "
+                                    f"{ela:.1f} s"},
+            "deep78_1core": {"value": round(vd, 3), "sample": f"8-page transfers, all layouts, {eld:.1f} s"},
+            "mla61_1core": {"value": round(vm, 3), "sample": f"32-page transfers, page_first, {elm:.1f} s"}}
 
 
 def reference_arm(args):
@@ -364,6 +416,7 @@ def bench_mla_overlap(torch, hc, args):
         # prio -1: the transfer stream outranks the compute stream, so the block
         # scheduler places the transfer's CTAs first as compute CTAs retire
         xfer = torch.cuda.Stream(priority=prio)
+        xfer2 = torch.cuda.Stream(priority=prio)
         comp = torch.cuda.Stream()
         t = wl.mla_transfer(s, tokens)
         n = len(t.device_pages)
@@ -380,10 +433,12 @@ def bench_mla_overlap(torch, hc, args):
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(xfer)
                 comp.wait_event(e0)
+                xfer2.wait_event(e0)
                 fn()
-                j = torch.cuda.Event()
-                j.record(comp)
-                xfer.wait_event(j)
+                for other in (comp, xfer2):
+                    j = torch.cuda.Event()
+                    j.record(other)
+                    xfer.wait_event(j)
                 e1.record(xfer)
                 torch.cuda.synchronize()
                 best.append(_elapsed(torch, e0, e1))
@@ -392,6 +447,19 @@ def bench_mla_overlap(torch, hc, args):
         def loads():
             for layer in range(L):
                 plan.execute(kv, layer=layer, stream=xfer)
+
+        def loads_two_streams():
+            # consecutive layers on alternating streams: the start of layer l+1
+            # overlaps the tail of layer l
+            for layer in range(L):
+                plan.execute(kv, layer=layer, stream=xfer if layer % 2 == 0 else xfer2)
+
+        def overlapped_two_streams(reps):
+            for layer in range(L):
+                plan.execute(kv, layer=layer, stream=xfer if layer % 2 == 0 else xfer2)
+                pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
 
         def one_load():
             plan.execute(kv, layer=-1, stream=xfer)
@@ -414,6 +482,8 @@ def bench_mla_overlap(torch, hc, args):
         reps = max(1, int(round(a / c1)))          # stand-in attention about as long as the loads
         b = timed(lambda: computes(reps))
         c = timed(lambda: overlapped(reps))
+        a2 = timed(loads_two_streams)
+        c2 = timed(lambda: overlapped_two_streams(reps))
         out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
             "pages": n, "bytes": nbytes,
             "per_layer_loads_ms": round(a * 1e3, 3), "per_layer_load_gbs": round(nbytes / a / GB, 1),
@@ -421,6 +491,10 @@ def bench_mla_overlap(torch, hc, args):
             "compute_ms": round(b * 1e3, 3), "compute_reps": reps,
             "overlapped_ms": round(c * 1e3, 3),
             "overlap_efficiency": round((a + b - c) / min(a, b), 3),
+            "per_layer_loads_2streams_ms": round(a2 * 1e3, 3),
+            "per_layer_load_2streams_gbs": round(nbytes / a2 / GB, 1),
+            "overlapped_2streams_ms": round(c2 * 1e3, 3),
+            "overlap_efficiency_2streams": round((a2 + b - c2) / min(a2, b), 3),
         }
         plan.close()
     launches = hc.launch_count() - launches0
@@ -511,7 +585,12 @@ def main():
                     choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
+    ap.add_argument("--layouts", default="pages",
+                    help="'pages' (layer_first, page_first, page_first_direct) or 'all' (adds "
+                         "page_first_direct_kv)")
     args = ap.parse_args()
+    if args.layouts == "all":
+        LAYOUT_NAMES.append("page_first_direct_kv")
     if args.impl == "reference":
         return reference_arm(args)
 
@@ -582,15 +661,11 @@ def main():
     barrier()
     launches = hc.launch_count() - launches0
     clk = clocks.stop()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, world)
     bpx = w["bytes_per_xfer"]
     step_bytes = len(LAYOUT_NAMES) * 6 * bpx
     npages = w["pages"]
-    value = world * args.steps * step_bytes / elapsed / GB
+    value = whole_job_gbs(args.steps * step_bytes, elapsed, world)
 
     per = {}
     for name, a, b in ev:
@@ -660,7 +735,7 @@ def main():
                    if args.workload == "llama3_8b_32k" else
                    (f"deep78_{npages * 64 // 1024}k: 78 layers, K+V, 8 kv heads x 128, bf16, page 64, "
                     f"{npages} pages per transfer, fully scattered device pages, contiguous host pages"),
-                   "step": "per layout (layer_first, page_first, page_first_direct): backup, load, "
+                   "step": f"per layout ({', '.join(LAYOUT_NAMES)}): backup, load, "
                            "concurrent backup+load of two requests on two streams, and the same pair "
                            f"as one fused launch; {step_bytes / 2**30:.0f} GiB per step",
                    "l2": f"inputs larger than L2 ({bpx / 2**20:.0f} MiB per transfer)",

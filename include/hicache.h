@@ -25,6 +25,12 @@
  *   HICACHE_LAYER_FIRST        (B, layer, size, kv_dim)               [Tuning ... 2.1]
  *   HICACHE_PAGE_FIRST         (B, size, layer, kv_dim)               [HiCache 설계, 데이터 전송 최적화]
  *   HICACHE_PAGE_FIRST_DIRECT  (B, page_num, layer_num, page_size, kv_dim) [Tuning ... 2.1]
+ * and one L3-ready variant without the leading buffer dim:
+ *   HICACHE_PAGE_FIRST_DIRECT_KV (page_num, B, layer_num, page_size, kv_dim): all KV of
+ *   a page -- K and V, every layer -- in one block, the single object per page that
+ *   L3 wants ("Baidu's KVCache Overhaul", sections "L2 Layout Choice" and "DMA
+ *   Segment Explosion & Batched Gather/Scatter"; "HiCache 시스템 설계와 최적화",
+ *   section "데이터 전송 최적화": a page's KV contiguous and handed to L3 zero-copy)
  * where size = host_num_pages * page_size.  Indices are page indices (int64);
  * the i-th device page pairs with the i-th host page.  Bytes are copied as-is:
  * no dtype conversion, elem_bytes only sizes the rows.
@@ -71,7 +77,8 @@ typedef enum {
   HICACHE_LAYOUT_POOL = -1,         /* the pool's own layout (desc.layout) */
   HICACHE_LAYER_FIRST = 0,
   HICACHE_PAGE_FIRST = 1,
-  HICACHE_PAGE_FIRST_DIRECT = 2
+  HICACHE_PAGE_FIRST_DIRECT = 2,
+  HICACHE_PAGE_FIRST_DIRECT_KV = 3  /* page_first_direct with the buffer dim inside the page */
 } hicache_layout;
 
 typedef enum {
@@ -243,6 +250,17 @@ int hicache_prepass(int64_t host_num_pages, int64_t device_num_pages, const int6
 int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *device_pages,
                               const int64_t *host_pages, int64_t n, int32_t layout,
                               int32_t layer_id);
+
+/* Byte range of one host page inside the host pool, for handing a page to L3
+ * storage without a copy (the pages' zero-copy L2 -> L3 path: "HiCache 시스템 설계와
+ * 최적화", section "데이터 전송 최적화" -- memory address and size passed directly).
+ * page_first / page_first_direct: the page of buffer `buffer` (0..B-1; -1 allowed
+ * when B == 1).  page_first_direct_kv: buffer -1 = the whole page, every buffer;
+ * 0..B-1 = that buffer's part.  layer_first keeps a page in L separate spans
+ * (INVALID_ARG), unless the pool has one layer.  Host-only: no CUDA call.
+ * Errors: INVALID_ARG, INDEX_RANGE. */
+int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t buffer,
+                      int64_t *offset_bytes, int64_t *nbytes);
 
 /* ---- measurement helper ------------------------------------------------------ */
 

@@ -199,3 +199,34 @@ def test_validation_before_any_cuda_call():
     assert hc.library().hicache_pool_create(ctypes.byref(d), 4096, 1024, ctypes.byref(h)) == -1
     assert "below" in hc.library().hicache_last_error().decode()
     assert hc.library().hicache_pool_create(ctypes.byref(d), 4104, 1 << 20, ctypes.byref(h)) == -4
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 4, 8, 5), (1, 4, 2, 16, 3), (3, 1, 2, 8, 4), (1, 1, 3, 8, 4)])
+def test_page_span_is_exactly_the_page(shape):
+    """A page span holds every element of that host page (and buffer) and
+    nothing else, by the oracle's element offsets."""
+    import oracle
+    o = oracle.Oracle()
+    B, L, P, R, Hp = shape
+    es = 2
+    for name, lid in hc.LAYOUTS.items():
+        d = hc._desc(L, B, P, R, Hp, lid, es)
+        for h in range(Hp):
+            for buf in [-1] + list(range(B)):
+                bufs = range(B) if buf < 0 else [buf]
+                offs = sorted(o.host_offset(lid, B, L, P, R, Hp, b, l, h, t, e) * es
+                              for b in bufs for l in range(L) for t in range(P) for e in range(R))
+                contiguous = offs == list(range(offs[0], offs[0] + es * len(offs), es))
+                try:
+                    off, nb = hc.page_span(d, h, buf)
+                except hc.HiCacheError as err:
+                    assert err.status == "INVALID_ARG"
+                    # refused only where the page (buffer) is not one contiguous span, or
+                    # where a single-buffer-only form was asked for several buffers
+                    assert not contiguous or (buf < 0 and B > 1), (name, h, buf)
+                    continue
+                assert contiguous, (name, h, buf)
+                assert (off, nb) == (offs[0], es * len(offs)), (name, h, buf)
+    with pytest.raises(hc.HiCacheError) as e:
+        hc.page_span(hc._desc(2, 2, 4, 8, 5, "page_first"), 5, 0)
+    assert e.value.status == "INDEX_RANGE"

@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
-    "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum",
+    "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
 
@@ -29,8 +29,9 @@ LAYOUT_POOL = -1
 LAYER_FIRST = 0
 PAGE_FIRST = 1
 PAGE_FIRST_DIRECT = 2
+PAGE_FIRST_DIRECT_KV = 3
 LAYOUTS = {"layer_first": LAYER_FIRST, "page_first": PAGE_FIRST,
-           "page_first_direct": PAGE_FIRST_DIRECT}
+           "page_first_direct": PAGE_FIRST_DIRECT, "page_first_direct_kv": PAGE_FIRST_DIRECT_KV}
 BACKUP = 0
 LOAD = 1
 HOST_THP = 0x1
@@ -93,6 +94,7 @@ def _bind(lib):
         "hicache_wait": (ctypes.c_int, [_vp, _i64]),
         "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
         "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
+        "hicache_page_span": (ctypes.c_int, [_P(PoolDesc), _i64, _i32, _P(_i64), _P(_i64)]),
         "hicache_layer_checksum": (ctypes.c_int, [_P(_DeviceKVStruct), _P(PoolDesc), _vp, _i64, _i32,
                                                   _i32, _vp, _vp]),
     }
@@ -212,6 +214,14 @@ def segment_count(num_layers, num_buffers, page_size, row_elems, host_num_pages,
     return int(r)
 
 
+def page_span(desc: PoolDesc, host_page: int, buffer: int = -1):
+    """(offset, nbytes) of one host page's contiguous span in the host pool."""
+    off, nb = ctypes.c_int64(), ctypes.c_int64()
+    _check(library().hicache_page_span(ctypes.byref(desc), host_page, buffer, ctypes.byref(off),
+                                       ctypes.byref(nb)))
+    return off.value, nb.value
+
+
 def layer_checksum(kv: DeviceKV, pool_or_desc, device_pages, layer: int, out_ptr: int,
                    reps: int = 1, stream=None):
     """Stand-in attention: adds the 32-bit words of `layer` of the given device
@@ -303,6 +313,14 @@ class Pool:
             layout = LAYOUTS[layout]
         _check(library().hicache_backup_load(self.handle, ctypes.byref(kv.struct), _ptr(bd), _ptr(bh), bd.size,
                                              _ptr(ld), _ptr(lh), ld.size, layout, _stream(stream)))
+
+    def page_span(self, host_page: int, buffer: int = -1):
+        return page_span(self.desc, host_page, buffer)
+
+    def page_view(self, host_page: int, buffer: int = -1) -> np.ndarray:
+        """The bytes of one host page (no copy), ready for an L3 write."""
+        off, nb = self.page_span(host_page, buffer)
+        return self.host_array(np.uint8)[off:off + nb]
 
     def wait_layer(self, layer: int, compute_stream=None):
         _check(library().hicache_wait_layer(self.handle, layer, _stream(compute_stream)))

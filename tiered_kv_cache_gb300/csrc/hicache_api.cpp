@@ -59,7 +59,7 @@ std::unordered_map<void *, HostAlloc> g_allocs;
 // ---- shape checks ------------------------------------------------------------
 struct Shape {
   int64_t L, B, P, R, es, Hp;
-  int64_t row_bytes, V, PV, LPV;
+  int64_t row_bytes, V, PV, LPV, BLPV;
   int32_t layout;
 };
 
@@ -75,7 +75,7 @@ int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
   if (int64_t(d->num_layers) * d->num_buffers > hicache::kMaxBufs)
     return set_error(HICACHE_ERR_INVALID_ARG, "num_buffers * num_layers = %lld exceeds %d",
                      (long long)d->num_layers * d->num_buffers, hicache::kMaxBufs);
-  if (d->layout < HICACHE_LAYER_FIRST || d->layout > HICACHE_PAGE_FIRST_DIRECT)
+  if (d->layout < HICACHE_LAYER_FIRST || d->layout > HICACHE_PAGE_FIRST_DIRECT_KV)
     return set_error(HICACHE_ERR_INVALID_ARG, "unknown pool layout %d", d->layout);
   if (d->launch_ctas < 0 || d->flags != 0 || d->reserved != 0)
     return set_error(HICACHE_ERR_INVALID_ARG, "launch_ctas must be >= 0; flags and reserved must be 0");
@@ -94,21 +94,22 @@ int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
   s->V = s->row_bytes / 16;
   s->PV = s->P * s->V;
   s->LPV = s->L * s->PV;
+  s->BLPV = s->B * s->LPV;
   if (need_alignment) {
     if (s->row_bytes % 16 != 0)
       return set_error(HICACHE_ERR_ALIGNMENT, "row of %lld bytes is not a multiple of 16",
                        (long long)s->row_bytes);
-    if (s->LPV >= INT32_MAX)
+    if (s->BLPV >= INT32_MAX)
       return set_error(HICACHE_ERR_INVALID_ARG,
-                       "one page of every layer (%lld x 16 bytes) must be < 32 GiB",
-                       (long long)s->LPV);
+                       "one page of every buffer and layer (%lld x 16 bytes) must be < 32 GiB",
+                       (long long)s->BLPV);
   }
   return HICACHE_OK;
 }
 
 int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out) {
   if (layout == HICACHE_LAYOUT_POOL) layout = pool_layout;
-  if (layout < HICACHE_LAYER_FIRST || layout > HICACHE_PAGE_FIRST_DIRECT)
+  if (layout < HICACHE_LAYER_FIRST || layout > HICACHE_PAGE_FIRST_DIRECT_KV)
     return set_error(HICACHE_ERR_INVALID_ARG, "unknown layout %d", layout);
   *out = layout;
   return HICACHE_OK;
@@ -188,7 +189,9 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
 
 constexpr int64_t kMaxTiles = int64_t(1) << 30;
 
-int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX - 1) / s.LPV); }
+// Runs are capped so that a unit (at most every buffer and layer of a run)
+// stays below 2^31 vectors: the kernels index units with 32-bit offsets.
+int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX - 1) / s.BLPV); }
 
 }  // namespace
 
@@ -273,9 +276,12 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   const Shape &s = pool->shape;
   const bool all = layer < 0;
   const int32_t nb = int32_t(s.B * s.L);
+  // units: (buffer, layer, run) for layer_first with every layer; (run) for
+  // page_first_direct_kv with every layer; (buffer, run) otherwise
   const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
-  const int64_t outers = lf_all ? s.B * s.L : s.B;
-  const int64_t upp = (all && layout != HICACHE_LAYER_FIRST) ? s.LPV : s.PV;
+  const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
+  const int64_t outers = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
+  const int64_t upp = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
   const int64_t capacity = (hicache::kBlobWords - nb) / 2;  // runs per launch
 
   thread_local hicache::XferParams params;
@@ -285,12 +291,15 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   h.P = int32_t(s.P);
   h.V = int32_t(s.V);
   h.num_bufs = nb;
+  h.B = int32_t(s.B);
   h.layer = all ? 0 : layer;
   h.Hp = int32_t(s.Hp);
   h.unit_per_page = uint32_t(upp);
   h.PV = uint32_t(s.PV);
   h.LV = uint32_t(s.L * s.V);
   h.LPV = uint32_t(s.LPV);
+  h.BLPV = uint32_t(s.BLPV);
+  h.fd_BLPV = hicache::make_fastdiv(uint32_t(s.BLPV));
   h.fd_V = hicache::make_fastdiv(uint32_t(s.V));
   h.fd_PV = hicache::make_fastdiv(uint32_t(s.PV));
   h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
@@ -719,12 +728,57 @@ int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *devi
     if (!cont) ++nruns;
   }
   const int64_t layers = layer_id < 0 ? s.L : 1;
-  // with one layer in the pool, every layout stores a buffer's pages back to back
-  if (lay == HICACHE_LAYER_FIRST || s.L == 1) return s.B * layers * nruns;
+  // with one layer in the pool, every layout stores a buffer's pages back to
+  // back, except page_first_direct_kv, which interleaves the buffers of a page
+  if (lay == HICACHE_LAYER_FIRST || (s.L == 1 && (lay != HICACHE_PAGE_FIRST_DIRECT_KV || s.B == 1)))
+    return s.B * layers * nruns;
   // one segment per (buffer, layer, page): the same layer of the next page is
-  // L*P rows further on the host
-  if (lay == HICACHE_PAGE_FIRST_DIRECT) return s.B * layers * n;
+  // (buffers x) L*P rows further on the host
+  if (lay == HICACHE_PAGE_FIRST_DIRECT || lay == HICACHE_PAGE_FIRST_DIRECT_KV) return s.B * layers * n;
   return s.B * layers * n * s.P;  // page_first: one row per (buffer, layer, token)
+}
+
+int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t buffer,
+                      int64_t *offset_bytes, int64_t *nbytes) {
+  g_last_error.clear();
+  Shape s{};
+  int rc = check_desc(desc, &s, false);
+  if (rc) return rc;
+  if (!offset_bytes || !nbytes) return set_error(HICACHE_ERR_INVALID_ARG, "output pointer is NULL");
+  if (host_page < 0 || host_page >= s.Hp)
+    return set_error(HICACHE_ERR_INDEX_RANGE, "host page %lld outside [0, %lld)", (long long)host_page,
+                     (long long)s.Hp);
+  if (buffer < -1 || buffer >= s.B)
+    return set_error(HICACHE_ERR_INVALID_ARG, "buffer %d outside [-1, %lld)", buffer, (long long)s.B);
+  const int64_t page_buf_bytes = s.L * s.P * s.R * s.es;  // one buffer's share of a page
+  switch (s.layout) {
+    case HICACHE_PAGE_FIRST:
+    case HICACHE_PAGE_FIRST_DIRECT:
+      if (buffer < 0 && s.B > 1)
+        return set_error(HICACHE_ERR_INVALID_ARG,
+                         "with %lld buffers a page is one span per buffer: name the buffer",
+                         (long long)s.B);
+      *offset_bytes = ((buffer < 0 ? 0 : buffer) * s.Hp + host_page) * page_buf_bytes;
+      *nbytes = page_buf_bytes;
+      return HICACHE_OK;
+    case HICACHE_PAGE_FIRST_DIRECT_KV:
+      if (buffer < 0) {
+        *offset_bytes = host_page * s.B * page_buf_bytes;
+        *nbytes = s.B * page_buf_bytes;
+      } else {
+        *offset_bytes = (host_page * s.B + buffer) * page_buf_bytes;
+        *nbytes = page_buf_bytes;
+      }
+      return HICACHE_OK;
+    default:
+      if (s.L == 1 && (buffer >= 0 || s.B == 1)) {
+        *offset_bytes = ((buffer < 0 ? 0 : buffer) * s.Hp + host_page) * page_buf_bytes;
+        *nbytes = page_buf_bytes;
+        return HICACHE_OK;
+      }
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "a layer_first page is one span per layer, not one contiguous span");
+  }
 }
 
 int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc *desc,

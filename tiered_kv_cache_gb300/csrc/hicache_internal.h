@@ -75,7 +75,7 @@ struct RunRec {
   int64_t len;
 };
 
-enum Layout : int32_t { kLayerFirst = 0, kPageFirst = 1, kPageFirstDirect = 2 };
+enum Layout : int32_t { kLayerFirst = 0, kPageFirst = 1, kPageFirstDirect = 2, kPageFirstDirectKV = 3 };
 
 // One direction of a launch: its run table and tile counts.
 struct Job {
@@ -89,11 +89,12 @@ struct Job {
 struct XferHeader {
   void *host;                 // device-visible alias of the host pool
   int32_t L, P, V, num_bufs;  // layers, page size, vectors per row, B*L
+  int32_t B;                  // buffers
   int32_t layer;              // the layer of a single-layer transfer
   int32_t Hp;                 // host pool pages
   uint32_t unit_per_page;     // vectors one page contributes to a unit
-  uint32_t PV, LV, LPV;       // P*V, L*V, L*P*V
-  FastDiv fd_V, fd_PV, fd_LV, fd_LPV;
+  uint32_t PV, LV, LPV, BLPV; // P*V, L*V, L*P*V, B*L*P*V
+  FastDiv fd_V, fd_PV, fd_LV, fd_LPV, fd_BLPV;
   Job job[2];                 // [0]: the transfer (the backup of a bidirectional
                               // launch); [1]: the load of a bidirectional launch
 };

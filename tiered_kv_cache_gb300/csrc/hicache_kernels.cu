@@ -18,6 +18,8 @@
 //       page_first(_direct), all layers   unit = (buffer, run): all layers of
 //                                         the run's pages are one host range
 //       page_first(_direct), one layer    unit = (buffer, run), host strided
+//       page_first_direct_kv, all layers  unit = run: every buffer and layer of
+//                                         the run's pages is one host range
 //     and every unit into tiles of 16 KiB (1024 vectors of 16 bytes).  CTAs
 //     take tiles in host-address order (grid-stride), so the host link sees
 //     long sequential streams of whole 128-byte lines in every layout.
@@ -69,12 +71,29 @@ __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bu
     const uint32_t v = rem - ll * h.V;
     dev = bufs[b * h.L + ll] + (int64_t(r.d0) * h.P + tok) * h.V + v;
     host = hbase + (int64_t(b) * h.Hp + r.h0) * h.P * h.LV + w;
+  } else if (LAYOUT == kPageFirstDirectKV && ALL) {
+    // host (Hp, B, L, P, R): the unit is the whole run, every buffer:
+    // [page j][buffer bb][layer ll][token, elem]
+    const uint32_t j = fast_div(w, h.fd_BLPV);
+    uint32_t rem = w - j * h.BLPV;
+    const uint32_t bb = fast_div(rem, h.fd_LPV);
+    rem -= bb * h.LPV;
+    const uint32_t ll = fast_div(rem, h.fd_PV);
+    const uint32_t q = rem - ll * h.PV;
+    dev = bufs[bb * h.L + ll] + int64_t(r.d0 + int32_t(j)) * h.PV + q;
+    host = hbase + int64_t(r.h0) * h.BLPV + w;
   } else if (LAYOUT == kPageFirstDirect) {
     // one layer: device contiguous over the run, host one P*R block per page
     const uint32_t j = fast_div(w, h.fd_PV);
     const uint32_t q = w - j * h.PV;
     dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
     host = hbase + ((int64_t(b) * h.Hp + r.h0 + j) * h.L + l) * h.PV + q;
+  } else if (LAYOUT == kPageFirstDirectKV) {
+    // one layer: device contiguous over the run, host one P*R block per page
+    const uint32_t j = fast_div(w, h.fd_PV);
+    const uint32_t q = w - j * h.PV;
+    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
+    host = hbase + ((int64_t(r.h0 + int32_t(j)) * h.B + b) * h.L + l) * h.PV + q;
   } else {
     // page_first, one layer: device contiguous over the run, host one row per token
     const uint32_t tok = fast_div(w, h.fd_V);
@@ -247,6 +266,7 @@ int launch_xfer(const XferLaunch &x) {
     case kLayerFirst: return int(launch_layout<kLayerFirst>(x));
     case kPageFirst: return int(launch_layout<kPageFirst>(x));
     case kPageFirstDirect: return int(launch_layout<kPageFirstDirect>(x));
+    case kPageFirstDirectKV: return int(launch_layout<kPageFirstDirectKV>(x));
     default: return int(cudaErrorInvalidValue);
   }
 }
