@@ -569,6 +569,54 @@ def bench_small_mix(torch, hc, args):
     return out
 
 
+def bench_host_alloc(torch, hc, args):
+    """Host pool allocation, plain cudaHostAlloc vs mmap + MADV_HUGEPAGE +
+    cudaHostRegister, at two pool sizes: time to allocate and pin, and the
+    backup / load rate of 512 Llama-3-8B pages whose host pages are scattered
+    over the whole pool (the case where host address translation is stressed)."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B
+    vals = [v.view(torch.int16) for v in wl.kv_values(s, device="cuda")]
+    kv = hc.DeviceKV(vals, s.device_pages)
+    st = torch.cuda.Stream()
+    rng = np.random.default_rng(9)
+    dp = wl.fragmented_pages(rng, s.device_pages, 512)
+    out = {}
+    for gib in (16, 64):
+        hp_pages = gib * 2**30 // s.page_bytes
+        hp = np.sort(rng.choice(hp_pages, 512, replace=False))
+        for thp in (False, True):
+            t0 = time.perf_counter()
+            mem = hc.PinnedHost(hp_pages * s.page_bytes, thp=thp)
+            t_alloc = time.perf_counter() - t0
+            pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, hp_pages, "layer_first",
+                           host_ptr=mem.ptr, host_bytes=mem.nbytes, launch_ctas=args.ctas)
+            rates = {}
+            for name, fn in (("backup", pool.backup), ("load", pool.load)):
+                for lay in (0, 2):
+                    for _ in range(2):
+                        fn(kv, dp, hp, lay, stream=st)
+                    ts = []
+                    for _ in range(max(3, args.steps)):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(st)
+                        fn(kv, dp, hp, lay, stream=st)
+                        e1.record(st)
+                        st.synchronize()
+                        ts.append(_elapsed(torch, e0, e1))
+                    rates[f"{name}_{'lf' if lay == 0 else 'pfd'}_gbs"] = round(
+                        512 * s.page_bytes / statistics.median(ts) / GB, 1)
+            pool.close()
+            t0 = time.perf_counter()
+            mem.free()
+            t_free = time.perf_counter() - t0
+            out[f"{gib}GiB_{'thp_mmap_register' if thp else 'cudaHostAlloc'}"] = {
+                "alloc_pin_s": round(t_alloc, 2), "alloc_pin_gbs": round(gib * 2**30 / t_alloc / GB, 1),
+                "free_s": round(t_free, 2), **rates}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -582,7 +630,7 @@ def main():
     ap.add_argument("--no-link-probe", action="store_true",
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
-                    choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix"],
+                    choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
     ap.add_argument("--layouts", default="pages",
@@ -610,9 +658,16 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch)
-    if args.workload in ("mla61_overlap", "small_mix"):
+    if args.workload in ("mla61_overlap", "small_mix", "host_alloc"):
         t0 = time.perf_counter()
-        if args.workload == "mla61_overlap":
+        if args.workload == "host_alloc":
+            res = bench_host_alloc(torch, hc, args)
+            launches = None
+            value = res["64GiB_cudaHostAlloc"]["load_lf_gbs"]
+            what = {"workload": "host pool allocation: cudaHostAlloc vs mmap+MADV_HUGEPAGE+cudaHostRegister, "
+                                "16 and 64 GiB pools; 512 Llama-3-8B pages scattered over the pool",
+                    "value": "load GB/s, layer_first, 64 GiB cudaHostAlloc pool"}
+        elif args.workload == "mla61_overlap":
             res, launches = bench_mla_overlap(torch, hc, args)
             value = res["64k"]["per_layer_load_gbs"]
             what = {"workload": "mla61: 61 layers, one latent buffer, kv_dim 576, bf16, page 64, "

@@ -262,6 +262,26 @@ int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *devi
 int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t buffer,
                       int64_t *offset_bytes, int64_t *nbytes);
 
+/* ---- host-page allocator (LIFO free list of page runs) ------------------------
+ * Hands out host pages of an L2 pool.  "Tuning ... section 2.4" and "Baidu's
+ * KVCache Overhaul", section "LIFO slot allocation": the most recently freed
+ * pages are handed out first, so writes stay on a small set of hot pages.  The
+ * free list is a stack of runs; alloc takes pages from the front of the top
+ * runs (ascending, as few runs as possible); free pushes the freed pages,
+ * merged into runs, on top.  Host-only, thread-safe.  Every error leaves the
+ * allocator unchanged. */
+typedef struct hicache_page_allocator hicache_page_allocator; /* opaque */
+/* num_pages in [1, 2^31).  Errors: INVALID_ARG, NOMEM. */
+int hicache_allocator_create(int64_t num_pages, hicache_page_allocator **out);
+int hicache_allocator_destroy(hicache_page_allocator *alloc);
+/* Writes n page indices to pages_out.  NOMEM if fewer than n pages are free. */
+int hicache_allocator_alloc(hicache_page_allocator *alloc, int64_t n, int64_t *pages_out);
+/* Returns n pages.  INDEX_RANGE for a page outside the pool, DUPLICATE_INDEX
+ * for a page named twice or not currently handed out. */
+int hicache_allocator_free(hicache_page_allocator *alloc, const int64_t *pages, int64_t n);
+/* Free pages, or a negative hicache_status. */
+int64_t hicache_allocator_available(hicache_page_allocator *alloc);
+
 /* ---- measurement helper ------------------------------------------------------ */
 
 /* A stand-in for attention on one layer: reads the given pages of every buffer

@@ -330,3 +330,53 @@ def test_backup_load_rejects_hazards():
             pool.backup_load(kv, [1, 2], [3, 3], [5, 6], [8, 9])
         assert e.value.status == "DUPLICATE_INDEX"
         assert hc.launch_count() == c0
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2], ids=["layer_first", "page_first", "page_first_direct"])
+def test_heterogeneous_buffer_sets_as_pools_in_one_allocation(layout):
+    """Buffers of different row sizes (an MLA latent of 576 bf16, an fp8
+    indexer key of 128 bytes, an fp32 scale row of 4 values): one pool per
+    buffer kind, carved out of a single pinned allocation.  With the buffer dim
+    outermost in these layouts, the sub-pools side by side are exactly the
+    mixed host pool; every sub-pool matches the oracle."""
+    L, P, Dp, Hp, n = 6, 16, 40, 48, 14
+    kinds = [(576, 2), (128, 1), (4, 4)]          # (row elements, element bytes)
+    sizes = [L * Hp * P * R * es for R, es in kinds]
+    total = sum(sizes)
+    mem = hc.PinnedHost(total)
+    rng = np.random.default_rng(50 + layout)
+    dp = wl.fragmented_pages(rng, Dp, n, max_run=3)
+    hp = rng.choice(Hp, n, replace=False)
+    off = 0
+    pools, bufsets = [], []
+    for (R, es), nbytes in zip(kinds, sizes):
+        pools.append(hc.Pool(L, 1, P, R, Hp, layout, elem_bytes=es, host_ptr=mem.ptr + off,
+                             host_bytes=nbytes))
+        bufsets.append(gh.random_device_bufs(1, L, P, R, Dp, es, seed=off % 97))
+        off += nbytes
+    s = torch.cuda.Stream()
+    for pool, bufs, (R, es) in zip(pools, bufsets, kinds):
+        pool.host_array(np.uint8)[:] = 0x3C
+        pool.backup(hc.DeviceKV(bufs, Dp), dp, hp, stream=s)
+    s.synchronize()
+    for pool, bufs, (R, es) in zip(pools, bufsets, kinds):
+        want = np.full(pool.nbytes, 0x3C, np.uint8).view(gh.NP_DT[es])
+        gh.orc().backup(gh.to_np(bufs, es), want, 1, L, P, R, Hp, dp, hp, layout)
+        assert np.array_equal(pool.host_array(gh.NP_DT[es]), want), (R, es)
+    # and back, per layer, into fresh device pages
+    dst = rng.permutation(Dp)[:n]
+    for pool, bufs, (R, es) in zip(pools, bufsets, kinds):
+        gh.sentinel_fill(bufs, 0x77)
+        for layer in range(L):
+            pool.load_layer(hc.DeviceKV(bufs, Dp), dst, hp, layer, stream=s)
+    s.synchronize()
+    for pool, bufs, (R, es) in zip(pools, bufsets, kinds):
+        want = [np.zeros((Dp * P, R), gh.NP_DT[es]) for _ in range(L)]
+        for w in want:
+            w.view(np.uint8)[:] = 0x77
+        gh.orc().load(want, pool.host_array(gh.NP_DT[es]), 1, L, P, R, Hp, dst, hp, layout)
+        got = gh.to_np(bufs, es)
+        for k in range(L):
+            assert np.array_equal(got[k], want[k]), (R, es, k)
+    for pool in pools:
+        pool.close()

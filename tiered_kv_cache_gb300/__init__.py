@@ -21,6 +21,7 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
+    "PageAllocator",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
@@ -95,6 +96,11 @@ def _bind(lib):
         "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
         "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
         "hicache_page_span": (ctypes.c_int, [_P(PoolDesc), _i64, _i32, _P(_i64), _P(_i64)]),
+        "hicache_allocator_create": (ctypes.c_int, [_i64, _P(_vp)]),
+        "hicache_allocator_destroy": (ctypes.c_int, [_vp]),
+        "hicache_allocator_alloc": (ctypes.c_int, [_vp, _i64, _vp]),
+        "hicache_allocator_free": (ctypes.c_int, [_vp, _vp, _i64]),
+        "hicache_allocator_available": (_i64, [_vp]),
         "hicache_layer_checksum": (ctypes.c_int, [_P(_DeviceKVStruct), _P(PoolDesc), _vp, _i64, _i32,
                                                   _i32, _vp, _vp]),
     }
@@ -344,6 +350,43 @@ class Pool:
 
     def __exit__(self, *exc):
         self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class PageAllocator:
+    """LIFO host-page allocator (hicache_allocator_*)."""
+
+    def __init__(self, num_pages: int):
+        h = ctypes.c_void_p()
+        _check(library().hicache_allocator_create(num_pages, ctypes.byref(h)))
+        self.handle = h.value
+        self.num_pages = num_pages
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.empty(n, np.int64)
+        _check(library().hicache_allocator_alloc(self.handle, n, _ptr(out)))
+        return out
+
+    def free(self, pages):
+        p = _idx(pages)
+        _check(library().hicache_allocator_free(self.handle, _ptr(p), p.size))
+
+    @property
+    def available(self) -> int:
+        r = library().hicache_allocator_available(self.handle)
+        if r < 0:
+            _check(int(r))
+        return int(r)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            library().hicache_allocator_destroy(self.handle)
+            self.handle = None
 
     def __del__(self):
         try:

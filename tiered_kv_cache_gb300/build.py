@@ -1,9 +1,10 @@
 """Build libhicache.so in-tree with nvcc for sm_103a (GB300).
 
-Two translation units, compiled in parallel, linked with the static CUDA
+Three translation units, compiled in parallel, linked with the static CUDA
 runtime so the library loads on a machine without a GPU driver:
   csrc/hicache_kernels.cu   transfer and stand-in compute kernels
   csrc/hicache_api.cpp      validation, pre-pass, pools, plans, events
+  csrc/hicache_alloc.cpp    LIFO host-page allocator
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["hicache_kernels.cu", "hicache_api.cpp"]
+SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_alloc.cpp"]
 
 
 def _nvcc() -> str:

@@ -195,6 +195,11 @@ int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX -
 
 }  // namespace
 
+int hicache::set_error_text(int code, const char *msg) {
+  g_last_error.clear();
+  return set_error(code, "%s", msg);
+}
+
 // ---- pool and plan objects -----------------------------------------------------
 struct hicache_pool {
   hicache_pool_desc desc;

@@ -134,6 +134,8 @@ struct XferLaunch {
   void *stream;
 };
 int launch_xfer(const XferLaunch &x);
+// Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).
+int set_error_text(int code, const char *msg);
 int launch_checksum(const ChecksumParams &p, int grid, void *stream);
 
 }  // namespace hicache
