@@ -151,6 +151,8 @@ int hicache_host_free(void *ptr);
  * NOT_PINNED, CUDA. */
 int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t host_bytes,
                         hicache_pool **out);
+/* Destroys the pool's events and the pool.  Transfers already enqueued still
+ * run; the host buffer must stay allocated until they finish. */
 int hicache_pool_destroy(hicache_pool *pool);
 
 /* ---- transfers -------------------------------------------------------------
@@ -203,7 +205,8 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
  * that the L per-layer loads of one request pay for validation and the pre-pass
  * once (the prepare-ahead idea of "Rethinking the SGLang HiCache Boundary",
  * section "PrepareBatch / ExecuteBatch").  device_num_pages bounds the device
- * indices.  A plan is immutable and may be executed from several threads. */
+ * indices.  A plan is immutable and may be executed from several threads; it
+ * refers to its pool, so it must be destroyed before the pool. */
 int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,
                         int64_t n, int64_t device_num_pages, int32_t direction,
                         hicache_plan **out);

@@ -380,3 +380,59 @@ def test_heterogeneous_buffer_sets_as_pools_in_one_allocation(layout):
             assert np.array_equal(got[k], want[k]), (R, es, k)
     for pool in pools:
         pool.close()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_more_runs_than_one_launch_holds(layout):
+    """4,000 scattered one-token pages are 4,000 runs: more than one launch's
+    parameter block takes, so the call is split into several launches; the
+    result must still equal the oracle, for one direction and for the fused
+    backup + load."""
+    B, L, P, R, Dp, Hp = 2, 3, 1, 8, 9000, 9000
+    rng = np.random.default_rng(60 + layout)
+    perm = rng.permutation(Dp)
+    hperm = rng.permutation(Hp)
+    n = 4000
+    dp, hp = perm[:n], hperm[:n]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=61)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        nruns = len(hc.prepass(Hp, Dp, dp, hp, hc.BACKUP))
+        assert nruns > 1536
+        c0 = hc.launch_count()
+        gh.check_backup(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2)
+        assert hc.launch_count() - c0 >= 2
+        gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2)
+        # fused, both directions over the launch capacity
+        a_dev, b_dev = perm[:n], perm[n:2 * n]
+        a_host, b_host = hperm[:n], hperm[n:2 * n]
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0 = host.copy()
+        dev0 = gh.to_np(bufs, 2)
+        c0 = hc.launch_count()
+        pool.backup_load(hc.DeviceKV(bufs, Dp), a_dev, a_host, b_dev, b_host)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 >= 3
+        want_host = host0.view(np.uint16).copy()
+        gh.orc().backup(dev0, want_host, B, L, P, R, Hp, a_dev, a_host, layout)
+        want_dev = [x.copy() for x in dev0]
+        gh.orc().load(want_dev, host0.view(np.uint16), B, L, P, R, Hp, b_dev, b_host, layout)
+        assert np.array_equal(host.view(np.uint16), want_host)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want_dev[k])
+
+
+def test_maximum_buffer_count():
+    """B * L = 512 device buffers, the most one call takes (a 256-layer K/V pool)."""
+    B, L, P, R, Dp, Hp, n = 2, 256, 2, 8, 12, 12, 7
+    rng = np.random.default_rng(70)
+    dp, hp = rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=70)
+    for layout in LAYOUTS:
+        with hc.Pool(L, B, P, R, Hp, layout) as pool:
+            gh.check_backup(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2)
+            gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2)
+            gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2, layer=L - 1)
+    with pytest.raises(hc.HiCacheError):
+        hc.Pool(257, 2, P, R, Hp, "layer_first")
