@@ -1,0 +1,116 @@
+/* A plain C caller of libhicache: a pool on huge-page pinned memory, a backup,
+ * per-layer loads into fresh device pages with a compute stream waiting on the
+ * layer events, a fused backup + load, and the error path.  Every element is
+ * checked against a position pattern (round trip = identity).  Prints "ok". */
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime_api.h>
+
+#include "hicache.h"
+
+#define CHECK(x)                                                                  \
+  do {                                                                            \
+    int rc_ = (x);                                                                \
+    if (rc_ != 0) {                                                               \
+      fprintf(stderr, "%s:%d: %s -> %d (%s)\n", __FILE__, __LINE__, #x, rc_,      \
+              hicache_last_error());                                              \
+      return 1;                                                                   \
+    }                                                                             \
+  } while (0)
+
+enum { L = 4, B = 2, P = 16, NB = B * L, N = 8 };
+static const int64_t R = 128, Hp = 40, Dp = 48;
+
+static uint16_t pattern(int k, int64_t row, int64_t e) {
+  return (uint16_t)(k * 7919 + row * 131 + e * 3 + 1);
+}
+
+int main(void) {
+  const size_t es = 2;
+  const size_t host_bytes = (size_t)(B * L * Hp * P * R) * es;
+  const size_t buf_bytes = (size_t)(Dp * P * R) * es;
+  hicache_pool_desc d;
+  memset(&d, 0, sizeof d);
+  d.num_layers = L;
+  d.num_buffers = B;
+  d.page_size = P;
+  d.elem_bytes = 2;
+  d.row_elems = R;
+  d.host_num_pages = Hp;
+  d.layout = HICACHE_PAGE_FIRST;
+  void *host = NULL;
+  CHECK(hicache_host_alloc(host_bytes, HICACHE_HOST_THP, &host));
+  hicache_pool *pool = NULL;
+  CHECK(hicache_pool_create(&d, host, host_bytes, &pool));
+
+  void *bufs[NB];
+  uint16_t *h = (uint16_t *)malloc(buf_bytes);
+  for (int k = 0; k < NB; ++k) {
+    if (cudaMalloc(&bufs[k], buf_bytes) != cudaSuccess) return 2;
+    for (int64_t row = 0; row < Dp * P; ++row)
+      for (int64_t e = 0; e < R; ++e) h[row * R + e] = pattern(k, row, e);
+    if (cudaMemcpy(bufs[k], h, buf_bytes, cudaMemcpyHostToDevice) != cudaSuccess) return 2;
+  }
+  hicache_device_kv kv = {bufs, Dp};
+  const int64_t src[N] = {3, 4, 5, 17, 30, 31, 9, 40};
+  const int64_t hp[N] = {0, 1, 2, 10, 11, 12, 39, 20};
+  const int64_t dst[N] = {41, 42, 43, 1, 2, 22, 23, 47};
+
+  cudaStream_t xfer, comp;
+  cudaStreamCreateWithFlags(&xfer, cudaStreamNonBlocking);
+  cudaStreamCreateWithFlags(&comp, cudaStreamNonBlocking);
+  CHECK(hicache_backup(pool, &kv, src, hp, N, HICACHE_LAYOUT_POOL, xfer));
+  for (int l = 0; l < L; ++l) {
+    CHECK(hicache_load_layer(pool, &kv, dst, hp, N, HICACHE_LAYOUT_POOL, l, xfer));
+    CHECK(hicache_wait_layer(pool, l, comp));
+  }
+  CHECK(hicache_wait(comp, -1));
+  CHECK(hicache_wait(xfer, 5 * 1000 * 1000));
+
+  for (int k = 0; k < NB; ++k) {
+    if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+    for (int i = 0; i < N; ++i)
+      for (int64_t t = 0; t < P; ++t)
+        for (int64_t e = 0; e < R; ++e) {
+          const uint16_t want = pattern(k, src[i] * P + t, e);
+          const uint16_t got = h[(dst[i] * P + t) * R + e];
+          if (got != want) {
+            fprintf(stderr, "buffer %d page %lld token %lld elem %lld: %u != %u\n", k,
+                    (long long)dst[i], (long long)t, (long long)e, got, want);
+            return 3;
+          }
+        }
+  }
+
+  /* fused: back up pages dst (now copies of src) to new host pages while
+   * loading host pages hp into other device pages */
+  const int64_t hp2[N] = {30, 31, 32, 33, 34, 35, 36, 37};
+  const int64_t dst2[N] = {10, 11, 12, 13, 14, 15, 16, 18};
+  CHECK(hicache_backup_load(pool, &kv, dst, hp2, N, dst2, hp, N, HICACHE_LAYOUT_POOL, xfer));
+  CHECK(hicache_wait(xfer, -1));
+  for (int k = 0; k < NB; ++k) {
+    if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+    for (int i = 0; i < N; ++i)
+      for (int64_t t = 0; t < P; ++t)
+        for (int64_t e = 0; e < R; ++e)
+          if (h[(dst2[i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 4;
+  }
+
+  /* errors enqueue nothing and explain themselves */
+  const int64_t bad[1] = {Dp};
+  const int64_t okh[1] = {0};
+  const int64_t before = hicache_launch_count();
+  if (hicache_load(pool, &kv, bad, okh, 1, HICACHE_LAYOUT_POOL, xfer) != HICACHE_ERR_INDEX_RANGE) return 5;
+  if (strlen(hicache_last_error()) == 0) return 5;
+  if (hicache_launch_count() != before) return 5;
+
+  CHECK(hicache_pool_destroy(pool));
+  CHECK(hicache_host_free(host));
+  for (int k = 0; k < NB; ++k) cudaFree(bufs[k]);
+  free(h);
+  printf("ok\n");
+  return 0;
+}

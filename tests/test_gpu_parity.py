@@ -436,3 +436,52 @@ def test_maximum_buffer_count():
             gh.check_load(pool, bufs, dp, hp, layout, B, L, P, R, Hp, 2, layer=L - 1)
     with pytest.raises(hc.HiCacheError):
         hc.Pool(257, 2, P, R, Hp, "layer_first")
+
+
+def test_backup_thread_and_load_thread_share_a_pool():
+    """A backup thread and a load thread (the pages' dedicated submitters), each
+    with its own stream, calling one pool at the same time; results equal the
+    oracle's for the same pairs."""
+    import threading
+    B, L, P, R, Dp, Hp = 2, 4, 16, 128, 128, 128
+    rng = np.random.default_rng(80)
+    perm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=80)
+    jobs_b = [(perm[i * 8:(i + 1) * 8], hperm[i * 8:(i + 1) * 8]) for i in range(6)]        # backups
+    jobs_l = [(perm[64 + i * 8:64 + (i + 1) * 8], hperm[64 + i * 8:64 + (i + 1) * 8]) for i in range(6)]
+    with hc.Pool(L, B, P, R, Hp, "page_first_direct") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0, dev0 = host.copy(), gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        errors = []
+
+        def worker(jobs, fn):
+            try:
+                st = torch.cuda.Stream()
+                for dp, hp in jobs:
+                    for layer in range(L) if fn == "load_layer" else [None]:
+                        if fn == "backup":
+                            pool.backup(kv, dp, hp, stream=st)
+                        else:
+                            pool.load_layer(kv, dp, hp, layer, stream=st)
+                hc.wait(st)
+            except Exception as e:  # reported below
+                errors.append(e)
+        ts = [threading.Thread(target=worker, args=(jobs_b, "backup")),
+              threading.Thread(target=worker, args=(jobs_l, "load_layer"))]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        assert not errors, errors
+        want_host = host0.view(np.uint16).copy()
+        want_dev = [x.copy() for x in dev0]
+        for dp, hp in jobs_b:
+            gh.orc().backup(dev0, want_host, B, L, P, R, Hp, dp, hp, 2)
+        for dp, hp in jobs_l:
+            gh.orc().load(want_dev, host0.view(np.uint16), B, L, P, R, Hp, dp, hp, 2)
+        assert np.array_equal(host.view(np.uint16), want_host)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want_dev[k])
