@@ -265,6 +265,47 @@ int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *devi
 int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t buffer,
                       int64_t *offset_bytes, int64_t *nbytes);
 
+/* ---- submission engine ---------------------------------------------------------
+ * Callers queue backups and loads (every layer); one worker thread launches
+ * them in submission order on the engine's own stream.  This is the pages'
+ * pair of submitter threads with request queues ("Tuning ... section 2.2";
+ * "Baidu's KVCache Overhaul", section "Bidirectional Async Transfer"), with one
+ * change for GB300: when the request at the head of the queue and the one right
+ * behind it go in opposite directions, use the same device buffers, and neither
+ * writes a page the other touches, the worker sends them as one fused launch
+ * (hicache_backup_load), which keeps both directions of the host link busy.
+ * The result is always that of running the requests one by one in submission
+ * order.  Validation and the pre-pass run in the submitting thread; a refused
+ * request is never queued.  An engine must be destroyed before its pool. */
+typedef struct hicache_engine hicache_engine; /* opaque */
+/* Starts the worker thread and creates the engine's stream on the pool's device. */
+int hicache_engine_create(hicache_pool *pool, hicache_engine **out);
+/* Launches whatever is still queued, waits for the engine's stream, stops the
+ * worker and frees the engine. */
+int hicache_engine_destroy(hicache_engine *engine);
+/* Queue a backup (direction HICACHE_DIR_BACKUP) or load of every layer of n
+ * pages, with the checks of hicache_backup / hicache_load.  If
+ * after_stream_valid is non-zero, the transfer starts only after the work
+ * already enqueued on after_stream (e.g. the compute that wrote the KV a
+ * backup reads); the dependency is recorded on after_stream during this call.
+ * kv's buffer table is copied.  *ticket receives the request's id (tickets
+ * complete in increasing order).  After a launch failure the engine refuses
+ * new requests (CUDA). */
+int hicache_engine_submit(hicache_engine *engine, const hicache_device_kv *kv,
+                          const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                          int32_t direction, int32_t layout, int32_t after_stream_valid,
+                          void *after_stream, uint64_t *ticket);
+/* Block until the transfer of `ticket` has finished on the GPU, for at most
+ * timeout_us (< 0: no limit).  Returns OK, TIMEOUT, INVALID_ARG (unknown
+ * ticket) or the engine's launch error. */
+int hicache_engine_wait(hicache_engine *engine, uint64_t ticket, int64_t timeout_us);
+/* Make `stream` wait on the device for the transfer of `ticket` (e.g. compute
+ * that reads loaded KV).  Blocks the host only until the worker has launched
+ * the ticket. */
+int hicache_engine_wait_on_stream(hicache_engine *engine, uint64_t ticket, void *stream);
+/* Launches made so far, and how many of them carried a backup and a load. */
+int hicache_engine_stats(hicache_engine *engine, int64_t *launches, int64_t *fused_launches);
+
 /* ---- host-page allocator (LIFO free list of page runs) ------------------------
  * Hands out host pages of an L2 pool.  "Tuning ... section 2.4" and "Baidu's
  * KVCache Overhaul", section "LIFO slot allocation": the most recently freed

@@ -1,0 +1,148 @@
+"""The submission engine on the GPU: results equal the oracle applying the
+requests one by one in submission order; adjacent hazard-free backup/load pairs
+leave as fused launches; dependencies on a caller's stream are honoured."""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gb300 as hc
+from tiered_kv_cache_gb300 import build as hc_build
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    hc_build.build()
+    torch.cuda.init()
+
+
+def oracle_apply(reqs, dev, host, B, L, P, R, Hp, layout):
+    for direction, dp, hp in reqs:
+        if direction == hc.BACKUP:
+            gh.orc().backup(dev, host, B, L, P, R, Hp, dp, hp, layout)
+        else:
+            gh.orc().load(dev, host, B, L, P, R, Hp, dp, hp, layout)
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2, 3], ids=list(hc.LAYOUTS))
+def test_sequential_semantics_with_hazards(layout):
+    """Small pools and many overlapping requests: whether or not the engine
+    fuses, the outcome is the oracle's in submission order."""
+    B, L, P, R, Dp, Hp = 2, 3, 4, 64, 20, 20
+    rng = np.random.default_rng(90 + layout)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=90)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        reqs = []
+        for _ in range(60):
+            n = int(rng.integers(1, 7))
+            reqs.append((int(rng.integers(0, 2)), rng.choice(Dp, n, replace=False), rng.choice(Hp, n, replace=False)))
+        with hc.Engine(pool) as eng:
+            tickets = [eng.submit(kv, dp, hp, d) for d, dp, hp in reqs]
+            assert tickets == sorted(tickets)
+            eng.wait(tickets[-1])
+            launches, fused = eng.stats()
+            assert launches + fused == len(reqs)
+        oracle_apply(reqs, dev0, host0, B, L, P, R, Hp, layout)
+        assert np.array_equal(host.view(np.uint16), host0)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], dev0[k])
+
+
+def test_backup_and_load_threads_get_fused():
+    """A backup thread and a load thread submit hazard-free requests while the
+    link is busy: the engine pairs them into fused launches, and the result is
+    the oracle's."""
+    B, L, P, R, Dp, Hp = 2, 8, 16, 1024, 192, 192
+    rng = np.random.default_rng(95)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=95)
+    perm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    back = [(hc.BACKUP, perm[i * 12:(i + 1) * 12], hperm[i * 12:(i + 1) * 12]) for i in range(8)]
+    load = [(hc.LOAD, perm[96 + i * 12:96 + (i + 1) * 12], hperm[96 + i * 12:96 + (i + 1) * 12]) for i in range(8)]
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        with hc.Engine(pool) as eng:
+            # a big first request keeps the link busy while the threads submit
+            first = eng.submit(kv, perm[:96], hperm[:96], hc.BACKUP)
+            got_tickets = []
+
+            def submitter(reqs):
+                for d, dp, hp in reqs:
+                    got_tickets.append(eng.submit(kv, dp, hp, d))
+            ts = [threading.Thread(target=submitter, args=(back,)),
+                  threading.Thread(target=submitter, args=(load,))]
+            for t in ts:
+                t.start()
+            for t in ts:
+                t.join()
+            eng.wait(max(got_tickets + [first]))
+            launches, fused = eng.stats()
+        assert fused >= 1, (launches, fused)
+        # all requests are hazard-free against each other except the first,
+        # which precedes them all: order among the rest does not matter
+        oracle_apply([(hc.BACKUP, perm[:96], hperm[:96])] + back + load, dev0, host0, B, L, P, R, Hp, 0)
+        assert np.array_equal(host.view(np.uint16), host0)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], dev0[k])
+
+
+def test_after_stream_dependency_and_wait_on_stream():
+    B, L, P, R, Dp, Hp = 1, 2, 4, 64, 8, 8
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    comp = torch.cuda.Stream()
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        pool.host_array()[:] = 0
+        kv = hc.DeviceKV(bufs, Dp)
+        torch.cuda.synchronize()
+        with hc.Engine(pool) as eng:
+            with torch.cuda.stream(comp):
+                torch.cuda._sleep(int(3e8))          # the "compute" is still running...
+                for b in bufs:
+                    b[3 * P:4 * P].fill_(1234)       # ...when it writes page 3
+            t = eng.submit(kv, [3], [5], hc.BACKUP, after_stream=comp)
+            eng.wait(t)
+            host = pool.host_array(np.int16)
+            assert (host != 0).sum() == L * P * R and set(np.unique(host)) == {0, 1234}
+            # a load, then compute that must see it
+            t2 = eng.submit(kv, [6], [5], hc.LOAD)
+            eng.wait_on_stream(t2, comp)
+            with torch.cuda.stream(comp):
+                s = torch.stack([b[6 * P:7 * P].float().sum() for b in bufs])
+            comp.synchronize()
+            assert torch.all(s == 1234.0 * P * R)
+
+
+def test_refused_requests_are_not_queued():
+    B, L, P, R, Dp, Hp = 1, 2, 4, 64, 8, 8
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        kv = hc.DeviceKV(bufs, Dp)
+        with hc.Engine(pool) as eng:
+            with pytest.raises(hc.HiCacheError) as e:
+                eng.submit(kv, [0, 0], [1, 2], hc.LOAD)
+            assert e.value.status == "DUPLICATE_INDEX"
+            with pytest.raises(hc.HiCacheError) as e:
+                eng.submit(kv, [9], [1], hc.BACKUP)
+            assert e.value.status == "INDEX_RANGE"
+            t = eng.submit(kv, [1], [1], hc.BACKUP)
+            assert t == 1                               # the refused ones took no ticket
+            eng.wait(t)
+            with pytest.raises(hc.HiCacheError) as e:
+                eng.wait(7)
+            assert e.value.status == "INVALID_ARG"
+            assert eng.stats() == (1, 0)

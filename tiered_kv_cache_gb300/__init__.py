@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
-    "PageAllocator",
+    "PageAllocator", "Engine",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
@@ -96,6 +96,13 @@ def _bind(lib):
         "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
         "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
         "hicache_page_span": (ctypes.c_int, [_P(PoolDesc), _i64, _i32, _P(_i64), _P(_i64)]),
+        "hicache_engine_create": (ctypes.c_int, [_vp, _P(_vp)]),
+        "hicache_engine_destroy": (ctypes.c_int, [_vp]),
+        "hicache_engine_submit": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _i32, _i32,
+                                                 _vp, _P(ctypes.c_uint64)]),
+        "hicache_engine_wait": (ctypes.c_int, [_vp, ctypes.c_uint64, _i64]),
+        "hicache_engine_wait_on_stream": (ctypes.c_int, [_vp, ctypes.c_uint64, _vp]),
+        "hicache_engine_stats": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
         "hicache_allocator_create": (ctypes.c_int, [_i64, _P(_vp)]),
         "hicache_allocator_destroy": (ctypes.c_int, [_vp]),
         "hicache_allocator_alloc": (ctypes.c_int, [_vp, _i64, _vp]),
@@ -344,6 +351,60 @@ class Pool:
             _check(library().hicache_pool_destroy(self.handle))
             self.handle = None
         self._mem = None   # freed once no host_array view is left
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Engine:
+    """Submission engine over a pool (hicache_engine_*): queue backups and loads,
+    one worker thread launches them in order, fusing adjacent opposite-direction
+    requests into one launch."""
+
+    def __init__(self, pool: "Pool"):
+        h = ctypes.c_void_p()
+        _check(library().hicache_engine_create(pool.handle, ctypes.byref(h)))
+        self.handle = h.value
+        self.pool = pool
+        self._kvs = []
+
+    def submit(self, kv: DeviceKV, device_pages, host_pages, direction: int, layout=LAYOUT_POOL,
+               after_stream=None) -> int:
+        dp, hp = _idx(device_pages), _idx(host_pages)
+        if dp.size != hp.size:
+            raise ValueError("device_pages and host_pages differ in length")
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        t = ctypes.c_uint64()
+        _check(library().hicache_engine_submit(self.handle, ctypes.byref(kv.struct), _ptr(dp), _ptr(hp), dp.size,
+                                               direction, layout, 0 if after_stream is None else 1,
+                                               _stream(after_stream), ctypes.byref(t)))
+        return t.value
+
+    def wait(self, ticket: int, timeout_us: int = -1):
+        _check(library().hicache_engine_wait(self.handle, ticket, timeout_us))
+
+    def wait_on_stream(self, ticket: int, stream=None):
+        _check(library().hicache_engine_wait_on_stream(self.handle, ticket, _stream(stream)))
+
+    def stats(self):
+        a, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(library().hicache_engine_stats(self.handle, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            h, self.handle = self.handle, None
+            _check(library().hicache_engine_destroy(h))
 
     def __enter__(self):
         return self

@@ -1,10 +1,11 @@
 """Build libhicache.so in-tree with nvcc for sm_103a (GB300).
 
-Three translation units, compiled in parallel, linked with the static CUDA
+Four translation units, compiled in parallel, linked with the static CUDA
 runtime so the library loads on a machine without a GPU driver:
   csrc/hicache_kernels.cu   transfer and stand-in compute kernels
   csrc/hicache_api.cpp      validation, pre-pass, pools, plans, events
   csrc/hicache_alloc.cpp    LIFO host-page allocator
+  csrc/hicache_engine.cpp   submission engine (queue + worker thread)
 """
 from __future__ import annotations
 
@@ -23,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_alloc.cpp"]
+SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_alloc.cpp", "hicache_engine.cpp"]
 
 
 def _nvcc() -> str:
@@ -49,7 +50,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     changed unless ``force``."""
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
-    headers = [os.path.join(CSRC, "hicache_internal.h"), os.path.join(INCLUDE, "hicache.h")]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    headers.append(os.path.join(INCLUDE, "hicache.h"))
     flags = COMMON + (extra_flags or [])
     objs, procs = [], []
     for src in SOURCES:

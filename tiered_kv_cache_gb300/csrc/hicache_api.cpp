@@ -25,11 +25,10 @@
 #include <unordered_map>
 #include <vector>
 
+#include "hicache_host.h"
 #include "hicache_internal.h"
 
-using hicache::RunRec;
-
-namespace {
+namespace hicache {
 
 thread_local std::string g_last_error;
 std::atomic<int64_t> g_launches{0};
@@ -57,11 +56,6 @@ std::mutex g_alloc_mu;
 std::unordered_map<void *, HostAlloc> g_allocs;
 
 // ---- shape checks ------------------------------------------------------------
-struct Shape {
-  int64_t L, B, P, R, es, Hp;
-  int64_t row_bytes, V, PV, LPV, BLPV;
-  int32_t layout;
-};
 
 int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
   if (!d) return set_error(HICACHE_ERR_INVALID_ARG, "pool descriptor is NULL");
@@ -193,7 +187,9 @@ constexpr int64_t kMaxTiles = int64_t(1) << 30;
 // stays below 2^31 vectors: the kernels index units with 32-bit offsets.
 int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX - 1) / s.BLPV); }
 
-}  // namespace
+void clear_error() { g_last_error.clear(); }
+
+}  // namespace hicache
 
 int hicache::set_error_text(int code, const char *msg) {
   g_last_error.clear();
@@ -201,26 +197,15 @@ int hicache::set_error_text(int code, const char *msg) {
 }
 
 // ---- pool and plan objects -----------------------------------------------------
-struct hicache_pool {
-  hicache_pool_desc desc;
-  Shape shape;
-  void *host = nullptr;       // host pointer of the pool
-  void *host_dev = nullptr;   // device-visible alias
-  size_t host_bytes = 0;
-  int device = 0;
-  int ctas = 0;
-  std::vector<cudaEvent_t> events;  // one per layer
-};
-
 struct hicache_plan {
   hicache_pool *pool = nullptr;
   int32_t direction = 0;
   int64_t n = 0;
   int64_t device_num_pages = 0;
-  std::vector<RunRec> runs;
+  std::vector<hicache::RunRec> runs;
 };
 
-namespace {
+namespace hicache {
 
 int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_pages) {
   if (!kv || !kv->buf_ptrs) return set_error(HICACHE_ERR_INVALID_ARG, "device KV is NULL");
@@ -385,7 +370,9 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
   return HICACHE_OK;
 }
 
-}  // namespace
+}  // namespace hicache
+
+using namespace hicache;
 
 extern "C" {
 

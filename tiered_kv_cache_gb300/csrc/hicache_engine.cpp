@@ -1,0 +1,388 @@
+// hicache_engine.cpp -- a submission engine over one pool: callers queue
+// backups and loads; one worker thread launches them, in submission order, on
+// the engine's own stream.
+//
+// The pages move transfer submission off the scheduler thread: a backup thread
+// and a load thread consume queues and submit on private streams ("Tuning
+// SGLang HiCache L2 on Kunlunxin P800/P900", section 2.2; "Baidu's KVCache
+// Overhaul", section "Bidirectional Async Transfer").  On GB300 two launches of
+// opposite directions on two streams reach about 0.82 of what the host link
+// carries both ways, while one launch carrying both reaches 1.00; so here one
+// worker owns the link: when the request at the head of the queue and the one
+// right behind it go in opposite directions, use the same device buffers and
+// touch no page that the other writes, they go out as one fused launch.
+// Everything else goes out alone, in order.
+//
+// Requests are validated, and pre-passed, in the submitting thread: a bad
+// request is refused at submit and never queued.  Completion is tracked per
+// launch with one event; tickets complete in ticket order (one stream).
+
+#include <algorithm>
+#include <chrono>
+#include <condition_variable>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "hicache_host.h"
+
+using hicache::RunRec;
+
+namespace {
+
+struct Request {
+  uint64_t ticket = 0;
+  int32_t direction = 0;
+  int32_t layout = 0;
+  std::vector<void *> bufs;           // copy of the caller's buffer table
+  int64_t device_num_pages = 0;
+  std::vector<RunRec> runs;
+  std::vector<int64_t> dev, host;     // the pages, for hazard checks
+  cudaEvent_t after = nullptr;        // recorded on the caller's stream, or null
+};
+
+struct Launched {
+  uint64_t max_ticket;
+  cudaEvent_t done;
+  int waiters;     // threads polling `done` right now: the event is not reused meanwhile
+  bool finished;   // `done` has been seen complete
+};
+
+// Launches kept unfinished on the engine stream at once: one running and one
+// queued behind it.  Requests submitted meanwhile wait in the queue, where a
+// backup and a load can meet and leave as one fused launch.
+constexpr size_t kDepth = 2;
+
+void poll_until_done(cudaEvent_t ev) {
+  const auto start = std::chrono::steady_clock::now();
+  while (cudaEventQuery(ev) == cudaErrorNotReady) {
+    const auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+                        std::chrono::steady_clock::now() - start)
+                        .count();
+    if (us < 500) std::this_thread::yield();
+    else std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+bool fusable(const Request &a, const Request &b) {
+  if (a.direction == b.direction || a.layout != b.layout) return false;
+  if (a.device_num_pages != b.device_num_pages || a.bufs != b.bufs) return false;
+  if (a.runs.empty() || b.runs.empty()) return false;
+  // the load must not write a device page the backup reads, nor the backup
+  // write a host page the load reads: then the order of the two is moot
+  int64_t page = 0;
+  return !hicache::intersects(a.dev, b.dev, &page) && !hicache::intersects(a.host, b.host, &page);
+}
+
+}  // namespace
+
+struct hicache_engine {
+  hicache_pool *pool = nullptr;
+  cudaStream_t stream = nullptr;
+  std::thread worker;
+  std::mutex mu;
+  std::condition_variable cv_work, cv_launched;
+  std::deque<Request> queue;
+  std::deque<Launched> inflight;      // launched, in ticket order
+  std::vector<cudaEvent_t> spare;     // events ready for reuse
+  uint64_t next_ticket = 1;
+  uint64_t launched_upto = 0;         // every ticket <= this is launched
+  uint64_t completed_upto = 0;        // every ticket <= this is known finished
+  bool stop = false;
+  int error = 0;
+  std::string error_text;
+  int64_t launches = 0, fused = 0;
+
+  // Under mu.  Mark launches whose event has fired (they finish in order);
+  // returns the number still unfinished.
+  size_t refresh() {
+    size_t unfinished = 0;
+    for (auto &l : inflight) {
+      if (!l.finished) {
+        if (unfinished == 0 && cudaEventQuery(l.done) == cudaSuccess) {
+          l.finished = true;
+          completed_upto = std::max(completed_upto, l.max_ticket);
+        } else {
+          ++unfinished;
+        }
+      }
+    }
+    return unfinished;
+  }
+
+  // Under mu.  An event for a new launch or dependency: a finished, unwatched
+  // launch's event if there is one, else a spare, else a new one.
+  cudaEvent_t take_event() {
+    refresh();
+    while (!inflight.empty() && inflight.front().finished && inflight.front().waiters == 0) {
+      spare.push_back(inflight.front().done);
+      inflight.pop_front();
+    }
+    if (!spare.empty()) {
+      cudaEvent_t e = spare.back();
+      spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    return e;
+  }
+
+  void run() {
+    cudaSetDevice(pool->device);
+    for (;;) {
+      std::unique_lock<std::mutex> lk(mu);
+      cv_work.wait(lk, [&] { return stop || !queue.empty(); });
+      if (queue.empty()) return;
+      // pace the launches by the GPU: wait while kDepth launches are unfinished
+      while (refresh() >= kDepth) {
+        cudaEvent_t oldest = nullptr;
+        for (auto &l : inflight)
+          if (!l.finished) {
+            oldest = l.done;
+            l.waiters++;
+            break;
+          }
+        lk.unlock();
+        poll_until_done(oldest);
+        lk.lock();
+        for (auto &l : inflight)  // our waiter count kept this entry (and its event) alive
+          if (l.done == oldest) {
+            l.waiters--;
+            break;
+          }
+      }
+      Request a = std::move(queue.front());
+      queue.pop_front();
+      bool pair = false;
+      Request b;
+      if (!queue.empty() && fusable(a, queue.front())) {
+        b = std::move(queue.front());
+        queue.pop_front();
+        pair = true;
+      }
+      cudaEvent_t done = take_event();
+      lk.unlock();
+
+      int rc = HICACHE_OK;
+      std::string text;
+      if (!done) rc = hicache::set_error(HICACHE_ERR_CUDA, "cudaEventCreate failed");
+      for (Request *r : {&a, pair ? &b : nullptr}) {
+        if (rc == HICACHE_OK && r && r->after && cudaStreamWaitEvent(stream, r->after, 0) != cudaSuccess)
+          rc = hicache::set_error(HICACHE_ERR_CUDA, "cudaStreamWaitEvent failed");
+      }
+      if (rc == HICACHE_OK) {
+        const hicache_device_kv kv{a.bufs.data(), a.device_num_pages};
+        if (pair) {
+          const Request &bk = a.direction == HICACHE_DIR_BACKUP ? a : b;
+          const Request &ld = a.direction == HICACHE_DIR_BACKUP ? b : a;
+          rc = hicache::enqueue(pool, &kv, bk.runs, &ld.runs, a.layout, -1, true, stream);
+        } else {
+          rc = hicache::enqueue(pool, &kv, a.runs, nullptr, a.layout, -1,
+                                a.direction == HICACHE_DIR_BACKUP, stream);
+        }
+      }
+      if (rc == HICACHE_OK && cudaEventRecord(done, stream) != cudaSuccess)
+        rc = hicache::set_error(HICACHE_ERR_CUDA, "cudaEventRecord failed");
+      if (rc != HICACHE_OK) text = hicache_last_error();
+
+      lk.lock();
+      for (Request *r : {&a, pair ? &b : nullptr})
+        if (r && r->after) spare.push_back(r->after);
+      const uint64_t top = pair ? std::max(a.ticket, b.ticket) : a.ticket;
+      if (rc == HICACHE_OK) {
+        inflight.push_back(Launched{top, done, 0, false});
+        ++launches;
+        if (pair) ++fused;
+      } else {
+        if (done) spare.push_back(done);
+        if (!error) {
+          error = rc;
+          error_text = text;
+        }
+      }
+      launched_upto = top;
+      lk.unlock();
+      cv_launched.notify_all();
+    }
+  }
+};
+
+extern "C" {
+
+int hicache_engine_create(hicache_pool *pool, hicache_engine **out) {
+  hicache::clear_error();
+  if (!pool || !out) return hicache::set_error(HICACHE_ERR_INVALID_ARG, "pool or out is NULL");
+  *out = nullptr;
+  hicache_engine *e = new (std::nothrow) hicache_engine();
+  if (!e) return hicache::set_error(HICACHE_ERR_NOMEM, "out of host memory");
+  e->pool = pool;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(pool->device);
+  const cudaError_t ce = cudaStreamCreateWithFlags(&e->stream, cudaStreamNonBlocking);
+  cudaSetDevice(prev);
+  if (ce != cudaSuccess) {
+    delete e;
+    return hicache::cuda_error(ce, "cudaStreamCreateWithFlags");
+  }
+  try {
+    e->worker = std::thread([e] { e->run(); });
+  } catch (...) {
+    cudaStreamDestroy(e->stream);
+    delete e;
+    return hicache::set_error(HICACHE_ERR_NOMEM, "could not start the engine thread");
+  }
+  *out = e;
+  return HICACHE_OK;
+}
+
+int hicache_engine_destroy(hicache_engine *e) {
+  hicache::clear_error();
+  if (!e) return HICACHE_OK;
+  {
+    std::lock_guard<std::mutex> g(e->mu);
+    e->stop = true;
+  }
+  e->cv_work.notify_all();
+  e->worker.join();
+  const cudaError_t ce = cudaStreamSynchronize(e->stream);
+  for (auto &l : e->inflight) cudaEventDestroy(l.done);
+  for (auto ev : e->spare) cudaEventDestroy(ev);
+  cudaStreamDestroy(e->stream);
+  delete e;
+  if (ce != cudaSuccess) return hicache::cuda_error(ce, "cudaStreamSynchronize");
+  return HICACHE_OK;
+}
+
+int hicache_engine_submit(hicache_engine *e, const hicache_device_kv *kv, const int64_t *device_pages,
+                          const int64_t *host_pages, int64_t n, int32_t direction, int32_t layout,
+                          int32_t after_stream_valid, void *after_stream, uint64_t *ticket) {
+  hicache::clear_error();
+  if (!e || !ticket) return hicache::set_error(HICACHE_ERR_INVALID_ARG, "engine or ticket is NULL");
+  hicache_pool *pool = e->pool;
+  int32_t lay = 0;
+  int rc = hicache::resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if ((rc = hicache::check_kv(pool, kv, 0))) return rc;
+  Request r;
+  if ((rc = hicache::prepass(pool->shape.Hp, kv->device_num_pages, device_pages, host_pages, n,
+                             direction, hicache::max_run_pages(pool->shape), &r.runs)))
+    return rc;
+  r.direction = direction;
+  r.layout = lay;
+  r.bufs.assign(kv->buf_ptrs, kv->buf_ptrs + pool->shape.B * pool->shape.L);
+  r.device_num_pages = kv->device_num_pages;
+  if (n > 0) {
+    r.dev.assign(device_pages, device_pages + n);
+    r.host.assign(host_pages, host_pages + n);
+  }
+  {
+    std::lock_guard<std::mutex> g(e->mu);
+    if (e->error) return hicache::set_error(e->error, "engine stopped after an error: %s", e->error_text.c_str());
+    if (after_stream_valid) {
+      r.after = e->take_event();
+      if (!r.after) return hicache::set_error(HICACHE_ERR_CUDA, "cudaEventCreate failed");
+      const cudaError_t ce = cudaEventRecord(r.after, static_cast<cudaStream_t>(after_stream));
+      if (ce != cudaSuccess) {
+        e->spare.push_back(r.after);
+        return hicache::cuda_error(ce, "cudaEventRecord(after_stream)");
+      }
+    }
+    r.ticket = e->next_ticket++;
+    *ticket = r.ticket;
+    e->queue.push_back(std::move(r));
+  }
+  e->cv_work.notify_one();
+  return HICACHE_OK;
+}
+
+int hicache_engine_wait(hicache_engine *e, uint64_t ticket, int64_t timeout_us) {
+  hicache::clear_error();
+  if (!e) return hicache::set_error(HICACHE_ERR_INVALID_ARG, "engine is NULL");
+  const auto start = std::chrono::steady_clock::now();
+  auto waited_us = [&] {
+    return std::chrono::duration_cast<std::chrono::microseconds>(std::chrono::steady_clock::now() - start)
+        .count();
+  };
+  std::unique_lock<std::mutex> lk(e->mu);
+  if (ticket == 0 || ticket >= e->next_ticket)
+    return hicache::set_error(HICACHE_ERR_INVALID_ARG, "unknown ticket %llu", (unsigned long long)ticket);
+  while (e->launched_upto < ticket) {
+    if (timeout_us >= 0) {
+      const int64_t left = timeout_us - waited_us();
+      if (left <= 0) return hicache::set_error(HICACHE_ERR_TIMEOUT, "ticket not launched yet");
+      e->cv_launched.wait_for(lk, std::chrono::microseconds(left));
+    } else {
+      e->cv_launched.wait(lk);
+    }
+  }
+  if (e->error) return hicache::set_error(e->error, "engine error: %s", e->error_text.c_str());
+  if (ticket <= e->completed_upto) return HICACHE_OK;
+  auto it = std::find_if(e->inflight.begin(), e->inflight.end(),
+                         [&](const Launched &l) { return l.max_ticket >= ticket; });
+  if (it == e->inflight.end()) return HICACHE_OK;  // already retired
+  it->waiters++;
+  cudaEvent_t ev = it->done;
+  const uint64_t top = it->max_ticket;
+  lk.unlock();
+  int rc = HICACHE_OK;
+  for (;;) {
+    const cudaError_t q = cudaEventQuery(ev);
+    if (q == cudaSuccess) break;
+    if (q != cudaErrorNotReady) {
+      rc = hicache::cuda_error(q, "cudaEventQuery");
+      break;
+    }
+    const int64_t w = waited_us();
+    if (timeout_us >= 0 && w >= timeout_us) {
+      rc = hicache::set_error(HICACHE_ERR_TIMEOUT, "transfer still running after %lld us", (long long)w);
+      break;
+    }
+    if (w < 500) std::this_thread::yield();
+    else std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  lk.lock();
+  for (auto &l : e->inflight)
+    if (l.done == ev && l.max_ticket == top) {
+      l.waiters--;
+      if (rc == HICACHE_OK) l.finished = true;
+    }
+  if (rc == HICACHE_OK) e->completed_upto = std::max(e->completed_upto, top);
+  return rc;
+}
+
+int hicache_engine_wait_on_stream(hicache_engine *e, uint64_t ticket, void *stream) {
+  hicache::clear_error();
+  if (!e) return hicache::set_error(HICACHE_ERR_INVALID_ARG, "engine is NULL");
+  std::unique_lock<std::mutex> lk(e->mu);
+  if (ticket == 0 || ticket >= e->next_ticket)
+    return hicache::set_error(HICACHE_ERR_INVALID_ARG, "unknown ticket %llu", (unsigned long long)ticket);
+  e->cv_launched.wait(lk, [&] { return e->launched_upto >= ticket; });
+  if (e->error) return hicache::set_error(e->error, "engine error: %s", e->error_text.c_str());
+  if (ticket <= e->completed_upto) return HICACHE_OK;
+  for (auto &l : e->inflight) {
+    if (l.max_ticket >= ticket) {
+      // under the lock: the event cannot be reused before the wait is enqueued
+      const cudaError_t ce = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), l.done, 0);
+      if (ce != cudaSuccess) return hicache::cuda_error(ce, "cudaStreamWaitEvent");
+      return HICACHE_OK;
+    }
+  }
+  return HICACHE_OK;
+}
+
+int hicache_engine_stats(hicache_engine *e, int64_t *launches, int64_t *fused_launches) {
+  hicache::clear_error();
+  if (!e) return hicache::set_error(HICACHE_ERR_INVALID_ARG, "engine is NULL");
+  std::lock_guard<std::mutex> g(e->mu);
+  if (launches) *launches = e->launches;
+  if (fused_launches) *fused_launches = e->fused;
+  return HICACHE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// hicache_host.h -- host-side internals shared by the API (hicache_api.cpp) and
+// the submission engine (hicache_engine.cpp).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "hicache.h"
+#include "hicache_internal.h"
+
+namespace hicache {
+
+// A validated pool shape, in elements and 16-byte vectors.
+struct Shape {
+  int64_t L, B, P, R, es, Hp;
+  int64_t row_bytes, V, PV, LPV, BLPV;
+  int32_t layout;
+};
+
+// Last-error text of the calling thread.
+int set_error(int code, const char *fmt, ...);
+int cuda_error(cudaError_t e, const char *what);
+void clear_error();
+
+int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment);
+int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out);
+// Validate n pairs and reduce them to runs (sorted by host page).
+int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+            int32_t direction, int64_t max_run, std::vector<RunRec> *runs);
+int64_t max_run_pages(const Shape &s);
+bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common);
+
+}  // namespace hicache
+
+struct hicache_pool {
+  hicache_pool_desc desc;
+  hicache::Shape shape;
+  void *host = nullptr;       // host pointer of the pool
+  void *host_dev = nullptr;   // device-visible alias
+  size_t host_bytes = 0;
+  int device = 0;
+  int ctas = 0;
+  std::vector<cudaEvent_t> events;  // one per layer
+};
+
+namespace hicache {
+
+int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_pages);
+// Enqueue validated runs (see hicache_api.cpp).
+int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
+            const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
+            void *stream);
+
+}  // namespace hicache
