@@ -617,6 +617,72 @@ def bench_host_alloc(torch, hc, args):
     return out
 
 
+def bench_engine_bidir(torch, hc, args):
+    """The pages' submitter design: a backup thread and a load thread, each
+    moving 512-page requests (Llama-3-8B shape) back to back.  (a) each thread
+    calls the library directly on its own stream; (b) both submit to one
+    engine, which fuses adjacent backup/load pairs.  Host wall clock from the
+    first submission to the last completion."""
+    import threading
+    w = build_workload("cuda", 512, args.ctas)
+    pool, kv = w["pool"], w["kv"]
+    reps = max(6, args.steps)
+    bpx = w["bytes_per_xfer"]
+    out = {}
+
+    def run_direct():
+        sb, sl = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def backups():
+            for _ in range(reps):
+                pool.backup(kv, w["a_dev"], w["a_host"], stream=sb)
+            hc.wait(sb)
+
+        def loads():
+            for _ in range(reps):
+                pool.load(kv, w["b_dev"], w["b_host"], stream=sl)
+            hc.wait(sl)
+        ts = [threading.Thread(target=backups), threading.Thread(target=loads)]
+        t0 = time.perf_counter()
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        return time.perf_counter() - t0
+
+    def run_engine(eng):
+        last = {}
+
+        def submit(name, direction, dev, host):
+            for _ in range(reps):
+                last[name] = eng.submit(kv, dev, host, direction)
+        ts = [threading.Thread(target=submit, args=("b", hc.BACKUP, w["a_dev"], w["a_host"])),
+              threading.Thread(target=submit, args=("l", hc.LOAD, w["b_dev"], w["b_host"]))]
+        t0 = time.perf_counter()
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        for t in last.values():
+            eng.wait(t)
+        return time.perf_counter() - t0
+
+    run_direct()
+    direct = min(run_direct() for _ in range(3))
+    with hc.Engine(pool) as eng:
+        run_engine(eng)
+        l0, f0 = eng.stats()
+        eng_t = min(run_engine(eng) for _ in range(3))
+        l1, f1 = eng.stats()
+    moved = 2 * reps * bpx
+    out["direct_two_streams_gbs"] = round(moved / direct / GB, 1)
+    out["engine_gbs"] = round(moved / eng_t / GB, 1)
+    out["engine_fused_fraction"] = round((f1 - f0) / max(1, l1 - l0), 3)
+    out["requests_per_thread"] = reps
+    pool.close()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,7 +696,8 @@ def main():
     ap.add_argument("--no-link-probe", action="store_true",
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
-                    choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc"],
+                    choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc",
+                             "engine_bidir"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
     ap.add_argument("--layouts", default="pages",
@@ -658,9 +725,16 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch)
-    if args.workload in ("mla61_overlap", "small_mix", "host_alloc"):
+    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir"):
         t0 = time.perf_counter()
-        if args.workload == "host_alloc":
+        if args.workload == "engine_bidir":
+            res = bench_engine_bidir(torch, hc, args)
+            launches = None
+            value = res["engine_gbs"]
+            what = {"workload": "engine_bidir: a backup thread and a load thread, 512-page Llama-3-8B requests "
+                                "back to back, direct on two streams vs one submission engine",
+                    "value": "GB/s through the engine, both directions"}
+        elif args.workload == "host_alloc":
             res = bench_host_alloc(torch, hc, args)
             launches = None
             value = res["64GiB_cudaHostAlloc"]["load_lf_gbs"]

@@ -270,10 +270,11 @@ int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t 
  * them in submission order on the engine's own stream.  This is the pages'
  * pair of submitter threads with request queues ("Tuning ... section 2.2";
  * "Baidu's KVCache Overhaul", section "Bidirectional Async Transfer"), with one
- * change for GB300: when the request at the head of the queue and the one right
- * behind it go in opposite directions, use the same device buffers, and neither
- * writes a page the other touches, the worker sends them as one fused launch
- * (hicache_backup_load), which keeps both directions of the host link busy.
+ * change for GB300: when the request at the head of the queue and the first
+ * request of the other direction among the next 8 use the same device buffers
+ * and commute (neither writes a page the other touches, nor one touched by the
+ * requests the second would move ahead of), the worker sends them as one fused
+ * launch (hicache_backup_load), which keeps both directions of the host link busy.
  * The result is always that of running the requests one by one in submission
  * order.  Validation and the pre-pass run in the submitting thread; a refused
  * request is never queued.  An engine must be destroyed before its pool. */
@@ -288,9 +289,9 @@ int hicache_engine_destroy(hicache_engine *engine);
  * after_stream_valid is non-zero, the transfer starts only after the work
  * already enqueued on after_stream (e.g. the compute that wrote the KV a
  * backup reads); the dependency is recorded on after_stream during this call.
- * kv's buffer table is copied.  *ticket receives the request's id (tickets
- * complete in increasing order).  After a launch failure the engine refuses
- * new requests (CUDA). */
+ * kv's buffer table is copied.  *ticket receives the request's id (a request
+ * paired ahead of earlier ones may finish before them).  After a launch failure
+ * the engine refuses new requests (CUDA). */
 int hicache_engine_submit(hicache_engine *engine, const hicache_device_kv *kv,
                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                           int32_t direction, int32_t layout, int32_t after_stream_valid,

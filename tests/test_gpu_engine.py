@@ -50,7 +50,8 @@ def test_sequential_semantics_with_hazards(layout):
         with hc.Engine(pool) as eng:
             tickets = [eng.submit(kv, dp, hp, d) for d, dp, hp in reqs]
             assert tickets == sorted(tickets)
-            eng.wait(tickets[-1])
+            for t in tickets:
+                eng.wait(t)
             launches, fused = eng.stats()
             assert launches + fused == len(reqs)
         oracle_apply(reqs, dev0, host0, B, L, P, R, Hp, layout)
@@ -89,7 +90,8 @@ def test_backup_and_load_threads_get_fused():
                 t.start()
             for t in ts:
                 t.join()
-            eng.wait(max(got_tickets + [first]))
+            for t in got_tickets + [first]:
+                eng.wait(t)
             launches, fused = eng.stats()
         assert fused >= 1, (launches, fused)
         # all requests are hazard-free against each other except the first,
@@ -146,3 +148,37 @@ def test_refused_requests_are_not_queued():
                 eng.wait(7)
             assert e.value.status == "INVALID_ARG"
             assert eng.stats() == (1, 0)
+
+
+@pytest.mark.parametrize("conflict", [False, True], ids=["commutes", "conflicts"])
+def test_lookahead_pairs_only_commuting_requests(conflict):
+    """Queue: a long backup B0 (keeps the link busy), then backups B1, B2 and a
+    load L1.  B1 goes out right behind B0; L1 is paired with B2 when it
+    commutes with it, and otherwise follows it alone.  Either way the result is
+    the oracle's in submission order."""
+    B, L, P, R, Dp, Hp = 2, 8, 16, 1024, 512, 512
+    rng = np.random.default_rng(97)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=97)
+    perm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    b0 = (hc.BACKUP, perm[:400], hperm[:400])
+    b1 = (hc.BACKUP, perm[400:404], hperm[400:404])
+    b2 = (hc.BACKUP, perm[404:408], hperm[404:408])
+    # the load writes device pages; in the conflicting case one of them is a page B2 reads
+    l_dev = np.concatenate([perm[408:411], perm[404:405]]) if conflict else perm[408:412]
+    l1 = (hc.LOAD, l_dev, hperm[420:424])
+    with hc.Pool(L, B, P, R, Hp, "page_first_direct") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        with hc.Engine(pool) as eng:
+            ts = [eng.submit(kv, dp, hp, d) for d, dp, hp in (b0, b1, b2, l1)]
+            for t in ts:
+                eng.wait(t)
+            launches, fused = eng.stats()
+        assert (launches, fused) == ((4, 0) if conflict else (3, 1))
+        oracle_apply([b0, b1, b2, l1], dev0, host0, B, L, P, R, Hp, 2)
+        assert np.array_equal(host.view(np.uint16), host0)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], dev0[k])

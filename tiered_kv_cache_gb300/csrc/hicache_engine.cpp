@@ -10,12 +10,15 @@
 // carries both ways, while one launch carrying both reaches 1.00; so here one
 // worker owns the link: when the request at the head of the queue and the one
 // right behind it go in opposite directions, use the same device buffers and
-// touch no page that the other writes, they go out as one fused launch.
-// Everything else goes out alone, in order.
+// touch no page that the other writes, they go out as one fused launch.  The
+// worker also looks a few requests further for the partner, and lets it move
+// ahead of same-direction requests only where the two commute, so the outcome
+// is always that of submission order.  Everything else goes out alone, in order.
 //
 // Requests are validated, and pre-passed, in the submitting thread: a bad
 // request is refused at submit and never queued.  Completion is tracked per
-// launch with one event; tickets complete in ticket order (one stream).
+// launch with one event; launches finish in launch order (one stream), and a
+// ticket moved ahead by pairing finishes before the tickets it overtook.
 
 #include <algorithm>
 #include <chrono>
@@ -24,6 +27,7 @@
 #include <deque>
 #include <mutex>
 #include <new>
+#include <set>
 #include <string>
 #include <thread>
 #include <vector>
@@ -46,7 +50,7 @@ struct Request {
 };
 
 struct Launched {
-  uint64_t max_ticket;
+  uint64_t t0, t1;   // the tickets of the launch (t1 = 0: a single request)
   cudaEvent_t done;
   int waiters;     // threads polling `done` right now: the event is not reused meanwhile
   bool finished;   // `done` has been seen complete
@@ -68,15 +72,24 @@ void poll_until_done(cudaEvent_t ev) {
   }
 }
 
+// Requests of opposite directions commute when the load writes no device
+// page the backup reads and the backup writes no host page the load reads
+// (checked on page numbers alone, which is conservative when the two use
+// different device buffers).
+bool commute(const Request &a, const Request &b) {
+  int64_t page = 0;
+  return !hicache::intersects(a.dev, b.dev, &page) && !hicache::intersects(a.host, b.host, &page);
+}
+
 bool fusable(const Request &a, const Request &b) {
   if (a.direction == b.direction || a.layout != b.layout) return false;
   if (a.device_num_pages != b.device_num_pages || a.bufs != b.bufs) return false;
   if (a.runs.empty() || b.runs.empty()) return false;
-  // the load must not write a device page the backup reads, nor the backup
-  // write a host page the load reads: then the order of the two is moot
-  int64_t page = 0;
-  return !hicache::intersects(a.dev, b.dev, &page) && !hicache::intersects(a.host, b.host, &page);
+  return commute(a, b);
 }
+
+// How far behind the head the worker looks for a partner of the other direction.
+constexpr size_t kLookahead = 8;
 
 }  // namespace
 
@@ -87,11 +100,11 @@ struct hicache_engine {
   std::mutex mu;
   std::condition_variable cv_work, cv_launched;
   std::deque<Request> queue;
-  std::deque<Launched> inflight;      // launched, in ticket order
+  std::deque<Launched> inflight;      // launched and not yet retired, in launch order
   std::vector<cudaEvent_t> spare;     // events ready for reuse
   uint64_t next_ticket = 1;
-  uint64_t launched_upto = 0;         // every ticket <= this is launched
-  uint64_t completed_upto = 0;        // every ticket <= this is known finished
+  uint64_t launched_prefix = 0;       // every ticket <= this is launched
+  std::set<uint64_t> launched_ahead;  // launched tickets above the prefix
   bool stop = false;
   int error = 0;
   std::string error_text;
@@ -103,15 +116,27 @@ struct hicache_engine {
     size_t unfinished = 0;
     for (auto &l : inflight) {
       if (!l.finished) {
-        if (unfinished == 0 && cudaEventQuery(l.done) == cudaSuccess) {
+        if (unfinished == 0 && cudaEventQuery(l.done) == cudaSuccess)
           l.finished = true;
-          completed_upto = std::max(completed_upto, l.max_ticket);
-        } else {
+        else
           ++unfinished;
-        }
       }
     }
     return unfinished;
+  }
+
+  // Under mu.
+  bool is_launched(uint64_t t) const { return t <= launched_prefix || launched_ahead.count(t) != 0; }
+  void mark_launched(uint64_t t) {
+    launched_ahead.insert(t);
+    while (launched_ahead.count(launched_prefix + 1)) launched_ahead.erase(++launched_prefix);
+  }
+  // Under mu.  The unretired launch holding ticket t, or nullptr (retired =
+  // finished: launches are retired only once their event has fired).
+  Launched *find(uint64_t t) {
+    for (auto &l : inflight)
+      if (l.t0 == t || l.t1 == t) return &l;
+    return nullptr;
   }
 
   // Under mu.  An event for a new launch or dependency: a finished, unwatched
@@ -158,12 +183,21 @@ struct hicache_engine {
       }
       Request a = std::move(queue.front());
       queue.pop_front();
+      // the first request of the other direction among the next kLookahead;
+      // it may move ahead of the same-direction requests before it only if it
+      // commutes with each of them
       bool pair = false;
       Request b;
-      if (!queue.empty() && fusable(a, queue.front())) {
-        b = std::move(queue.front());
-        queue.pop_front();
-        pair = true;
+      for (size_t i = 0; i < queue.size() && i < kLookahead; ++i) {
+        if (queue[i].direction == a.direction) continue;
+        bool ok = fusable(a, queue[i]);
+        for (size_t k = 0; ok && k < i; ++k) ok = commute(queue[k], queue[i]);
+        if (ok) {
+          b = std::move(queue[i]);
+          queue.erase(queue.begin() + std::ptrdiff_t(i));
+          pair = true;
+        }
+        break;
       }
       cudaEvent_t done = take_event();
       lk.unlock();
@@ -193,9 +227,8 @@ struct hicache_engine {
       lk.lock();
       for (Request *r : {&a, pair ? &b : nullptr})
         if (r && r->after) spare.push_back(r->after);
-      const uint64_t top = pair ? std::max(a.ticket, b.ticket) : a.ticket;
       if (rc == HICACHE_OK) {
-        inflight.push_back(Launched{top, done, 0, false});
+        inflight.push_back(Launched{a.ticket, pair ? b.ticket : 0, done, 0, false});
         ++launches;
         if (pair) ++fused;
       } else {
@@ -205,7 +238,8 @@ struct hicache_engine {
           error_text = text;
         }
       }
-      launched_upto = top;
+      mark_launched(a.ticket);
+      if (pair) mark_launched(b.ticket);
       lk.unlock();
       cv_launched.notify_all();
     }
@@ -312,7 +346,7 @@ int hicache_engine_wait(hicache_engine *e, uint64_t ticket, int64_t timeout_us) 
   std::unique_lock<std::mutex> lk(e->mu);
   if (ticket == 0 || ticket >= e->next_ticket)
     return hicache::set_error(HICACHE_ERR_INVALID_ARG, "unknown ticket %llu", (unsigned long long)ticket);
-  while (e->launched_upto < ticket) {
+  while (!e->is_launched(ticket)) {
     if (timeout_us >= 0) {
       const int64_t left = timeout_us - waited_us();
       if (left <= 0) return hicache::set_error(HICACHE_ERR_TIMEOUT, "ticket not launched yet");
@@ -322,13 +356,10 @@ int hicache_engine_wait(hicache_engine *e, uint64_t ticket, int64_t timeout_us) 
     }
   }
   if (e->error) return hicache::set_error(e->error, "engine error: %s", e->error_text.c_str());
-  if (ticket <= e->completed_upto) return HICACHE_OK;
-  auto it = std::find_if(e->inflight.begin(), e->inflight.end(),
-                         [&](const Launched &l) { return l.max_ticket >= ticket; });
-  if (it == e->inflight.end()) return HICACHE_OK;  // already retired
-  it->waiters++;
-  cudaEvent_t ev = it->done;
-  const uint64_t top = it->max_ticket;
+  Launched *l = e->find(ticket);
+  if (!l || l->finished) return HICACHE_OK;
+  l->waiters++;  // keeps the entry (and its event) from being retired
+  cudaEvent_t ev = l->done;
   lk.unlock();
   int rc = HICACHE_OK;
   for (;;) {
@@ -347,12 +378,11 @@ int hicache_engine_wait(hicache_engine *e, uint64_t ticket, int64_t timeout_us) 
     else std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
   lk.lock();
-  for (auto &l : e->inflight)
-    if (l.done == ev && l.max_ticket == top) {
-      l.waiters--;
-      if (rc == HICACHE_OK) l.finished = true;
-    }
-  if (rc == HICACHE_OK) e->completed_upto = std::max(e->completed_upto, top);
+  l = e->find(ticket);  // still there: its waiter count was held
+  if (l) {
+    l->waiters--;
+    if (rc == HICACHE_OK) l->finished = true;
+  }
   return rc;
 }
 
@@ -362,17 +392,13 @@ int hicache_engine_wait_on_stream(hicache_engine *e, uint64_t ticket, void *stre
   std::unique_lock<std::mutex> lk(e->mu);
   if (ticket == 0 || ticket >= e->next_ticket)
     return hicache::set_error(HICACHE_ERR_INVALID_ARG, "unknown ticket %llu", (unsigned long long)ticket);
-  e->cv_launched.wait(lk, [&] { return e->launched_upto >= ticket; });
+  e->cv_launched.wait(lk, [&] { return e->is_launched(ticket); });
   if (e->error) return hicache::set_error(e->error, "engine error: %s", e->error_text.c_str());
-  if (ticket <= e->completed_upto) return HICACHE_OK;
-  for (auto &l : e->inflight) {
-    if (l.max_ticket >= ticket) {
-      // under the lock: the event cannot be reused before the wait is enqueued
-      const cudaError_t ce = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), l.done, 0);
-      if (ce != cudaSuccess) return hicache::cuda_error(ce, "cudaStreamWaitEvent");
-      return HICACHE_OK;
-    }
-  }
+  Launched *l = e->find(ticket);
+  if (!l || l->finished) return HICACHE_OK;
+  // under the lock: the event cannot be reused before the wait is enqueued
+  const cudaError_t ce = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), l->done, 0);
+  if (ce != cudaSuccess) return hicache::cuda_error(ce, "cudaStreamWaitEvent");
   return HICACHE_OK;
 }
 
