@@ -44,8 +44,11 @@
  *     against the caller's compute is the caller's (record an event before a
  *     backup; use hicache_wait_layer for loads).
  *   - Every argument is validated BEFORE anything is enqueued: a call that
- *     returns an error has enqueued nothing.  n == 0 is valid and launches no
- *     kernel (hicache_load_layer still records its layer event).
+ *     returns a validation error has enqueued nothing.  (A CUDA error while
+ *     launching the second or later launch of a call split over several
+ *     launches leaves the earlier ones enqueued.)  n == 0 is valid and launches
+ *     no kernel (hicache_load_layer still records its layer event).
+ *   - Transfers must be called with the pool's device current.
  *   - Return value: HICACHE_OK (0) or a negative hicache_status; the text of
  *     the last error of the calling thread is in hicache_last_error().
  *   - Thread safety: a pool may be used from several host threads at once

@@ -229,7 +229,9 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
 // Copy runs[next..] into job `j` of the parameters, starting at blob word
 // `word`: at most max_runs runs and kMaxTiles tiles (so the kernel's 32-bit
 // grid-stride index never overflows).  Returns the number of runs taken, or -1
-// if even one run is too large.
+// if even one run is too large -- which the run cap of the pre-pass rules out:
+// a unit stays below 2^31 vectors, i.e. 2^21 tiles, times at most 512 outer
+// units is 2^30 = kMaxTiles.
 int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
                  int64_t max_runs, hicache::XferParams &params, int32_t word, int j) {
   hicache::Job &job = params.h.job[j];
@@ -263,6 +265,10 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
             void *stream) {
   const bool bidir = load_runs != nullptr;
   if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != pool->device)
+    return set_error(HICACHE_ERR_INVALID_ARG, "the calling thread's device (%d) is not the pool's (%d)",
+                     cur, pool->device);
   const Shape &s = pool->shape;
   const bool all = layer < 0;
   const int32_t nb = int32_t(s.B * s.L);
