@@ -77,8 +77,12 @@ def test_backup_and_load_threads_get_fused():
         host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
         kv = hc.DeviceKV(bufs, Dp)
         with hc.Engine(pool) as eng:
-            # a big first request keeps the link busy while the threads submit
-            first = eng.submit(kv, perm[:96], hperm[:96], hc.BACKUP)
+            # the first request waits on a stream that is busy for ~50 ms, so the
+            # threads' requests queue up behind it
+            blocker = torch.cuda.Stream()
+            with torch.cuda.stream(blocker):
+                torch.cuda._sleep(int(1e8))
+            first = eng.submit(kv, perm[:96], hperm[:96], hc.BACKUP, after_stream=blocker)
             got_tickets = []
 
             def submitter(reqs):
@@ -152,10 +156,10 @@ def test_refused_requests_are_not_queued():
 
 @pytest.mark.parametrize("conflict", [False, True], ids=["commutes", "conflicts"])
 def test_lookahead_pairs_only_commuting_requests(conflict):
-    """Queue: a long backup B0 (keeps the link busy), then backups B1, B2 and a
-    load L1.  B1 goes out right behind B0; L1 is paired with B2 when it
-    commutes with it, and otherwise follows it alone.  Either way the result is
-    the oracle's in submission order."""
+    """Queue: a backup B0 held back by a busy stream, then backups B1, B2 and a
+    load L1.  B1 goes out right behind B0; L1 is paired with B2 (or with B1,
+    overtaking B2) when it commutes, and otherwise follows alone.  Either way
+    the result is the oracle's in submission order."""
     B, L, P, R, Dp, Hp = 2, 8, 16, 1024, 512, 512
     rng = np.random.default_rng(97)
     bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=97)
@@ -172,12 +176,67 @@ def test_lookahead_pairs_only_commuting_requests(conflict):
         host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
         kv = hc.DeviceKV(bufs, Dp)
         with hc.Engine(pool) as eng:
-            ts = [eng.submit(kv, dp, hp, d) for d, dp, hp in (b0, b1, b2, l1)]
+            blocker = torch.cuda.Stream()        # holds B0 for ~50 ms while the rest queue
+            with torch.cuda.stream(blocker):
+                torch.cuda._sleep(int(1e8))
+            ts = [eng.submit(kv, b0[1], b0[2], b0[0], after_stream=blocker)]
+            ts += [eng.submit(kv, dp, hp, d) for d, dp, hp in (b1, b2, l1)]
             for t in ts:
                 eng.wait(t)
             launches, fused = eng.stats()
         assert (launches, fused) == ((4, 0) if conflict else (3, 1))
         oracle_apply([b0, b1, b2, l1], dev0, host0, B, L, P, R, Hp, 2)
+        assert np.array_equal(host.view(np.uint16), host0)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], dev0[k])
+
+
+def test_three_threads_hammer_one_engine():
+    """Three threads each submit 80 random requests on their own disjoint
+    device and host pages (so the outcome does not depend on how the threads
+    interleave) and wait on their own tickets as they go."""
+    B, L, P, R, Dp, Hp = 2, 4, 8, 256, 96, 96
+    rng = np.random.default_rng(99)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=99)
+    dperm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    parts = [(dperm[i::3], hperm[i::3]) for i in range(3)]
+    plans = []
+    for t, (dpages, hpages) in enumerate(parts):
+        r = np.random.default_rng(200 + t)
+        reqs = []
+        for _ in range(80):
+            n = int(r.integers(1, 9))
+            reqs.append((int(r.integers(0, 2)), r.choice(dpages, n, replace=False), r.choice(hpages, n, replace=False)))
+        plans.append(reqs)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        host0, dev0 = host.view(np.uint16).copy(), gh.to_np(bufs, 2)
+        kv = hc.DeviceKV(bufs, Dp)
+        errors = []
+        with hc.Engine(pool) as eng:
+            def worker(reqs):
+                try:
+                    ts = []
+                    for k, (d, dp, hp) in enumerate(reqs):
+                        ts.append(eng.submit(kv, dp, hp, d))
+                        if k % 7 == 6:
+                            eng.wait(ts[k - 3])
+                    for t in ts:
+                        eng.wait(t)
+                except Exception as e:  # reported below
+                    errors.append(e)
+            ths = [threading.Thread(target=worker, args=(p,)) for p in plans]
+            for t in ths:
+                t.start()
+            for t in ths:
+                t.join()
+            launches, fused = eng.stats()
+        assert not errors, errors
+        assert launches + fused == 240
+        for reqs in plans:
+            oracle_apply(reqs, dev0, host0, B, L, P, R, Hp, 1)
         assert np.array_equal(host.view(np.uint16), host0)
         got = gh.to_np(bufs, 2)
         for k in range(B * L):
