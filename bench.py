@@ -476,12 +476,24 @@ def bench_mla_overlap(torch, hc, args):
                 hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
                                   stream=comp)
 
+        def pipelined():
+            plan.load_pipelined(kv, stream=xfer)
+
+        def overlapped_pipelined(reps):
+            plan.load_pipelined(kv, stream=xfer)
+            for layer in range(L):
+                pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
         a = timed(loads)
         whole = timed(one_load)
+        ap = timed(pipelined)
         c1 = timed(lambda: computes(1))
         reps = max(1, int(round(a / c1)))          # stand-in attention about as long as the loads
         b = timed(lambda: computes(reps))
         c = timed(lambda: overlapped(reps))
+        cp = timed(lambda: overlapped_pipelined(reps))
         a2 = timed(loads_two_streams)
         c2 = timed(lambda: overlapped_two_streams(reps))
         out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
@@ -491,6 +503,9 @@ def bench_mla_overlap(torch, hc, args):
             "compute_ms": round(b * 1e3, 3), "compute_reps": reps,
             "overlapped_ms": round(c * 1e3, 3),
             "overlap_efficiency": round((a + b - c) / min(a, b), 3),
+            "pipelined_load_ms": round(ap * 1e3, 3), "pipelined_load_gbs": round(nbytes / ap / GB, 1),
+            "overlapped_pipelined_ms": round(cp * 1e3, 3),
+            "overlap_efficiency_pipelined": round((ap + b - cp) / min(ap, b), 3),
             "per_layer_loads_2streams_ms": round(a2 * 1e3, 3),
             "per_layer_load_2streams_gbs": round(nbytes / a2 / GB, 1),
             "overlapped_2streams_ms": round(c2 * 1e3, 3),

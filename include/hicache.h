@@ -203,6 +203,27 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
                         const int64_t *load_host_pages, int64_t n_load, int32_t layout,
                         void *stream);
 
+/* L2 -> L1, every layer in ONE launch that moves the layers in order and marks
+ * each layer done on the device as it lands: after this call,
+ * hicache_wait_layer(pool, l, stream) makes `stream` wait for layer l alone
+ * (a stream memory wait on a per-layer counter, cuStreamWaitValue32), so
+ * attention on layer l can start while later layers still load -- the
+ * per-layer overlap of "HiCache 시스템 설계와 최적화", section "CPU→GPU 전송
+ * 최적화", without a launch and an event per layer.  The layer events are
+ * recorded too, once the whole load is in.  Checks as hicache_load.  A
+ * pipelined load may only go on another stream than the pool's previous one
+ * once that one's pipelined loads have finished (INVALID_ARG otherwise): the
+ * per-layer counts must rise in load order.  CUDA if the driver offers no
+ * stream memory wait. */
+int hicache_load_pipelined(hicache_pool *pool, const hicache_device_kv *kv,
+                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                           int32_t layout, void *stream);
+
+/* Diagnostic: the value of layer `layer`'s counter now (*done; reads device
+ * memory, synchronously on the legacy stream) and the value the pipelined loads
+ * enqueued so far will bring it to (*target). */
+int hicache_pipeline_status(hicache_pool *pool, int32_t layer, uint32_t *done, uint32_t *target);
+
 /* ---- plans: pre-pass once, execute many times -------------------------------
  * A plan holds the validated, sorted, run-merged index set of one transfer, so
  * that the L per-layer loads of one request pay for validation and the pre-pass
@@ -217,6 +238,9 @@ int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const i
  * records that layer's event).  kv->device_num_pages must be >= the plan's. */
 int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                          int32_t layer_id, void *stream);
+/* hicache_load_pipelined for a load plan. */
+int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                                void *stream);
 /* Number of pages and of merged runs in a plan. */
 int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs);
 int hicache_plan_destroy(hicache_plan *plan);
@@ -224,10 +248,12 @@ int hicache_plan_destroy(hicache_plan *plan);
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
 /* The pool-owned event recorded by the last load of `layer` (*event_out is a
- * cudaEvent_t; do not destroy it). */
+ * cudaEvent_t; do not destroy it).  After a pipelined load it fires when the
+ * whole load is in; hicache_wait_layer waits for the layer alone. */
 int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
 /* Make `compute_stream` wait (on the device; the host does not block) for the
- * last load of `layer` enqueued before this call. */
+ * last load of `layer` enqueued before this call: its layer event, or, if that
+ * load was pipelined, that layer's counter. */
 int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
 
 /* Block the calling host thread until all work on `stream` is done, for at

@@ -1,0 +1,121 @@
+"""Pipelined loads: every layer in one launch, each layer signalled on the
+device as it lands.  The counting is checked first without any wait; the
+tests that wait on it use a bounded host wait, so a counting error fails a
+test instead of blocking a stream for good."""
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gb300 as hc
+from tiered_kv_cache_gb300 import build as hc_build
+from tiered_kv_cache_gb300 import workloads as wl
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+LAYOUTS = list(hc.LAYOUTS.values())
+TEN_S = 10_000_000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    hc_build.build()
+    torch.cuda.init()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_pipelined_load_parity_and_counts(layout):
+    B, L, P, R, Dp, Hp, n = 2, 5, 16, 128, 64, 64, 30
+    rng = np.random.default_rng(300 + layout)
+    dp = wl.fragmented_pages(rng, Dp, n)
+    hp = rng.choice(Hp, n, replace=False)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=300)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        gh.sentinel_fill(bufs)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        c0 = hc.launch_count()
+        for rep in range(2):                   # the counts accumulate over loads
+            pool.load_pipelined(hc.DeviceKV(bufs, Dp), dp, hp, stream=s)
+        s.synchronize()
+        assert hc.launch_count() - c0 == 2
+        targets = set()
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target and target > 0, (layer, done, target)
+            targets.add(target)
+        assert len(targets) == 1               # every layer has the same tiles
+        want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, layout)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k])
+
+
+def test_compute_waits_for_each_layer():
+    """The stand-in attention on a second stream, behind wait_layer per layer,
+    sees every layer fully loaded; the transfer is one launch."""
+    B, L, P, R, Dp, Hp, n = 1, 12, 64, 576, 128, 128, 100
+    rng = np.random.default_rng(310)
+    dp = wl.fragmented_pages(rng, Dp, n)
+    hp = np.arange(n)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=310)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        gh.sentinel_fill(bufs, 0)
+        torch.cuda.synchronize()
+        kv = hc.DeviceKV(bufs, Dp)
+        xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        c0 = hc.launch_count()
+        plan.load_pipelined(kv, stream=xfer)
+        assert hc.launch_count() - c0 == 1
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        hc.wait(comp, TEN_S)
+        hc.wait(xfer, TEN_S)
+        want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+        got = sums.cpu().numpy().view(np.uint64)
+        for layer in range(L):
+            words = want[layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+            assert int(got[layer]) == int(words.astype(np.uint64).sum(dtype=np.uint64)), layer
+        plan.close()
+
+
+def test_wait_layer_follows_the_last_load_kind_and_stream_rule():
+    B, L, P, R, Dp, Hp = 1, 3, 4, 64, 8, 8
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        pool.host_array()[:] = 7
+        kv = hc.DeviceKV(bufs, Dp)
+        s1, s2, comp = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        with torch.cuda.stream(s1):
+            torch.cuda._sleep(int(2e8))                     # keep s1 busy for ~0.1 s
+        pool.load_pipelined(kv, [1], [2], stream=s1)
+        with pytest.raises(hc.HiCacheError) as e:          # still running on s1: not on s2
+            pool.load_pipelined(kv, [1], [2], stream=s2)
+        assert e.value.status == "INVALID_ARG"
+        pool.load_layer(kv, [3], [4], 1, stream=s2)         # an event-signalled load of layer 1
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+        with torch.cuda.stream(comp):
+            a = torch.stack([b[1 * P:2 * P].sum() for b in bufs])
+            c = bufs[1][3 * P:4 * P].sum()
+        hc.wait(comp, TEN_S)
+        assert torch.all(a == 7 * P * R) and int(c) == 7 * P * R
+        hc.wait(s1, TEN_S)
+        pool.load_pipelined(kv, [5], [2], stream=s2)        # s1's load is done: s2 may go on
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+        with torch.cuda.stream(comp):
+            d = torch.stack([b[5 * P:6 * P].sum() for b in bufs])
+        hc.wait(comp, TEN_S)
+        assert torch.all(d == 7 * P * R)

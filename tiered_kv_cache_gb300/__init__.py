@@ -86,6 +86,9 @@ def _bind(lib):
         "hicache_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _i32, _vp]),
         "hicache_backup_load": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _vp, _vp, _i64,
                                                _i32, _vp]),
+        "hicache_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
+        "hicache_plan_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
+        "hicache_pipeline_status": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_uint32), _P(ctypes.c_uint32)]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
@@ -311,6 +314,11 @@ class Pool:
     def load(self, kv: DeviceKV, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
         self._xfer(library().hicache_load, kv, device_pages, host_pages, layout, stream)
 
+    def load_pipelined(self, kv: DeviceKV, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
+        """Every layer in one launch, each layer marked done on the device as it
+        lands (wait_layer then waits for that layer alone)."""
+        self._xfer(library().hicache_load_pipelined, kv, device_pages, host_pages, layout, stream)
+
     def load_layer(self, kv: DeviceKV, device_pages, host_pages, layer: int, layout=LAYOUT_POOL,
                    stream=None):
         self._xfer(library().hicache_load_layer, kv, device_pages, host_pages, layout, stream, layer)
@@ -334,6 +342,12 @@ class Pool:
         """The bytes of one host page (no copy), ready for an L3 write."""
         off, nb = self.page_span(host_page, buffer)
         return self.host_array(np.uint8)[off:off + nb]
+
+    def pipeline_status(self, layer: int):
+        """(counter now, value it will reach) for a layer's pipelined loads."""
+        d, t = ctypes.c_uint32(), ctypes.c_uint32()
+        _check(library().hicache_pipeline_status(self.handle, layer, ctypes.byref(d), ctypes.byref(t)))
+        return d.value, t.value
 
     def wait_layer(self, layer: int, compute_stream=None):
         _check(library().hicache_wait_layer(self.handle, layer, _stream(compute_stream)))
@@ -475,6 +489,12 @@ class Plan:
             layout = LAYOUTS[layout]
         _check(library().hicache_plan_execute(self.handle, ctypes.byref(kv.struct), layout, layer,
                                               _stream(stream)))
+
+    def load_pipelined(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_plan_load_pipelined(self.handle, ctypes.byref(kv.struct), layout,
+                                                     _stream(stream)))
 
     def info(self):
         n, r = ctypes.c_int64(), ctypes.c_int64()

@@ -7,6 +7,7 @@
 
 #include "hicache.h"
 
+#include <cuda.h>  // driver types for the stream memory wait (fetched at run time)
 #include <cuda_runtime.h>
 #include <sys/mman.h>
 #include <unistd.h>
@@ -233,7 +234,8 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
 // a unit stays below 2^31 vectors, i.e. 2^21 tiles, times at most 512 outer
 // units is 2^30 = kMaxTiles.
 int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
-                 int64_t max_runs, hicache::XferParams &params, int32_t word, int j) {
+                 int64_t max_runs, hicache::XferParams &params, int32_t word, int j,
+                 int64_t launch_factor = 1) {
   hicache::Job &job = params.h.job[j];
   hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
   int64_t tiles = 0;
@@ -241,7 +243,7 @@ int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int6
   while (next + size_t(count) < runs.size() && count < max_runs) {
     const RunRec &r = runs[next + size_t(count)];
     const int64_t t = (r.len * upp + hicache::kTileVecs - 1) / hicache::kTileVecs;
-    if ((tiles + t) * outers > kMaxTiles) {
+    if ((tiles + t) * outers * launch_factor > kMaxTiles) {
       if (count == 0) return -1;
       break;
     }
@@ -256,31 +258,11 @@ int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int6
   return count;
 }
 
-// Enqueue validated runs.  One direction: `runs` moves towards the host if
-// to_host; layer < 0 means every layer.  Both directions (`load_runs` not
-// NULL): `runs` is a backup and `load_runs` a load, every layer, one kernel
-// per chunk so the two directions share every CTA.
-int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
-            const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
-            void *stream) {
-  const bool bidir = load_runs != nullptr;
-  if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess || cur != pool->device)
-    return set_error(HICACHE_ERR_INVALID_ARG, "the calling thread's device (%d) is not the pool's (%d)",
-                     cur, pool->device);
+// Header fields shared by every launch of a pool (shape, host alias, dividers).
+void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, hicache::XferParams &params,
+                 int64_t upp, int32_t layer) {
   const Shape &s = pool->shape;
-  const bool all = layer < 0;
   const int32_t nb = int32_t(s.B * s.L);
-  // units: (buffer, layer, run) for layer_first with every layer; (run) for
-  // page_first_direct_kv with every layer; (buffer, run) otherwise
-  const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
-  const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
-  const int64_t outers = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
-  const int64_t upp = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
-  const int64_t capacity = (hicache::kBlobWords - nb) / 2;  // runs per launch
-
-  thread_local hicache::XferParams params;
   hicache::XferHeader &h = params.h;
   h.host = pool->host_dev;
   h.L = int32_t(s.L);
@@ -288,7 +270,7 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   h.V = int32_t(s.V);
   h.num_bufs = nb;
   h.B = int32_t(s.B);
-  h.layer = all ? 0 : layer;
+  h.layer = layer;
   h.Hp = int32_t(s.Hp);
   h.unit_per_page = uint32_t(upp);
   h.PV = uint32_t(s.PV);
@@ -303,6 +285,40 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   h.job[1] = hicache::Job{0, nb, 0, 0};
   for (int32_t i = 0; i < nb; ++i)
     params.blob[i] = uint64_t(reinterpret_cast<uintptr_t>(kv->buf_ptrs[i]));
+}
+
+int check_device(const hicache_pool *pool) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != pool->device)
+    return set_error(HICACHE_ERR_INVALID_ARG, "the calling thread's device (%d) is not the pool's (%d)",
+                     cur, pool->device);
+  return HICACHE_OK;
+}
+
+// Enqueue validated runs.  One direction: `runs` moves towards the host if
+// to_host; layer < 0 means every layer.  Both directions (`load_runs` not
+// NULL): `runs` is a backup and `load_runs` a load, every layer, one kernel
+// per chunk so the two directions share every CTA.
+int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
+            const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
+            void *stream) {
+  const bool bidir = load_runs != nullptr;
+  if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
+  if (int rc = check_device(pool)) return rc;
+  const Shape &s = pool->shape;
+  const bool all = layer < 0;
+  const int32_t nb = int32_t(s.B * s.L);
+  // units: (buffer, layer, run) for layer_first with every layer; (run) for
+  // page_first_direct_kv with every layer; (buffer, run) otherwise
+  const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
+  const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
+  const int64_t outers = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
+  const int64_t upp = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
+  const int64_t capacity = (hicache::kBlobWords - nb) / 2;  // runs per launch
+
+  thread_local hicache::XferParams params;
+  hicache::XferHeader &h = params.h;
+  fill_header(pool, kv, params, upp, all ? 0 : layer);
 
   size_t next0 = 0, next1 = 0;
   const size_t n1 = bidir ? load_runs->size() : 0;
@@ -333,6 +349,77 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     next0 += size_t(c0);
     next1 += size_t(c1);
   }
+  return HICACHE_OK;
+}
+
+using WaitValue32Fn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+// cuStreamWaitValue32 from the driver, fetched through the runtime (no link
+// against the driver library); nullptr if the driver does not offer it.
+WaitValue32Fn wait_value32() {
+  static WaitValue32Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WaitValue32Fn>(p);
+  });
+  return fn;
+}
+
+int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
+                      int32_t layout, void *stream) {
+  if (int rc = check_device(pool)) return rc;
+  if (!wait_value32())
+    return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  // the counts stay in order while pipelined loads follow one another on one
+  // stream; another stream is fine once the earlier ones have finished
+  if (pool->pipeline_stream_set && pool->pipeline_stream != stream &&
+      cudaEventQuery(pool->pipeline_last) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "a pipelined load of this pool is still running on another stream");
+  }
+  pool->pipeline_stream_set = true;
+  pool->pipeline_stream = stream;
+  const Shape &s = pool->shape;
+  const int32_t nb = int32_t(s.B * s.L);
+  thread_local hicache::XferParams params;
+  fill_header(pool, kv, params, s.PV, 0);
+  size_t next = 0;
+  while (next < runs.size()) {
+    // one layer's units are (buffer, run); the launch covers L layers of them
+    const int32_t c = fill_job(runs, next, s.PV, s.B, (hicache::kBlobWords - nb) / 2, params, nb, 0, s.L);
+    if (c < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+    hicache::XferLaunch x;
+    x.params = &params;
+    x.words = nb + 2 * c;
+    x.layout = layout;
+    x.all_layers = false;
+    x.to_host = false;
+    x.bidir = false;
+    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_pipelined_load(x, pool->layer_done);
+    if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    for (int64_t l = 0; l < s.L; ++l) {
+      pool->layer_target[size_t(l)] += uint32_t(params.h.job[0].total_tiles);
+      pool->layer_signal[size_t(l)] = 1;
+    }
+    next += size_t(c);
+  }
+  // the layer events also fire, once the whole load is in
+  for (int64_t l = 0; l < s.L; ++l) {
+    const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+  }
+  const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
   return HICACHE_OK;
 }
 
@@ -372,6 +459,8 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
   if (layer >= 0) {
     const cudaError_t e = cudaEventRecord(pool->events[size_t(layer)], static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+    std::lock_guard<std::mutex> g(pool->signal_mu);
+    pool->layer_signal[size_t(layer)] = 0;
   }
   return HICACHE_OK;
 }
@@ -499,6 +588,19 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
       return cuda_error(e, "cudaEventCreateWithFlags");
     }
   }
+  e = cudaEventCreateWithFlags(&p->pipeline_last, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    hicache_pool_destroy(p);
+    return cuda_error(e, "cudaEventCreateWithFlags");
+  }
+  p->layer_target.assign(size_t(s.L), 0);
+  p->layer_signal.assign(size_t(s.L), 0);
+  e = cudaMalloc(reinterpret_cast<void **>(&p->layer_done), size_t(s.L) * sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(p->layer_done, 0, size_t(s.L) * sizeof(unsigned int));
+  if (e != cudaSuccess) {
+    hicache_pool_destroy(p);
+    return cuda_error(e, "per-layer counters");
+  }
   *out = p;
   return HICACHE_OK;
 }
@@ -507,6 +609,8 @@ int hicache_pool_destroy(hicache_pool *pool) {
   if (!pool) return HICACHE_OK;
   for (auto ev : pool->events)
     if (ev) cudaEventDestroy(ev);
+  if (pool->layer_done) cudaFree(pool->layer_done);
+  if (pool->pipeline_last) cudaEventDestroy(pool->pipeline_last);
   delete pool;
   return HICACHE_OK;
 }
@@ -610,8 +714,52 @@ int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, 
     const cudaError_t e =
         cudaEventRecord(pool->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+    std::lock_guard<std::mutex> g(pool->signal_mu);
+    pool->layer_signal[size_t(layer_id)] = 0;
   }
   return HICACHE_OK;
+}
+
+int hicache_load_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
+                           const int64_t *host_pages, int64_t n, int32_t layout, void *stream) {
+  g_last_error.clear();
+  if (!pool) return set_error(HICACHE_ERR_INVALID_ARG, "pool is NULL");
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, 0))) return rc;
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, device_pages, host_pages, n, HICACHE_DIR_LOAD,
+                    max_run_pages(pool->shape), &runs)))
+    return rc;
+  return enqueue_pipelined(pool, kv, runs, lay, stream);
+}
+
+int hicache_pipeline_status(hicache_pool *pool, int32_t layer, uint32_t *done, uint32_t *target) {
+  g_last_error.clear();
+  if (!pool || !done || !target) return set_error(HICACHE_ERR_INVALID_ARG, "NULL argument");
+  if (layer < 0 || layer >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer, (long long)pool->shape.L);
+  unsigned int v = 0;
+  const cudaError_t e = cudaMemcpy(&v, pool->layer_done + layer, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_error(e, "cudaMemcpy(layer counter)");
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  *done = v;
+  *target = pool->layer_target[size_t(layer)];
+  return HICACHE_OK;
+}
+
+int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                                void *stream) {
+  g_last_error.clear();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a pipelined transfer must be a load");
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, plan->pool->shape.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(plan->pool, kv, plan->device_num_pages))) return rc;
+  return enqueue_pipelined(plan->pool, kv, plan->runs, lay, stream);
 }
 
 int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs) {
@@ -643,6 +791,16 @@ int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream) 
   if (layer < 0 || layer >= pool->shape.L)
     return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
                      (long long)pool->shape.L);
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  if (pool->layer_signal[size_t(layer)] == 1) {
+    // the last load of this layer was pipelined: wait for its counter
+    const CUresult r = wait_value32()(static_cast<CUstream>(compute_stream),
+                                      reinterpret_cast<CUdeviceptr>(pool->layer_done + layer),
+                                      pool->layer_target[size_t(layer)], CU_STREAM_WAIT_VALUE_GEQ);
+    if (r != CUDA_SUCCESS)
+      return set_error(HICACHE_ERR_CUDA, "cuStreamWaitValue32 failed (%d)", int(r));
+    return HICACHE_OK;
+  }
   const cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream),
                                             pool->events[size_t(layer)], 0);
   if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent");

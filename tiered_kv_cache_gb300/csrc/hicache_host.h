@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "hicache.h"
@@ -43,6 +44,19 @@ struct hicache_pool {
   int device = 0;
   int ctas = 0;
   std::vector<cudaEvent_t> events;  // one per layer
+
+  // Per-layer completion of pipelined loads (hicache_load_pipelined): device
+  // counters that the kernel raises as layers land, the value each must reach
+  // for the last pipelined load, which signal hicache_wait_layer should use
+  // for each layer (0: the layer event, 1: the counter), and the one stream
+  // all pipelined loads of the pool go on (which keeps the counts in order).
+  unsigned int *layer_done = nullptr;
+  std::mutex signal_mu;
+  std::vector<uint32_t> layer_target;
+  std::vector<uint8_t> layer_signal;
+  bool pipeline_stream_set = false;
+  void *pipeline_stream = nullptr;
+  cudaEvent_t pipeline_last = nullptr;  // recorded after each pipelined load
 };
 
 namespace hicache {
@@ -52,5 +66,9 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
             void *stream);
+// Enqueue validated load runs as pipelined launches (every layer, layer by
+// layer, per-layer counters) and update the pool's per-layer signals.
+int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
+                      int32_t layout, void *stream);
 
 }  // namespace hicache

@@ -134,6 +134,9 @@ struct XferLaunch {
   void *stream;
 };
 int launch_xfer(const XferLaunch &x);
+// Every layer of a load, layer by layer, in one launch; layer_done[l] grows by
+// job[0].total_tiles (the tiles of one layer) once layer l has landed.
+int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done);
 // Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).
 int set_error_text(int code, const char *msg);
 int launch_checksum(const ChecksumParams &p, int grid, void *stream);

@@ -107,7 +107,7 @@ __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bu
 // loads issued before the first store.
 template <int LAYOUT, bool ALL, bool TO_HOST>
 __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, const Run *runs,
-                                          uint4 *const *bufs, int32_t g) {
+                                          uint4 *const *bufs, int32_t g, int layer) {
   const int32_t outer = g / job.tiles_per_outer;
   const int32_t inner = g - outer * job.tiles_per_outer;
   int b, l;
@@ -116,7 +116,7 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
     l = outer - b * h.L;
   } else {
     b = outer;
-    l = h.layer;
+    l = layer;
   }
   // the run holding tile `inner`: the last run with tile0 <= inner
   int lo = 0, hi = job.n_runs - 1;
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
   const Job &job = p.h.job[0];
   const Run *runs = job_runs(p, 0);
   for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x)
-    move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g);
+    move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g, p.h.layer);
 }
 
 // Both directions in one launch: job 0 is a backup, job 1 a load, every layer.
@@ -191,13 +191,37 @@ __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__
   while (ib < jb.total_tiles || il < jl.total_tiles) {
     const bool do_backup = il >= jl.total_tiles || (backup_turn && ib < jb.total_tiles);
     if (do_backup) {
-      move_tile<LAYOUT, true, true>(p.h, jb, rb, s_bufs, ib);
+      move_tile<LAYOUT, true, true>(p.h, jb, rb, s_bufs, ib, 0);
       ib += gridDim.x;
     } else {
-      move_tile<LAYOUT, true, false>(p.h, jl, rl, s_bufs, il);
+      move_tile<LAYOUT, true, false>(p.h, jl, rl, s_bufs, il, 0);
       il += gridDim.x;
     }
     backup_turn = !backup_turn;
+  }
+}
+
+// Every layer of a load in one launch, layer by layer: tile g of the launch
+// is tile (g mod T) of layer g / T, where T = the tiles of one layer.  After
+// each tile the CTA adds one to its layer's counter, behind a fence, so a
+// layer's counter grows by T once the whole layer has landed; a compute stream
+// waits for that with a stream memory wait instead of a per-layer launch and
+// event.  CTAs walk the tiles in order, so layers finish about in order.
+template <int LAYOUT, class Params>
+__global__ void __launch_bounds__(kThreads)
+    pipelined_load_kernel(const __grid_constant__ Params p, unsigned int *layer_done) {
+  __shared__ uint4 *s_bufs[kMaxBufs];
+  load_buffer_table(p, s_bufs);
+  const Job &job = p.h.job[0];
+  const Run *runs = job_runs(p, 0);
+  const int32_t per_layer = job.total_tiles;            // tiles of one layer
+  const int32_t total = per_layer * p.h.L;
+  for (int32_t g = blockIdx.x; g < total; g += gridDim.x) {
+    const int32_t layer = g / per_layer;
+    move_tile<LAYOUT, false, false>(p.h, job, runs, s_bufs, g - layer * per_layer, layer);
+    __threadfence();                                    // this thread's stores, device-wide
+    __syncthreads();                                    // every thread of the tile is past its fence
+    if (threadIdx.x == 0) atomicAdd(&layer_done[layer], 1u);
   }
 }
 
@@ -259,7 +283,29 @@ cudaError_t launch_layout(const XferLaunch &x) {
   return x.to_host ? launch_one<LAYOUT, false, true>(x) : launch_one<LAYOUT, false, false>(x);
 }
 
+template <int LAYOUT>
+cudaError_t launch_pipelined_layout(const XferLaunch &x, unsigned int *layer_done) {
+  const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  if (x.words <= kBlobWordsSmall) {
+    XferParamsSmall small;
+    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small), layer_done);
+  } else {
+    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params, layer_done);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done) {
+  switch (x.layout) {
+    case kLayerFirst: return int(launch_pipelined_layout<kLayerFirst>(x, layer_done));
+    case kPageFirst: return int(launch_pipelined_layout<kPageFirst>(x, layer_done));
+    case kPageFirstDirect: return int(launch_pipelined_layout<kPageFirstDirect>(x, layer_done));
+    case kPageFirstDirectKV: return int(launch_pipelined_layout<kPageFirstDirectKV>(x, layer_done));
+    default: return int(cudaErrorInvalidValue);
+  }
+}
 
 int launch_xfer(const XferLaunch &x) {
   switch (x.layout) {
