@@ -238,6 +238,29 @@ int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const i
  * records that layer's event).  kv->device_num_pages must be >= the plan's. */
 int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                          int32_t layer_id, void *stream);
+/* hicache_load_pipelined without any allocation.  The pages have no
+ * counterpart to this entry point: it serves callers that cannot allocate
+ * device memory when they load -- for example an engine whose device memory is
+ * all handed out by its own allocator, or a code path that must not call
+ * cudaMalloc.  hicache_load_pipelined keeps its per-layer counters in memory
+ * the pool allocated; this one keeps them in a fixed array inside the library
+ * (256 layers at most, 1 KiB), which every GPU that loads the library holds
+ * until the process exits, so the call itself allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.  Inputs and outputs are the
+ * caller's, as for hicache_load_pipelined, and hicache_wait_layer waits for
+ * each layer the same way.
+ *   - More than 256 layers: INVALID_ARG, nothing enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its counts there;
+ *     the library tracks the values they reach, so nothing needs clearing
+ *     between calls.  Calls whose loads overlap on the GPU (e.g. on two
+ *     streams at once, from any pool) race on the counts: issue them one
+ *     after another.
+ * Other errors as hicache_load_pipelined. */
+int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *kv,
+                                   const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                                   int32_t layout, void *stream);
 /* hicache_load_pipelined for a load plan. */
 int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                                 void *stream);

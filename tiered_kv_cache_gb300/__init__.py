@@ -88,6 +88,7 @@ def _bind(lib):
                                                _i32, _vp]),
         "hicache_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
         "hicache_plan_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
+        "hicache_load_pipelined_noalloc": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
         "hicache_pipeline_status": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_uint32), _P(ctypes.c_uint32)]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),

@@ -762,6 +762,76 @@ int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_k
   return enqueue_pipelined(plan->pool, kv, plan->runs, lay, stream);
 }
 
+// ---- allocation-free pipelined load ---------------------------------------------
+namespace {
+// The value the library's static counters reach once every allocation-free
+// pipelined load enqueued so far on a device has landed, per device and layer.
+std::mutex g_noalloc_mu;
+uint32_t g_noalloc_target[hicache::kNoAllocMaxDevices][hicache::kNoAllocMaxLayers];
+}  // namespace
+
+int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *kv,
+                                   const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                                   int32_t layout, void *stream) {
+  g_last_error.clear();
+  if (!pool) return set_error(HICACHE_ERR_INVALID_ARG, "pool is NULL");
+  const Shape &s = pool->shape;
+  if (s.L > hicache::kNoAllocMaxLayers)
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "the allocation-free pipelined load takes at most %d layers; this pool has %lld",
+                     hicache::kNoAllocMaxLayers, (long long)s.L);
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, s.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, 0))) return rc;
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(s.Hp, kv->device_num_pages, device_pages, host_pages, n, HICACHE_DIR_LOAD,
+                    max_run_pages(s), &runs)))
+    return rc;
+  if ((rc = check_device(pool))) return rc;
+  if (!wait_value32())
+    return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
+  unsigned int *counters = nullptr;
+  const int ce = hicache::noalloc_layer_counters(&counters);
+  if (ce != 0) return cuda_error(cudaError_t(ce), "address of the static layer counters");
+  const int32_t nb = int32_t(s.B * s.L);
+  thread_local hicache::XferParams params;
+  fill_header(pool, kv, params, s.PV, 0);
+  std::lock_guard<std::mutex> gg(g_noalloc_mu);
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  uint32_t *target = g_noalloc_target[pool->device];
+  size_t next = 0;
+  while (next < runs.size()) {
+    const int32_t c = fill_job(runs, next, s.PV, s.B, (hicache::kBlobWords - nb) / 2, params, nb, 0, s.L);
+    if (c < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+    hicache::XferLaunch x;
+    x.params = &params;
+    x.words = nb + 2 * c;
+    x.layout = lay;
+    x.all_layers = false;
+    x.to_host = false;
+    x.bidir = false;
+    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_pipelined_load(x, counters);
+    if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    for (int64_t l = 0; l < s.L; ++l) target[l] += uint32_t(params.h.job[0].total_tiles);
+    next += size_t(c);
+  }
+  pool->noalloc_done = counters;
+  if (pool->noalloc_target.size() != size_t(s.L)) pool->noalloc_target.assign(size_t(s.L), 0);
+  for (int64_t l = 0; l < s.L; ++l) {
+    pool->noalloc_target[size_t(l)] = target[l];
+    pool->layer_signal[size_t(l)] = 2;
+  }
+  for (int64_t l = 0; l < s.L; ++l) {
+    const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+  }
+  return HICACHE_OK;
+}
+
 int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs) {
   g_last_error.clear();
   if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
@@ -792,6 +862,15 @@ int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream) 
     return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
                      (long long)pool->shape.L);
   std::lock_guard<std::mutex> g(pool->signal_mu);
+  if (pool->layer_signal[size_t(layer)] == 2) {
+    // the last load of this layer was an allocation-free pipelined load
+    const CUresult r = wait_value32()(static_cast<CUstream>(compute_stream),
+                                      reinterpret_cast<CUdeviceptr>(pool->noalloc_done + layer),
+                                      pool->noalloc_target[size_t(layer)], CU_STREAM_WAIT_VALUE_GEQ);
+    if (r != CUDA_SUCCESS)
+      return set_error(HICACHE_ERR_CUDA, "cuStreamWaitValue32 failed (%d)", int(r));
+    return HICACHE_OK;
+  }
   if (pool->layer_signal[size_t(layer)] == 1) {
     // the last load of this layer was pipelined: wait for its counter
     const CUresult r = wait_value32()(static_cast<CUstream>(compute_stream),

@@ -57,6 +57,10 @@ struct hicache_pool {
   bool pipeline_stream_set = false;
   void *pipeline_stream = nullptr;
   cudaEvent_t pipeline_last = nullptr;  // recorded after each pipelined load
+  // Allocation-free pipelined loads (signal 2): the library's static counters
+  // on this device and, per layer, the value the last such load brings them to.
+  unsigned int *noalloc_done = nullptr;
+  std::vector<uint32_t> noalloc_target;
 };
 
 namespace hicache {

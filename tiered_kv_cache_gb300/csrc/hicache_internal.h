@@ -137,6 +137,12 @@ int launch_xfer(const XferLaunch &x);
 // Every layer of a load, layer by layer, in one launch; layer_done[l] grows by
 // job[0].total_tiles (the tiles of one layer) once layer l has landed.
 int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done);
+// Counters of allocation-free pipelined loads: a static device array of
+// kNoAllocMaxLayers entries; *out receives its device address on the current
+// device (looked up once per device).  Returns a cudaError_t value.
+constexpr int kNoAllocMaxLayers = 256;
+constexpr int kNoAllocMaxDevices = 64;
+int noalloc_layer_counters(unsigned int **out);
 // Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).
 int set_error_text(int code, const char *msg);
 int launch_checksum(const ChecksumParams &p, int grid, void *stream);

@@ -35,6 +35,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "hicache_internal.h"
 
 namespace hicache {
@@ -305,6 +307,34 @@ int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done) {
     case kPageFirstDirectKV: return int(launch_pipelined_layout<kPageFirstDirectKV>(x, layer_done));
     default: return int(cudaErrorInvalidValue);
   }
+}
+
+// Per-layer counters for pipelined loads made without any allocation
+// (hicache_load_pipelined_noalloc): a fixed array in the library's own device
+// memory, loaded with the module on every GPU that uses the library and kept
+// until the process exits.  Every such call on a device shares it; the counts
+// only ever grow (the host keeps the matching targets), so nothing needs
+// clearing between calls -- the array starts at zero when the module loads.
+static __device__ __align__(256) unsigned int g_noalloc_layer_done[kNoAllocMaxLayers];
+
+int noalloc_layer_counters(unsigned int **out) {
+  // The array's name is only a stand-in in host code: the kernel needs its
+  // device address, looked up once per device with that device current.
+  static std::mutex mu;
+  static unsigned int *addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return int(e);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return int(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> g(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_layer_done);
+    if (e != cudaSuccess) return int(e);
+    addr[dev] = static_cast<unsigned int *>(p);
+  }
+  *out = addr[dev];
+  return 0;
 }
 
 int launch_xfer(const XferLaunch &x) {
