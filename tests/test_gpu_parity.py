@@ -485,3 +485,32 @@ def test_backup_thread_and_load_thread_share_a_pool():
         got = gh.to_np(bufs, 2)
         for k in range(B * L):
             assert np.array_equal(got[k], want_dev[k])
+
+
+def test_layer_first_contiguous_equals_plain_range_copies():
+    """In layer_first with pages contiguous on both sides, a backup is one range
+    copy per (buffer, layer): the same bytes a plain cudaMemcpyAsync of each
+    buffer's range into the host pool gives (the library-routine special case)."""
+    B, L, P, R, Dp, Hp, n, d0, h0 = 2, 5, 16, 256, 64, 80, 24, 9, 31
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=400)
+    dp, hp = np.arange(d0, d0 + n), np.arange(h0, h0 + n)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = 0
+        c0 = hc.launch_count()
+        pool.backup(hc.DeviceKV(bufs, Dp), dp, hp)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 == 1
+        got = host.copy()
+        assert hc.segment_count(L, B, P, R, Hp, "layer_first", dp, hp) == B * L
+        # the same ranges with the copy engine
+        host[:] = 0
+        row = R * 2
+        dst = torch.from_numpy(host)
+        for b in range(B):
+            for l in range(L):
+                off = ((b * L + l) * Hp * P + h0 * P) * row
+                src = bufs[b * L + l].view(torch.uint8).reshape(-1)[d0 * P * row:(d0 + n) * P * row]
+                dst[off:off + n * P * row].copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(got, host)
