@@ -119,3 +119,42 @@ def test_wait_layer_follows_the_last_load_kind_and_stream_rule():
             d = torch.stack([b[5 * P:6 * P].sum() for b in bufs])
         hc.wait(comp, TEN_S)
         assert torch.all(d == 7 * P * R)
+
+
+def test_pipelined_load_split_over_several_launches():
+    """4,000 scattered one-token pages are more runs than one launch holds: the
+    pipelined load is split, each launch adds its tiles to every layer's count,
+    and each layer is waited for correctly."""
+    B, L, P, R, Dp, Hp, n = 2, 3, 1, 8, 9000, 9000, 4000
+    rng = np.random.default_rng(320)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=320)
+    with hc.Pool(L, B, P, R, Hp, "page_first_direct") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        gh.sentinel_fill(bufs, 0)
+        torch.cuda.synchronize()
+        kv = hc.DeviceKV(bufs, Dp)
+        xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        c0 = hc.launch_count()
+        pool.load_pipelined(kv, dp, hp, stream=xfer)
+        assert hc.launch_count() - c0 >= 3
+        hc.wait(xfer, TEN_S)
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target > 0
+        want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 2)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k])
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        hc.wait(comp, TEN_S)
+        got_s = sums.cpu().numpy().view(np.uint64)
+        for layer in range(L):
+            words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+                                    for b in range(B)])
+            assert int(got_s[layer]) == int(words.astype(np.uint64).sum(dtype=np.uint64))

@@ -74,6 +74,32 @@ def test_noalloc_load_matches_the_allocating_load(layout):
                 assert int(got[layer]) == int(words.astype(np.uint64).sum(dtype=np.uint64)), (call, layer)
 
 
+def test_noalloc_load_split_over_several_launches_matches():
+    """4,000 scattered one-token pages need several launches; two such calls in
+    a row give the same device buffers as the allocating entry point."""
+    B, L, P, R, Dp, Hp, n = 2, 3, 1, 8, 9000, 9000, 4000
+    rng = np.random.default_rng(510)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        ref = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+        out = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+        xfer = torch.cuda.Stream()
+        for call in range(2):
+            dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+            pool.load_pipelined(hc.DeviceKV(ref, Dp), dp, hp, stream=xfer)
+            c0 = hc.launch_count()
+            assert noalloc_load(pool, hc.DeviceKV(out, Dp), dp, hp, xfer) == 0
+            assert hc.launch_count() - c0 >= 3
+            comp = torch.cuda.Stream()
+            for layer in range(L):
+                pool.wait_layer(layer, comp)
+            hc.wait(comp, TEN_S)
+            hc.wait(xfer, TEN_S)
+            for k in range(B * L):
+                assert torch.equal(out[k], ref[k]), (call, k)
+
+
 def test_noalloc_load_refuses_more_layers_than_it_holds():
     L, P, R, Dp, Hp = 257, 2, 8, 4, 4
     bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(L)]
