@@ -103,8 +103,9 @@ typedef struct {
   int64_t row_elems;        /* R: kv_heads*head_dim, or kv_dim (e.g. 576) */
   int64_t host_num_pages;   /* Hp: pages in the host pool */
   int32_t layout;           /* hicache_layout of the host pool (not POOL) */
-  int32_t launch_ctas;      /* CTAs per direction of a transfer launch (a fused
-                               backup+load gets twice as many); 0 = one per SM */
+  int32_t launch_ctas;      /* CTAs of a transfer launch (a fused backup+load
+                               gets twice as many); 0 = the default: one per SM
+                               for a load, five per eight SMs for a backup */
   int32_t flags;            /* must be 0 */
   int32_t reserved;         /* must be 0 */
 } hicache_pool_desc;

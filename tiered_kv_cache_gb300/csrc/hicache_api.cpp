@@ -340,8 +340,9 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     x.to_host = to_host;
     x.bidir = bidir;
     const int64_t tiles = int64_t(h.job[0].total_tiles) + (bidir ? h.job[1].total_tiles : 0);
-    // a fused launch carries both directions: one share of CTAs for each
-    x.grid = int(std::min<int64_t>(tiles, (bidir ? 2 : 1) * int64_t(pool->ctas)));
+    // a fused launch carries both directions: one load share of CTAs for each
+    const int64_t ctas = bidir ? 2 * int64_t(pool->ctas) : to_host ? pool->backup_ctas : pool->ctas;
+    x.grid = int(std::min<int64_t>(tiles, ctas));
     x.stream = stream;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
@@ -580,6 +581,9 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
   p->host_bytes = host_bytes;
   p->device = dev;
   p->ctas = desc->launch_ctas > 0 ? desc->launch_ctas : sms * hicache::kDefaultCtasPerSm;
+  p->backup_ctas = desc->launch_ctas > 0
+                       ? desc->launch_ctas
+                       : std::max(1, sms * hicache::kDefaultBackupCtasPer8Sm / 8);
   p->events.resize(size_t(s.L), nullptr);
   for (auto &ev : p->events) {
     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);

@@ -42,7 +42,8 @@ struct hicache_pool {
   void *host_dev = nullptr;   // device-visible alias
   size_t host_bytes = 0;
   int device = 0;
-  int ctas = 0;
+  int ctas = 0;         // grid of a load (a fused launch takes twice this)
+  int backup_ctas = 0;  // grid of a backup
   std::vector<cudaEvent_t> events;  // one per layer
 
   // Per-layer completion of pipelined loads (hicache_load_pipelined): device

@@ -24,9 +24,15 @@ constexpr int kBlobWords = 3584;                 // 28 KiB of kernel parameters:
                                                  // pointers, then the run table
 constexpr int kBlobWordsSmall = 480;             // the same in under 4 KiB, for calls
                                                  // whose table fits (cheaper to launch)
-// One CTA per SM and direction saturates the host link (16 KiB in flight per
+// One CTA per SM saturates the host link for a load (16 KiB in flight per
 // CTA) and leaves the rest of each SM to the compute the transfer overlaps.
 constexpr int kDefaultCtasPerSm = 1;
+// A backup saturates the link with far fewer CTAs: its host writes are posted,
+// so it needs no round trip per tile.  With a whole SM's share it also takes
+// more than its half of the link from a load running at the same time on
+// another stream, and the pair finishes late.  Five CTAs per eight SMs keeps a
+// backup alone at the link's rate and lets the two directions finish together.
+constexpr int kDefaultBackupCtasPer8Sm = 5;
 
 // ---- division by a run-time constant ---------------------------------------
 // q = floor(n / d) for 0 <= n < 2^31 by one multiply-high, an add and a shift:
