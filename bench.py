@@ -827,6 +827,10 @@ def main():
             "load_frac_of_link": frac(ld, link["h2d_gbs"]),
             "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
             "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
+            # per-op launch times over the timed steps (GB/s above are from the mean)
+            "ms": {op: {"median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
+                        "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"])}
+                   for op in ("backup", "load", "bidir", "bidir_fused")},
         }
     # dominant single-direction kernel: the largest total time
     singles = {k: sum(v) for k, v in per.items() if "bidir" not in k}

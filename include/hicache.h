@@ -239,6 +239,15 @@ int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const i
  * records that layer's event).  kv->device_num_pages must be >= the plan's. */
 int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                          int32_t layer_id, void *stream);
+/* Load one layer of a load plan and record that layer's event: the per-layer
+ * load of the pages ("Why compute, H2D, and D2H should stay in one GPU
+ * execution domain"), with the index pre-pass done once at plan creation.
+ * Same as hicache_plan_execute with layer_id >= 0, except that a negative
+ * layer_id is INVALID_ARG here.  Errors: INVALID_ARG (NULL plan, backup plan,
+ * layer_id outside [0, num_layers), bad layout or kv), CUDA; on error nothing
+ * is enqueued. */
+int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                            int32_t layer_id, void *stream);
 /* hicache_load_pipelined without any allocation.  The pages have no
  * counterpart to this entry point: it serves callers that cannot allocate
  * device memory when they load -- for example an engine whose device memory is

@@ -133,6 +133,42 @@ def test_plan_execute_matches_direct_calls(layout):
         lplan.close()
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_plan_load_layer_touches_one_layer(layout):
+    """hicache_plan_load_layer equals the oracle's load of that layer alone and
+    leaves the other layers as they were; its layer event gates a stream."""
+    B, L, P, R, Dp, Hp, n = 2, 5, 8, 64, 40, 50, 17
+    dp, hp = indices("runs", Dp, Hp, n, seed=41)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=42)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = np.random.default_rng(43).integers(0, 256, host.size, dtype=np.uint8)
+        kv = hc.DeviceKV(bufs, Dp)
+        lplan = pool.plan(dp, hp, Dp, hc.LOAD)
+        s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        for layer in (3, 0):
+            gh.sentinel_fill(bufs)
+            torch.cuda.synchronize()
+            lplan.load_layer(kv, layer, stream=s)
+            pool.wait_layer(layer, comp)
+            hc.wait(comp, 10_000_000)
+            want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+            gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, layout, layer)
+            got = gh.to_np(bufs, 2)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want[k]), (layer, k)
+        c0 = hc.launch_count()
+        for bad in (-1, L):
+            with pytest.raises(hc.HiCacheError):
+                lplan.load_layer(kv, bad, stream=s)
+        bplan = pool.plan(dp, hp, Dp, hc.BACKUP)
+        with pytest.raises(hc.HiCacheError):
+            bplan.load_layer(kv, 0, stream=s)
+        assert hc.launch_count() == c0
+        bplan.close()
+        lplan.close()
+
+
 def test_one_launch_per_call_and_errors_enqueue_nothing():
     B, L, P, R, Dp, Hp = 2, 32, 16, 1024, 64, 64
     bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]

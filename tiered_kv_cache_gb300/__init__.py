@@ -92,6 +92,7 @@ def _bind(lib):
         "hicache_pipeline_status": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_uint32), _P(ctypes.c_uint32)]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
+        "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
         "hicache_plan_destroy": (ctypes.c_int, [_vp]),
         "hicache_layer_event": (ctypes.c_int, [_vp, _i32, _P(_vp)]),
@@ -490,6 +491,13 @@ class Plan:
             layout = LAYOUTS[layout]
         _check(library().hicache_plan_execute(self.handle, ctypes.byref(kv.struct), layout, layer,
                                               _stream(stream)))
+
+    def load_layer(self, kv: DeviceKV, layer: int, layout=LAYOUT_POOL, stream=None):
+        """Load one layer of a load plan and record that layer's event."""
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_plan_load_layer(self.handle, ctypes.byref(kv.struct), layout, layer,
+                                                 _stream(stream)))
 
     def load_pipelined(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
         if isinstance(layout, str):

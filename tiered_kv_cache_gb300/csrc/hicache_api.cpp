@@ -724,6 +724,13 @@ int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, 
   return HICACHE_OK;
 }
 
+int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                            int32_t layer_id, void *stream) {
+  g_last_error.clear();
+  if (layer_id < 0) return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d is negative", layer_id);
+  return hicache_plan_execute(plan, kv, layout, layer_id, stream);
+}
+
 int hicache_load_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *device_pages,
                            const int64_t *host_pages, int64_t n, int32_t layout, void *stream) {
   g_last_error.clear();
