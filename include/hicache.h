@@ -254,7 +254,8 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
  * all handed out by its own allocator, or a code path that must not call
  * cudaMalloc.  hicache_load_pipelined keeps its per-layer counters in memory
  * the pool allocated; this one keeps them in a fixed array inside the library
- * (256 layers at most, 1 KiB), which every GPU that loads the library holds
+ * (256 layers at most; 1.5 KiB with the kernel's tile-scheduling words, which
+ * calls take in turn from 64 pairs), which every GPU that loads the library holds
  * until the process exits, so the call itself allocates nothing: no cudaMalloc,
  * no cudaFree, no allocating library routine.  Inputs and outputs are the
  * caller's, as for hicache_load_pipelined, and hicache_wait_layer waits for

@@ -158,3 +158,32 @@ def test_pipelined_load_split_over_several_launches():
             words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
                                     for b in range(B)])
             assert int(got_s[layer]) == int(words.astype(np.uint64).sum(dtype=np.uint64))
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 300])
+def test_tile_counter_covers_every_tile_and_resets(ctas):
+    """CTAs take tiles from the pool's scheduler word: with 1, 7 or 300 CTAs
+    every tile is moved, and three loads in a row each start from tile 0 (a
+    scheduler left non-zero would skip the first tiles of the next load)."""
+    B, L, P, R, Dp, Hp, n = 2, 6, 8, 256, 96, 96, 40
+    rng = np.random.default_rng(700 + ctas)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=701)
+    with hc.Pool(L, B, P, R, Hp, "page_first", launch_ctas=ctas) as pool:
+        host = pool.host_array(np.uint8)
+        kv = hc.DeviceKV(bufs, Dp)
+        s = torch.cuda.Stream()
+        for call in range(3):
+            dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+            host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+            gh.sentinel_fill(bufs)
+            torch.cuda.synchronize()
+            pool.load_pipelined(kv, dp, hp, stream=s)
+            hc.wait(s, TEN_S)
+            want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+            gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+            got = gh.to_np(bufs, 2)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want[k]), (call, k)
+            for layer in range(L):
+                done, target = pool.pipeline_status(layer)
+                assert done == target

@@ -405,7 +405,7 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
     x.bidir = false;
     x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
     x.stream = stream;
-    const int e = hicache::launch_pipelined_load(x, pool->layer_done);
+    const int e = hicache::launch_pipelined_load(x, pool->layer_done, pool->layer_done + s.L);
     if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     for (int64_t l = 0; l < s.L; ++l) {
@@ -599,8 +599,9 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
   }
   p->layer_target.assign(size_t(s.L), 0);
   p->layer_signal.assign(size_t(s.L), 0);
-  e = cudaMalloc(reinterpret_cast<void **>(&p->layer_done), size_t(s.L) * sizeof(unsigned int));
-  if (e == cudaSuccess) e = cudaMemset(p->layer_done, 0, size_t(s.L) * sizeof(unsigned int));
+  // L layer counters, then the two scheduler words of the pipelined kernel
+  e = cudaMalloc(reinterpret_cast<void **>(&p->layer_done), size_t(s.L + 2) * sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(p->layer_done, 0, size_t(s.L + 2) * sizeof(unsigned int));
   if (e != cudaSuccess) {
     hicache_pool_destroy(p);
     return cuda_error(e, "per-layer counters");
@@ -779,6 +780,7 @@ namespace {
 // pipelined load enqueued so far on a device has landed, per device and layer.
 std::mutex g_noalloc_mu;
 uint32_t g_noalloc_target[hicache::kNoAllocMaxDevices][hicache::kNoAllocMaxLayers];
+uint32_t g_noalloc_slot[hicache::kNoAllocMaxDevices];  // next scheduler pair, per device
 }  // namespace
 
 int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *kv,
@@ -824,7 +826,9 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
     x.bidir = false;
     x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
     x.stream = stream;
-    const int e = hicache::launch_pipelined_load(x, counters);
+    unsigned int *sched = counters + hicache::kNoAllocMaxLayers +
+                          2 * (g_noalloc_slot[pool->device]++ % hicache::kNoAllocSchedSlots);
+    const int e = hicache::launch_pipelined_load(x, counters, sched);
     if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     for (int64_t l = 0; l < s.L; ++l) target[l] += uint32_t(params.h.job[0].total_tiles);

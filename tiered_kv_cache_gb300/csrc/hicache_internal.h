@@ -142,11 +142,16 @@ struct XferLaunch {
 int launch_xfer(const XferLaunch &x);
 // Every layer of a load, layer by layer, in one launch; layer_done[l] grows by
 // job[0].total_tiles (the tiles of one layer) once layer l has landed.
-int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done);
+// sched: two device words, zero at launch, that the launch leaves at zero (its
+// tile counter and exit count); launches that may overlap on the GPU need
+// their own.
+int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done, unsigned int *sched);
 // Counters of allocation-free pipelined loads: a static device array of
-// kNoAllocMaxLayers entries; *out receives its device address on the current
-// device (looked up once per device).  Returns a cudaError_t value.
+// kNoAllocMaxLayers layer counters followed by kNoAllocSchedSlots scheduler
+// pairs; *out receives its device address on the current device (looked up
+// once per device).  Returns a cudaError_t value.
 constexpr int kNoAllocMaxLayers = 256;
+constexpr int kNoAllocSchedSlots = 64;
 constexpr int kNoAllocMaxDevices = 64;
 int noalloc_layer_counters(unsigned int **out);
 // Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).

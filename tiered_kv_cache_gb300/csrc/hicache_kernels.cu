@@ -208,22 +208,47 @@ __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__
 // each tile the CTA adds one to its layer's counter, behind a fence, so a
 // layer's counter grows by T once the whole layer has landed; a compute stream
 // waits for that with a stream memory wait instead of a per-layer launch and
-// event.  CTAs walk the tiles in order, so layers finish about in order.
+// event.
+//
+// CTAs take tiles from a counter (sched[0]) rather than by grid stride.  The
+// CTAs do not all move at the same rate over the host link, and with a fixed
+// share each a layer is only complete when its slowest CTA gets there: the
+// fast CTAs run layers ahead while the early layers finish late and the last
+// ones all at once.  Taken from a counter, the tiles in flight are always the
+// next ones in order, so layer l lands at about (l + 1) / L of the load.
+// sched[1] counts the CTAs that are done; the last one puts both words back
+// to zero for the next launch on the same scheduler words.
 template <int LAYOUT, class Params>
 __global__ void __launch_bounds__(kThreads)
-    pipelined_load_kernel(const __grid_constant__ Params p, unsigned int *layer_done) {
+    pipelined_load_kernel(const __grid_constant__ Params p, unsigned int *layer_done,
+                          unsigned int *sched) {
   __shared__ uint4 *s_bufs[kMaxBufs];
+  __shared__ int32_t s_next;
   load_buffer_table(p, s_bufs);
   const Job &job = p.h.job[0];
   const Run *runs = job_runs(p, 0);
   const int32_t per_layer = job.total_tiles;            // tiles of one layer
   const int32_t total = per_layer * p.h.L;
-  for (int32_t g = blockIdx.x; g < total; g += gridDim.x) {
+  if (threadIdx.x == 0) s_next = int32_t(atomicAdd(&sched[0], 1u));
+  __syncthreads();
+  for (int32_t g = s_next; g < total; g = s_next) {
     const int32_t layer = g / per_layer;
     move_tile<LAYOUT, false, false>(p.h, job, runs, s_bufs, g - layer * per_layer, layer);
     __threadfence();                                    // this thread's stores, device-wide
-    __syncthreads();                                    // every thread of the tile is past its fence
-    if (threadIdx.x == 0) atomicAdd(&layer_done[layer], 1u);
+    __syncthreads();                                    // every thread is past its fence and has read s_next
+    if (threadIdx.x == 0) {
+      atomicAdd(&layer_done[layer], 1u);
+      s_next = int32_t(atomicAdd(&sched[0], 1u));
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();                                    // this CTA's last take before its exit count
+    if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+      __threadfence();                                  // every CTA's takes before the reset
+      atomicExch(&sched[0], 0u);
+      atomicExch(&sched[1], 0u);
+    }
   }
 }
 
@@ -286,36 +311,39 @@ cudaError_t launch_layout(const XferLaunch &x) {
 }
 
 template <int LAYOUT>
-cudaError_t launch_pipelined_layout(const XferLaunch &x, unsigned int *layer_done) {
+cudaError_t launch_pipelined_layout(const XferLaunch &x, unsigned int *layer_done, unsigned int *sched) {
   const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
   if (x.words <= kBlobWordsSmall) {
     XferParamsSmall small;
-    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small), layer_done);
+    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small), layer_done, sched);
   } else {
-    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params, layer_done);
+    pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params, layer_done, sched);
   }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done) {
+int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done, unsigned int *sched) {
   switch (x.layout) {
-    case kLayerFirst: return int(launch_pipelined_layout<kLayerFirst>(x, layer_done));
-    case kPageFirst: return int(launch_pipelined_layout<kPageFirst>(x, layer_done));
-    case kPageFirstDirect: return int(launch_pipelined_layout<kPageFirstDirect>(x, layer_done));
-    case kPageFirstDirectKV: return int(launch_pipelined_layout<kPageFirstDirectKV>(x, layer_done));
+    case kLayerFirst: return int(launch_pipelined_layout<kLayerFirst>(x, layer_done, sched));
+    case kPageFirst: return int(launch_pipelined_layout<kPageFirst>(x, layer_done, sched));
+    case kPageFirstDirect: return int(launch_pipelined_layout<kPageFirstDirect>(x, layer_done, sched));
+    case kPageFirstDirectKV: return int(launch_pipelined_layout<kPageFirstDirectKV>(x, layer_done, sched));
     default: return int(cudaErrorInvalidValue);
   }
 }
 
-// Per-layer counters for pipelined loads made without any allocation
-// (hicache_load_pipelined_noalloc): a fixed array in the library's own device
-// memory, loaded with the module on every GPU that uses the library and kept
-// until the process exits.  Every such call on a device shares it; the counts
-// only ever grow (the host keeps the matching targets), so nothing needs
-// clearing between calls -- the array starts at zero when the module loads.
-static __device__ __align__(256) unsigned int g_noalloc_layer_done[kNoAllocMaxLayers];
+// Per-layer counters and scheduler words for pipelined loads made without any
+// allocation (hicache_load_pipelined_noalloc): a fixed array in the library's
+// own device memory, loaded with the module on every GPU that uses the library
+// and kept until the process exits.  Every such call on a device shares the
+// layer counters; the counts only ever grow (the host keeps the matching
+// targets), so nothing needs clearing between calls -- the array starts at
+// zero when the module loads.  The scheduler words come in kNoAllocSchedSlots
+// pairs that calls take in turn; each launch leaves its pair at zero.
+static __device__ __align__(256) unsigned int
+    g_noalloc_counters[kNoAllocMaxLayers + 2 * kNoAllocSchedSlots];
 
 int noalloc_layer_counters(unsigned int **out) {
   // The array's name is only a stand-in in host code: the kernel needs its
@@ -329,7 +357,7 @@ int noalloc_layer_counters(unsigned int **out) {
   std::lock_guard<std::mutex> g(mu);
   if (!addr[dev]) {
     void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_layer_done);
+    e = cudaGetSymbolAddress(&p, g_noalloc_counters);
     if (e != cudaSuccess) return int(e);
     addr[dev] = static_cast<unsigned int *>(p);
   }
