@@ -517,6 +517,80 @@ def bench_mla_overlap(torch, hc, args):
     return out, launches
 
 
+def bench_nsa_group(torch, hc, args):
+    """A buffer group: an MLA latent (576 bf16) beside an fp8 indexer key (128)
+    and its fp32 scales (4 per row), 61 layers, page 64, three page_first pools
+    carved from one pinned allocation.  Loads of 4K / 16K / 64K tokens, every
+    layer and layer by layer: one launch per pool vs one group launch.  Each
+    variant is enqueued behind a sleep kernel on a gate stream, so the device
+    time excludes the host's enqueue cost, which is reported beside it."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.MLA_LATENT
+    L, P, Dp, Hp = s.num_layers, s.page_size, s.device_pages, s.host_pages
+    kinds = [(576, 2), (128, 1), (4, 4)]
+    sizes = [L * Hp * P * R * es for R, es in kinds]
+    mem = hc.PinnedHost(sum(sizes))
+    pools, kvs, keep, off = [], [], [], 0
+    g = torch.Generator(device="cuda")
+    g.manual_seed(s.seed)
+    for (R, es), nbytes in zip(kinds, sizes):
+        pools.append(hc.Pool(L, 1, P, R, Hp, "page_first", elem_bytes=es, host_ptr=mem.ptr + off,
+                             host_bytes=nbytes, launch_ctas=args.ctas))
+        bufs = [torch.randint(0, 256, (Dp * P, R * es), dtype=torch.uint8, device="cuda", generator=g)
+                for _ in range(L)]
+        keep.append(bufs)
+        kvs.append(hc.DeviceKV(bufs, Dp))
+        off += nbytes
+    page_bytes = sum(L * P * R * es for R, es in kinds)
+    gate, stream = torch.cuda.Stream(), torch.cuda.Stream()
+    launches0 = hc.launch_count()
+
+    def gated(fn):
+        dev, host = [], []
+        for it in range(max(args.warmup, 3) + args.steps):
+            torch.cuda.synchronize()
+            with torch.cuda.stream(gate):
+                torch.cuda._sleep(int(4e7))        # ~20 ms: longer than any enqueue below
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(gate)
+            stream.wait_event(e0)
+            h0 = time.perf_counter()
+            fn()
+            h1 = time.perf_counter()
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= max(args.warmup, 3):
+                dev.append(_elapsed(torch, e0, e1))
+                host.append(h1 - h0)
+        return statistics.median(dev), statistics.median(host)
+
+    out = {}
+    for tokens in (4096, 16384, 65536):
+        t = wl.mla_transfer(s, tokens)
+        dp, hp = t.device_pages, t.host_pages
+        nbytes = len(dp) * page_bytes
+        variants = {
+            "per_layer_per_pool": lambda: [pool.load_layer(kv, dp, hp, layer, stream=stream)
+                                           for layer in range(L) for pool, kv in zip(pools, kvs)],
+            "per_layer_group": lambda: [hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, layer=layer,
+                                                          stream=stream) for layer in range(L)],
+            "all_layers_per_pool": lambda: [pool.load(kv, dp, hp, stream=stream) for pool, kv in zip(pools, kvs)],
+            "all_layers_group": lambda: hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, stream=stream),
+        }
+        r = {"pages": len(dp), "bytes": nbytes}
+        for name, fn in variants.items():
+            d, h = gated(fn)
+            r[name] = {"device_ms": round(d * 1e3, 3), "gbs": round(nbytes / d / GB, 1),
+                       "host_enqueue_ms": round(h * 1e3, 3)}
+        out[f"{tokens // 1024}k"] = r
+    launches = hc.launch_count() - launches0
+    for pool in pools:
+        pool.close()
+    del keep
+    return out, launches
+
+
 def bench_small_mix(torch, hc, args):
     """10,000 seeded requests, 1-256 pages log-uniform, 30% backup / 70% load,
     random pages, layer_first.  Per-call latency = host wall clock from the API
@@ -712,7 +786,7 @@ def main():
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc",
-                             "engine_bidir"],
+                             "engine_bidir", "nsa_group"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
     ap.add_argument("--layouts", default="pages",
@@ -740,9 +814,17 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch)
-    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir"):
+    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group"):
         t0 = time.perf_counter()
-        if args.workload == "engine_bidir":
+        if args.workload == "nsa_group":
+            res, launches = bench_nsa_group(torch, hc, args)
+            value = res["4k"]["per_layer_group"]["gbs"]
+            what = {"workload": "nsa_group: 61 layers, page 64, page_first; an MLA latent (576 bf16), an fp8 "
+                                "indexer key (128) and fp32 scales (4) as three pools of one pinned "
+                                "allocation; 4K/16K/64K-token loads, per layer and every layer, one launch "
+                                "per pool vs one group launch; device time behind a gate stream",
+                    "value": "GB/s of the 61 per-layer group loads at 4K tokens"}
+        elif args.workload == "engine_bidir":
             res = bench_engine_bidir(torch, hc, args)
             launches = None
             value = res["engine_gbs"]

@@ -279,6 +279,34 @@ int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_k
 int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs);
 int hicache_plan_destroy(hicache_plan *plan);
 
+/* ---- buffer groups: several buffer kinds, one launch -------------------------
+ * Models whose layers keep more than one kind of KV row hold one pool per
+ * kind, each with its own row size and element size: the MLA and NSA models
+ * of "Tuning SGLang HiCache L2 on Kunlunxin P800/P900" (section 2.7) and the
+ * MLA-class CSA/HCA caches of "Baidu's KVCache Overhaul" (section
+ * "Optimization Techniques"), e.g. a 576-element bf16 latent beside a
+ * sparse-attention indexer key of 128 fp8 and its fp32 scales.  Those pools share the page
+ * numbering: page p of the request is page p in every pool.  This call moves
+ * the same page pairs for all of them in ONE kernel launch (the run table is
+ * worked out once; every pool gets its own tile range and shape constants),
+ * where separate calls would launch once per pool.
+ *   pools[i], kvs[i]: pool i and its device buffers, i < npools, 1 <= npools
+ *     <= HICACHE_MAX_GROUP.  All pools on one device, with equal num_layers
+ *     and page_size and the same resolved layout; the sum of B*L over the
+ *     pools <= 512.
+ *   device_pages / host_pages / n: as hicache_backup and hicache_load; every
+ *     index must be inside every pool (and every kvs[i]).
+ *   direction: HICACHE_DIR_BACKUP or HICACHE_DIR_LOAD.
+ *   layer_id: < 0 moves every layer; >= 0 moves that layer only (a load only)
+ *     and records that layer's event in every pool, as hicache_load_layer.
+ * Errors as hicache_backup / hicache_load, plus INVALID_ARG for a mismatch
+ * between the pools; on error nothing is enqueued.  A call whose run table
+ * does not fit one launch is split into several, as the single-pool calls. */
+#define HICACHE_MAX_GROUP 4
+int hicache_group_transfer(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools,
+                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                           int32_t layout, int32_t layer_id, int32_t direction, void *stream);
+
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
 /* The pool-owned event recorded by the last load of `layer` (*event_out is a

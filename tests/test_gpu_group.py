@@ -1,0 +1,205 @@
+"""Buffer groups on the GPU: several pools with different row shapes, sharing
+the page numbering, moved in one launch (hicache_group_transfer).  Every pool
+of the group must match the oracle's own transfer of that pool."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import tiered_kv_cache_gb300 as hc
+from tiered_kv_cache_gb300 import workloads as wl
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = list(hc.LAYOUTS.values())
+TEN_S = 10_000_000
+# (buffers, row elements, element bytes): an MLA latent of 576 bf16, an fp8
+# indexer key of 128, and its fp32 scales (4 per row, 16 bytes)
+NSA_KINDS = [(1, 576, 2), (1, 128, 1), (1, 4, 4)]
+
+
+class Group:
+    """Pools carved from one pinned allocation, with their device buffers."""
+
+    def __init__(self, kinds, L, P, Dp, Hp, layout, seed, hps=None):
+        self.kinds, self.L, self.P, self.Dp = kinds, L, P, Dp
+        self.hps = hps or [Hp] * len(kinds)
+        sizes = [B * L * h * P * R * es for (B, R, es), h in zip(kinds, self.hps)]
+        self.mem = hc.PinnedHost(sum(sizes))
+        self.pools, self.bufs, off = [], [], 0
+        for (B, R, es), h, nbytes in zip(kinds, self.hps, sizes):
+            self.pools.append(hc.Pool(L, B, P, R, h, layout, elem_bytes=es, host_ptr=self.mem.ptr + off,
+                                      host_bytes=nbytes))
+            self.bufs.append(gh.random_device_bufs(B, L, P, R, Dp, es, seed=seed + off % 89))
+            off += nbytes
+        self.kvs = [hc.DeviceKV(b, Dp) for b in self.bufs]
+
+    def close(self):
+        for p in self.pools:
+            p.close()
+
+
+def _want_backup(grp, dp, hp, layout, fill):
+    out = []
+    for pool, bufs, (B, R, es), h in zip(grp.pools, grp.bufs, grp.kinds, grp.hps):
+        want = np.full(pool.nbytes, fill, np.uint8).view(gh.NP_DT[es])
+        gh.orc().backup(gh.to_np(bufs, es), want, B, grp.L, grp.P, R, h, dp, hp, layout)
+        out.append(want)
+    return out
+
+
+def _want_load(grp, dp, hp, layout, fill, layer=-1):
+    out = []
+    for pool, (B, R, es), h in zip(grp.pools, grp.kinds, grp.hps):
+        want = [np.zeros((grp.Dp * grp.P, R), gh.NP_DT[es]) for _ in range(B * grp.L)]
+        for w in want:
+            w.view(np.uint8)[:] = fill
+        gh.orc().load(want, pool.host_array(gh.NP_DT[es]), B, grp.L, grp.P, R, h, dp, hp, layout, layer)
+        out.append(want)
+    return out
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_group_backup_and_load_match_the_oracle_in_one_launch(layout):
+    L, P, Dp, Hp, n = 6, 16, 40, 48, 14
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, layout, seed=60 + layout)
+    rng = np.random.default_rng(61 + layout)
+    dp = wl.fragmented_pages(rng, Dp, n, max_run=3)
+    hp = rng.choice(Hp, n, replace=False)
+    s = torch.cuda.Stream()
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = 0x3C
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP, stream=s)
+    assert hc.launch_count() - c0 == 1
+    hc.wait(s, TEN_S)
+    for pool, want, (B, R, es) in zip(grp.pools, _want_backup(grp, dp, hp, layout, 0x3C), grp.kinds):
+        assert np.array_equal(pool.host_array(gh.NP_DT[es]), want), (R, es)
+    # all layers back into other device pages, one launch
+    dst = rng.permutation(Dp)[:n]
+    for bufs in grp.bufs:
+        gh.sentinel_fill(bufs, 0x77)
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    hc.group_transfer(grp.pools, grp.kvs, dst, hp, hc.LOAD, stream=s)
+    assert hc.launch_count() - c0 == 1
+    hc.wait(s, TEN_S)
+    for bufs, want, (B, R, es) in zip(grp.bufs, _want_load(grp, dst, hp, layout, 0x77), grp.kinds):
+        got = gh.to_np(bufs, es)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k]), (R, es, k)
+    grp.close()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_group_layer_loads_touch_one_layer_and_record_every_pool_event(layout):
+    L, P, Dp, Hp, n = 5, 8, 32, 40, 11
+    kinds = [(2, 64, 2), (1, 32, 1), (1, 8, 2)]       # K,V beside two single-buffer kinds
+    grp = Group(kinds, L, P, Dp, Hp, layout, seed=70 + layout)
+    rng = np.random.default_rng(71 + layout)
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    dp = rng.permutation(Dp)[:n]
+    hp = wl.fragmented_pages(rng, Hp, n, max_run=4)
+    s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    sums = torch.zeros(len(kinds), dtype=torch.int64, device="cuda")
+    for layer in (4, 1):
+        for bufs in grp.bufs:
+            gh.sentinel_fill(bufs, 0x5A)
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.LOAD, layer=layer, stream=s)
+        assert hc.launch_count() - c0 == 1
+        # every pool's layer event gates a compute stream that reads the layer
+        sums.zero_()
+        for i, (pool, kv) in enumerate(zip(grp.pools, grp.kvs)):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * i, stream=comp)
+        hc.wait(comp, TEN_S)
+        for i, (bufs, want, (B, R, es)) in enumerate(
+                zip(grp.bufs, _want_load(grp, dp, hp, layout, 0x5A, layer), grp.kinds)):
+            got = gh.to_np(bufs, es)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want[k]), (layer, R, k)
+            words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+                                    for b in range(B)])
+            assert int(sums[i].item()) & (2**64 - 1) == int(words.astype(np.uint64).sum(dtype=np.uint64))
+    grp.close()
+
+
+def test_group_of_one_equals_the_single_pool_call():
+    L, P, Dp, Hp, n = 4, 16, 24, 24, 9
+    grp = Group([(2, 128, 2)], L, P, Dp, Hp, "page_first", seed=80)
+    rng = np.random.default_rng(81)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    pool = grp.pools[0]
+    pool.host_array(np.uint8)[:] = 0
+    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP)
+    torch.cuda.synchronize()
+    a = pool.host_array(np.uint8).copy()
+    pool.host_array(np.uint8)[:] = 0
+    pool.backup(grp.kvs[0], dp, hp)
+    torch.cuda.synchronize()
+    assert np.array_equal(a, pool.host_array(np.uint8))
+    grp.close()
+
+
+def test_group_with_more_runs_than_one_launch_holds():
+    """Scattered one-page runs beyond one launch's table: the group call is
+    split, every pool still matches the oracle."""
+    L, P, Dp, Hp, n = 2, 1, 6000, 6000, 2500
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "page_first_direct", seed=90)
+    rng = np.random.default_rng(91)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = 0xA5
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP)
+    assert hc.launch_count() - c0 >= 2
+    torch.cuda.synchronize()
+    for pool, want, (B, R, es) in zip(grp.pools, _want_backup(grp, dp, hp, 2, 0xA5), grp.kinds):
+        assert np.array_equal(pool.host_array(gh.NP_DT[es]), want), (R, es)
+    grp.close()
+
+
+def test_group_rejects_mismatches_and_enqueues_nothing():
+    L, P, Dp, Hp = 3, 8, 16, 16
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "layer_first", seed=95, hps=[16, 16, 12])
+    dp, hp = np.arange(4), np.arange(4)
+    other_l = hc.Pool(L + 1, 1, P, 64, Hp, "layer_first")
+    other_p = hc.Pool(L, 1, P * 2, 64, Hp, "layer_first")
+    other_lay = hc.Pool(L, 1, P, 64, Hp, "page_first")
+    kv_l = hc.DeviceKV(gh.random_device_bufs(1, L + 1, P, 64, Dp), Dp)
+    kv_p = hc.DeviceKV(gh.random_device_bufs(1, L, P * 2, 64, Dp), Dp)
+    kv_lay = hc.DeviceKV(gh.random_device_bufs(1, L, P, 64, Dp), Dp)
+    c0 = hc.launch_count()
+    bad = [
+        ([], [], dp, hp, hc.BACKUP, -1),                                        # no pools
+        (grp.pools + [other_lay, other_lay], grp.kvs + [kv_lay, kv_lay], dp, hp, hc.BACKUP, -1),  # 5 pools
+        (grp.pools[:1] + [other_l], grp.kvs[:1] + [kv_l], dp, hp, hc.BACKUP, -1),  # layers differ
+        (grp.pools[:1] + [other_p], grp.kvs[:1] + [kv_p], dp, hp, hc.BACKUP, -1),  # page sizes differ
+        (grp.pools[:1] + [other_lay], grp.kvs[:1] + [kv_lay], dp, hp, hc.BACKUP, -1),  # layouts differ
+        (grp.pools[:1] * 2, grp.kvs[:1] * 2, dp, hp, hc.BACKUP, -1),            # a pool twice
+        ([grp.pools[0], grp.pools[1]], [grp.kvs[0], grp.kvs[0]], dp, hp, hc.LOAD, -1),  # buffers shared
+        (grp.pools, grp.kvs, dp, hp, hc.BACKUP, 0),                             # per-layer backup
+        (grp.pools, grp.kvs, dp, hp, hc.LOAD, L),                               # layer out of range
+        (grp.pools, grp.kvs, dp, np.array([0, 1, 2, 13]), hc.LOAD, -1),         # past the smallest pool
+        (grp.pools, grp.kvs, np.array([0, 1, 2, 16]), hp, hc.BACKUP, -1),        # past the device pool
+        (grp.pools, grp.kvs, np.array([0, 1, 1, 2]), hp, hc.LOAD, -1),           # duplicate destination
+        (grp.pools, grp.kvs, dp, hp, 7, -1),                                     # no such direction
+    ]
+    for pools, kvs, d, h, direction, layer in bad:
+        with pytest.raises((hc.HiCacheError, ValueError)):
+            hc.group_transfer(pools, kvs, d, h, direction, layer=layer)
+    assert hc.launch_count() == c0
+    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP, layer=-1)   # the same call, valid
+    torch.cuda.synchronize()
+    assert hc.launch_count() == c0 + 1
+    for p in (other_l, other_p, other_lay):
+        p.close()
+    grp.close()

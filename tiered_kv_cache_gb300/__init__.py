@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
-    "PageAllocator", "Engine",
+    "PageAllocator", "Engine", "group_transfer", "MAX_GROUP",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
@@ -90,6 +90,8 @@ def _bind(lib):
         "hicache_plan_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
         "hicache_load_pipelined_noalloc": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _vp, _vp, _i64, _i32, _vp]),
         "hicache_pipeline_status": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_uint32), _P(ctypes.c_uint32)]),
+        "hicache_group_transfer": (ctypes.c_int, [_P(_vp), _P(_DeviceKVStruct), _i32, _vp, _vp, _i64, _i32,
+                                                  _i32, _i32, _vp]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
@@ -248,6 +250,27 @@ def layer_checksum(kv: DeviceKV, pool_or_desc, device_pages, layer: int, out_ptr
     dp = _idx(device_pages)
     _check(library().hicache_layer_checksum(ctypes.byref(kv.struct), ctypes.byref(desc), _ptr(dp),
                                             dp.size, layer, reps, out_ptr, _stream(stream)))
+
+
+MAX_GROUP = 4
+
+
+def group_transfer(pools, kvs, device_pages, host_pages, direction: int, layer: int = -1,
+                   layout=LAYOUT_POOL, stream=None):
+    """Move the same page pairs for several pools (buffer kinds with different
+    rows that share the page numbering) in one launch.  ``layer`` >= 0 loads
+    that layer alone and records its event in every pool."""
+    if len(pools) != len(kvs):
+        raise ValueError("pools and kvs differ in length")
+    dp, hp = _idx(device_pages), _idx(host_pages)
+    if dp.size != hp.size:
+        raise ValueError("device_pages and host_pages differ in length")
+    if isinstance(layout, str):
+        layout = LAYOUTS[layout]
+    handles = (ctypes.c_void_p * len(pools))(*[p.handle for p in pools])
+    structs = (_DeviceKVStruct * len(kvs))(*[k.struct for k in kvs])
+    _check(library().hicache_group_transfer(handles, structs, len(pools), _ptr(dp), _ptr(hp), dp.size,
+                                            layout, layer, direction, _stream(stream)))
 
 
 class PinnedHost:

@@ -233,11 +233,9 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
 // if even one run is too large -- which the run cap of the pre-pass rules out:
 // a unit stays below 2^31 vectors, i.e. 2^21 tiles, times at most 512 outer
 // units is 2^30 = kMaxTiles.
-int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
-                 int64_t max_runs, hicache::XferParams &params, int32_t word, int j,
-                 int64_t launch_factor = 1) {
-  hicache::Job &job = params.h.job[j];
-  hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
+int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
+                  int64_t max_runs, hicache::Job &job, hicache::Run *table, int32_t word,
+                  int64_t launch_factor) {
   int64_t tiles = 0;
   int32_t count = 0;
   while (next + size_t(count) < runs.size() && count < max_runs) {
@@ -258,12 +256,17 @@ int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int6
   return count;
 }
 
-// Header fields shared by every launch of a pool (shape, host alias, dividers).
-void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, hicache::XferParams &params,
-                 int64_t upp, int32_t layer) {
+int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
+                 int64_t max_runs, hicache::XferParams &params, int32_t word, int j,
+                 int64_t launch_factor = 1) {
+  return fill_runs(runs, next, upp, outers, max_runs, params.h.job[j],
+                   reinterpret_cast<hicache::Run *>(&params.blob[word]), word, launch_factor);
+}
+
+// A pool's shape, host alias and dividers, as one launch header.
+void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, hicache::XferHeader &h) {
   const Shape &s = pool->shape;
   const int32_t nb = int32_t(s.B * s.L);
-  hicache::XferHeader &h = params.h;
   h.host = pool->host_dev;
   h.L = int32_t(s.L);
   h.P = int32_t(s.P);
@@ -283,6 +286,13 @@ void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, hicache:
   h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
   h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
   h.job[1] = hicache::Job{0, nb, 0, 0};
+}
+
+// Header fields shared by every launch of a pool, and its buffer pointers.
+void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, hicache::XferParams &params,
+                 int64_t upp, int32_t layer) {
+  fill_shape(pool, upp, layer, params.h);
+  const int32_t nb = int32_t(pool->shape.B * pool->shape.L);
   for (int32_t i = 0; i < nb; ++i)
     params.blob[i] = uint64_t(reinterpret_cast<uintptr_t>(kv->buf_ptrs[i]));
 }
@@ -675,6 +685,141 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
   if (lrun.empty()) return enqueue(pool, kv, brun, nullptr, lay, -1, true, stream);
   if (brun.empty()) return enqueue(pool, kv, lrun, nullptr, lay, -1, false, stream);
   return enqueue(pool, kv, brun, &lrun, lay, -1, true, stream);
+}
+
+// ---- buffer groups ------------------------------------------------------------
+namespace hicache {
+
+// Enqueue validated runs for every pool of a group, one launch per chunk of
+// runs that fits the parameters of all of them.
+int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t np,
+                  const std::vector<RunRec> &runs, int32_t layout, int32_t layer, bool to_host,
+                  void *stream) {
+  if (runs.empty()) return HICACHE_OK;
+  const bool all = layer < 0;
+  thread_local hicache::GroupParams params;
+  hicache::GroupHeader &g = params.g;
+  g.njobs = np;
+  int32_t word = 0;
+  int64_t outers[hicache::kMaxGroup], upp[hicache::kMaxGroup];
+  for (int32_t j = 0; j < np; ++j) {
+    const Shape &s = pools[j]->shape;
+    const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
+    const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
+    outers[j] = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
+    upp[j] = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
+    fill_shape(pools[j], upp[j], all ? 0 : layer, g.h[j]);
+    g.bufs_word[j] = word;
+    for (int64_t i = 0; i < s.B * s.L; ++i)
+      params.blob[word++] = uint64_t(reinterpret_cast<uintptr_t>(kvs[j].buf_ptrs[i]));
+  }
+  g.num_bufs = word;
+  const int64_t capacity = (hicache::kGroupBlobWords - word) / (2 * np);  // runs per launch
+  const hicache_pool *p0 = pools[0];
+  size_t next = 0;
+  while (next < runs.size()) {
+    // the most runs every job's table and tile budget can take
+    int64_t c = capacity;
+    for (int32_t j = 0; j < np; ++j) {
+      hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
+      const int32_t cj = fill_runs(runs, next, upp[j], outers[j], c, g.h[j].job[0], table, word, np);
+      if (cj < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+      c = std::min<int64_t>(c, cj);
+    }
+    int64_t tiles = 0;
+    for (int32_t j = 0; j < np; ++j) {
+      const int32_t w = word + int32_t(2 * c) * j;
+      hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[w]);
+      fill_runs(runs, next, upp[j], outers[j], c, g.h[j].job[0], table, w, np);
+      g.tile_start[j] = int32_t(tiles);
+      tiles += g.h[j].job[0].total_tiles;
+    }
+    g.tile_start[np] = int32_t(tiles);
+    hicache::GroupLaunch x;
+    x.params = &params;
+    x.words = word + int32_t(2 * c) * np;
+    x.layout = layout;
+    x.all_layers = all;
+    x.to_host = to_host;
+    x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : p0->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_group(x);
+    if (e != 0) return cuda_error(cudaError_t(e), "group transfer kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    next += size_t(c);
+  }
+  return HICACHE_OK;
+}
+
+}  // namespace hicache
+
+int hicache_group_transfer(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools,
+                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                           int32_t layout, int32_t layer_id, int32_t direction, void *stream) {
+  g_last_error.clear();
+  if (!pools || !kvs) return set_error(HICACHE_ERR_INVALID_ARG, "pools or kvs is NULL");
+  if (npools < 1 || npools > HICACHE_MAX_GROUP)
+    return set_error(HICACHE_ERR_INVALID_ARG, "npools = %d outside [1, %d]", npools, HICACHE_MAX_GROUP);
+  if (direction != HICACHE_DIR_BACKUP && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "direction %d is neither backup nor load", direction);
+  for (int32_t i = 0; i < npools; ++i)
+    if (!pools[i]) return set_error(HICACHE_ERR_INVALID_ARG, "pool %d is NULL", i);
+  const hicache_pool *p0 = pools[0];
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, p0->shape.layout, &lay);
+  if (rc) return rc;
+  if (layer_id >= p0->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)p0->shape.L);
+  if (layer_id >= 0 && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  int64_t Hp = INT64_MAX, Dp = INT64_MAX, max_run = INT64_MAX, bufs = 0;
+  std::vector<uintptr_t> ptrs;
+  for (int32_t i = 0; i < npools; ++i) {
+    const hicache_pool *p = pools[i];
+    for (int32_t k = 0; k < i; ++k)
+      if (pools[k] == p) return set_error(HICACHE_ERR_INVALID_ARG, "pool %d appears twice in the group", i);
+    if (p->device != p0->device)
+      return set_error(HICACHE_ERR_INVALID_ARG, "pool %d is on device %d, pool 0 on %d", i, p->device,
+                       p0->device);
+    if (p->shape.L != p0->shape.L || p->shape.P != p0->shape.P)
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "pool %d has %lld layers of %lld-token pages; pool 0 has %lld of %lld", i,
+                       (long long)p->shape.L, (long long)p->shape.P, (long long)p0->shape.L,
+                       (long long)p0->shape.P);
+    int32_t li = 0;
+    if ((rc = resolve_layout(layout, p->shape.layout, &li))) return rc;
+    if (li != lay)
+      return set_error(HICACHE_ERR_INVALID_ARG, "pool %d resolves to layout %d, pool 0 to %d", i, li, lay);
+    if ((rc = check_kv(p, &kvs[i], 0))) return rc;
+    Hp = std::min(Hp, p->shape.Hp);
+    Dp = std::min(Dp, kvs[i].device_num_pages);
+    max_run = std::min(max_run, max_run_pages(p->shape));
+    bufs += p->shape.B * p->shape.L;
+    for (int64_t b = 0; b < p->shape.B * p->shape.L; ++b)
+      ptrs.push_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]));
+  }
+  if (bufs > hicache::kMaxBufs)
+    return set_error(HICACHE_ERR_INVALID_ARG, "the group has %lld device buffers; at most %d", (long long)bufs,
+                     hicache::kMaxBufs);
+  std::sort(ptrs.begin(), ptrs.end());
+  if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
+    return set_error(HICACHE_ERR_INVALID_ARG, "a device buffer is named twice in the group");
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(Hp, Dp, device_pages, host_pages, n, direction, max_run, &runs))) return rc;
+  if ((rc = check_device(p0))) return rc;
+  if ((rc = enqueue_group(pools, kvs, npools, runs, lay, layer_id, direction == HICACHE_DIR_BACKUP, stream)))
+    return rc;
+  if (layer_id >= 0) {
+    for (int32_t i = 0; i < npools; ++i) {
+      hicache_pool *p = pools[i];
+      const cudaError_t e = cudaEventRecord(p->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+      std::lock_guard<std::mutex> g(p->signal_mu);
+      p->layer_signal[size_t(layer_id)] = 0;
+    }
+  }
+  return HICACHE_OK;
 }
 
 int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,

@@ -128,6 +128,33 @@ struct ChecksumParams {
 };
 static_assert(sizeof(ChecksumParams) <= 32764, "kernel parameter limit");
 
+// ---- buffer groups ---------------------------------------------------------
+// One launch for several pools that share the page numbering but not the row
+// shape (hicache_group_transfer): job j is pool j, with its own header (shape,
+// host alias, dividers; its run table in h[j].job[0]) and the tiles
+// [tile_start[j], tile_start[j + 1]) of the launch.  The blob holds every
+// job's buffer pointers (job j's from word bufs_word[j]), then the run tables.
+constexpr int kMaxGroup = 4;
+struct GroupHeader {
+  int32_t njobs;
+  int32_t num_bufs;                   // buffer pointers of all jobs
+  int32_t tile_start[kMaxGroup + 1];
+  int32_t bufs_word[kMaxGroup];
+  XferHeader h[kMaxGroup];
+};
+template <int WORDS>
+struct GroupParamsT {
+  GroupHeader g;
+  uint64_t blob[WORDS];
+};
+constexpr int kGroupBlobWords = int((32764 - sizeof(GroupHeader)) / 8);
+constexpr int kGroupBlobWordsSmall = int((4096 - sizeof(GroupHeader)) / 8);
+using GroupParams = GroupParamsT<kGroupBlobWords>;
+using GroupParamsSmall = GroupParamsT<kGroupBlobWordsSmall>;
+static_assert(sizeof(GroupParams) <= 32764, "kernel parameter limit");
+static_assert(sizeof(GroupParamsSmall) <= 4096, "small parameter block");
+static_assert(kGroupBlobWordsSmall >= 64, "room for a small group's tables");
+
 // Launch entry points (hicache_kernels.cu).  Return a cudaError_t value.
 struct XferLaunch {
   XferParams *params;         // filled header + blob
@@ -140,6 +167,16 @@ struct XferLaunch {
   void *stream;
 };
 int launch_xfer(const XferLaunch &x);
+struct GroupLaunch {
+  GroupParams *params;        // filled header + blob
+  int words;                  // blob words in use (selects the small parameter block)
+  int layout;
+  bool all_layers;
+  bool to_host;
+  int grid;
+  void *stream;
+};
+int launch_group(const GroupLaunch &x);
 // Every layer of a load, layer by layer, in one launch; layer_done[l] grows by
 // job[0].total_tiles (the tiles of one layer) once layer l has landed.
 // sched: two device words, zero at launch, that the launch leaves at zero (its

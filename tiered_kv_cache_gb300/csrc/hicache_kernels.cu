@@ -203,6 +203,28 @@ __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__
   }
 }
 
+// Several pools in one launch (a buffer group): job j owns the tiles
+// [tile_start[j], tile_start[j + 1]) and moves them with its own pool's shape,
+// host alias, run table and buffer pointers.  The tiles of all jobs are one
+// grid-stride range, so the group costs one launch and one ramp whatever the
+// number of pools.
+template <int LAYOUT, bool ALL, bool TO_HOST, class Params>
+__global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__ Params p) {
+  __shared__ uint4 *s_bufs[kMaxBufs];
+  for (int i = threadIdx.x; i < p.g.num_bufs; i += kThreads)
+    s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
+  __syncthreads();
+  const int32_t total = p.g.tile_start[p.g.njobs];
+  for (int32_t g = blockIdx.x; g < total; g += gridDim.x) {
+    int j = 0;
+    while (j + 1 < p.g.njobs && g >= p.g.tile_start[j + 1]) ++j;
+    const XferHeader &h = p.g.h[j];
+    const Run *runs = reinterpret_cast<const Run *>(&p.blob[h.job[0].runs_word]);
+    move_tile<LAYOUT, ALL, TO_HOST>(h, h.job[0], runs, s_bufs + p.g.bufs_word[j], g - p.g.tile_start[j],
+                                    h.layer);
+  }
+}
+
 // Every layer of a load in one launch, layer by layer: tile g of the launch
 // is tile (g mod T) of layer g / T, where T = the tiles of one layer.  After
 // each tile the CTA adds one to its layer's counter, behind a fence, so a
@@ -363,6 +385,41 @@ int noalloc_layer_counters(unsigned int **out) {
   }
   *out = addr[dev];
   return 0;
+}
+
+namespace {
+
+template <int LAYOUT, bool ALL, bool TO_HOST>
+cudaError_t launch_group_one(const GroupLaunch &x) {
+  const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  if (x.words <= kGroupBlobWordsSmall) {
+    GroupParamsSmall small;
+    small.g = x.params->g;
+    for (int i = 0; i < x.words; ++i) small.blob[i] = x.params->blob[i];
+    group_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(small);
+  } else {
+    group_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(*x.params);
+  }
+  return cudaGetLastError();
+}
+
+template <int LAYOUT>
+cudaError_t launch_group_layout(const GroupLaunch &x) {
+  if (x.all_layers)
+    return x.to_host ? launch_group_one<LAYOUT, true, true>(x) : launch_group_one<LAYOUT, true, false>(x);
+  return x.to_host ? launch_group_one<LAYOUT, false, true>(x) : launch_group_one<LAYOUT, false, false>(x);
+}
+
+}  // namespace
+
+int launch_group(const GroupLaunch &x) {
+  switch (x.layout) {
+    case kLayerFirst: return int(launch_group_layout<kLayerFirst>(x));
+    case kPageFirst: return int(launch_group_layout<kPageFirst>(x));
+    case kPageFirstDirect: return int(launch_group_layout<kPageFirstDirect>(x));
+    case kPageFirstDirectKV: return int(launch_group_layout<kPageFirstDirectKV>(x));
+    default: return int(cudaErrorInvalidValue);
+  }
 }
 
 int launch_xfer(const XferLaunch &x) {
