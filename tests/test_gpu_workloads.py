@@ -214,3 +214,77 @@ def test_small_mix_one_launch_per_call():
                                          1000, k), k
     del bufs, kv
     torch.cuda.empty_cache()
+
+
+def untouched_bytes_ok(bufs, P, moved, sentinel8):
+    """Every device page not in `moved` still holds the sentinel byte (any dtype)."""
+    Dp = bufs[0].shape[0] // P
+    mask = torch.ones(Dp, dtype=torch.bool, device="cuda")
+    mask[torch.as_tensor(np.asarray(moved), device="cuda")] = False
+    for b in bufs:
+        rows = b.view(torch.uint8).view(Dp, -1)[mask]
+        if rows.numel() and not bool((rows == sentinel8).all()):
+            return False
+    return True
+
+
+def test_nsa_group_full_size_per_layer_and_all_layers():
+    """An MLA latent (576 bf16), an fp8 indexer key (128) and fp32 scales (4)
+    as three pools of one pinned allocation, at 64K tokens: 61 per-layer group
+    loads, each gating per-pool checksums through the pools' layer events, then
+    one all-layer group backup; every pool checked on sampled oracle offsets."""
+    s = wl.MLA_LATENT
+    L, P, Dp, Hp = s.num_layers, s.page_size, s.device_pages, s.host_pages
+    kinds = [(576, 2), (128, 1), (4, 4)]
+    t = wl.mla_transfer(s, 65536)
+    dp, hp = t.device_pages, t.host_pages
+    sizes = [L * Hp * P * R * es for R, es in kinds]
+    mem = hc.PinnedHost(sum(sizes))
+    pools, bufsets, kvs, off = [], [], [], 0
+    for (R, es), nbytes in zip(kinds, sizes):
+        pools.append(hc.Pool(L, 1, P, R, Hp, "page_first", elem_bytes=es, host_ptr=mem.ptr + off,
+                             host_bytes=nbytes))
+        bufs = [torch.full((Dp * P, R * es), 0xC3, dtype=torch.uint8, device="cuda").view(gh.TORCH_DT[es])
+                for _ in range(L)]
+        bufsets.append(bufs)
+        kvs.append(hc.DeviceKV(bufs, Dp))
+        position_fill(pools[-1].host_array(np.uint32))
+        off += nbytes
+    xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    sums = torch.zeros((len(kinds), L), dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    for layer in range(L):
+        hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, layer=layer, stream=xfer)
+        for i, (pool, kv) in enumerate(zip(pools, kvs)):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums[i].data_ptr() + 8 * layer, stream=comp)
+    torch.cuda.synchronize()
+    assert hc.launch_count() - c0 == L + len(kinds) * L
+    after = torch.zeros_like(sums)
+    for i, (pool, kv) in enumerate(zip(pools, kvs)):
+        for layer in range(L):
+            hc.layer_checksum(kv, pool, dp, layer, after[i].data_ptr() + 8 * layer)
+    torch.cuda.synchronize()
+    assert torch.equal(sums, after)
+    for i, (pool, bufs, (R, es)) in enumerate(zip(pools, bufsets, kinds)):
+        host = pool.host_array(gh.NP_DT[es])
+        assert gh.sampled_host_check(host, bufs, dp, hp, 1, 1, L, P, R, Hp, 20000, 10 + i), (R, es)
+        assert untouched_bytes_ok(bufs, P, dp, 0xC3), (R, es)
+    # every layer back to the host in one launch, over a sentinel-filled pool
+    for pool in pools:
+        pool.host_array(np.uint8)[:] = 0xC3
+    c0 = hc.launch_count()
+    hc.group_transfer(pools, kvs, dp, hp, hc.BACKUP)
+    torch.cuda.synchronize()
+    assert hc.launch_count() - c0 == 1
+    for i, (pool, bufs, (R, es)) in enumerate(zip(pools, bufsets, kinds)):
+        host = pool.host_array(np.uint8)
+        assert gh.sampled_host_check(pool.host_array(gh.NP_DT[es]), bufs, dp, hp, 1, 1, L, P, R, Hp, 20000,
+                                     20 + i), (R, es)
+        moved = len(dp) * L * P * R * es
+        assert count_equal(host, 0xC3) >= host.size - moved
+    for pool in pools:
+        pool.close()
+    del bufsets, kvs
+    torch.cuda.empty_cache()
