@@ -521,7 +521,9 @@ def bench_nsa_group(torch, hc, args):
     """A buffer group: an MLA latent (576 bf16) beside an fp8 indexer key (128)
     and its fp32 scales (4 per row), 61 layers, page 64, three page_first pools
     carved from one pinned allocation.  Loads of 4K / 16K / 64K tokens, every
-    layer and layer by layer: one launch per pool vs one group launch.  Each
+    layer and layer by layer: one launch per pool vs one group launch, and the
+    pipelined group load (every layer of every pool in one launch, each
+    pool's layers signalled as they land).  Each
     variant is enqueued behind a sleep kernel on a gate stream, so the device
     time excludes the host's enqueue cost, which is reported beside it."""
     from tiered_kv_cache_gb300 import workloads as wl
@@ -577,6 +579,7 @@ def bench_nsa_group(torch, hc, args):
                                                           stream=stream) for layer in range(L)],
             "all_layers_per_pool": lambda: [pool.load(kv, dp, hp, stream=stream) for pool, kv in zip(pools, kvs)],
             "all_layers_group": lambda: hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, stream=stream),
+            "pipelined_group": lambda: hc.group_load_pipelined(pools, kvs, dp, hp, stream=stream),
         }
         r = {"pages": len(dp), "bytes": nbytes}
         for name, fn in variants.items():

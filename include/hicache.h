@@ -307,6 +307,18 @@ int hicache_group_transfer(hicache_pool *const *pools, const hicache_device_kv *
                            const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                            int32_t layout, int32_t layer_id, int32_t direction, void *stream);
 
+/* hicache_load_pipelined for a buffer group: every layer of every pool in ONE
+ * launch, layer by layer (all pools' tiles of layer l before any of layer
+ * l + 1), each pool's layers marked done on the device as they land, so that
+ * hicache_wait_layer(pools[i], l, stream) waits for pool i's layer l alone.
+ * Arguments and checks as hicache_group_transfer with a load of every layer;
+ * every pool follows the stream rule of hicache_load_pipelined (INVALID_ARG
+ * while one of them has a pipelined load still running on another stream);
+ * CUDA if the driver offers no stream memory wait. */
+int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools,
+                                 const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                                 int32_t layout, void *stream);
+
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
 /* The pool-owned event recorded by the last load of `layer` (*event_out is a

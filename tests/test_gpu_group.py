@@ -203,3 +203,114 @@ def test_group_rejects_mismatches_and_enqueues_nothing():
     for p in (other_l, other_p, other_lay):
         p.close()
     grp.close()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_pipelined_group_matches_the_oracle_and_counts(layout):
+    """Every layer of three pools in one launch; each pool equals the oracle's
+    load, every pool's per-layer counts reach their targets, and a second load
+    in a row (the scheduler words back at zero) is right too."""
+    L, P, Dp, Hp, n = 5, 16, 40, 48, 13
+    kinds = [(1, 576, 2), (2, 64, 1), (1, 4, 4)]
+    grp = Group(kinds, L, P, Dp, Hp, layout, seed=110 + layout)
+    rng = np.random.default_rng(111 + layout)
+    s = torch.cuda.Stream()
+    for call in range(2):
+        for pool in grp.pools:
+            pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+        dp = wl.fragmented_pages(rng, Dp, n, max_run=3)
+        hp = rng.choice(Hp, n, replace=False)
+        for bufs in grp.bufs:
+            gh.sentinel_fill(bufs, 0x5A)
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=s)
+        assert hc.launch_count() - c0 == 1
+        hc.wait(s, TEN_S)
+        for bufs, want, (B, R, es) in zip(grp.bufs, _want_load(grp, dp, hp, layout, 0x5A), grp.kinds):
+            got = gh.to_np(bufs, es)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want[k]), (call, R, k)
+        for pool in grp.pools:
+            for layer in range(L):
+                done, target = pool.pipeline_status(layer)
+                assert done == target > 0
+    grp.close()
+
+
+def test_pipelined_group_layers_gate_compute():
+    """Compute on a second stream waits for each pool's layer alone and reads
+    it: the checksums taken behind the waits equal those taken afterwards."""
+    L, P, Dp, Hp, n = 8, 16, 64, 64, 40
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "page_first", seed=120)
+    rng = np.random.default_rng(121)
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    sums = torch.zeros((len(NSA_KINDS), L), dtype=torch.int64, device="cuda")
+    for pool in grp.pools:                     # counts are checked before any wait relies on them
+        assert all(pool.pipeline_status(layer)[0] == pool.pipeline_status(layer)[1] for layer in range(L))
+    hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=xfer)
+    for layer in range(L):
+        for i, (pool, kv) in enumerate(zip(grp.pools, grp.kvs)):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, dp, layer, sums[i].data_ptr() + 8 * layer, stream=comp)
+    hc.wait(comp, TEN_S)
+    hc.wait(xfer, TEN_S)
+    after = torch.zeros_like(sums)
+    for i, (pool, kv) in enumerate(zip(grp.pools, grp.kvs)):
+        for layer in range(L):
+            hc.layer_checksum(kv, pool, dp, layer, after[i].data_ptr() + 8 * layer)
+    torch.cuda.synchronize()
+    assert torch.equal(sums, after)
+    grp.close()
+
+
+def test_pipelined_group_split_over_several_launches():
+    L, P, Dp, Hp, n = 3, 1, 8000, 8000, 3000
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "page_first_direct", seed=130)
+    rng = np.random.default_rng(131)
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    for bufs in grp.bufs:
+        gh.sentinel_fill(bufs, 0x5A)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    c0 = hc.launch_count()
+    hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=s)
+    assert hc.launch_count() - c0 >= 3
+    hc.wait(s, TEN_S)
+    for bufs, want, (B, R, es) in zip(grp.bufs, _want_load(grp, dp, hp, 2, 0x5A), grp.kinds):
+        got = gh.to_np(bufs, es)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k]), (R, k)
+    for pool in grp.pools:
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target
+    grp.close()
+
+
+def test_pipelined_group_stream_rule():
+    """While a pool's pipelined load runs on one stream, a group that holds
+    that pool may not start a pipelined load on another (nothing enqueued)."""
+    L, P, Dp, Hp, n = 2, 8, 16, 16, 4
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "page_first", seed=140)
+    dp, hp = np.arange(n), np.arange(n)
+    a, b = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(a):
+        torch.cuda._sleep(int(2e8))           # keeps stream a busy for ~0.1 s
+    grp.pools[1].load_pipelined(grp.kvs[1], dp, hp, stream=a)
+    c0 = hc.launch_count()
+    with pytest.raises(hc.HiCacheError):
+        hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=b)
+    assert hc.launch_count() == c0
+    hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=a)   # same stream: fine
+    hc.wait(a, TEN_S)
+    for pool in grp.pools:
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target
+    grp.close()

@@ -21,7 +21,7 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
-    "PageAllocator", "Engine", "group_transfer", "MAX_GROUP",
+    "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "MAX_GROUP",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
@@ -92,6 +92,8 @@ def _bind(lib):
         "hicache_pipeline_status": (ctypes.c_int, [_vp, _i32, _P(ctypes.c_uint32), _P(ctypes.c_uint32)]),
         "hicache_group_transfer": (ctypes.c_int, [_P(_vp), _P(_DeviceKVStruct), _i32, _vp, _vp, _i64, _i32,
                                                   _i32, _i32, _vp]),
+        "hicache_group_load_pipelined": (ctypes.c_int, [_P(_vp), _P(_DeviceKVStruct), _i32, _vp, _vp, _i64,
+                                                        _i32, _vp]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
@@ -271,6 +273,22 @@ def group_transfer(pools, kvs, device_pages, host_pages, direction: int, layer: 
     structs = (_DeviceKVStruct * len(kvs))(*[k.struct for k in kvs])
     _check(library().hicache_group_transfer(handles, structs, len(pools), _ptr(dp), _ptr(hp), dp.size,
                                             layout, layer, direction, _stream(stream)))
+
+
+def group_load_pipelined(pools, kvs, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
+    """Every layer of every pool of a group in one launch, layer by layer;
+    each pool's wait_layer then waits for that pool's layer alone."""
+    if len(pools) != len(kvs):
+        raise ValueError("pools and kvs differ in length")
+    dp, hp = _idx(device_pages), _idx(host_pages)
+    if dp.size != hp.size:
+        raise ValueError("device_pages and host_pages differ in length")
+    if isinstance(layout, str):
+        layout = LAYOUTS[layout]
+    handles = (ctypes.c_void_p * len(pools))(*[p.handle for p in pools])
+    structs = (_DeviceKVStruct * len(kvs))(*[k.struct for k in kvs])
+    _check(library().hicache_group_load_pipelined(handles, structs, len(pools), _ptr(dp), _ptr(hp), dp.size,
+                                                  layout, _stream(stream)))
 
 
 class PinnedHost:

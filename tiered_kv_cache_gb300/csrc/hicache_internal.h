@@ -141,6 +141,10 @@ struct GroupHeader {
   int32_t tile_start[kMaxGroup + 1];
   int32_t bufs_word[kMaxGroup];
   XferHeader h[kMaxGroup];
+  // pipelined groups only: job j's layer counters and the launch's two
+  // scheduler words (as launch_pipelined_load)
+  unsigned int *layer_done[kMaxGroup];
+  unsigned int *sched;
 };
 template <int WORDS>
 struct GroupParamsT {
@@ -177,6 +181,10 @@ struct GroupLaunch {
   void *stream;
 };
 int launch_group(const GroupLaunch &x);
+// Every layer of every pool of a group, layer by layer, in one launch:
+// g.layer_done[j][l] grows by pool j's tiles of one layer once pool j's layer
+// l has landed.
+int launch_pipelined_group(const GroupLaunch &x);
 // Every layer of a load, layer by layer, in one launch; layer_done[l] grows by
 // job[0].total_tiles (the tiles of one layer) once layer l has landed.
 // sched: two device words, zero at launch, that the launch leaves at zero (its

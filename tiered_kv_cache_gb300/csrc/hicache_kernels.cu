@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "hicache_internal.h"
 
@@ -240,6 +241,19 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__
 // next ones in order, so layer l lands at about (l + 1) / L of the load.
 // sched[1] counts the CTAs that are done; the last one puts both words back
 // to zero for the next launch on the same scheduler words.
+// End of a CTA of a counter-scheduled launch: count it out; the last one out
+// puts the two scheduler words back to zero for the next launch.
+__device__ __forceinline__ void release_schedule(unsigned int *sched) {
+  if (threadIdx.x == 0) {
+    __threadfence();                                    // this CTA's last take before its exit count
+    if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+      __threadfence();                                  // every CTA's takes before the reset
+      atomicExch(&sched[0], 0u);
+      atomicExch(&sched[1], 0u);
+    }
+  }
+}
+
 template <int LAYOUT, class Params>
 __global__ void __launch_bounds__(kThreads)
     pipelined_load_kernel(const __grid_constant__ Params p, unsigned int *layer_done,
@@ -264,14 +278,46 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    __threadfence();                                    // this CTA's last take before its exit count
-    if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
-      __threadfence();                                  // every CTA's takes before the reset
-      atomicExch(&sched[0], 0u);
-      atomicExch(&sched[1], 0u);
+  release_schedule(sched);
+}
+
+// Every layer of several pools in one launch (a pipelined buffer group): tile
+// g is in layer g / T, where T = the tiles of one layer over all pools, and
+// within that layer pool j owns [tile_start[j], tile_start[j + 1]).  After each
+// tile the CTA adds one to that pool's counter of that layer, so each pool's
+// counters behave as those of its own pipelined load; tiles come from the
+// counter sched[0], as in pipelined_load_kernel, so all pools' tiles of layer l
+// land before those of layer l + 1.
+template <int LAYOUT, class Params>
+__global__ void __launch_bounds__(kThreads)
+    pipelined_group_kernel(const __grid_constant__ Params p) {
+  __shared__ uint4 *s_bufs[kMaxBufs];
+  __shared__ int32_t s_next;
+  for (int i = threadIdx.x; i < p.g.num_bufs; i += kThreads)
+    s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
+  const int32_t per_layer = p.g.tile_start[p.g.njobs];   // tiles of one layer, every pool
+  const int32_t total = per_layer * p.g.h[0].L;
+  unsigned int *const sched = p.g.sched;
+  if (threadIdx.x == 0) s_next = int32_t(atomicAdd(&sched[0], 1u));
+  __syncthreads();
+  for (int32_t g = s_next; g < total; g = s_next) {
+    const int32_t layer = g / per_layer;
+    const int32_t r = g - layer * per_layer;
+    int j = 0;
+    while (j + 1 < p.g.njobs && r >= p.g.tile_start[j + 1]) ++j;
+    const XferHeader &h = p.g.h[j];
+    const Run *runs = reinterpret_cast<const Run *>(&p.blob[h.job[0].runs_word]);
+    move_tile<LAYOUT, false, false>(h, h.job[0], runs, s_bufs + p.g.bufs_word[j], r - p.g.tile_start[j],
+                                    layer);
+    __threadfence();                                    // this thread's stores, device-wide
+    __syncthreads();                                    // every thread is past its fence and has read s_next
+    if (threadIdx.x == 0) {
+      atomicAdd(&p.g.layer_done[j][layer], 1u);
+      s_next = int32_t(atomicAdd(&sched[0], 1u));
     }
+    __syncthreads();
   }
+  release_schedule(sched);
 }
 
 // Stand-in for attention on one layer: read every vector of the given pages of
@@ -411,6 +457,29 @@ cudaError_t launch_group_layout(const GroupLaunch &x) {
 }
 
 }  // namespace
+
+int launch_pipelined_group(const GroupLaunch &x) {
+  const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  auto go = [&](auto layout_tag) -> cudaError_t {
+    constexpr int LAYOUT = decltype(layout_tag)::value;
+    if (x.words <= kGroupBlobWordsSmall) {
+      GroupParamsSmall small;
+      small.g = x.params->g;
+      for (int i = 0; i < x.words; ++i) small.blob[i] = x.params->blob[i];
+      pipelined_group_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(small);
+    } else {
+      pipelined_group_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params);
+    }
+    return cudaGetLastError();
+  };
+  switch (x.layout) {
+    case kLayerFirst: return int(go(std::integral_constant<int, kLayerFirst>()));
+    case kPageFirst: return int(go(std::integral_constant<int, kPageFirst>()));
+    case kPageFirstDirect: return int(go(std::integral_constant<int, kPageFirstDirect>()));
+    case kPageFirstDirectKV: return int(go(std::integral_constant<int, kPageFirstDirectKV>()));
+    default: return int(cudaErrorInvalidValue);
+  }
+}
 
 int launch_group(const GroupLaunch &x) {
   switch (x.layout) {
