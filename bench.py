@@ -349,6 +349,22 @@ def cpu_baseline(seconds_target=10.0, pages=24):
             "mla61_1core": {"value": round(vm, 3), "sample": f"32-page transfers, page_first, {elm:.1f} s"}}
 
 
+def step_config(args, npages, bpx):
+    """The `config` of a step line: the same for both arms."""
+    step_bytes = len(LAYOUT_NAMES) * 6 * bpx
+    return {"workload": (f"llama3_8b_{npages * 64 // 1024}k: 32 layers, K+V, 8 kv heads x 128, "
+                         f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
+                         "fragmented device pages, contiguous host pages")
+            if args.workload == "llama3_8b_32k" else
+            (f"deep78_{npages * 64 // 1024}k: 78 layers, K+V, 8 kv heads x 128, bf16, page 64, "
+             f"{npages} pages per transfer, fully scattered device pages, contiguous host pages"),
+            "step": f"per layout ({', '.join(LAYOUT_NAMES)}): backup, load, "
+                    "concurrent backup+load of two requests on two streams, and the same pair "
+                    f"as one fused launch; {step_bytes / 2**30:.0f} GiB per step",
+            "l2": f"inputs larger than L2 ({bpx / 2**20:.0f} MiB per transfer)",
+            "launch_ctas": args.ctas or "auto"}
+
+
 def reference_arm(args):
     """`--impl reference`: the oracle on the host cores, timed on the same
     workload shape, a bounded sample per step."""
@@ -380,13 +396,14 @@ def reference_arm(args):
     moved = sum(step() for _ in range(args.steps))
     el = time.perf_counter() - t0
     v = moved / el / GB
-    sample = f"per step: backup+load of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB) in each layout"
+    sample = (f"per step: backup+load of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB) in each of "
+              "layer_first, page_first and page_first_direct, on host arrays")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "llama3_8b_32k (oracle sample)", "sample": sample},
+        "config": step_config(args, args.pages, args.pages * s.page_bytes),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -962,17 +979,7 @@ def main():
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": (f"llama3_8b_{npages * 64 // 1024}k: 32 layers, K+V, 8 kv heads x 128, "
-                                f"bf16, page 64, {npages} pages = {npages * 64} tokens per transfer, "
-                                "fragmented device pages, contiguous host pages")
-                   if args.workload == "llama3_8b_32k" else
-                   (f"deep78_{npages * 64 // 1024}k: 78 layers, K+V, 8 kv heads x 128, bf16, page 64, "
-                    f"{npages} pages per transfer, fully scattered device pages, contiguous host pages"),
-                   "step": f"per layout ({', '.join(LAYOUT_NAMES)}): backup, load, "
-                           "concurrent backup+load of two requests on two streams, and the same pair "
-                           f"as one fused launch; {step_bytes / 2**30:.0f} GiB per step",
-                   "l2": f"inputs larger than L2 ({bpx / 2**20:.0f} MiB per transfer)",
-                   "launch_ctas": args.ctas or "auto"},
+        "config": step_config(args, npages, bpx),
         "roofline": roofline,
         "roofline_hbm": roofline_hbm,
         "link_peak": {**{k: round(v, 1) if isinstance(v, float) else v for k, v in link.items()}, **NOMINAL},
