@@ -230,3 +230,24 @@ def test_page_span_is_exactly_the_page(shape):
     with pytest.raises(hc.HiCacheError) as e:
         hc.page_span(hc._desc(2, 2, 4, 8, 5, "page_first"), 5, 0)
     assert e.value.status == "INDEX_RANGE"
+
+
+def test_group_calls_reject_bad_arguments_before_any_cuda_call():
+    """A group call with no pools, too many, NULL arrays or a NULL pool is
+    refused on the host; the Python group size matches the header's."""
+    hdr = open(os.path.join(ROOT, "include", "hicache.h")).read()
+    assert int(re.search(r"#define HICACHE_MAX_GROUP (\d+)", hdr).group(1)) == hc.MAX_GROUP
+    lib = hc.library()
+    kvs = (hc._DeviceKVStruct * 1)()
+    none = (ctypes.c_void_p * 1)(None)
+    for pools, structs, n in ((none, kvs, 0), (none, kvs, hc.MAX_GROUP + 1), (None, kvs, 1), (none, None, 1),
+                              (none, kvs, 1)):
+        c0 = hc.launch_count()
+        assert lib.hicache_group_transfer(pools, structs, n, None, None, 0, -1, -1, 0, None) == -1
+        assert lib.hicache_group_load_pipelined(pools, structs, n, None, None, 0, -1, None) == -1
+        assert lib.hicache_last_error()
+        assert hc.launch_count() == c0
+    with pytest.raises(ValueError):
+        hc.group_transfer([object()], [], [0], [0], hc.LOAD)
+    with pytest.raises(ValueError):
+        hc.group_load_pipelined([], [], [0, 1], [0])
