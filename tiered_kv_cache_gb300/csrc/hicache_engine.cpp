@@ -6,7 +6,7 @@
 // and a load thread consume queues and submit on private streams ("Tuning
 // SGLang HiCache L2 on Kunlunxin P800/P900", section 2.2; "Baidu's KVCache
 // Overhaul", section "Bidirectional Async Transfer").  On GB300 two launches of
-// opposite directions on two streams reach about 0.82 of what the host link
+// opposite directions on two streams reach about 0.95 of what the host link
 // carries both ways, while one launch carrying both reaches 1.00; so here one
 // worker owns the link: when the request at the head of the queue and the one
 // right behind it go in opposite directions, use the same device buffers and
