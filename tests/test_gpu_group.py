@@ -314,3 +314,48 @@ def test_pipelined_group_stream_rule():
             done, target = pool.pipeline_status(layer)
             assert done == target
     grp.close()
+
+
+def test_group_at_the_buffer_limit_and_beyond():
+    """Four pools of 128 layers each: 512 device buffers, the most one launch
+    takes; every pool matches the oracle.  A fifth buffer set is refused."""
+    L, P, Dp, Hp, n = 128, 2, 12, 12, 5
+    kinds = [(1, 8, 2), (1, 16, 1), (1, 4, 4), (1, 64, 2)]
+    grp = Group(kinds, L, P, Dp, Hp, "page_first", seed=150)
+    rng = np.random.default_rng(151)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = 0x3C
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP)
+    torch.cuda.synchronize()
+    assert hc.launch_count() - c0 == 1
+    for pool, want, (B, R, es) in zip(grp.pools, _want_backup(grp, dp, hp, 1, 0x3C), grp.kinds):
+        assert np.array_equal(pool.host_array(gh.NP_DT[es]), want), (R, es)
+    extra = Group([(2, 8, 2)], L, P, Dp, Hp, "page_first", seed=152)   # 256 more buffers
+    c0 = hc.launch_count()
+    with pytest.raises(hc.HiCacheError):
+        hc.group_transfer(grp.pools[:3] + extra.pools, grp.kvs[:3] + extra.kvs, dp, hp, hc.BACKUP)
+    assert hc.launch_count() == c0
+    extra.close()
+    grp.close()
+
+
+def test_empty_group_call_launches_nothing_and_layer_calls_still_record_events():
+    L, P, Dp, Hp = 3, 4, 8, 8
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "layer_first", seed=160)
+    empty = np.zeros(0, np.int64)
+    s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(int(5e7))           # the events below must wait for this
+    c0 = hc.launch_count()
+    hc.group_transfer(grp.pools, grp.kvs, empty, empty, hc.BACKUP, stream=s)
+    hc.group_transfer(grp.pools, grp.kvs, empty, empty, hc.LOAD, layer=2, stream=s)
+    hc.group_load_pipelined(grp.pools, grp.kvs, empty, empty, stream=s)
+    assert hc.launch_count() == c0
+    for pool in grp.pools:                   # recorded on s, behind the sleep
+        pool.wait_layer(2, comp)
+    hc.wait(comp, TEN_S)
+    assert s.query()
+    grp.close()
