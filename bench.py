@@ -247,8 +247,14 @@ def link_peaks(torch, nbytes=1 << 30, reps=5):
     res = {"h2d_gbs": nbytes / t_h2d / GB, "d2h_gbs": nbytes / t_d2h / GB,
            "bidir_gbs": 2 * nbytes / t_bi / GB, "bytes": nbytes, "how": "pinned cudaMemcpyAsync, best of 5"}
     dev_d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    t_dd = timed(lambda: dev_d.copy_(dev_a))
-    res["d2d_gbs"] = 2 * nbytes / t_dd / GB
+
+    def d2d():
+        with torch.cuda.stream(s1):
+            dev_d.copy_(dev_a)
+
+    t_dd = timed(d2d)
+    res["d2d_gbs"] = 2 * nbytes / t_dd / GB      # bytes read + written
+    res["d2d_how"] = "device-to-device copy of 1 GiB on the same stream, bytes read + written, best of 5"
     del host_a, host_b, dev_a, dev_b, dev_d
     return res
 
