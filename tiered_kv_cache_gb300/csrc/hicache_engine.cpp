@@ -58,7 +58,9 @@ struct Launched {
 
 // Launches kept unfinished on the engine stream at once: one running and one
 // queued behind it.  Requests submitted meanwhile wait in the queue, where a
-// backup and a load can meet and leave as one fused launch.
+// backup and a load can meet and leave as one fused launch.  A request with
+// no partner is held while any launch is unfinished: launched early it would
+// only queue behind that launch, and held it can still meet a partner.
 constexpr size_t kDepth = 2;
 
 void poll_until_done(cudaEvent_t ev) {
@@ -181,24 +183,34 @@ struct hicache_engine {
             break;
           }
       }
-      Request a = std::move(queue.front());
-      queue.pop_front();
-      // the first request of the other direction among the next kLookahead;
-      // it may move ahead of the same-direction requests before it only if it
-      // commutes with each of them
-      bool pair = false;
-      Request b;
-      for (size_t i = 0; i < queue.size() && i < kLookahead; ++i) {
-        if (queue[i].direction == a.direction) continue;
-        bool ok = fusable(a, queue[i]);
-        for (size_t k = 0; ok && k < i; ++k) ok = commute(queue[k], queue[i]);
-        if (ok) {
-          b = std::move(queue[i]);
-          queue.erase(queue.begin() + std::ptrdiff_t(i));
-          pair = true;
-        }
+      // the first request of the other direction among the kLookahead behind
+      // the head; it may move ahead of the same-direction requests before it
+      // only if it commutes with each of them
+      size_t partner = 0;  // its index in the queue (0: none)
+      for (size_t i = 1; i < queue.size() && i <= kLookahead; ++i) {
+        if (queue[i].direction == queue.front().direction) continue;
+        bool ok = fusable(queue.front(), queue[i]);
+        for (size_t k = 1; ok && k < i; ++k) ok = commute(queue[k], queue[i]);
+        if (ok) partner = i;
         break;
       }
+      if (partner == 0 && !stop && refresh() > 0) {
+        // no partner yet and the link is busy: a request launched now would
+        // only wait behind the running launch on the engine stream, so hold
+        // it until that launch ends or another request arrives
+        const size_t seen = queue.size();
+        cv_work.wait_for(lk, std::chrono::microseconds(50),
+                         [&] { return stop || queue.size() != seen; });
+        continue;
+      }
+      const bool pair = partner != 0;
+      Request b;
+      if (pair) {
+        b = std::move(queue[partner]);
+        queue.erase(queue.begin() + std::ptrdiff_t(partner));
+      }
+      Request a = std::move(queue.front());
+      queue.pop_front();
       cudaEvent_t done = take_event();
       lk.unlock();
 
