@@ -359,3 +359,56 @@ def test_empty_group_call_launches_nothing_and_layer_calls_still_record_events()
     hc.wait(comp, TEN_S)
     assert s.query()
     grp.close()
+
+
+def test_group_backup_thread_and_pipelined_load_thread():
+    """A backup thread and a load thread calling one group at once, each on its
+    own stream: group backups of one set of pages, pipelined group loads of
+    another; both equal the oracle's per-pool results for the same pairs."""
+    import threading
+    L, P, Dp, Hp = 4, 8, 96, 96
+    grp = Group(NSA_KINDS, L, P, Dp, Hp, "page_first_direct", seed=170)
+    rng = np.random.default_rng(171)
+    perm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    jobs_b = [(perm[i * 6:(i + 1) * 6], hperm[i * 6:(i + 1) * 6]) for i in range(5)]
+    jobs_l = [(perm[48 + i * 6:48 + (i + 1) * 6], hperm[48 + i * 6:48 + (i + 1) * 6]) for i in range(5)]
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    torch.cuda.synchronize()
+    host0 = [pool.host_array(np.uint8).copy() for pool in grp.pools]
+    dev0 = [gh.to_np(bufs, es) for bufs, (B, R, es) in zip(grp.bufs, grp.kinds)]
+    errors = []
+
+    def worker(jobs, load):
+        try:
+            st = torch.cuda.Stream()
+            for dp, hp in jobs:
+                if load:
+                    hc.group_load_pipelined(grp.pools, grp.kvs, dp, hp, stream=st)
+                else:
+                    hc.group_transfer(grp.pools, grp.kvs, dp, hp, hc.BACKUP, stream=st)
+            hc.wait(st, TEN_S)
+        except Exception as e:  # reported below
+            errors.append(e)
+    ts = [threading.Thread(target=worker, args=(jobs_b, False)),
+          threading.Thread(target=worker, args=(jobs_l, True))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    for i, (pool, bufs, (B, R, es)) in enumerate(zip(grp.pools, grp.bufs, grp.kinds)):
+        want_host = host0[i].view(gh.NP_DT[es]).copy()
+        want_dev = [x.copy() for x in dev0[i]]
+        for dp, hp in jobs_b:
+            gh.orc().backup(dev0[i], want_host, B, L, P, R, Hp, dp, hp, 2)
+        for dp, hp in jobs_l:
+            gh.orc().load(want_dev, host0[i].view(gh.NP_DT[es]), B, L, P, R, Hp, dp, hp, 2)
+        assert np.array_equal(pool.host_array(gh.NP_DT[es]), want_host), R
+        got = gh.to_np(bufs, es)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want_dev[k]), (R, k)
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target
+    grp.close()
