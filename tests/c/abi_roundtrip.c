@@ -1,7 +1,9 @@
 /* A plain C caller of libhicache: a pool on huge-page pinned memory, a backup,
  * per-layer loads into fresh device pages with a compute stream waiting on the
- * layer events, a fused backup + load, and the error path.  Every element is
- * checked against a position pattern (round trip = identity).  Prints "ok". */
+ * layer events, a fused backup + load, a buffer group (a second pool with
+ * 32-byte fp32 rows) backed up and then loaded back by one pipelined launch,
+ * and the error path.  Every element is checked against a position pattern
+ * (round trip = identity).  Prints "ok". */
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -98,6 +100,62 @@ int main(void) {
         for (int64_t e = 0; e < R; ++e)
           if (h[(dst2[i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 4;
   }
+
+  /* a buffer group: the K,V pool beside a pool of fp32 rows (8 per token) that
+   * shares its page numbering; one launch backs up both, one pipelined launch
+   * loads both back into other device pages */
+  enum { R2 = 8 };
+  hicache_pool_desc d2 = d;
+  d2.num_buffers = 1;
+  d2.elem_bytes = 4;
+  d2.row_elems = R2;
+  const size_t host2_bytes = (size_t)(L * Hp * P * R2) * 4;
+  const size_t buf2_bytes = (size_t)(Dp * P * R2) * 4;
+  void *host2 = NULL;
+  CHECK(hicache_host_alloc(host2_bytes, 0, &host2));
+  hicache_pool *pool2 = NULL;
+  CHECK(hicache_pool_create(&d2, host2, host2_bytes, &pool2));
+  void *bufs2[L];
+  uint32_t *h2 = (uint32_t *)malloc(buf2_bytes);
+  for (int l = 0; l < L; ++l) {
+    if (cudaMalloc(&bufs2[l], buf2_bytes) != cudaSuccess) return 2;
+    for (int64_t row = 0; row < Dp * P; ++row)
+      for (int64_t e = 0; e < R2; ++e) h2[row * R2 + e] = 0x9E3779B9u * (uint32_t)(l + 1) + (uint32_t)(row * R2 + e);
+    if (cudaMemcpy(bufs2[l], h2, buf2_bytes, cudaMemcpyHostToDevice) != cudaSuccess) return 2;
+  }
+  hicache_device_kv kv2 = {bufs2, Dp};
+  hicache_pool *group[2] = {pool, pool2};
+  const hicache_device_kv kvs[2] = {kv, kv2};
+  const int64_t hp3[N] = {21, 22, 23, 24, 25, 26, 27, 28};
+  const int64_t dst3[N] = {19, 20, 21, 24, 25, 26, 27, 28};
+  CHECK(hicache_group_transfer(group, kvs, 2, src, hp3, N, HICACHE_LAYOUT_POOL, -1, HICACHE_DIR_BACKUP, xfer));
+  CHECK(hicache_group_load_pipelined(group, kvs, 2, dst3, hp3, N, HICACHE_LAYOUT_POOL, xfer));
+  for (int l = 0; l < L; ++l) {
+    CHECK(hicache_wait_layer(pool, l, comp));
+    CHECK(hicache_wait_layer(pool2, l, comp));
+  }
+  CHECK(hicache_wait(comp, -1));
+  CHECK(hicache_wait(xfer, -1));
+  for (int k = 0; k < NB; ++k) {
+    if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+    for (int i = 0; i < N; ++i)
+      for (int64_t t = 0; t < P; ++t)
+        for (int64_t e = 0; e < R; ++e)
+          if (h[(dst3[i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 6;
+  }
+  for (int l = 0; l < L; ++l) {
+    if (cudaMemcpy(h2, bufs2[l], buf2_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+    for (int i = 0; i < N; ++i)
+      for (int64_t t = 0; t < P; ++t)
+        for (int64_t e = 0; e < R2; ++e) {
+          const uint32_t want = 0x9E3779B9u * (uint32_t)(l + 1) + (uint32_t)((src[i] * P + t) * R2 + e);
+          if (h2[(dst3[i] * P + t) * R2 + e] != want) return 7;
+        }
+  }
+  CHECK(hicache_pool_destroy(pool2));
+  CHECK(hicache_host_free(host2));
+  for (int l = 0; l < L; ++l) cudaFree(bufs2[l]);
+  free(h2);
 
   /* errors enqueue nothing and explain themselves */
   const int64_t bad[1] = {Dp};
