@@ -156,7 +156,9 @@ int hicache_host_free(void *ptr);
 int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t host_bytes,
                         hicache_pool **out);
 /* Destroys the pool's events and the pool.  Transfers already enqueued still
- * run; the host buffer must stay allocated until they finish. */
+ * run; the host buffer must stay allocated until they finish.  The pool's
+ * pipelined loads count into device words the pool owns, so this first waits
+ * on the host for the last of them to finish. */
 int hicache_pool_destroy(hicache_pool *pool);
 
 /* ---- transfers -------------------------------------------------------------

@@ -120,7 +120,7 @@ inline bool pair_less(const Pair &a, const Pair &b) {
 
 // Validate n index pairs and reduce them to runs: pairs sorted by (host page,
 // device page), merged while both pages step by one (at most max_run pages per
-// run).  On error nothing is changed but the last-error text.
+// run).  On error the last-error text is set and *runs holds no usable table.
 int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
             int32_t direction, int64_t max_run, std::vector<RunRec> *runs) {
   if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n = %lld is negative", (long long)n);
@@ -622,6 +622,9 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
 
 int hicache_pool_destroy(hicache_pool *pool) {
   if (!pool) return HICACHE_OK;
+  // pipelined loads count into the pool's device words: let the last one end
+  // (they all follow one another on one stream) before the words are freed
+  if (pool->pipeline_stream_set && pool->pipeline_last) (void)cudaEventSynchronize(pool->pipeline_last);
   for (auto ev : pool->events)
     if (ev) cudaEventDestroy(ev);
   if (pool->layer_done) cudaFree(pool->layer_done);
