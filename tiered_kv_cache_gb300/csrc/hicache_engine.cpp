@@ -59,8 +59,9 @@ struct Launched {
 // Launches kept unfinished on the engine stream at once: one running and one
 // queued behind it.  Requests submitted meanwhile wait in the queue, where a
 // backup and a load can meet and leave as one fused launch.  A request with
-// no partner is held while any launch is unfinished: launched early it would
-// only queue behind that launch, and held it can still meet a partner.
+// no partner, and fewer than kLookahead requests behind it, is held while any
+// launch is unfinished: launched early it would only queue behind that launch,
+// and held it can still meet a partner.
 constexpr size_t kDepth = 2;
 
 void poll_until_done(cudaEvent_t ev) {
@@ -194,12 +195,14 @@ struct hicache_engine {
         if (ok) partner = i;
         break;
       }
-      if (partner == 0 && !stop && refresh() > 0) {
-        // no partner yet and the link is busy: a request launched now would
-        // only wait behind the running launch on the engine stream, so hold
-        // it until that launch ends or another request arrives
+      if (partner == 0 && !stop && queue.size() <= kLookahead && refresh() > 0) {
+        // no partner yet, room behind the head for one to arrive, and the link
+        // busy: a request launched now would only wait behind the running
+        // launch on the engine stream, so hold it until that launch ends or
+        // another request arrives.  (With the window full, a later arrival
+        // could not pair with the head anyway.)
         const size_t seen = queue.size();
-        cv_work.wait_for(lk, std::chrono::microseconds(50),
+        cv_work.wait_for(lk, std::chrono::microseconds(10),
                          [&] { return stop || queue.size() != seen; });
         continue;
       }
