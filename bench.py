@@ -503,6 +503,16 @@ def bench_mla_overlap(torch, hc, args):
         def pipelined():
             plan.load_pipelined(kv, stream=xfer)
 
+        def loads_graph():
+            plan.load_layers(kv, stream=xfer)
+
+        def overlapped_graph(reps):
+            plan.load_layers(kv, stream=xfer)
+            for layer in range(L):
+                pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
         def overlapped_pipelined(reps):
             plan.load_pipelined(kv, stream=xfer)
             for layer in range(L):
@@ -520,6 +530,8 @@ def bench_mla_overlap(torch, hc, args):
         cp = timed(lambda: overlapped_pipelined(reps))
         a2 = timed(loads_two_streams)
         c2 = timed(lambda: overlapped_two_streams(reps))
+        ag = timed(loads_graph)
+        cg = timed(lambda: overlapped_graph(reps))
         out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
             "pages": n, "bytes": nbytes,
             "per_layer_loads_ms": round(a * 1e3, 3), "per_layer_load_gbs": round(nbytes / a / GB, 1),
@@ -534,6 +546,9 @@ def bench_mla_overlap(torch, hc, args):
             "per_layer_load_2streams_gbs": round(nbytes / a2 / GB, 1),
             "overlapped_2streams_ms": round(c2 * 1e3, 3),
             "overlap_efficiency_2streams": round((a2 + b - c2) / min(a2, b), 3),
+            "per_layer_graph_ms": round(ag * 1e3, 3), "per_layer_graph_gbs": round(nbytes / ag / GB, 1),
+            "overlapped_graph_ms": round(cg * 1e3, 3),
+            "overlap_efficiency_graph": round((ag + b - cg) / min(ag, b), 3),
         }
         plan.close()
     launches = hc.launch_count() - launches0

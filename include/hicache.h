@@ -277,6 +277,19 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
 /* hicache_load_pipelined for a load plan. */
 int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                                 void *stream);
+/* Every layer of a load plan, layer by layer, as hicache_plan_load_layer for
+ * l = 0..L-1 (L per-layer launches, each followed by that layer's event), from
+ * one CUDA graph: the first call for a given device KV and layout captures the
+ * launches and event records into a graph that the plan keeps, and every call
+ * replays it with one graph launch.  This cuts the host's per-layer launch cost
+ * and the gaps between the per-layer kernels (the per-layer load of "Why
+ * compute, H2D, and D2H should stay in one GPU execution domain", "Rethinking
+ * the SGLang HiCache Boundary").  A call with other buffer pointers, page count
+ * or layout re-captures.  Errors: INVALID_ARG (NULL plan, backup plan, bad
+ * layout or kv), CUDA; on error nothing is enqueued.  Destroying the plan
+ * while a replay is still running is allowed: CUDA frees the graph once the
+ * replay ends. */
+int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout, void *stream);
 /* Number of pages and of merged runs in a plan. */
 int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs);
 int hicache_plan_destroy(hicache_plan *plan);

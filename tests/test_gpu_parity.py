@@ -550,3 +550,50 @@ def test_layer_first_contiguous_equals_plain_range_copies():
                 dst[off:off + n * P * row].copy_(src, non_blocking=True)
         torch.cuda.synchronize()
         assert np.array_equal(got, host)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_plan_load_layers_graph_replay(layout):
+    """The per-layer loads of a plan replayed from a CUDA graph equal the
+    oracle's load, fire every layer's event (a compute stream waits on each and
+    reads the layer), count their launches on every replay, and re-capture for
+    other device buffers."""
+    B, L, P, R, Dp, Hp, n = 2, 5, 8, 64, 40, 48, 15
+    dp, hp = indices("runs", Dp, Hp, n, seed=61)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = np.random.default_rng(62).integers(0, 256, host.size, dtype=np.uint8)
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, layout)
+        for bufset_seed in (63, 64):          # the second buffer set forces a re-capture
+            bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=bufset_seed)
+            kv = hc.DeviceKV(bufs, Dp)
+            for rep in range(2):
+                gh.sentinel_fill(bufs)
+                torch.cuda.synchronize()
+                c0 = hc.launch_count()
+                plan.load_layers(kv, stream=s)
+                assert hc.launch_count() - c0 == L
+                sums.zero_()
+                for layer in range(L):
+                    pool.wait_layer(layer, comp)
+                    hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+                hc.wait(comp, 10_000_000)
+                hc.wait(s, 10_000_000)
+                got = gh.to_np(bufs, 2)
+                for k in range(B * L):
+                    assert np.array_equal(got[k], want[k]), (bufset_seed, rep, k)
+                for layer in range(L):
+                    words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+                                            for b in range(B)])
+                    assert int(sums[layer].item()) & (2**64 - 1) == int(words.astype(np.uint64).sum(dtype=np.uint64))
+        with pytest.raises(hc.HiCacheError):      # a backup plan has no per-layer loads
+            bplan = pool.plan(dp, hp, Dp, hc.BACKUP)
+            try:
+                bplan.load_layers(kv, stream=s)
+            finally:
+                bplan.close()
+        plan.close()

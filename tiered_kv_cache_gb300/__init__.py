@@ -97,6 +97,7 @@ def _bind(lib):
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
+        "hicache_plan_load_layers": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
         "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
         "hicache_plan_destroy": (ctypes.c_int, [_vp]),
         "hicache_layer_event": (ctypes.c_int, [_vp, _i32, _P(_vp)]),
@@ -532,6 +533,14 @@ class Plan:
             layout = LAYOUTS[layout]
         _check(library().hicache_plan_execute(self.handle, ctypes.byref(kv.struct), layout, layer,
                                               _stream(stream)))
+
+    def load_layers(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
+        """Every layer, layer by layer, each followed by its layer event, replayed
+        from a CUDA graph the plan captures on first use."""
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_plan_load_layers(self.handle, ctypes.byref(kv.struct), layout,
+                                                  _stream(stream)))
 
     def load_layer(self, kv: DeviceKV, layer: int, layout=LAYOUT_POOL, stream=None):
         """Load one layer of a load plan and record that layer's event."""

@@ -204,6 +204,14 @@ struct hicache_plan {
   int64_t n = 0;
   int64_t device_num_pages = 0;
   std::vector<hicache::RunRec> runs;
+  // hicache_plan_load_layers: the per-layer launches and layer events of one
+  // device KV and layout, captured once as a CUDA graph and replayed
+  std::mutex graph_mu;
+  cudaGraphExec_t graph = nullptr;
+  std::vector<void *> graph_bufs;     // the key: buffer pointers, page count, layout
+  int64_t graph_pages = 0;
+  int32_t graph_layout = -1;
+  int64_t graph_launches = 0;         // kernel launches one replay makes
 };
 
 namespace hicache {
@@ -1130,7 +1138,91 @@ int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num
   return HICACHE_OK;
 }
 
+int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout, void *stream) {
+  g_last_error.clear();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  hicache_pool *pool = plan->pool;
+  const Shape &s = pool->shape;
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, s.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
+  if ((rc = check_device(pool))) return rc;
+  std::lock_guard<std::mutex> g(plan->graph_mu);
+  const std::vector<void *> bufs(kv->buf_ptrs, kv->buf_ptrs + s.B * s.L);
+  if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != kv->device_num_pages ||
+      plan->graph_layout != lay) {
+    if (plan->graph) {
+      cudaGraphExecDestroy(plan->graph);
+      plan->graph = nullptr;
+    }
+    // Capture the L per-layer launches on a private stream, the kernels one
+    // after another.  Each layer's event is recorded (as an external event
+    // node) on a side branch that forks off after that layer's kernel, so the
+    // kernel chain itself has no node between consecutive launches.
+    cudaStream_t cap = nullptr, side = nullptr;
+    std::vector<cudaEvent_t> forks(size_t(s.L) + 1, nullptr);
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+    for (auto &f : forks)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    auto release = [&] {
+      for (auto f : forks)
+        if (f) cudaEventDestroy(f);
+      if (side) cudaStreamDestroy(side);
+      if (cap) cudaStreamDestroy(cap);
+    };
+    if (e != cudaSuccess) {
+      release();
+      return cuda_error(e, "setting up the layer-load capture");
+    }
+    const int64_t before = g_launches.load();
+    for (int64_t l = 0; l < s.L && rc == HICACHE_OK; ++l) {
+      rc = enqueue(pool, kv, plan->runs, nullptr, lay, int32_t(l), false, cap);
+      if (rc != HICACHE_OK) break;
+      e = cudaEventRecord(forks[size_t(l)], cap);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
+      if (e == cudaSuccess) e = cudaEventRecordWithFlags(pool->events[size_t(l)], side, cudaEventRecordExternal);
+      if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer event");
+    }
+    if (rc == HICACHE_OK) {                // join the side branch back
+      e = cudaEventRecord(forks[size_t(s.L)], side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(s.L)], 0);
+      if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
+    }
+    const int64_t captured = g_launches.load() - before;
+    g_launches.fetch_sub(captured);      // counted when replayed
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(cap, &graph);
+    release();
+    if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
+    if (rc == HICACHE_OK) {
+      e = cudaGraphInstantiate(&plan->graph, graph, 0);
+      if (e != cudaSuccess) {
+        plan->graph = nullptr;
+        rc = cuda_error(e, "cudaGraphInstantiate");
+      }
+    }
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != HICACHE_OK) return rc;
+    plan->graph_bufs = bufs;
+    plan->graph_pages = kv->device_num_pages;
+    plan->graph_layout = lay;
+    plan->graph_launches = captured;
+  }
+  const cudaError_t e = cudaGraphLaunch(plan->graph, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
+  g_launches.fetch_add(plan->graph_launches, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> gs(pool->signal_mu);
+  for (int64_t l = 0; l < s.L; ++l) pool->layer_signal[size_t(l)] = 0;
+  return HICACHE_OK;
+}
+
 int hicache_plan_destroy(hicache_plan *plan) {
+  if (plan && plan->graph) cudaGraphExecDestroy(plan->graph);
   delete plan;
   return HICACHE_OK;
 }
