@@ -16,7 +16,7 @@ import gpu_helpers as gh
 pytestmark = pytest.mark.gpu
 
 TEN_S = 10_000_000
-OPS = ["backup", "load", "load_layer", "pipelined", "noalloc", "fused", "plan_layers",
+OPS = ["backup", "load", "load_layer", "pipelined", "noalloc", "fused", "plan_layers", "plan_graph",
        "group_backup", "group_load", "group_layer", "group_pipelined"]
 
 
@@ -59,6 +59,7 @@ def test_random_call_sequence(seed):
     def pairs(n):
         return rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
 
+    plans = []
     for step in range(30):
         op = str(rng.choice(OPS))
         i = int(rng.integers(0, 2))
@@ -93,6 +94,12 @@ def test_random_call_sequence(seed):
                 plan.load_layer(kv, int(l), stream=st)
                 shadow(i, "load", dp, hp, int(l))
             plan.close()
+        elif op == "plan_graph":
+            plan = pool.plan(dp, hp, Dp, hc.LOAD)
+            for _ in range(int(rng.integers(1, 3))):
+                plan.load_layers(kv, stream=st)
+                shadow(i, "load", dp, hp)
+            plans.append(plan)                 # kept until the stream is done
         elif op == "group_backup":
             hc.group_transfer(pools, kvs, dp, hp, hc.BACKUP, stream=st)
             shadow(0, "backup", dp, hp)
@@ -110,6 +117,8 @@ def test_random_call_sequence(seed):
             shadow(0, "load", dp, hp)
             shadow(1, "load", dp, hp)
     hc.wait(st, TEN_S)
+    for plan in plans:
+        plan.close()
     for i, (pool, bufs, (B, R, es)) in enumerate(zip(pools, bufsets, kinds)):
         assert np.array_equal(pool.host_array(gh.NP_DT[es]), host[i]), (seed, i)
         got = gh.to_np(bufs, es)
