@@ -251,3 +251,53 @@ def test_group_calls_reject_bad_arguments_before_any_cuda_call():
         hc.group_transfer([object()], [], [0], [0], hc.LOAD)
     with pytest.raises(ValueError):
         hc.group_load_pipelined([], [], [0, 1], [0])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prepass_large_sets(seed):
+    """Sets large enough for the radix sort of the pairs and the bitmap
+    duplicate check: the runs equal the plain sort-and-merge, and repeated
+    destinations are found wherever they sit."""
+    rng = np.random.default_rng(300 + seed)
+    Dp, Hp, n = 50000, 70000, 6000
+    if seed % 2:
+        dp = rng.choice(Dp, n, replace=False)
+        hp = rng.choice(Hp, n, replace=False)
+    else:                                      # runs: both sides step by one in stretches
+        starts = np.sort(rng.choice(Dp // 16, n // 16, replace=False)) * 16
+        dp = np.concatenate([np.arange(s, s + 16) for s in starts])
+        hp = np.arange(dp.size) + 3
+        perm = rng.permutation(dp.size)        # the pairs arrive shuffled
+        dp, hp = dp[perm], hp[perm]
+        n = dp.size
+    for direction in (hc.BACKUP, hc.LOAD):
+        runs = hc.prepass(Hp, Dp, dp, hp, direction)
+        assert np.array_equal(runs, py_runs(np.asarray(dp, np.int64), np.asarray(hp, np.int64)))
+        assert runs[:, 2].sum() == n
+    # a repeated destination, at the end, in the middle, at the start
+    for pos in (n - 1, n // 2, 1):
+        bad = np.array(dp, np.int64).copy()
+        bad[pos] = bad[pos - 1]
+        with pytest.raises(hc.HiCacheError) as e:
+            hc.prepass(Hp, Dp, bad, hp, hc.LOAD)
+        assert e.value.status == "DUPLICATE_INDEX"
+        assert str(bad[pos]) in str(e.value)
+        badh = np.array(hp, np.int64).copy()
+        badh[pos] = badh[pos - 1]
+        with pytest.raises(hc.HiCacheError) as e:
+            hc.prepass(Hp, Dp, dp, badh, hc.BACKUP)
+        assert e.value.status == "DUPLICATE_INDEX"
+    # a failed check leaves nothing behind: the same valid set passes right after
+    assert hc.prepass(Hp, Dp, dp, hp, hc.LOAD)[:, 2].sum() == n
+
+
+def test_prepass_duplicate_check_beyond_the_bitmap():
+    """Device pools above 2^27 pages take the sorting duplicate check."""
+    Dp = (1 << 28) + 5
+    dp = np.array([5, 1 << 27, (1 << 28) + 4, 77] * 10 + [9], np.int64)   # 41 pages, repeats
+    with pytest.raises(hc.HiCacheError) as e:
+        hc.prepass(100, Dp, dp, np.arange(41), hc.LOAD)
+    assert e.value.status == "DUPLICATE_INDEX"
+    ok = np.array([(1 << 28) + 4 - k for k in range(41)], np.int64)
+    runs = hc.prepass(100, Dp, ok, np.arange(41), hc.LOAD)
+    assert np.array_equal(runs, py_runs(ok, np.arange(41, dtype=np.int64)))

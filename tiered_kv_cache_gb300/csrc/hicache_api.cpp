@@ -94,9 +94,9 @@ int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
     if (s->row_bytes % 16 != 0)
       return set_error(HICACHE_ERR_ALIGNMENT, "row of %lld bytes is not a multiple of 16",
                        (long long)s->row_bytes);
-    if (s->BLPV >= INT32_MAX)
+    if (s->BLPV > INT32_MAX - hicache::kTileVecs)
       return set_error(HICACHE_ERR_INVALID_ARG,
-                       "one page of every buffer and layer (%lld x 16 bytes) must be < 32 GiB",
+                       "one page of every buffer and layer (%lld x 16 bytes) must be < 32 GiB - 16 KiB",
                        (long long)s->BLPV);
   }
   return HICACHE_OK;
@@ -118,6 +118,85 @@ inline bool pair_less(const Pair &a, const Pair &b) {
   return a.h < b.h || (a.h == b.h && a.d < b.d);
 }
 
+int bit_length(uint64_t v) {
+  int b = 0;
+  while (v) {
+    ++b;
+    v >>= 1;
+  }
+  return b;
+}
+
+// Sort pairs by (host page, device page).  Large sets go through an LSD radix
+// sort on the key h * 2^dbits + d (11-bit digits, only as many passes as the
+// largest key needs): a few linear passes where a comparison sort spends
+// ~n log n compares, which for the tens of thousands of one-token pages of a
+// long prefix was most of the host's cost of a call.
+void sort_pairs(std::vector<Pair> &pairs, int64_t Dp) {
+  const size_t n = pairs.size();
+  if (n < 2048) {
+    std::sort(pairs.begin(), pairs.end(), pair_less);
+    return;
+  }
+  const int dbits = bit_length(uint64_t(Dp - 1));
+  uint64_t max_key = 0;
+  thread_local std::vector<uint64_t> tls_keys, tls_tmp;
+  std::vector<uint64_t> &keys = tls_keys, &tmp = tls_tmp;
+  keys.resize(n);
+  tmp.resize(n);
+  for (size_t i = 0; i < n; ++i) {
+    keys[i] = (uint64_t(pairs[i].h) << dbits) | uint64_t(pairs[i].d);
+    max_key = std::max(max_key, keys[i]);
+  }
+  constexpr int kDigit = 11;
+  constexpr size_t kBuckets = size_t(1) << kDigit;
+  const int bits = bit_length(max_key);
+  for (int shift = 0; shift < bits; shift += kDigit) {
+    size_t count[kBuckets + 1] = {};
+    for (size_t i = 0; i < n; ++i) ++count[((keys[i] >> shift) & (kBuckets - 1)) + 1];
+    for (size_t b = 1; b <= kBuckets; ++b) count[b] += count[b - 1];
+    for (size_t i = 0; i < n; ++i) tmp[count[(keys[i] >> shift) & (kBuckets - 1)]++] = keys[i];
+    keys.swap(tmp);
+  }
+  const uint64_t dmask = (uint64_t(1) << dbits) - 1;
+  for (size_t i = 0; i < n; ++i) pairs[i] = Pair{int64_t(keys[i] >> dbits), int64_t(keys[i] & dmask)};
+}
+
+// Whether a load names a destination page twice.  For device pools of up to
+// 2^27 pages, one bit per page in a per-thread bitmap, cleared again for just
+// the pages set; beyond that, a sort.
+bool first_repeated(const int64_t *dev, int64_t n, int64_t Dp, int64_t *repeated) {
+  if (Dp <= (int64_t(1) << 27)) {
+    thread_local std::vector<uint64_t> tls_bits;
+    std::vector<uint64_t> &vbits = tls_bits;
+    if (vbits.size() < size_t((Dp + 63) / 64)) vbits.resize(size_t((Dp + 63) / 64), 0);
+    uint64_t *const bits = vbits.data();
+    int64_t i = 0;
+    bool dup = false;
+    for (; i < n; ++i) {
+      const uint64_t bit = uint64_t(1) << (dev[i] & 63);
+      uint64_t &w = bits[size_t(dev[i] >> 6)];
+      if (w & bit) {
+        dup = true;
+        *repeated = dev[i];
+        break;
+      }
+      w |= bit;
+    }
+    for (int64_t k = 0; k < i; ++k) bits[size_t(dev[k] >> 6)] = 0;
+    return dup;
+  }
+  thread_local std::vector<int64_t> ds;
+  ds.assign(dev, dev + n);
+  std::sort(ds.begin(), ds.end());
+  for (int64_t i = 1; i < n; ++i)
+    if (ds[size_t(i)] == ds[size_t(i - 1)]) {
+      *repeated = ds[size_t(i)];
+      return true;
+    }
+  return false;
+}
+
 // Validate n index pairs and reduce them to runs: pairs sorted by (host page,
 // device page), merged while both pages step by one (at most max_run pages per
 // run).  On error the last-error text is set and *runs holds no usable table.
@@ -132,7 +211,10 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
   runs->clear();
   if (n == 0) return HICACHE_OK;
   if (!dev || !host) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
-  thread_local std::vector<Pair> pairs;
+  // one lookup of the per-thread buffer: in a shared library every access to
+  // a thread_local can be a call, too slow inside a per-page loop
+  thread_local std::vector<Pair> tls_pairs;
+  std::vector<Pair> &pairs = tls_pairs;
   pairs.resize(size_t(n));
   bool sorted = true;
   for (int64_t i = 0; i < n; ++i) {
@@ -146,7 +228,7 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
     pairs[size_t(i)] = Pair{h, d};
     if (i > 0 && pair_less(pairs[size_t(i)], pairs[size_t(i - 1)])) sorted = false;
   }
-  if (!sorted) std::sort(pairs.begin(), pairs.end(), pair_less);
+  if (!sorted) sort_pairs(pairs, Dp);
   if (direction == HICACHE_DIR_BACKUP) {
     for (int64_t i = 1; i < n; ++i)
       if (pairs[size_t(i)].h == pairs[size_t(i - 1)].h)
@@ -160,13 +242,10 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
           return set_error(HICACHE_ERR_DUPLICATE_INDEX,
                            "device page %lld is a load destination twice", (long long)dev[i]);
   } else {
-    thread_local std::vector<int64_t> ds;
-    ds.assign(dev, dev + n);
-    std::sort(ds.begin(), ds.end());
-    for (int64_t i = 1; i < n; ++i)
-      if (ds[size_t(i)] == ds[size_t(i - 1)])
-        return set_error(HICACHE_ERR_DUPLICATE_INDEX,
-                         "device page %lld is a load destination twice", (long long)ds[size_t(i)]);
+    int64_t page = 0;
+    if (first_repeated(dev, n, Dp, &page))
+      return set_error(HICACHE_ERR_DUPLICATE_INDEX, "device page %lld is a load destination twice",
+                       (long long)page);
   }
   for (int64_t i = 0; i < n; ++i) {
     const Pair &p = pairs[size_t(i)];
@@ -183,10 +262,11 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
 }
 
 constexpr int64_t kMaxTiles = int64_t(1) << 30;
+constexpr int64_t kMaxOuterVecs = INT32_MAX - hicache::kTileVecs;
 
 // Runs are capped so that a unit (at most every buffer and layer of a run)
-// stays below 2^31 vectors: the kernels index units with 32-bit offsets.
-int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, (INT32_MAX - 1) / s.BLPV); }
+// stays below 2^31 - 1024 vectors: the kernels index units with 32-bit offsets.
+int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, kMaxOuterVecs / s.BLPV); }
 
 void clear_error() { g_last_error.clear(); }
 
@@ -235,32 +315,34 @@ int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_
   return HICACHE_OK;
 }
 
-// Copy runs[next..] into job `j` of the parameters, starting at blob word
-// `word`: at most max_runs runs and kMaxTiles tiles (so the kernel's 32-bit
-// grid-stride index never overflows).  Returns the number of runs taken, or -1
-// if even one run is too large -- which the run cap of the pre-pass rules out:
-// a unit stays below 2^31 vectors, i.e. 2^21 tiles, times at most 512 outer
-// units is 2^30 = kMaxTiles.
+// Copy runs[next..] into a job's run table (at blob word `word`): at most
+// max_runs runs, fewer than 2^31 - 1024 vectors per outer unit (the kernels'
+// 32-bit vector offsets), and kMaxTiles / launch_factor tiles (so the 32-bit
+// tile index never overflows).  Returns the number of runs taken, or -1 if even
+// one run is too large -- which the run cap of the pre-pass rules out.
 int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
                   int64_t max_runs, hicache::Job &job, hicache::Run *table, int32_t word,
                   int64_t launch_factor) {
-  int64_t tiles = 0;
+  int64_t vecs = 0;
   int32_t count = 0;
   while (next + size_t(count) < runs.size() && count < max_runs) {
     const RunRec &r = runs[next + size_t(count)];
-    const int64_t t = (r.len * upp + hicache::kTileVecs - 1) / hicache::kTileVecs;
-    if ((tiles + t) * outers * launch_factor > kMaxTiles) {
+    const int64_t nv = vecs + r.len * upp;
+    const int64_t tiles = (nv + hicache::kTileVecs - 1) / hicache::kTileVecs;
+    if (nv > kMaxOuterVecs || tiles * outers * launch_factor > kMaxTiles) {
       if (count == 0) return -1;
       break;
     }
-    table[count] = hicache::Run{int32_t(r.h0), int32_t(r.d0), int32_t(r.len), int32_t(tiles)};
-    tiles += t;
+    table[count] = hicache::Run{int32_t(r.h0), int32_t(r.d0), int32_t(r.len), int32_t(vecs)};
+    vecs = nv;
     ++count;
   }
   job.n_runs = count;
   job.runs_word = word;
-  job.tiles_per_outer = int32_t(tiles);
-  job.total_tiles = int32_t(tiles * outers);
+  job.vecs_per_outer = uint32_t(vecs);
+  job.pad = 0;
+  job.tiles_per_outer = int32_t((vecs + hicache::kTileVecs - 1) / hicache::kTileVecs);
+  job.total_tiles = int32_t(job.tiles_per_outer * outers);
   return count;
 }
 
@@ -1300,7 +1382,8 @@ int hicache_prepass(int64_t host_num_pages, int64_t device_num_pages, const int6
   if (!num_runs) return set_error(HICACHE_ERR_INVALID_ARG, "num_runs is NULL");
   if (host_num_pages < 1 || host_num_pages >= INT32_MAX)
     return set_error(HICACHE_ERR_INVALID_ARG, "host_num_pages must be in [1, 2^31)");
-  std::vector<RunRec> runs;
+  thread_local std::vector<RunRec> tls_runs;
+  std::vector<RunRec> &runs = tls_runs;
   const int rc = prepass(host_num_pages, device_num_pages, device_pages, host_pages, n, direction,
                          INT32_MAX, &runs);
   if (rc) return rc;

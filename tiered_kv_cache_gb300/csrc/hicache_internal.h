@@ -66,12 +66,14 @@ HC_HD uint32_t fast_div(uint32_t n, const FastDiv &f) {
 
 // ---- run table -------------------------------------------------------------
 // A run: `len` pages whose host pages h0.. and device pages d0.. both step by
-// one.  tile0 = tiles of the runs before it within one "outer" unit.
+// one.  vec0 = vectors of the runs before it within one "outer" unit: the runs
+// of an outer are laid end to end in one vector range, which tiles cut in
+// 1024-vector pieces whatever the run boundaries.
 struct Run {
   int32_t h0;
   int32_t d0;
   int32_t len;
-  int32_t tile0;
+  int32_t vec0;
 };
 
 // Host-side run record (before tiling).
@@ -89,6 +91,8 @@ struct Job {
   int32_t runs_word;          // first word of the job's run table in XferParams::blob
   int32_t tiles_per_outer;    // tiles of one outer unit (a buffer, or a buffer-layer)
   int32_t total_tiles;
+  uint32_t vecs_per_outer;    // vectors of one outer unit: every run end to end (< 2^31)
+  uint32_t pad;
 };
 
 // Everything a transfer launch needs, in vectors of 16 bytes.

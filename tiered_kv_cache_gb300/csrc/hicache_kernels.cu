@@ -20,9 +20,12 @@
 //       page_first(_direct), one layer    unit = (buffer, run), host strided
 //       page_first_direct_kv, all layers  unit = run: every buffer and layer of
 //                                         the run's pages is one host range
-//     and every unit into tiles of 16 KiB (1024 vectors of 16 bytes).  CTAs
-//     take tiles in host-address order (grid-stride), so the host link sees
-//     long sequential streams of whole 128-byte lines in every layout.
+//     The units of one outer index (a buffer, a buffer-layer, or everything)
+//     lie end to end in one vector range, cut into tiles of 16 KiB (1024
+//     vectors of 16 bytes); a tile spans several units where runs are short,
+//     so short runs still fill whole tiles.  CTAs take tiles in host-address
+//     order (grid-stride), so the host link sees long sequential streams of
+//     whole 128-byte lines in every layout.
 //   * Each thread of a tile moves 4 independent 16-byte vectors: 4 loads in
 //     flight before the first store.  The device-side address of every vector
 //     is decoded on the fly (a multiply-high division per dimension), which
@@ -106,8 +109,26 @@ __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bu
   }
 }
 
-// Move tile `g` of one job: 16 KiB of one unit, 4 vectors per thread, all
-// loads issued before the first store.
+// The run holding vector w of an outer unit: the last run with vec0 <= w.
+__device__ __forceinline__ int find_run(const Run *runs, int n_runs, uint32_t w) {
+  int lo = 0, hi = n_runs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (uint32_t(runs[mid].vec0) <= w) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Move tile `g` of one job: 1024 consecutive vectors (16 KiB) of one outer
+// unit's vector range, 4 per thread, all loads issued before the first store.
+// The runs of an outer lie end to end in that range, so a tile may span
+// several short runs and every tile but an outer's last is full.
+//
+// The run table sits in the kernel parameters, where loads from different
+// addresses within a warp are served one address at a time.  So each warp
+// finds the run of its first vector (the same address in every lane) and each
+// lane then steps forward from it to its own run: no step where runs are
+// longer than a warp's span, one or two where they are a few rows long.
 template <int LAYOUT, bool ALL, bool TO_HOST>
 __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, const Run *runs,
                                           uint4 *const *bufs, int32_t g, int layer) {
@@ -121,31 +142,40 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
     b = outer;
     l = layer;
   }
-  // the run holding tile `inner`: the last run with tile0 <= inner
-  int lo = 0, hi = job.n_runs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (runs[mid].tile0 <= inner) lo = mid; else hi = mid - 1;
-  }
-  const Run r = runs[lo];
-  const uint32_t w0 = uint32_t(inner - r.tile0) * kTileVecs + threadIdx.x;
-  const uint32_t unit = uint32_t(r.len) * h.unit_per_page;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp0 = uint32_t(inner) * kTileVecs + (threadIdx.x - lane);  // the warp's first vector
+  int rb = 0;                      // the run of the warp's first vector at step k (warp-uniform)
+  uint32_t rb_end = 0;
 
   uint4 v[kUnroll];
   uint4 *dst[kUnroll];
 #pragma unroll
   for (int k = 0; k < kUnroll; ++k) {
-    const uint32_t w = w0 + k * kThreads;
+    const uint32_t base = warp0 + k * kThreads;
+    const uint32_t w = base + lane;
     dst[k] = nullptr;
-    if (w < unit) {
-      uint4 *dev, *host;
-      map_vector<LAYOUT, ALL>(h, bufs, b, l, r, w, dev, host);
-      if (TO_HOST) {
-        v[k] = ld_stream(dev);
-        dst[k] = host;
-      } else {
-        v[k] = ld_stream(host);
-        dst[k] = dev;
+    if (base < job.vecs_per_outer) {                       // warp-uniform
+      if (k == 0 || base >= rb_end) {
+        rb = find_run(runs, job.n_runs, base);
+        rb_end = uint32_t(runs[rb].vec0) + uint32_t(runs[rb].len) * h.unit_per_page;
+      }
+      if (w < job.vecs_per_outer) {
+        int r = rb;
+        uint32_t end = rb_end;
+        while (w >= end) {                                 // runs shorter than the warp's span
+          ++r;
+          end = uint32_t(runs[r].vec0) + uint32_t(runs[r].len) * h.unit_per_page;
+        }
+        const Run cur = runs[r];
+        uint4 *dev, *host;
+        map_vector<LAYOUT, ALL>(h, bufs, b, l, cur, w - uint32_t(cur.vec0), dev, host);
+        if (TO_HOST) {
+          v[k] = ld_stream(dev);
+          dst[k] = host;
+        } else {
+          v[k] = ld_stream(host);
+          dst[k] = dev;
+        }
       }
     }
   }
