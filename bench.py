@@ -47,11 +47,20 @@ GB = 1e9
 
 
 def kernel_fingerprint() -> str:
+    """sha256 (first 16 hex digits) of the transfer kernels' source with comments
+    and blank lines removed: a comment edit keeps recorded counters valid, a code
+    change voids them."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("hicache_kernels.cu", "hicache_internal.h"):
-        with open(os.path.join(ROOT, "tiered_kv_cache_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tiered_kv_cache_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"//[^\n]*", "", src)
+        for line in src.splitlines():
+            line = line.strip()
+            if line:
+                h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

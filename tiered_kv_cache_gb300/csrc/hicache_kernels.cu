@@ -1,18 +1,20 @@
 // hicache_kernels.cu -- sm_103a transfer kernels for the L1 <-> L2 KV movement.
 //
-// One kernel body serves backup (device -> host) and load (host -> device) for
-// the three host layouts, for every layer at once or for one layer:
+// One tile mover serves backup (device -> host) and load (host -> device) for
+// the four host layouts, for every layer at once or for one layer, in every
+// kernel here: one direction, both directions fused, a pipelined load that
+// signals each layer as it lands, and the same for a group of pools:
 //
 //   * The pre-pass (host side) sorts the index pairs by host page and merges
 //     pages that are consecutive on BOTH sides into runs.  The run table and
 //     the B*L device-buffer pointers travel in the kernel parameters, so a
-//     call of up to 1536 runs is exactly one launch and no descriptor or
-//     per-segment submission ever reaches the GPU.  (The pages trace the
-//     cost of page_first_direct to one DMA descriptor per page x layer
-//     segment: "Tuning SGLang HiCache L2 on Kunlunxin P800/P900", sections
-//     2.1 and 2.3; "Baidu's KVCache Overhaul", section "DMA Segment Explosion
-//     & Batched Gather/Scatter".  Here every segment boundary is just address
-//     arithmetic inside a warp.)
+//     call of up to 1536 runs (more with fewer buffers) is exactly one launch
+//     and no descriptor or per-segment submission ever reaches the GPU.  (The
+//     pages trace the cost of page_first_direct to one DMA descriptor per
+//     page x layer segment: "Tuning SGLang HiCache L2 on Kunlunxin P800/P900",
+//     sections 2.1 and 2.3; "Baidu's KVCache Overhaul", section "DMA Segment
+//     Explosion & Batched Gather/Scatter".  Here every segment boundary is just
+//     address arithmetic inside a warp.)
 //   * The work is cut into "units" that are contiguous on the HOST side:
 //       layer_first, any layer count      unit = (buffer, layer, run)
 //       page_first(_direct), all layers   unit = (buffer, run): all layers of
