@@ -642,6 +642,51 @@ def bench_nsa_group(torch, hc, args):
     return out, launches
 
 
+def bench_shapes(torch, hc, args):
+    """Row size x page size sweep: about 1 GiB per call of fully scattered
+    device pages (a permutation) and contiguous host pages, 8 layers, K+V, one
+    byte per element, load and backup in layer_first and page_first.  Short
+    rows at small page sizes give many short runs: the case where tiles span
+    runs and the host pre-pass is linear in the pages."""
+    st = torch.cuda.Stream()
+
+    def timed(fn, n=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            torch.cuda.synchronize()
+            out.append(_elapsed(torch, e0, e1))
+        return statistics.median(out)
+
+    L, B = 8, 2
+    res = []
+    for row_bytes in (256, 1152, 2048):
+        for P in (1, 16, 64):
+            page_bytes = B * L * P * row_bytes
+            n = (1 << 30) // page_bytes
+            bufs = [torch.empty((n * P, row_bytes), dtype=torch.uint8, device="cuda") for _ in range(B * L)]
+            kv = hc.DeviceKV(bufs, n)
+            rng = np.random.default_rng(0)
+            dp, hp = rng.permutation(n), np.arange(n)
+            r = {"row_bytes": row_bytes, "page_size": P, "pages": n}
+            for lay, name in ((0, "layer_first"), (1, "page_first")):
+                with hc.Pool(L, B, P, row_bytes, n, lay, elem_bytes=1, launch_ctas=args.ctas) as pool:
+                    nb = n * page_bytes
+                    r[f"load_{name}_gbs"] = round(nb / timed(lambda: pool.load(kv, dp, hp, stream=st)) / GB, 1)
+                    r[f"backup_{name}_gbs"] = round(nb / timed(lambda: pool.backup(kv, dp, hp, stream=st)) / GB, 1)
+            res.append(r)
+            del bufs, kv
+            torch.cuda.empty_cache()
+    return res
+
+
 def bench_small_mix(torch, hc, args):
     """10,000 seeded requests, 1-256 pages log-uniform, 30% backup / 70% load,
     random pages, layer_first.  Per-call latency = host wall clock from the API
@@ -853,7 +898,7 @@ def main():
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc",
-                             "engine_bidir", "nsa_group"],
+                             "engine_bidir", "nsa_group", "shapes"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
     ap.add_argument("--tokens", default="",
@@ -884,9 +929,16 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch)
-    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group"):
+    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group", "shapes"):
         t0 = time.perf_counter()
-        if args.workload == "nsa_group":
+        if args.workload == "shapes":
+            res = bench_shapes(torch, hc, args)
+            launches = None
+            value = next(r["load_layer_first_gbs"] for r in res if r["row_bytes"] == 1152 and r["page_size"] == 1)
+            what = {"workload": "shapes: rows of 256 / 1152 / 2048 bytes x page sizes 1 / 16 / 64, 8 layers, "
+                                "K+V, about 1 GiB per call of fully scattered device pages, contiguous host",
+                    "value": "load GB/s, layer_first, 1152-byte rows, page size 1"}
+        elif args.workload == "nsa_group":
             res, launches = bench_nsa_group(torch, hc, args)
             value = res["4k"]["per_layer_group"]["gbs"]
             what = {"workload": "nsa_group: 61 layers, page 64, page_first; an MLA latent (576 bf16), an fp8 "
