@@ -597,3 +597,24 @@ def test_plan_load_layers_graph_replay(layout):
             finally:
                 bplan.close()
         plan.close()
+
+
+def test_plan_load_layers_of_an_empty_plan_records_every_event():
+    """A plan of no pages replays a graph of event records alone: no launch,
+    and every layer's event still fires behind the stream's earlier work."""
+    B, L, P, R, Dp, Hp = 1, 3, 4, 32, 8, 8
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=70)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        kv = hc.DeviceKV(bufs, Dp)
+        plan = pool.plan(np.zeros(0, np.int64), np.zeros(0, np.int64), Dp, hc.LOAD)
+        s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(int(5e7))
+        c0 = hc.launch_count()
+        plan.load_layers(kv, stream=s)
+        assert hc.launch_count() == c0
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+        hc.wait(comp, 10_000_000)
+        assert s.query()
+        plan.close()
