@@ -31,12 +31,13 @@ def oracle_apply(reqs, dev, host, B, L, P, R, Hp, layout):
             gh.orc().load(dev, host, B, L, P, R, Hp, dp, hp, layout)
 
 
+@pytest.mark.parametrize("seed", range(3))
 @pytest.mark.parametrize("layout", [0, 1, 2, 3], ids=list(hc.LAYOUTS))
-def test_sequential_semantics_with_hazards(layout):
+def test_sequential_semantics_with_hazards(layout, seed):
     """Small pools and many overlapping requests: whether or not the engine
-    fuses, the outcome is the oracle's in submission order."""
+    fuses or holds a request, the outcome is the oracle's in submission order."""
     B, L, P, R, Dp, Hp = 2, 3, 4, 64, 20, 20
-    rng = np.random.default_rng(90 + layout)
+    rng = np.random.default_rng(90 + layout + 10 * seed)
     bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=90)
     with hc.Pool(L, B, P, R, Hp, layout) as pool:
         host = pool.host_array(np.uint8)
