@@ -400,7 +400,8 @@ typedef struct hicache_engine hicache_engine; /* opaque */
 /* Starts the worker thread and creates the engine's stream on the pool's device. */
 int hicache_engine_create(hicache_pool *pool, hicache_engine **out);
 /* Launches whatever is still queued, waits for the engine's stream, stops the
- * worker and frees the engine. */
+ * worker and frees the engine.  No other thread may be inside a call on the
+ * engine (submit, wait, wait_on_stream, stats) meanwhile or afterwards. */
 int hicache_engine_destroy(hicache_engine *engine);
 /* Queue a backup (direction HICACHE_DIR_BACKUP) or load of every layer of n
  * pages, with the checks of hicache_backup / hicache_load.  If
