@@ -158,7 +158,9 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
 /* Destroys the pool's events and the pool.  Transfers already enqueued still
  * run; the host buffer must stay allocated until they finish.  The pool's
  * pipelined loads count into device words the pool owns, so this first waits
- * on the host for the last of them to finish. */
+ * on the host for the last of them to finish.  Plans and engines of the pool
+ * must be destroyed first, and no other thread may be inside a call on the
+ * pool meanwhile. */
 int hicache_pool_destroy(hicache_pool *pool);
 
 /* ---- transfers -------------------------------------------------------------
