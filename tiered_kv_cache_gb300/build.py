@@ -1,11 +1,15 @@
 """Build libhicache.so in-tree with nvcc for sm_103a (GB300).
 
-Four translation units, compiled in parallel, linked with the static CUDA
+Eight translation units, compiled in parallel, linked with the static CUDA
 runtime so the library loads on a machine without a GPU driver:
-  csrc/hicache_kernels.cu   transfer and stand-in compute kernels
-  csrc/hicache_api.cpp      validation, pre-pass, pools, plans, events
-  csrc/hicache_alloc.cpp    LIFO host-page allocator
-  csrc/hicache_engine.cpp   submission engine (queue + worker thread)
+  csrc/hicache_kernels.cu    transfer and stand-in compute kernels
+  csrc/hicache_api.cpp       errors, pinned memory, pools, transfers, events
+  csrc/hicache_index.cpp     validation and the index pre-pass (host only)
+  csrc/hicache_pipeline.cpp  pipelined loads and per-layer waits
+  csrc/hicache_plan.cpp      plans (pre-passed index sets, graph replay)
+  csrc/hicache_group.cpp     buffer groups
+  csrc/hicache_alloc.cpp     LIFO host-page allocator
+  csrc/hicache_engine.cpp    submission engine (queue + worker thread)
 """
 from __future__ import annotations
 
@@ -24,7 +28,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{INCLUDE}", f"-I{CSRC}"]
-SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_alloc.cpp", "hicache_engine.cpp"]
+SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_index.cpp", "hicache_pipeline.cpp",
+           "hicache_plan.cpp", "hicache_group.cpp", "hicache_alloc.cpp", "hicache_engine.cpp"]
 
 
 def _nvcc() -> str:

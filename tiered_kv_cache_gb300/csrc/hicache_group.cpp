@@ -1,0 +1,277 @@
+// hicache_group.cpp -- buffer groups: up to HICACHE_MAX_GROUP pools (buffer
+// kinds with different rows) moved by one index set in one launch per chunk,
+// all layers, one layer, or pipelined with per-layer counters for every pool.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <mutex>
+#include <vector>
+
+#include "hicache.h"
+#include "hicache_host.h"
+#include "hicache_internal.h"
+
+namespace hicache {
+
+// Enqueue validated runs for every pool of a group, one launch per chunk of
+// runs that fits the parameters of all of them.
+int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t np,
+                  const std::vector<RunRec> &runs, int32_t layout, int32_t layer, bool to_host,
+                  void *stream) {
+  if (runs.empty()) return HICACHE_OK;
+  const bool all = layer < 0;
+  thread_local hicache::GroupParams params;
+  hicache::GroupHeader &g = params.g;
+  g.njobs = np;
+  int32_t word = 0;
+  int64_t outers[hicache::kMaxGroup], upp[hicache::kMaxGroup];
+  for (int32_t j = 0; j < np; ++j) {
+    const Shape &s = pools[j]->shape;
+    const bool lf_all = (layout == HICACHE_LAYER_FIRST) && all;
+    const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
+    outers[j] = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
+    upp[j] = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
+    fill_shape(pools[j], upp[j], all ? 0 : layer, g.h[j]);
+    g.bufs_word[j] = word;
+    for (int64_t i = 0; i < s.B * s.L; ++i)
+      params.blob[word++] = uint64_t(reinterpret_cast<uintptr_t>(kvs[j].buf_ptrs[i]));
+  }
+  g.num_bufs = word;
+  const int64_t capacity = (hicache::kGroupBlobWords - word) / (2 * np);  // runs per launch
+  const hicache_pool *p0 = pools[0];
+  size_t next = 0;
+  while (next < runs.size()) {
+    // the most runs every job's table and tile budget can take
+    int64_t c = capacity;
+    for (int32_t j = 0; j < np; ++j) {
+      hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
+      const int32_t cj = fill_runs(runs, next, upp[j], outers[j], c, g.h[j].job[0], table, word, np);
+      if (cj < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+      c = std::min<int64_t>(c, cj);
+    }
+    int64_t tiles = 0;
+    for (int32_t j = 0; j < np; ++j) {
+      const int32_t w = word + int32_t(2 * c) * j;
+      hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[w]);
+      fill_runs(runs, next, upp[j], outers[j], c, g.h[j].job[0], table, w, np);
+      g.tile_start[j] = int32_t(tiles);
+      tiles += g.h[j].job[0].total_tiles;
+    }
+    g.tile_start[np] = int32_t(tiles);
+    hicache::GroupLaunch x;
+    x.params = &params;
+    x.words = word + int32_t(2 * c) * np;
+    x.layout = layout;
+    x.all_layers = all;
+    x.to_host = to_host;
+    x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : p0->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_group(x);
+    if (e != 0) return cuda_error(cudaError_t(e), "group transfer kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    next += size_t(c);
+  }
+  return HICACHE_OK;
+}
+
+// Enqueue validated load runs for every pool of a group as pipelined launches:
+// every layer of every pool, layer by layer, one counter per pool and layer.
+// The caller holds every pool's signal lock.
+int enqueue_group_pipelined(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t np,
+                            const std::vector<RunRec> &runs, int32_t layout, void *stream) {
+  const int64_t L = pools[0]->shape.L;
+  thread_local hicache::GroupParams params;
+  hicache::GroupHeader &g = params.g;
+  g.njobs = np;
+  int32_t word = 0;
+  for (int32_t j = 0; j < np; ++j) {
+    const Shape &s = pools[j]->shape;
+    fill_shape(pools[j], s.PV, 0, g.h[j]);
+    g.bufs_word[j] = word;
+    for (int64_t i = 0; i < s.B * s.L; ++i)
+      params.blob[word++] = uint64_t(reinterpret_cast<uintptr_t>(kvs[j].buf_ptrs[i]));
+    g.layer_done[j] = pools[j]->layer_done;
+  }
+  for (int32_t j = np; j < hicache::kMaxGroup; ++j) g.layer_done[j] = nullptr;
+  g.sched = pools[0]->layer_done + L;       // pool 0's scheduler words
+  g.num_bufs = word;
+  const int64_t capacity = (hicache::kGroupBlobWords - word) / (2 * np);
+  size_t next = 0;
+  while (next < runs.size()) {
+    // one layer's units of pool j are (buffer, run); the launch covers L layers
+    int64_t c = capacity;
+    for (int32_t j = 0; j < np; ++j) {
+      const Shape &s = pools[j]->shape;
+      hicache::Run *table = reinterpret_cast<hicache::Run *>(&params.blob[word]);
+      const int32_t cj = fill_runs(runs, next, s.PV, s.B, c, g.h[j].job[0], table, word, np * L);
+      if (cj < 0) return set_error(HICACHE_ERR_INVALID_ARG, "transfer too large for one launch");
+      c = std::min<int64_t>(c, cj);
+    }
+    int64_t tiles = 0;
+    for (int32_t j = 0; j < np; ++j) {
+      const Shape &s = pools[j]->shape;
+      const int32_t w = word + int32_t(2 * c) * j;
+      fill_runs(runs, next, s.PV, s.B, c, g.h[j].job[0], reinterpret_cast<hicache::Run *>(&params.blob[w]), w,
+                np * L);
+      g.tile_start[j] = int32_t(tiles);
+      tiles += g.h[j].job[0].total_tiles;
+    }
+    g.tile_start[np] = int32_t(tiles);
+    hicache::GroupLaunch x;
+    x.params = &params;
+    x.words = word + int32_t(2 * c) * np;
+    x.layout = layout;
+    x.all_layers = false;
+    x.to_host = false;
+    x.grid = int(std::min<int64_t>(tiles * L, pools[0]->ctas));
+    x.stream = stream;
+    const int e = hicache::launch_pipelined_group(x);
+    if (e != 0) return cuda_error(cudaError_t(e), "pipelined group kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    for (int32_t j = 0; j < np; ++j)
+      for (int64_t l = 0; l < L; ++l) {
+        pools[j]->layer_target[size_t(l)] += uint32_t(g.h[j].job[0].total_tiles);
+        pools[j]->layer_signal[size_t(l)] = 1;
+      }
+    next += size_t(c);
+  }
+  return HICACHE_OK;
+}
+
+// The checks every group call shares: 1..HICACHE_MAX_GROUP distinct pools on
+// one device with equal layers, page size and resolved layout, valid device KV
+// for each, at most kMaxBufs buffers, no buffer named twice.  Returns the
+// resolved layout and the bounds the pre-pass must apply to every pool.
+int check_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools, int32_t layout,
+                int32_t *lay, int64_t *Hp, int64_t *Dp, int64_t *max_run) {
+  if (!pools || !kvs) return set_error(HICACHE_ERR_INVALID_ARG, "pools or kvs is NULL");
+  if (npools < 1 || npools > HICACHE_MAX_GROUP)
+    return set_error(HICACHE_ERR_INVALID_ARG, "npools = %d outside [1, %d]", npools, HICACHE_MAX_GROUP);
+  for (int32_t i = 0; i < npools; ++i)
+    if (!pools[i]) return set_error(HICACHE_ERR_INVALID_ARG, "pool %d is NULL", i);
+  const hicache_pool *p0 = pools[0];
+  int rc = resolve_layout(layout, p0->shape.layout, lay);
+  if (rc) return rc;
+  *Hp = INT64_MAX;
+  *Dp = INT64_MAX;
+  *max_run = INT64_MAX;
+  int64_t bufs = 0;
+  std::vector<uintptr_t> ptrs;
+  for (int32_t i = 0; i < npools; ++i) {
+    const hicache_pool *p = pools[i];
+    for (int32_t k = 0; k < i; ++k)
+      if (pools[k] == p) return set_error(HICACHE_ERR_INVALID_ARG, "pool %d appears twice in the group", i);
+    if (p->device != p0->device)
+      return set_error(HICACHE_ERR_INVALID_ARG, "pool %d is on device %d, pool 0 on %d", i, p->device,
+                       p0->device);
+    if (p->shape.L != p0->shape.L || p->shape.P != p0->shape.P)
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "pool %d has %lld layers of %lld-token pages; pool 0 has %lld of %lld", i,
+                       (long long)p->shape.L, (long long)p->shape.P, (long long)p0->shape.L,
+                       (long long)p0->shape.P);
+    int32_t li = 0;
+    if ((rc = resolve_layout(layout, p->shape.layout, &li))) return rc;
+    if (li != *lay)
+      return set_error(HICACHE_ERR_INVALID_ARG, "pool %d resolves to layout %d, pool 0 to %d", i, li, *lay);
+    if ((rc = check_kv(p, &kvs[i], 0))) return rc;
+    *Hp = std::min(*Hp, p->shape.Hp);
+    *Dp = std::min(*Dp, kvs[i].device_num_pages);
+    *max_run = std::min(*max_run, max_run_pages(p->shape));
+    bufs += p->shape.B * p->shape.L;
+    for (int64_t b = 0; b < p->shape.B * p->shape.L; ++b)
+      ptrs.push_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]));
+  }
+  if (bufs > hicache::kMaxBufs)
+    return set_error(HICACHE_ERR_INVALID_ARG, "the group has %lld device buffers; at most %d", (long long)bufs,
+                     hicache::kMaxBufs);
+  std::sort(ptrs.begin(), ptrs.end());
+  if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
+    return set_error(HICACHE_ERR_INVALID_ARG, "a device buffer is named twice in the group");
+  return HICACHE_OK;
+}
+
+}  // namespace hicache
+
+using namespace hicache;
+
+extern "C" {
+
+int hicache_group_transfer(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools,
+                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                           int32_t layout, int32_t layer_id, int32_t direction, void *stream) {
+  clear_error();
+  int32_t lay = 0;
+  int64_t Hp = 0, Dp = 0, max_run = 0;
+  int rc = check_group(pools, kvs, npools, layout, &lay, &Hp, &Dp, &max_run);
+  if (rc) return rc;
+  if (direction != HICACHE_DIR_BACKUP && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "direction %d is neither backup nor load", direction);
+  if (layer_id >= pools[0]->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)pools[0]->shape.L);
+  if (layer_id >= 0 && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(Hp, Dp, device_pages, host_pages, n, direction, max_run, &runs))) return rc;
+  if ((rc = check_device(pools[0]))) return rc;
+  if ((rc = enqueue_group(pools, kvs, npools, runs, lay, layer_id, direction == HICACHE_DIR_BACKUP, stream)))
+    return rc;
+  if (layer_id >= 0) {
+    for (int32_t i = 0; i < npools; ++i) {
+      hicache_pool *p = pools[i];
+      const cudaError_t e = cudaEventRecord(p->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+      std::lock_guard<std::mutex> g(p->signal_mu);
+      p->layer_signal[size_t(layer_id)] = 0;
+    }
+  }
+  return HICACHE_OK;
+}
+
+int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools,
+                                 const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                                 int32_t layout, void *stream) {
+  clear_error();
+  int32_t lay = 0;
+  int64_t Hp = 0, Dp = 0, max_run = 0;
+  int rc = check_group(pools, kvs, npools, layout, &lay, &Hp, &Dp, &max_run);
+  if (rc) return rc;
+  thread_local std::vector<RunRec> runs;
+  if ((rc = prepass(Hp, Dp, device_pages, host_pages, n, HICACHE_DIR_LOAD, max_run, &runs))) return rc;
+  if ((rc = check_device(pools[0]))) return rc;
+  if (!wait_value32())
+    return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
+  // every pool's signal lock, in address order (the pools are distinct)
+  std::vector<hicache_pool *> order(pools, pools + npools);
+  std::sort(order.begin(), order.end());
+  std::vector<std::unique_lock<std::mutex>> locks;
+  for (hicache_pool *p : order) locks.emplace_back(p->signal_mu);
+  for (int32_t i = 0; i < npools; ++i) {
+    hicache_pool *p = pools[i];
+    if (p->pipeline_stream_set && p->pipeline_stream != stream &&
+        cudaEventQuery(p->pipeline_last) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "a pipelined load of pool %d is still running on another stream", i);
+    }
+  }
+  for (int32_t i = 0; i < npools; ++i) {
+    pools[i]->pipeline_stream_set = true;
+    pools[i]->pipeline_stream = stream;
+  }
+  if ((rc = enqueue_group_pipelined(pools, kvs, npools, runs, lay, stream))) return rc;
+  for (int32_t i = 0; i < npools; ++i) {
+    hicache_pool *p = pools[i];
+    for (int64_t l = 0; l < p->shape.L; ++l) {
+      const cudaError_t e = cudaEventRecord(p->events[size_t(l)], static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+    }
+    const cudaError_t e = cudaEventRecord(p->pipeline_last, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
+  }
+  return HICACHE_OK;
+}
+
+}  // extern "C"

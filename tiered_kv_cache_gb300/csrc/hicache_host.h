@@ -1,9 +1,13 @@
-// hicache_host.h -- host-side internals shared by the API (hicache_api.cpp) and
-// the submission engine (hicache_engine.cpp).  Not part of the public ABI.
+// hicache_host.h -- host-side internals shared by the host files of the
+// library (API, index pre-pass, pipelined loads, plans, groups, engine).  Not
+// part of the public ABI.
 #pragma once
 
+#include <cuda.h>  // driver types for the stream memory wait (fetched at run time)
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <climits>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -25,6 +29,15 @@ int set_error(int code, const char *fmt, ...);
 int cuda_error(cudaError_t e, const char *what);
 void clear_error();
 
+// Kernel launches made by the library (hicache_launch_count).
+extern std::atomic<int64_t> g_launches;
+
+// Launch limits: tiles per launch (32-bit tile index) and vectors per outer
+// unit (32-bit vector offsets inside a unit, with a tile of headroom).
+constexpr int64_t kMaxTiles = int64_t(1) << 30;
+constexpr int64_t kMaxOuterVecs = INT32_MAX - kTileVecs;
+
+// hicache_index.cpp: validation and the pre-pass.
 int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment);
 int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out);
 // Validate n pairs and reduce them to runs (sorted by host page).
@@ -32,6 +45,11 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
             int32_t direction, int64_t max_run, std::vector<RunRec> *runs);
 int64_t max_run_pages(const Shape &s);
 bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common);
+
+// cuStreamWaitValue32 from the driver (hicache_pipeline.cpp); nullptr if the
+// driver does not offer it.
+using WaitValue32Fn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+WaitValue32Fn wait_value32();
 
 }  // namespace hicache
 
@@ -66,13 +84,29 @@ struct hicache_pool {
 
 namespace hicache {
 
+// hicache_api.cpp: launch helpers.
 int check_kv(const hicache_pool *pool, const hicache_device_kv *kv, int64_t min_pages);
+// The calling thread's device must be the pool's.
+int check_device(const hicache_pool *pool);
+// Copy runs[next..] into a job's run table at blob word `word` (at most
+// max_runs runs, within the launch limits for `launch_factor` repeats of the
+// job's tiles); returns the runs taken, or -1 if even one run is too large.
+int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
+                  int64_t max_runs, Job &job, Run *table, int32_t word, int64_t launch_factor);
+int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
+                 int64_t max_runs, XferParams &params, int32_t word, int j, int64_t launch_factor = 1);
+// A pool's shape, host alias and dividers, as one launch header.
+void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, XferHeader &h);
+// fill_shape plus the device buffer pointers at the start of the blob.
+void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, XferParams &params, int64_t upp,
+                 int32_t layer);
 // Enqueue validated runs (see hicache_api.cpp).
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
             void *stream);
 // Enqueue validated load runs as pipelined launches (every layer, layer by
-// layer, per-layer counters) and update the pool's per-layer signals.
+// layer, per-layer counters) and update the pool's per-layer signals
+// (hicache_pipeline.cpp).
 int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
                       int32_t layout, void *stream);
 

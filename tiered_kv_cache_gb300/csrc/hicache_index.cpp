@@ -1,0 +1,353 @@
+// hicache_index.cpp -- host-only argument validation and the index pre-pass:
+// pool-shape and layout checks, the sort of (host page, device page) pairs and
+// their merge into runs, and the host-only calls built on them (the pre-pass
+// itself, segment counts and page spans).  Nothing here touches a GPU.
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <vector>
+
+#include "hicache.h"
+#include "hicache_host.h"
+#include "hicache_internal.h"
+
+namespace hicache {
+
+// ---- shape checks ------------------------------------------------------------
+
+int check_desc(const hicache_pool_desc *d, Shape *s, bool need_alignment) {
+  if (!d) return set_error(HICACHE_ERR_INVALID_ARG, "pool descriptor is NULL");
+  if (d->num_layers < 1 || d->num_buffers < 1 || d->page_size < 1 || d->elem_bytes < 1 ||
+      d->row_elems < 1 || d->host_num_pages < 1)
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "pool descriptor sizes must be >= 1 (layers %d, buffers %d, page_size %d, "
+                     "elem_bytes %d, row_elems %lld, host pages %lld)",
+                     d->num_layers, d->num_buffers, d->page_size, d->elem_bytes,
+                     (long long)d->row_elems, (long long)d->host_num_pages);
+  if (int64_t(d->num_layers) * d->num_buffers > hicache::kMaxBufs)
+    return set_error(HICACHE_ERR_INVALID_ARG, "num_buffers * num_layers = %lld exceeds %d",
+                     (long long)d->num_layers * d->num_buffers, hicache::kMaxBufs);
+  if (d->layout < HICACHE_LAYER_FIRST || d->layout > HICACHE_PAGE_FIRST_DIRECT_KV)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown pool layout %d", d->layout);
+  if (d->launch_ctas < 0 || d->flags != 0 || d->reserved != 0)
+    return set_error(HICACHE_ERR_INVALID_ARG, "launch_ctas must be >= 0; flags and reserved must be 0");
+  if (d->host_num_pages >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "host_num_pages must be < 2^31");
+  s->L = d->num_layers;
+  s->B = d->num_buffers;
+  s->P = d->page_size;
+  s->R = d->row_elems;
+  s->es = d->elem_bytes;
+  s->Hp = d->host_num_pages;
+  s->layout = d->layout;
+  if (s->R > (int64_t(1) << 40) / s->es)
+    return set_error(HICACHE_ERR_INVALID_ARG, "row of %lld elements is too large", (long long)s->R);
+  s->row_bytes = s->R * s->es;
+  s->V = s->row_bytes / 16;
+  s->PV = s->P * s->V;
+  s->LPV = s->L * s->PV;
+  s->BLPV = s->B * s->LPV;
+  if (need_alignment) {
+    if (s->row_bytes % 16 != 0)
+      return set_error(HICACHE_ERR_ALIGNMENT, "row of %lld bytes is not a multiple of 16",
+                       (long long)s->row_bytes);
+    if (s->BLPV > INT32_MAX - hicache::kTileVecs)
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "one page of every buffer and layer (%lld x 16 bytes) must be < 32 GiB - 16 KiB",
+                       (long long)s->BLPV);
+  }
+  return HICACHE_OK;
+}
+
+int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out) {
+  if (layout == HICACHE_LAYOUT_POOL) layout = pool_layout;
+  if (layout < HICACHE_LAYER_FIRST || layout > HICACHE_PAGE_FIRST_DIRECT_KV)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown layout %d", layout);
+  *out = layout;
+  return HICACHE_OK;
+}
+
+// ---- the pre-pass ------------------------------------------------------------
+struct Pair {
+  int64_t h, d;
+};
+inline bool pair_less(const Pair &a, const Pair &b) {
+  return a.h < b.h || (a.h == b.h && a.d < b.d);
+}
+
+int bit_length(uint64_t v) {
+  int b = 0;
+  while (v) {
+    ++b;
+    v >>= 1;
+  }
+  return b;
+}
+
+// Sort pairs by (host page, device page).  Large sets go through an LSD radix
+// sort on the key h * 2^dbits + d (11-bit digits, only as many passes as the
+// largest key needs): a few linear passes where a comparison sort spends
+// ~n log n compares, which for the tens of thousands of one-token pages of a
+// long prefix was most of the host's cost of a call.
+void sort_pairs(std::vector<Pair> &pairs, int64_t Dp) {
+  const size_t n = pairs.size();
+  if (n < 2048) {
+    std::sort(pairs.begin(), pairs.end(), pair_less);
+    return;
+  }
+  const int dbits = bit_length(uint64_t(Dp - 1));
+  uint64_t max_key = 0;
+  thread_local std::vector<uint64_t> tls_keys, tls_tmp;
+  std::vector<uint64_t> &keys = tls_keys, &tmp = tls_tmp;
+  keys.resize(n);
+  tmp.resize(n);
+  for (size_t i = 0; i < n; ++i) {
+    keys[i] = (uint64_t(pairs[i].h) << dbits) | uint64_t(pairs[i].d);
+    max_key = std::max(max_key, keys[i]);
+  }
+  constexpr int kDigit = 11;
+  constexpr size_t kBuckets = size_t(1) << kDigit;
+  const int bits = bit_length(max_key);
+  for (int shift = 0; shift < bits; shift += kDigit) {
+    size_t count[kBuckets + 1] = {};
+    for (size_t i = 0; i < n; ++i) ++count[((keys[i] >> shift) & (kBuckets - 1)) + 1];
+    for (size_t b = 1; b <= kBuckets; ++b) count[b] += count[b - 1];
+    for (size_t i = 0; i < n; ++i) tmp[count[(keys[i] >> shift) & (kBuckets - 1)]++] = keys[i];
+    keys.swap(tmp);
+  }
+  const uint64_t dmask = (uint64_t(1) << dbits) - 1;
+  for (size_t i = 0; i < n; ++i) pairs[i] = Pair{int64_t(keys[i] >> dbits), int64_t(keys[i] & dmask)};
+}
+
+// Whether a load names a destination page twice.  For device pools of up to
+// 2^27 pages, one bit per page in a per-thread bitmap, cleared again for just
+// the pages set; beyond that, a sort.
+bool first_repeated(const int64_t *dev, int64_t n, int64_t Dp, int64_t *repeated) {
+  if (Dp <= (int64_t(1) << 27)) {
+    thread_local std::vector<uint64_t> tls_bits;
+    std::vector<uint64_t> &vbits = tls_bits;
+    if (vbits.size() < size_t((Dp + 63) / 64)) vbits.resize(size_t((Dp + 63) / 64), 0);
+    uint64_t *const bits = vbits.data();
+    int64_t i = 0;
+    bool dup = false;
+    for (; i < n; ++i) {
+      const uint64_t bit = uint64_t(1) << (dev[i] & 63);
+      uint64_t &w = bits[size_t(dev[i] >> 6)];
+      if (w & bit) {
+        dup = true;
+        *repeated = dev[i];
+        break;
+      }
+      w |= bit;
+    }
+    for (int64_t k = 0; k < i; ++k) bits[size_t(dev[k] >> 6)] = 0;
+    return dup;
+  }
+  thread_local std::vector<int64_t> ds;
+  ds.assign(dev, dev + n);
+  std::sort(ds.begin(), ds.end());
+  for (int64_t i = 1; i < n; ++i)
+    if (ds[size_t(i)] == ds[size_t(i - 1)]) {
+      *repeated = ds[size_t(i)];
+      return true;
+    }
+  return false;
+}
+
+// Validate n index pairs and reduce them to runs: pairs sorted by (host page,
+// device page), merged while both pages step by one (at most max_run pages per
+// run).  On error the last-error text is set and *runs holds no usable table.
+int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+            int32_t direction, int64_t max_run, std::vector<RunRec> *runs) {
+  if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n = %lld is negative", (long long)n);
+  if (direction != HICACHE_DIR_BACKUP && direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "unknown direction %d", direction);
+  if (Dp < 1 || Dp >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "device_num_pages = %lld must be in [1, 2^31)",
+                     (long long)Dp);
+  runs->clear();
+  if (n == 0) return HICACHE_OK;
+  if (!dev || !host) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
+  // one lookup of the per-thread buffer: in a shared library every access to
+  // a thread_local can be a call, too slow inside a per-page loop
+  thread_local std::vector<Pair> tls_pairs;
+  std::vector<Pair> &pairs = tls_pairs;
+  pairs.resize(size_t(n));
+  bool sorted = true;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t d = dev[i], h = host[i];
+    if (d < 0 || d >= Dp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] = %lld outside [0, %lld)",
+                       (long long)i, (long long)d, (long long)Dp);
+    if (h < 0 || h >= Hp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "host_pages[%lld] = %lld outside [0, %lld)",
+                       (long long)i, (long long)h, (long long)Hp);
+    pairs[size_t(i)] = Pair{h, d};
+    if (i > 0 && pair_less(pairs[size_t(i)], pairs[size_t(i - 1)])) sorted = false;
+  }
+  if (!sorted) sort_pairs(pairs, Dp);
+  if (direction == HICACHE_DIR_BACKUP) {
+    for (int64_t i = 1; i < n; ++i)
+      if (pairs[size_t(i)].h == pairs[size_t(i - 1)].h)
+        return set_error(HICACHE_ERR_DUPLICATE_INDEX,
+                         "host page %lld is a backup destination twice",
+                         (long long)pairs[size_t(i)].h);
+  } else if (n <= 32) {
+    for (int64_t i = 0; i < n; ++i)
+      for (int64_t k = i + 1; k < n; ++k)
+        if (dev[i] == dev[k])
+          return set_error(HICACHE_ERR_DUPLICATE_INDEX,
+                           "device page %lld is a load destination twice", (long long)dev[i]);
+  } else {
+    int64_t page = 0;
+    if (first_repeated(dev, n, Dp, &page))
+      return set_error(HICACHE_ERR_DUPLICATE_INDEX, "device page %lld is a load destination twice",
+                       (long long)page);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    const Pair &p = pairs[size_t(i)];
+    if (!runs->empty()) {
+      RunRec &r = runs->back();
+      if (p.h == r.h0 + r.len && p.d == r.d0 + r.len && r.len < max_run) {
+        ++r.len;
+        continue;
+      }
+    }
+    runs->push_back(RunRec{p.h, p.d, 1});
+  }
+  return HICACHE_OK;
+}
+
+// Runs are capped so that a unit (at most every buffer and layer of a run)
+// stays below 2^31 - 1024 vectors: the kernels index units with 32-bit offsets.
+int64_t max_run_pages(const Shape &s) { return std::max<int64_t>(1, kMaxOuterVecs / s.BLPV); }
+
+// Sorted-merge test: do two page sets share a page?
+bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common) {
+  std::sort(a.begin(), a.end());
+  std::sort(b.begin(), b.end());
+  size_t i = 0, k = 0;
+  while (i < a.size() && k < b.size()) {
+    if (a[i] == b[k]) {
+      *common = a[i];
+      return true;
+    }
+    if (a[i] < b[k]) ++i; else ++k;
+  }
+  return false;
+}
+
+}  // namespace hicache
+
+using namespace hicache;
+
+extern "C" {
+
+int hicache_prepass(int64_t host_num_pages, int64_t device_num_pages, const int64_t *device_pages,
+                    const int64_t *host_pages, int64_t n, int32_t direction, int64_t *num_runs,
+                    int64_t *runs_out, int64_t runs_capacity) {
+  clear_error();
+  if (!num_runs) return set_error(HICACHE_ERR_INVALID_ARG, "num_runs is NULL");
+  if (host_num_pages < 1 || host_num_pages >= INT32_MAX)
+    return set_error(HICACHE_ERR_INVALID_ARG, "host_num_pages must be in [1, 2^31)");
+  thread_local std::vector<RunRec> tls_runs;
+  std::vector<RunRec> &runs = tls_runs;
+  const int rc = prepass(host_num_pages, device_num_pages, device_pages, host_pages, n, direction,
+                         INT32_MAX, &runs);
+  if (rc) return rc;
+  *num_runs = int64_t(runs.size());
+  if (runs_out && runs_capacity >= int64_t(runs.size())) {
+    for (size_t i = 0; i < runs.size(); ++i) {
+      runs_out[3 * i] = runs[i].h0;
+      runs_out[3 * i + 1] = runs[i].d0;
+      runs_out[3 * i + 2] = runs[i].len;
+    }
+  }
+  return HICACHE_OK;
+}
+
+int64_t hicache_segment_count(const hicache_pool_desc *desc, const int64_t *device_pages,
+                              const int64_t *host_pages, int64_t n, int32_t layout,
+                              int32_t layer_id) {
+  clear_error();
+  Shape s{};
+  int rc = check_desc(desc, &s, false);
+  if (rc) return rc;
+  int32_t lay = 0;
+  if ((rc = resolve_layout(layout, s.layout, &lay))) return rc;
+  if (layer_id >= s.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)s.L);
+  if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n is negative");
+  if (n == 0) return 0;
+  if (!device_pages || !host_pages) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
+  // runs over the set of pairs; repeated sources are fine for a count
+  std::vector<Pair> pairs(static_cast<size_t>(n));
+  for (int64_t i = 0; i < n; ++i) {
+    if (device_pages[i] < 0 || host_pages[i] < 0 || host_pages[i] >= s.Hp)
+      return set_error(HICACHE_ERR_INDEX_RANGE, "page index out of range at %lld", (long long)i);
+    pairs[size_t(i)] = Pair{host_pages[i], device_pages[i]};
+  }
+  std::sort(pairs.begin(), pairs.end(), pair_less);
+  int64_t nruns = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const bool cont = i > 0 && pairs[size_t(i)].h == pairs[size_t(i - 1)].h + 1 &&
+                      pairs[size_t(i)].d == pairs[size_t(i - 1)].d + 1;
+    if (!cont) ++nruns;
+  }
+  const int64_t layers = layer_id < 0 ? s.L : 1;
+  // with one layer in the pool, every layout stores a buffer's pages back to
+  // back, except page_first_direct_kv, which interleaves the buffers of a page
+  if (lay == HICACHE_LAYER_FIRST || (s.L == 1 && (lay != HICACHE_PAGE_FIRST_DIRECT_KV || s.B == 1)))
+    return s.B * layers * nruns;
+  // one segment per (buffer, layer, page): the same layer of the next page is
+  // (buffers x) L*P rows further on the host
+  if (lay == HICACHE_PAGE_FIRST_DIRECT || lay == HICACHE_PAGE_FIRST_DIRECT_KV) return s.B * layers * n;
+  return s.B * layers * n * s.P;  // page_first: one row per (buffer, layer, token)
+}
+
+int hicache_page_span(const hicache_pool_desc *desc, int64_t host_page, int32_t buffer,
+                      int64_t *offset_bytes, int64_t *nbytes) {
+  clear_error();
+  Shape s{};
+  int rc = check_desc(desc, &s, false);
+  if (rc) return rc;
+  if (!offset_bytes || !nbytes) return set_error(HICACHE_ERR_INVALID_ARG, "output pointer is NULL");
+  if (host_page < 0 || host_page >= s.Hp)
+    return set_error(HICACHE_ERR_INDEX_RANGE, "host page %lld outside [0, %lld)", (long long)host_page,
+                     (long long)s.Hp);
+  if (buffer < -1 || buffer >= s.B)
+    return set_error(HICACHE_ERR_INVALID_ARG, "buffer %d outside [-1, %lld)", buffer, (long long)s.B);
+  const int64_t page_buf_bytes = s.L * s.P * s.R * s.es;  // one buffer's share of a page
+  switch (s.layout) {
+    case HICACHE_PAGE_FIRST:
+    case HICACHE_PAGE_FIRST_DIRECT:
+      if (buffer < 0 && s.B > 1)
+        return set_error(HICACHE_ERR_INVALID_ARG,
+                         "with %lld buffers a page is one span per buffer: name the buffer",
+                         (long long)s.B);
+      *offset_bytes = ((buffer < 0 ? 0 : buffer) * s.Hp + host_page) * page_buf_bytes;
+      *nbytes = page_buf_bytes;
+      return HICACHE_OK;
+    case HICACHE_PAGE_FIRST_DIRECT_KV:
+      if (buffer < 0) {
+        *offset_bytes = host_page * s.B * page_buf_bytes;
+        *nbytes = s.B * page_buf_bytes;
+      } else {
+        *offset_bytes = (host_page * s.B + buffer) * page_buf_bytes;
+        *nbytes = page_buf_bytes;
+      }
+      return HICACHE_OK;
+    default:
+      if (s.L == 1 && (buffer >= 0 || s.B == 1)) {
+        *offset_bytes = ((buffer < 0 ? 0 : buffer) * s.Hp + host_page) * page_buf_bytes;
+        *nbytes = page_buf_bytes;
+        return HICACHE_OK;
+      }
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "a layer_first page is one span per layer, not one contiguous span");
+  }
+}
+
+}  // extern "C"

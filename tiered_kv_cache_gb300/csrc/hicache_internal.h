@@ -1,4 +1,4 @@
-// hicache_internal.h -- types shared by the host API (hicache_api.cpp) and the
+// hicache_internal.h -- types shared by the host files (hicache_*.cpp) and the
 // transfer kernels (hicache_kernels.cu).  Not part of the public ABI.
 #pragma once
 

@@ -1,0 +1,200 @@
+// hicache_plan.cpp -- plans: an index set validated and reduced to runs once,
+// then executed many times (all layers, one layer, pipelined, or every layer's
+// launch replayed from one CUDA graph).
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "hicache.h"
+#include "hicache_host.h"
+#include "hicache_internal.h"
+
+using namespace hicache;
+
+struct hicache_plan {
+  hicache_pool *pool = nullptr;
+  int32_t direction = 0;
+  int64_t n = 0;
+  int64_t device_num_pages = 0;
+  std::vector<hicache::RunRec> runs;
+  // hicache_plan_load_layers: the per-layer launches and layer events of one
+  // device KV and layout, captured once as a CUDA graph and replayed
+  std::mutex graph_mu;
+  cudaGraphExec_t graph = nullptr;
+  std::vector<void *> graph_bufs;     // the key: buffer pointers, page count, layout
+  int64_t graph_pages = 0;
+  int32_t graph_layout = -1;
+  int64_t graph_launches = 0;         // kernel launches one replay makes
+};
+
+extern "C" {
+
+int hicache_plan_create(hicache_pool *pool, const int64_t *device_pages, const int64_t *host_pages,
+                        int64_t n, int64_t device_num_pages, int32_t direction,
+                        hicache_plan **out) {
+  clear_error();
+  if (!pool || !out) return set_error(HICACHE_ERR_INVALID_ARG, "pool or out is NULL");
+  *out = nullptr;
+  std::vector<RunRec> runs;
+  int rc = prepass(pool->shape.Hp, device_num_pages, device_pages, host_pages, n, direction,
+                   max_run_pages(pool->shape), &runs);
+  if (rc) return rc;
+  hicache_plan *p = new (std::nothrow) hicache_plan();
+  if (!p) return set_error(HICACHE_ERR_NOMEM, "out of host memory");
+  p->pool = pool;
+  p->direction = direction;
+  p->n = n;
+  p->device_num_pages = device_num_pages;
+  p->runs = std::move(runs);
+  *out = p;
+  return HICACHE_OK;
+}
+
+int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                         int32_t layer_id, void *stream) {
+  clear_error();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  hicache_pool *pool = plan->pool;
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, pool->shape.layout, &lay);
+  if (rc) return rc;
+  if (layer_id >= pool->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)pool->shape.L);
+  if (layer_id >= 0 && plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
+  if ((rc = enqueue(pool, kv, plan->runs, nullptr, lay, layer_id < 0 ? -1 : layer_id,
+                    plan->direction == HICACHE_DIR_BACKUP, stream)))
+    return rc;
+  if (layer_id >= 0) {
+    const cudaError_t e =
+        cudaEventRecord(pool->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+    std::lock_guard<std::mutex> g(pool->signal_mu);
+    pool->layer_signal[size_t(layer_id)] = 0;
+  }
+  return HICACHE_OK;
+}
+
+int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                            int32_t layer_id, void *stream) {
+  clear_error();
+  if (layer_id < 0) return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d is negative", layer_id);
+  return hicache_plan_execute(plan, kv, layout, layer_id, stream);
+}
+
+int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                                void *stream) {
+  clear_error();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a pipelined transfer must be a load");
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, plan->pool->shape.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(plan->pool, kv, plan->device_num_pages))) return rc;
+  return enqueue_pipelined(plan->pool, kv, plan->runs, lay, stream);
+}
+
+int hicache_plan_info(const hicache_plan *plan, int64_t *num_pages, int64_t *num_runs) {
+  clear_error();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (num_pages) *num_pages = plan->n;
+  if (num_runs) *num_runs = int64_t(plan->runs.size());
+  return HICACHE_OK;
+}
+
+int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout, void *stream) {
+  clear_error();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  hicache_pool *pool = plan->pool;
+  const Shape &s = pool->shape;
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, s.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
+  if ((rc = check_device(pool))) return rc;
+  std::lock_guard<std::mutex> g(plan->graph_mu);
+  const std::vector<void *> bufs(kv->buf_ptrs, kv->buf_ptrs + s.B * s.L);
+  if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != kv->device_num_pages ||
+      plan->graph_layout != lay) {
+    if (plan->graph) {
+      cudaGraphExecDestroy(plan->graph);
+      plan->graph = nullptr;
+    }
+    // Capture the L per-layer launches on a private stream, the kernels one
+    // after another.  Each layer's event is recorded (as an external event
+    // node) on a side branch that forks off after that layer's kernel, so the
+    // kernel chain itself has no node between consecutive launches.
+    cudaStream_t cap = nullptr, side = nullptr;
+    std::vector<cudaEvent_t> forks(size_t(s.L) + 1, nullptr);
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+    for (auto &f : forks)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    auto release = [&] {
+      for (auto f : forks)
+        if (f) cudaEventDestroy(f);
+      if (side) cudaStreamDestroy(side);
+      if (cap) cudaStreamDestroy(cap);
+    };
+    if (e != cudaSuccess) {
+      release();
+      return cuda_error(e, "setting up the layer-load capture");
+    }
+    const int64_t before = g_launches.load();
+    for (int64_t l = 0; l < s.L && rc == HICACHE_OK; ++l) {
+      rc = enqueue(pool, kv, plan->runs, nullptr, lay, int32_t(l), false, cap);
+      if (rc != HICACHE_OK) break;
+      e = cudaEventRecord(forks[size_t(l)], cap);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
+      if (e == cudaSuccess) e = cudaEventRecordWithFlags(pool->events[size_t(l)], side, cudaEventRecordExternal);
+      if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer event");
+    }
+    if (rc == HICACHE_OK) {                // join the side branch back
+      e = cudaEventRecord(forks[size_t(s.L)], side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(s.L)], 0);
+      if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
+    }
+    const int64_t captured = g_launches.load() - before;
+    g_launches.fetch_sub(captured);      // counted when replayed
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(cap, &graph);
+    release();
+    if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
+    if (rc == HICACHE_OK) {
+      e = cudaGraphInstantiate(&plan->graph, graph, 0);
+      if (e != cudaSuccess) {
+        plan->graph = nullptr;
+        rc = cuda_error(e, "cudaGraphInstantiate");
+      }
+    }
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != HICACHE_OK) return rc;
+    plan->graph_bufs = bufs;
+    plan->graph_pages = kv->device_num_pages;
+    plan->graph_layout = lay;
+    plan->graph_launches = captured;
+  }
+  const cudaError_t e = cudaGraphLaunch(plan->graph, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
+  g_launches.fetch_add(plan->graph_launches, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> gs(pool->signal_mu);
+  for (int64_t l = 0; l < s.L; ++l) pool->layer_signal[size_t(l)] = 0;
+  return HICACHE_OK;
+}
+
+int hicache_plan_destroy(hicache_plan *plan) {
+  if (plan && plan->graph) cudaGraphExecDestroy(plan->graph);
+  delete plan;
+  return HICACHE_OK;
+}
+
+}  // extern "C"
