@@ -288,3 +288,85 @@ def test_nsa_group_full_size_per_layer_and_all_layers():
         pool.close()
     del bufsets, kvs
     torch.cuda.empty_cache()
+
+
+def _mem_available_bytes() -> int:
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
+@pytest.mark.parametrize("layout,B,L", [("layer_first", 1, 1), ("page_first_direct_kv", 2, 2)])
+def test_run_past_the_unit_limit_is_split(layout, B, L):
+    """The largest unit a launch can index: 2^31 - 1024 vectors of 16 bytes.
+    With one-token pages of 1 GiB (every buffer and layer), a run of 34 pages
+    contiguous on both sides would make one unit of 34 GiB.  The pre-pass caps
+    runs at 31 such pages and the call becomes two launches; every page still
+    lands where the oracle's offsets put it (checked page block by page block,
+    each block's first and last element placed by the oracle, and on sampled
+    elements)."""
+    GiB = 1 << 30
+    n, Dp, shift = 34, 36, 2
+    P, es = 1, 2
+    R = GiB // (B * L * es)                 # one page of every buffer and layer = 1 GiB
+    dev_free = torch.cuda.mem_get_info()[0]
+    if dev_free < (Dp + 4) * GiB or _mem_available_bytes() < 2 * n * GiB:
+        pytest.skip("needs 40 GiB of free device memory and 68 GiB of available host memory")
+    lay = hc.LAYOUTS[layout]
+    o = gh.orc()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(34)
+    bufs = []
+    for _ in range(B * L):
+        x = torch.empty(Dp * P, R, dtype=torch.int16, device="cuda")
+        x.random_(generator=g)
+        bufs.append(x)
+    kv = hc.DeviceKV(bufs, Dp)
+    host_pages = np.arange(n)
+
+    def blocks(dev_pages):
+        # (buffer index, device page, host byte offset) of every page block,
+        # each block R contiguous elements on both sides per the oracle
+        for i, (d, h) in enumerate(zip(dev_pages, host_pages)):
+            for b in range(B):
+                for l in range(L):
+                    h0 = o.host_offset(lay, B, L, P, R, n, b, l, int(h), 0, 0)
+                    assert o.host_offset(lay, B, L, P, R, n, b, l, int(h), 0, R - 1) == h0 + R - 1
+                    assert o.dev_offset(P, R, int(d), 0, R - 1) == o.dev_offset(P, R, int(d), 0, 0) + R - 1
+                    yield b * L + l, int(d), h0 * es
+
+    def same(host_u8, dev_pages):
+        for k, d, hb in blocks(dev_pages):
+            h = torch.from_numpy(host_u8[hb:hb + R * es]).to("cuda")
+            if not torch.equal(h, bufs[k][d].view(torch.uint8)):
+                return False
+            del h
+        return True
+
+    with hc.Pool(L, B, P, R, n, layout) as pool:
+        host = pool.host_array(np.uint8)
+        src = np.arange(n)
+        c0 = hc.launch_count()
+        pool.backup(kv, src, host_pages)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 == 2
+        assert same(host, src)
+        assert gh.sampled_host_check(host.view(np.uint16), bufs, src, host_pages, lay, B, L, P, R, n, 4000, 1)
+        # load into device pages shifted by two, over a sentinel
+        keep = [b[:shift].clone() for b in bufs]
+        for b in bufs:
+            b[shift:].view(torch.uint8).fill_(0xC3)
+        dst = src + shift
+        c0 = hc.launch_count()
+        pool.load(kv, dst, host_pages)
+        torch.cuda.synchronize()
+        assert hc.launch_count() - c0 == 2
+        assert same(host, dst)
+        assert gh.sampled_host_check(host.view(np.uint16), bufs, dst, host_pages, lay, B, L, P, R, n, 4000, 2)
+        for b, k in zip(bufs, keep):
+            assert torch.equal(b[:shift], k)
+        del host
+    del bufs, kv, keep
+    torch.cuda.empty_cache()

@@ -68,7 +68,7 @@ def test_fast_division(tmp_path):
 int main() {
   std::mt19937_64 rng(1);
   uint32_t divisors[] = {1,2,3,5,7,16,72,128,576,1000,4608,8192,9216,281088,299520,1048575,
-                         (1u<<30)+3u, 2147483647u};
+                         (1u<<24), (1u<<25), (1u<<26), (1u<<30)+3u, 2147483647u};
   long bad = 0;
   for (uint32_t d : divisors) {
     hicache::FastDiv f = hicache::make_fastdiv(d);
