@@ -618,3 +618,77 @@ def test_plan_load_layers_of_an_empty_plan_records_every_event():
         hc.wait(comp, 10_000_000)
         assert s.query()
         plan.close()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_plan_load_layers_graph_with_split_layers(layout):
+    """A plan of 4,000 scattered one-token pages needs several launches per
+    layer.  In the graph only the first launch of each layer may start while
+    the previous layer drains; the chunks of one layer follow one another.  The
+    replay must equal the oracle's load, three times over."""
+    B, L, P, R, Dp, Hp, n = 2, 3, 1, 8, 9000, 9000, 4000
+    rng = np.random.default_rng(80 + layout)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=81)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        kv = hc.DeviceKV(bufs, Dp)
+        s = torch.cuda.Stream()
+        want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, layout)
+        for rep in range(3):
+            gh.sentinel_fill(bufs)
+            torch.cuda.synchronize()
+            c0 = hc.launch_count()
+            plan.load_layers(kv, stream=s)
+            assert hc.launch_count() - c0 >= 2 * L
+            hc.wait(s, 10_000_000)
+            got = gh.to_np(bufs, 2)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want[k]), (rep, k)
+        plan.close()
+
+
+def test_plan_load_layers_last_event_means_every_layer():
+    """The event of layer l fires only once layers 0..l have all landed, even
+    though a layer's kernel may start before the previous one ends: a compute
+    stream that waits on the last layer's event alone reads every layer
+    complete (64K-token MLA load, where layer kernels overlap the most)."""
+    s_ = wl.MLA_LATENT
+    B, L, P, R, Hp = s_.num_buffers, s_.num_layers, s_.page_size, s_.row_elems, s_.host_pages
+    Dp = s_.device_pages
+    t = wl.mla_transfer(s_, 65536)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=90)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = np.random.default_rng(91).integers(0, 256, host.size, dtype=np.uint8)
+        plan = pool.plan(t.device_pages, t.host_pages, Dp, hc.LOAD)
+        kv = hc.DeviceKV(bufs, Dp)
+        s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        # the expected per-layer sums, from a plain all-layer load checked
+        # against the oracle on sampled elements
+        pool.load(kv, t.device_pages, t.host_pages)
+        torch.cuda.synchronize()
+        assert gh.sampled_host_check(host.view(np.uint16), bufs, t.device_pages, t.host_pages, hc.PAGE_FIRST,
+                                     B, L, P, R, Hp, 20000, 92)
+        for layer in range(L):
+            hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer)
+        torch.cuda.synchronize()
+        want = sums.clone()
+        for rep in range(4):
+            gh.sentinel_fill(bufs)
+            sums.zero_()
+            torch.cuda.synchronize()
+            plan.load_layers(kv, stream=s)
+            pool.wait_layer(L - 1, comp)
+            for layer in range(L):
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, stream=comp)
+            hc.wait(comp, 10_000_000)
+            hc.wait(s, 10_000_000)
+            assert torch.equal(sums, want), rep
+        plan.close()
+    del bufs
+    torch.cuda.empty_cache()

@@ -172,7 +172,7 @@ int check_device(const hicache_pool *pool) {
 // per chunk so the two directions share every CTA.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
-            void *stream) {
+            void *stream, bool pdl_first) {
   const bool bidir = load_runs != nullptr;
   if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
   if (int rc = check_device(pool)) return rc;
@@ -215,6 +215,8 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     const int64_t ctas = bidir ? 2 * int64_t(pool->ctas) : to_host ? pool->backup_ctas : pool->ctas;
     x.grid = int(std::min<int64_t>(tiles, ctas));
     x.stream = stream;
+    // only the first chunk: the chunks of one layer follow one another fully
+    x.pdl = pdl_first && next0 == 0 && next1 == 0;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

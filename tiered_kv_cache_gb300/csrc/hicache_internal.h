@@ -173,6 +173,10 @@ struct XferLaunch {
   bool bidir;                 // job[0] backup and job[1] load, all layers, one launch
   int grid;
   void *stream;
+  // Programmatic dependent launch: the kernel may start while the kernel
+  // before it on the stream moves its last tiles (one-layer loads only; that
+  // kernel must be a one-layer load of other buffers).
+  bool pdl = false;
 };
 int launch_xfer(const XferLaunch &x);
 struct GroupLaunch {

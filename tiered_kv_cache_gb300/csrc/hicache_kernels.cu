@@ -205,8 +205,15 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
   load_buffer_table(p, s_bufs);
   const Job &job = p.h.job[0];
   const Run *runs = job_runs(p, 0);
-  for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x)
+  for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x) {
+    // A one-layer load lets the next layer's load, launched programmatically
+    // behind it, start once every CTA has reached its last tile: the next
+    // layer's first host reads then fill the link while this layer's last
+    // tiles drain.  (Nothing waits on this: it only allows an earlier start.)
+    if (!ALL && !TO_HOST && g + int32_t(gridDim.x) >= job.total_tiles)
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g, p.h.layer);
+  }
 }
 
 // Both directions in one launch: job 0 is a backup, job 1 a load, every layer.
@@ -381,13 +388,34 @@ const Params &params_for(const XferLaunch &x, Params &small) {
   return small;
 }
 
+// Launch with programmatic stream serialization: the kernel may begin once
+// every CTA of the kernel before it on the stream has signalled
+// griddepcontrol.launch_dependents (or exited).
+template <class Params>
+cudaError_t launch_programmatic(void (*kernel)(Params), const XferLaunch &x, const Params &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(x.grid));
+  cfg.blockDim = dim3(unsigned(kThreads));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(x.stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int LAYOUT, bool ALL, bool TO_HOST>
 cudaError_t launch_one(const XferLaunch &x) {
   const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  const bool pdl = x.pdl && !ALL && !TO_HOST;
   if (x.words <= kBlobWordsSmall) {
     XferParamsSmall small;
+    if (pdl) return launch_programmatic(&xfer_kernel<LAYOUT, ALL, TO_HOST, XferParamsSmall>, x, params_for(x, small));
     xfer_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(params_for(x, small));
   } else {
+    if (pdl) return launch_programmatic(&xfer_kernel<LAYOUT, ALL, TO_HOST, XferParams>, x, *x.params);
     xfer_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(*x.params);
   }
   return cudaGetLastError();
