@@ -288,11 +288,11 @@ int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_k
  * compute, H2D, and D2H should stay in one GPU execution domain", "Rethinking
  * the SGLang HiCache Boundary"): each layer's kernel after the first is a
  * programmatic dependent launch that may start while the previous layer's
- * kernel moves its last tiles, so the device buffers of different layers must
- * not overlap (as for every all-layer call).  The event of layer l fires once
- * layers 0..l have all landed.  A call with other buffer pointers, page count
- * or layout re-captures.  Errors: INVALID_ARG (NULL plan, backup plan, bad
- * layout or kv), CUDA; on error nothing is enqueued.  Destroying the plan
+ * kernel moves its last tiles, so no two device buffers may overlap (as for
+ * every all-layer call; checked here).  The event of layer l fires once layers
+ * 0..l have all landed.  A call with other buffer pointers, page count or
+ * layout re-captures.  Errors: INVALID_ARG (NULL plan, backup plan, bad layout
+ * or kv, overlapping buffers), CUDA; on error nothing is enqueued.  Destroying the plan
  * while a replay is still running is allowed: CUDA frees the graph once the
  * replay ends. */
 int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout, void *stream);

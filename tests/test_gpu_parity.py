@@ -590,6 +590,14 @@ def test_plan_load_layers_graph_replay(layout):
                     words = np.concatenate([want[b * L + layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
                                             for b in range(B)])
                     assert int(sums[layer].item()) & (2**64 - 1) == int(words.astype(np.uint64).sum(dtype=np.uint64))
+        # consecutive layers may run at once: overlapping buffers are refused
+        big = torch.empty(B * L * Dp * P * R + R, dtype=torch.int16, device="cuda")
+        step = Dp * P * R - R                    # each buffer starts one row before the last ends
+        shared = [big[i * step:i * step + Dp * P * R].view(Dp * P, R) for i in range(B * L)]
+        c0 = hc.launch_count()
+        with pytest.raises(hc.HiCacheError, match="overlap"):
+            plan.load_layers(hc.DeviceKV(shared, Dp), stream=s)
+        assert hc.launch_count() == c0
         with pytest.raises(hc.HiCacheError):      # a backup plan has no per-layer loads
             bplan = pool.plan(dp, hp, Dp, hc.BACKUP)
             try:

@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -124,6 +126,17 @@ int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, in
   const std::vector<void *> bufs(kv->buf_ptrs, kv->buf_ptrs + s.B * s.L);
   if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != kv->device_num_pages ||
       plan->graph_layout != lay) {
+    // consecutive layers' kernels may run at the same time: no two buffers
+    // may share a byte
+    const uint64_t buf_bytes = uint64_t(kv->device_num_pages) * uint64_t(s.PV) * 16u;
+    std::vector<uintptr_t> starts;
+    for (void *b : bufs) starts.push_back(reinterpret_cast<uintptr_t>(b));
+    std::sort(starts.begin(), starts.end());
+    for (size_t i = 1; i < starts.size(); ++i)
+      if (starts[i] - starts[i - 1] < buf_bytes)
+        return set_error(HICACHE_ERR_INVALID_ARG,
+                         "device buffers overlap: each of the %lld buffers must be %llu bytes of its own",
+                         (long long)bufs.size(), (unsigned long long)buf_bytes);
     if (plan->graph) {
       cudaGraphExecDestroy(plan->graph);
       plan->graph = nullptr;
