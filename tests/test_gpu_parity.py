@@ -700,3 +700,43 @@ def test_plan_load_layers_last_event_means_every_layer():
         plan.close()
     del bufs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("op", ["load", "fused"])
+def test_split_call_is_complete_for_the_next_work_on_the_stream(op):
+    """The launches of a split call overlap one another, yet work queued behind
+    the call on the same stream sees every launch of it finished: a checksum of
+    every loaded page, queued right after, equals the oracle's.  The last launch
+    is the smallest, so it would finish first if it did not wait for the one
+    before it."""
+    B, L, P, R, Dp, Hp, n = 2, 3, 1, 8, 9000, 9000, 4000
+    rng = np.random.default_rng(95)
+    perm, hperm = rng.permutation(Dp), rng.permutation(Hp)
+    dp, hp = perm[:n], hperm[:n]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=96)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        want = [np.full((Dp * P, R), 0x5A5A, np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, hc.LAYER_FIRST)
+        expect = [int(np.concatenate([want[b * L + l].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32)
+                                      for b in range(B)]).astype(np.uint64).sum(dtype=np.uint64))
+                  for l in range(L)]
+        kv = hc.DeviceKV(bufs, Dp)
+        s = torch.cuda.Stream()
+        sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+        for rep in range(5):
+            gh.sentinel_fill(bufs)
+            sums.zero_()
+            torch.cuda.synchronize()
+            c0 = hc.launch_count()
+            if op == "load":
+                pool.load(kv, dp, hp, stream=s)
+            else:                              # a backup of other pages fused with the load
+                pool.backup_load(kv, perm[n:2 * n], hperm[n:2 * n], dp, hp, stream=s)
+            assert hc.launch_count() - c0 >= 3
+            for layer in range(L):
+                hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=s)
+            hc.wait(s, 10_000_000)
+            got = [int(v) & (2**64 - 1) for v in sums.tolist()]
+            assert got == expect, rep

@@ -215,8 +215,9 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     const int64_t ctas = bidir ? 2 * int64_t(pool->ctas) : to_host ? pool->backup_ctas : pool->ctas;
     x.grid = int(std::min<int64_t>(tiles, ctas));
     x.stream = stream;
-    // only the first chunk: the chunks of one layer follow one another fully
-    x.pdl = pdl_first && next0 == 0 && next1 == 0;
+    // the launches of one call move disjoint destinations: each after the
+    // first may start as the one before it drains
+    x.pdl = (next0 == 0 && next1 == 0) ? pdl_first : true;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -100,9 +100,10 @@ void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, XferHeader
 // fill_shape plus the device buffer pointers at the start of the blob.
 void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, XferParams &params, int64_t upp,
                  int32_t layer);
-// Enqueue validated runs (see hicache_api.cpp).  pdl_first: launch the first
-// kernel of a one-layer load programmatically behind the kernel before it on
-// the stream, which must be a one-layer load of another layer.
+// Enqueue validated runs (see hicache_api.cpp).  A call split over several
+// launches has each launch after the first start programmatically behind the
+// one before it.  pdl_first: the first launch too, behind the kernel before it
+// on the stream, which must be a one-layer load of another layer.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
             void *stream, bool pdl_first = false);

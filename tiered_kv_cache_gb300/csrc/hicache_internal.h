@@ -174,8 +174,9 @@ struct XferLaunch {
   int grid;
   void *stream;
   // Programmatic dependent launch: the kernel may start while the kernel
-  // before it on the stream moves its last tiles (one-layer loads only; that
-  // kernel must be a one-layer load of other buffers).
+  // before it on the stream moves its last tiles, and finishes after it.  The
+  // kernel before it must be a transfer kernel whose destinations are disjoint
+  // from this one's (an earlier launch of the same call, or another layer).
   bool pdl = false;
 };
 int launch_xfer(const XferLaunch &x);
@@ -187,6 +188,7 @@ struct GroupLaunch {
   bool to_host;
   int grid;
   void *stream;
+  bool pdl = false;           // as XferLaunch::pdl (group_kernel only)
 };
 int launch_group(const GroupLaunch &x);
 // Every layer of every pool of a group, layer by layer, in one launch:

@@ -35,8 +35,16 @@
 //     >= 16 bytes, so each warp's device accesses stay whole 32-byte sectors,
 //     and the host side is touched strictly in order.
 //
+//   * The launches of one call (a run table larger than one parameter block,
+//     or the layers of a per-layer graph) overlap: each after the first is a
+//     programmatic dependent launch that starts once every CTA of the one
+//     before it is on its last tile, so the link does not idle between them.
+//
 // No tensor cores: nothing here is a contraction.  No TMA multicast, no
-// cross-CTA waits, no spin loops: a kernel always runs to completion.
+// cross-CTA waits, no spin loops: a kernel always runs to completion.  The one
+// wait is griddepcontrol.wait at the end of a programmatically launched
+// kernel, for the launch before it, which was already running and waits on
+// nothing later.
 
 #include <cuda_runtime.h>
 
@@ -51,6 +59,20 @@ namespace {
 // Streaming (evict-first) 16-byte accesses: every byte is touched once.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// Programmatic dependent launch.  Consecutive launches of one call (a run
+// table larger than one parameter block, or one layer after another in a
+// per-layer graph) move disjoint destinations, so the next may start while
+// this one drains: each CTA allows it on reaching its last tile.  A launch
+// started that way finishes only after the one before it has (the wait at the
+// end of the kernel), so whatever follows the call on the stream still sees
+// every launch of it complete.  Both are no-ops for a kernel launched plainly.
+__device__ __forceinline__ void allow_next_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void finish_after_previous_launch() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // Address of vector w of the current unit.  `dev` and `host` receive vector
 // pointers; b, l, run describe the unit (l is ignored where the unit spans all
@@ -206,14 +228,10 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
   const Job &job = p.h.job[0];
   const Run *runs = job_runs(p, 0);
   for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x) {
-    // A one-layer load lets the next layer's load, launched programmatically
-    // behind it, start once every CTA has reached its last tile: the next
-    // layer's first host reads then fill the link while this layer's last
-    // tiles drain.  (Nothing waits on this: it only allows an earlier start.)
-    if (!ALL && !TO_HOST && g + int32_t(gridDim.x) >= job.total_tiles)
-      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (g + int32_t(gridDim.x) >= job.total_tiles) allow_next_launch();
     move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g, p.h.layer);
   }
+  finish_after_previous_launch();
 }
 
 // Both directions in one launch: job 0 is a backup, job 1 a load, every layer.
@@ -232,6 +250,9 @@ __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__
   bool backup_turn = true;
   while (ib < jb.total_tiles || il < jl.total_tiles) {
     const bool do_backup = il >= jl.total_tiles || (backup_turn && ib < jb.total_tiles);
+    const bool last = (do_backup ? ib + int32_t(gridDim.x) : ib) >= jb.total_tiles &&
+                      (do_backup ? il : il + int32_t(gridDim.x)) >= jl.total_tiles;
+    if (last) allow_next_launch();
     if (do_backup) {
       move_tile<LAYOUT, true, true>(p.h, jb, rb, s_bufs, ib, 0);
       ib += gridDim.x;
@@ -241,6 +262,7 @@ __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__
     }
     backup_turn = !backup_turn;
   }
+  finish_after_previous_launch();
 }
 
 // Several pools in one launch (a buffer group): job j owns the tiles
@@ -256,6 +278,7 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__
   __syncthreads();
   const int32_t total = p.g.tile_start[p.g.njobs];
   for (int32_t g = blockIdx.x; g < total; g += gridDim.x) {
+    if (g + int32_t(gridDim.x) >= total) allow_next_launch();
     int j = 0;
     while (j + 1 < p.g.njobs && g >= p.g.tile_start[j + 1]) ++j;
     const XferHeader &h = p.g.h[j];
@@ -263,6 +286,7 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__
     move_tile<LAYOUT, ALL, TO_HOST>(h, h.job[0], runs, s_bufs + p.g.bufs_word[j], g - p.g.tile_start[j],
                                     h.layer);
   }
+  finish_after_previous_launch();
 }
 
 // Every layer of a load in one launch, layer by layer: tile g of the launch
@@ -391,8 +415,8 @@ const Params &params_for(const XferLaunch &x, Params &small) {
 // Launch with programmatic stream serialization: the kernel may begin once
 // every CTA of the kernel before it on the stream has signalled
 // griddepcontrol.launch_dependents (or exited).
-template <class Params>
-cudaError_t launch_programmatic(void (*kernel)(Params), const XferLaunch &x, const Params &p) {
+template <class Params, class Launch>
+cudaError_t launch_programmatic(void (*kernel)(Params), const Launch &x, const Params &p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(x.grid));
   cfg.blockDim = dim3(unsigned(kThreads));
@@ -409,7 +433,7 @@ cudaError_t launch_programmatic(void (*kernel)(Params), const XferLaunch &x, con
 template <int LAYOUT, bool ALL, bool TO_HOST>
 cudaError_t launch_one(const XferLaunch &x) {
   const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
-  const bool pdl = x.pdl && !ALL && !TO_HOST;
+  const bool pdl = x.pdl;
   if (x.words <= kBlobWordsSmall) {
     XferParamsSmall small;
     if (pdl) return launch_programmatic(&xfer_kernel<LAYOUT, ALL, TO_HOST, XferParamsSmall>, x, params_for(x, small));
@@ -427,8 +451,10 @@ cudaError_t launch_layout(const XferLaunch &x) {
     const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
     if (x.words <= kBlobWordsSmall) {
       XferParamsSmall small;
+      if (x.pdl) return launch_programmatic(&bidir_kernel<LAYOUT, XferParamsSmall>, x, params_for(x, small));
       bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small));
     } else {
+      if (x.pdl) return launch_programmatic(&bidir_kernel<LAYOUT, XferParams>, x, *x.params);
       bidir_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params);
     }
     return cudaGetLastError();
@@ -502,8 +528,10 @@ cudaError_t launch_group_one(const GroupLaunch &x) {
     GroupParamsSmall small;
     small.g = x.params->g;
     for (int i = 0; i < x.words; ++i) small.blob[i] = x.params->blob[i];
+    if (x.pdl) return launch_programmatic(&group_kernel<LAYOUT, ALL, TO_HOST, GroupParamsSmall>, x, small);
     group_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(small);
   } else {
+    if (x.pdl) return launch_programmatic(&group_kernel<LAYOUT, ALL, TO_HOST, GroupParams>, x, *x.params);
     group_kernel<LAYOUT, ALL, TO_HOST><<<x.grid, kThreads, 0, st>>>(*x.params);
   }
   return cudaGetLastError();

@@ -144,12 +144,12 @@ int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, in
     // Capture the L per-layer launches on a private stream, the kernels one
     // after another.  Each layer's event is recorded (as an external event
     // node) on a side branch that forks off after that layer's kernel, so the
-    // kernel chain itself has no node between consecutive launches.  The
-    // first kernel of each layer after the first is a programmatic dependent
-    // launch: it may start as the previous layer's kernel moves its last tiles
-    // (the layers write different buffers and only read the host pool).  A
-    // layer's event node follows that layer's kernel in full and the event
-    // node before it, so event l still means layers 0..l have landed.
+    // kernel chain itself has no node between consecutive launches.  Every
+    // kernel after the first is a programmatic dependent launch: it may start
+    // as the previous kernel moves its last tiles (the layers write different
+    // buffers and only read the host pool) and ends after it.  A layer's event
+    // node follows that layer's last kernel and the event node before it, so
+    // event l means layers 0..l have landed.
     cudaStream_t cap = nullptr, side = nullptr;
     std::vector<cudaEvent_t> forks(size_t(s.L) + 1, nullptr);
     cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
