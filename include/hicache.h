@@ -53,6 +53,15 @@
  *     the last error of the calling thread is in hicache_last_error().
  *   - Thread safety: a pool may be used from several host threads at once
  *     (e.g. a backup thread and a load thread), each on its own stream.
+ *   - Launches overlap where they can.  A call split over several launches
+ *     (more page runs than one launch's parameters hold) and the layers of a
+ *     per-layer graph replay start each launch as the one before it drains;
+ *     the call still completes, for whatever follows it on the stream, only
+ *     once every launch of it has.  A kernel of the caller's that is launched
+ *     programmatically (programmatic stream serialization) right behind a
+ *     transfer may likewise start while the transfer's last tiles move: as
+ *     for any programmatic launch, it must call cudaGridDependencySynchronize
+ *     before it reads what the transfer wrote.
  */
 #ifndef HICACHE_H_
 #define HICACHE_H_
