@@ -113,8 +113,11 @@ typedef struct {
   int64_t host_num_pages;   /* Hp: pages in the host pool */
   int32_t layout;           /* hicache_layout of the host pool (not POOL) */
   int32_t launch_ctas;      /* CTAs of a transfer launch (a fused backup+load
-                               gets twice as many); 0 = the default: one per SM
-                               for a load, five per eight SMs for a backup */
+                               gets twice as many); 0 = the defaults: one per
+                               SM for a load of every layer, one per two SMs
+                               for a per-layer or pipelined load, five per
+                               eight SMs for a backup, two per SM for a fused
+                               backup+load */
   int32_t flags;            /* must be 0 */
   int32_t reserved;         /* must be 0 */
 } hicache_pool_desc;

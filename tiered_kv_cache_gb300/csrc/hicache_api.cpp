@@ -211,8 +211,10 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     x.to_host = to_host;
     x.bidir = bidir;
     const int64_t tiles = int64_t(h.job[0].total_tiles) + (bidir ? h.job[1].total_tiles : 0);
-    // a fused launch carries both directions: one load share of CTAs for each
-    const int64_t ctas = bidir ? 2 * int64_t(pool->ctas) : to_host ? pool->backup_ctas : pool->ctas;
+    const int64_t ctas = bidir     ? pool->fused_ctas
+                         : to_host ? pool->backup_ctas
+                         : all     ? pool->ctas
+                                   : pool->layer_ctas;
     x.grid = int(std::min<int64_t>(tiles, ctas));
     x.stream = stream;
     // the launches of one call move disjoint destinations: each after the
@@ -368,7 +370,9 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
   p->host_dev = attr.devicePointer;
   p->host_bytes = host_bytes;
   p->device = dev;
-  p->ctas = desc->launch_ctas > 0 ? desc->launch_ctas : sms * hicache::kDefaultCtasPerSm;
+  p->ctas = desc->launch_ctas > 0 ? desc->launch_ctas : sms * hicache::kDefaultLoadCtasPerSm;
+  p->layer_ctas = desc->launch_ctas > 0 ? desc->launch_ctas : std::max(1, sms * hicache::kDefaultLayerCtasPer2Sm / 2);
+  p->fused_ctas = desc->launch_ctas > 0 ? 2 * desc->launch_ctas : sms * hicache::kDefaultFusedCtasPerSm;
   p->backup_ctas = desc->launch_ctas > 0
                        ? desc->launch_ctas
                        : std::max(1, sms * hicache::kDefaultBackupCtasPer8Sm / 8);

@@ -66,7 +66,7 @@ int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int3
     x.layout = layout;
     x.all_layers = all;
     x.to_host = to_host;
-    x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : p0->ctas));
+    x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : all ? p0->ctas : p0->layer_ctas));
     x.stream = stream;
     x.pdl = next > 0;                  // disjoint destinations: overlap the previous launch's drain
     const int e = hicache::launch_group(x);
@@ -126,7 +126,7 @@ int enqueue_group_pipelined(hicache_pool *const *pools, const hicache_device_kv 
     x.layout = layout;
     x.all_layers = false;
     x.to_host = false;
-    x.grid = int(std::min<int64_t>(tiles * L, pools[0]->ctas));
+    x.grid = int(std::min<int64_t>(tiles * L, pools[0]->layer_ctas));
     x.stream = stream;
     const int e = hicache::launch_pipelined_group(x);
     if (e != 0) return cuda_error(cudaError_t(e), "pipelined group kernel launch");

@@ -60,8 +60,10 @@ struct hicache_pool {
   void *host_dev = nullptr;   // device-visible alias
   size_t host_bytes = 0;
   int device = 0;
-  int ctas = 0;         // grid of a load (a fused launch takes twice this)
+  int ctas = 0;         // grid of a load of every layer
+  int layer_ctas = 0;   // grid of a per-layer or pipelined load
   int backup_ctas = 0;  // grid of a backup
+  int fused_ctas = 0;   // grid of a fused backup + load
   std::vector<cudaEvent_t> events;  // one per layer
 
   // Per-layer completion of pipelined loads (hicache_load_pipelined): device

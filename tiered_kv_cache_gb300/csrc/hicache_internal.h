@@ -24,9 +24,18 @@ constexpr int kBlobWords = 3584;                 // 28 KiB of kernel parameters:
                                                  // pointers, then the run table
 constexpr int kBlobWordsSmall = 480;             // the same in under 4 KiB, for calls
                                                  // whose table fits (cheaper to launch)
-// One CTA per SM saturates the host link for a load (16 KiB in flight per
-// CTA) and leaves the rest of each SM to the compute the transfer overlaps.
-constexpr int kDefaultCtasPerSm = 1;
+// One CTA per SM for a load of every layer: 16 KiB in flight per CTA saturates
+// the host link, and holds the link's share against a backup running at the
+// same time on another stream.
+constexpr int kDefaultLoadCtasPerSm = 1;
+// One CTA per two SMs for per-layer and pipelined loads, whose purpose is to
+// overlap compute: half the grid still saturates the link (1.2 MiB in flight
+// against the ~0.4 MiB its rate times its latency asks for) and leaves more of
+// the GPU to that compute.  At one CTA per SM the compute held the transfer's
+// CTAs back, and a 4K-token MLA load plus per-layer attention took 15% longer.
+constexpr int kDefaultLayerCtasPer2Sm = 1;
+// A fused backup + load alternates the directions in every CTA: two per SM.
+constexpr int kDefaultFusedCtasPerSm = 2;
 // A backup saturates the link with far fewer CTAs: its host writes are posted,
 // so it needs no round trip per tile.  With a whole SM's share it also takes
 // more than its half of the link from a load running at the same time on

@@ -64,7 +64,7 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
     x.all_layers = false;
     x.to_host = false;
     x.bidir = false;
-    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
+    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->layer_ctas));
     x.stream = stream;
     const int e = hicache::launch_pipelined_load(x, pool->layer_done, pool->layer_done + s.L);
     if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
@@ -170,7 +170,7 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
     x.all_layers = false;
     x.to_host = false;
     x.bidir = false;
-    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->ctas));
+    x.grid = int(std::min<int64_t>(int64_t(params.h.job[0].total_tiles) * s.L, pool->layer_ctas));
     x.stream = stream;
     unsigned int *sched = counters + hicache::kNoAllocMaxLayers +
                           2 * (g_noalloc_slot[pool->device]++ % hicache::kNoAllocSchedSlots);
