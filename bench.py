@@ -569,9 +569,11 @@ def bench_nsa_group(torch, hc, args):
     """A buffer group: an MLA latent (576 bf16) beside an fp8 indexer key (128)
     and its fp32 scales (4 per row), 61 layers, page 64, three page_first pools
     carved from one pinned allocation.  Loads of 4K / 16K / 64K tokens, every
-    layer and layer by layer: one launch per pool vs one group launch, and the
+    layer and layer by layer: one launch per pool vs one group launch, the
     pipelined group load (every layer of every pool in one launch, each
-    pool's layers signalled as they land).  Each
+    pool's layers signalled as they land), and a group plan's per-layer
+    launches replayed from one CUDA graph (its first, capturing call is a
+    warm-up).  Each
     variant is enqueued behind a sleep kernel on a gate stream, so the device
     time excludes the host's enqueue cost, which is reported beside it."""
     from tiered_kv_cache_gb300 import workloads as wl
@@ -628,12 +630,15 @@ def bench_nsa_group(torch, hc, args):
             "all_layers_per_pool": lambda: [pool.load(kv, dp, hp, stream=stream) for pool, kv in zip(pools, kvs)],
             "all_layers_group": lambda: hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, stream=stream),
             "pipelined_group": lambda: hc.group_load_pipelined(pools, kvs, dp, hp, stream=stream),
+            "per_layer_group_graph": lambda: plan.load_layers(kvs, stream=stream),
         }
+        plan = hc.group_plan(pools, dp, hp, Dp)
         r = {"pages": len(dp), "bytes": nbytes}
         for name, fn in variants.items():
             d, h = gated(fn)
             r[name] = {"device_ms": round(d * 1e3, 3), "gbs": round(nbytes / d / GB, 1),
                        "host_enqueue_ms": round(h * 1e3, 3)}
+        plan.close()
         out[f"{tokens // 1024}k"] = r
     launches = hc.launch_count() - launches0
     for pool in pools:

@@ -352,6 +352,40 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
                                  const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                                  int32_t layout, void *stream);
 
+/* A load plan for a buffer group: the page pairs validated and reduced to runs
+ * once, as hicache_plan_create, for pools that share the page numbering; then
+ * loaded many times, every layer at once or layer by layer.
+ *   pools / npools: as hicache_group_transfer (1..HICACHE_MAX_GROUP distinct
+ *     pools on one device with equal num_layers and page_size).  The plan keeps
+ *     the pool pointers: the pools must outlive it.
+ *   device_pages / host_pages / n / device_num_pages: as hicache_plan_create
+ *     with HICACHE_DIR_LOAD; every host page must be inside every pool.
+ * Errors: INVALID_ARG (bad pools or sizes, NULL out), INDEX_RANGE,
+ * DUPLICATE_INDEX (a device page twice), NOMEM. */
+typedef struct hicache_group_plan hicache_group_plan;
+int hicache_group_plan_create(hicache_pool *const *pools, int32_t npools, const int64_t *device_pages,
+                              const int64_t *host_pages, int64_t n, int64_t device_num_pages,
+                              hicache_group_plan **out);
+/* hicache_group_transfer (a load) of a group plan: every layer (layer_id < 0)
+ * in one launch, or one layer, recording that layer's event in every pool.
+ * kvs[i] belongs to the plan's pool i and holds at least the plan's
+ * device_num_pages.  Errors as hicache_group_transfer. */
+int hicache_group_plan_execute(const hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
+                               int32_t layer_id, void *stream);
+/* hicache_plan_load_layers for a buffer group: every layer, layer by layer,
+ * one group launch per layer followed by that layer's event in every pool,
+ * captured into a CUDA graph on the first call for a set of device buffers and
+ * a layout and replayed with one graph launch afterwards.  As for a single
+ * pool, each layer's launch may start while the previous one drains, so no two
+ * device buffers of the group may overlap (checked); the event of layer l in
+ * any pool fires once layers 0..l of every pool have landed.  Errors as
+ * hicache_group_plan_execute, plus INVALID_ARG for overlapping buffers and
+ * CUDA; on error nothing is enqueued.  Destroying the plan while a replay runs
+ * is allowed. */
+int hicache_group_plan_load_layers(hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
+                                   void *stream);
+int hicache_group_plan_destroy(hicache_group_plan *plan);
+
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
 /* The pool-owned event recorded by the last load of `layer` (*event_out is a

@@ -412,3 +412,106 @@ def test_group_backup_thread_and_pipelined_load_thread():
             done, target = pool.pipeline_status(layer)
             assert done == target
     grp.close()
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_group_plan_execute_and_graph_replay_match_the_oracle(layout):
+    """A group plan loads every layer at once, one layer, or every layer
+    layer by layer from a CUDA graph; each pool equals the oracle's load of that
+    pool, every pool's layer events fire, a second buffer set re-captures, and
+    overlapping buffers are refused before anything is enqueued."""
+    L, P, Dp, Hp, n = 5, 8, 36, 40, 13
+    kinds = [(1, 576, 2), (2, 64, 1), (1, 4, 4)]
+    grp = Group(kinds, L, P, Dp, Hp, layout, seed=110 + layout)
+    rng = np.random.default_rng(111 + layout)
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    dp = wl.fragmented_pages(rng, Dp, n, max_run=3)
+    hp = rng.choice(Hp, n, replace=False)
+    plan = hc.group_plan(grp.pools, dp, hp, Dp)
+    s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    want_all = _want_load(grp, dp, hp, layout, 0x6B)
+
+    def check(want):
+        for bufs, w, (B, R, es) in zip(grp.bufs, want, kinds):
+            got = gh.to_np(bufs, es)
+            for k in range(B * L):
+                assert np.array_equal(got[k], w[k]), (R, es, k)
+
+    # every layer at once: one launch
+    for bufs in grp.bufs:
+        gh.sentinel_fill(bufs, 0x6B)
+    torch.cuda.synchronize()
+    c0 = hc.launch_count()
+    plan.execute(grp.kvs, stream=s)
+    assert hc.launch_count() - c0 == 1
+    hc.wait(s, TEN_S)
+    check(want_all)
+    # one layer
+    for bufs in grp.bufs:
+        gh.sentinel_fill(bufs, 0x6B)
+    torch.cuda.synchronize()
+    plan.execute(grp.kvs, layer=3, stream=s)
+    for pool in grp.pools:
+        pool.wait_layer(3, comp)
+    hc.wait(comp, TEN_S)
+    hc.wait(s, TEN_S)
+    check(_want_load(grp, dp, hp, layout, 0x6B, layer=3))
+    # layer by layer from a graph, for two buffer sets
+    for seed in (112, 113):
+        if seed == 113:
+            grp.bufs = [gh.random_device_bufs(B, L, P, R, Dp, es, seed=seed + i)
+                        for i, (B, R, es) in enumerate(kinds)]
+            grp.kvs = [hc.DeviceKV(b, Dp) for b in grp.bufs]
+        for rep in range(2):
+            for bufs in grp.bufs:
+                gh.sentinel_fill(bufs, 0x6B)
+            torch.cuda.synchronize()
+            c0 = hc.launch_count()
+            plan.load_layers(grp.kvs, stream=s)
+            assert hc.launch_count() - c0 == L
+            for pool in grp.pools:
+                pool.wait_layer(L - 1, comp)
+            hc.wait(comp, TEN_S)
+            hc.wait(s, TEN_S)
+            check(want_all)
+    # two pools' buffers overlapping: refused, nothing enqueued
+    big = torch.empty(Dp * P * 576 * 2 * L + 64, dtype=torch.uint8, device="cuda")
+    lat = [big[i * Dp * P * 1152:(i + 1) * Dp * P * 1152].view(torch.int16).view(Dp * P, 576) for i in range(L)]
+    fp8 = [big[16 + i * Dp * P * 64:16 + (i + 1) * Dp * P * 64].view(Dp * P, 64) for i in range(2 * L)]
+    bad = [hc.DeviceKV(lat, Dp), hc.DeviceKV(fp8, Dp), grp.kvs[2]]
+    c0 = hc.launch_count()
+    with pytest.raises(hc.HiCacheError, match="overlap"):
+        plan.load_layers(bad, stream=s)
+    assert hc.launch_count() == c0
+    plan.close()
+    grp.close()
+
+
+def test_group_plan_graph_with_split_layers():
+    """A group plan of 3,000 scattered one-token pages needs several launches
+    per layer; the graph replay still equals the oracle for every pool."""
+    L, P, Dp, Hp, n = 3, 1, 6000, 6000, 3000
+    kinds = [(1, 576, 2), (1, 128, 1), (1, 4, 4)]
+    grp = Group(kinds, L, P, Dp, Hp, "page_first", seed=120)
+    rng = np.random.default_rng(121)
+    for pool in grp.pools:
+        pool.host_array(np.uint8)[:] = rng.integers(0, 256, pool.nbytes, dtype=np.uint8)
+    dp, hp = rng.permutation(Dp)[:n], rng.permutation(Hp)[:n]
+    plan = hc.group_plan(grp.pools, dp, hp, Dp)
+    s = torch.cuda.Stream()
+    want = _want_load(grp, dp, hp, hc.PAGE_FIRST, 0x2E)
+    for rep in range(2):
+        for bufs in grp.bufs:
+            gh.sentinel_fill(bufs, 0x2E)
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        plan.load_layers(grp.kvs, stream=s)
+        assert hc.launch_count() - c0 >= 2 * L
+        hc.wait(s, TEN_S)
+        for bufs, w, (B, R, es) in zip(grp.bufs, want, kinds):
+            got = gh.to_np(bufs, es)
+            for k in range(B * L):
+                assert np.array_equal(got[k], w[k]), (rep, R, k)
+    plan.close()
+    grp.close()

@@ -1,6 +1,7 @@
 """Seeded random sequences of every kind of call -- backup, load, per-layer
-load, pipelined (plain and allocation-free), fused backup + load, plans, and
-group calls -- on two pools that share the page numbering, all on one stream.
+load, pipelined (plain and allocation-free), fused backup + load, plans, group
+calls and group plans -- on two pools that share the page numbering, all on one
+stream.
 A shadow copy of the device buffers and host pools is updated by the oracle in
 the same order; at the end every byte must agree (GB300)."""
 import ctypes
@@ -17,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 TEN_S = 10_000_000
 OPS = ["backup", "load", "load_layer", "pipelined", "noalloc", "fused", "plan_layers", "plan_graph",
-       "group_backup", "group_load", "group_layer", "group_pipelined"]
+       "group_backup", "group_load", "group_layer", "group_pipelined", "group_plan_graph"]
 
 
 def _noalloc(pool, kv, dp, hp, stream):
@@ -112,10 +113,16 @@ def test_random_call_sequence(seed):
             hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, layer=layer, stream=st)
             shadow(0, "load", dp, hp, layer)
             shadow(1, "load", dp, hp, layer)
-        else:
+        elif op == "group_pipelined":
             hc.group_load_pipelined(pools, kvs, dp, hp, stream=st)
             shadow(0, "load", dp, hp)
             shadow(1, "load", dp, hp)
+        else:
+            gplan = hc.group_plan(pools, dp, hp, Dp)
+            gplan.load_layers(kvs, stream=st)
+            shadow(0, "load", dp, hp)
+            shadow(1, "load", dp, hp)
+            plans.append(gplan)                # kept until the stream is done
     hc.wait(st, TEN_S)
     for plan in plans:
         plan.close()

@@ -247,6 +247,14 @@ def test_group_calls_reject_bad_arguments_before_any_cuda_call():
         assert lib.hicache_group_load_pipelined(pools, structs, n, None, None, 0, -1, None) == -1
         assert lib.hicache_last_error()
         assert hc.launch_count() == c0
+    for pools, n in ((none, 0), (none, hc.MAX_GROUP + 1), (None, 1), (none, 1)):
+        out = ctypes.c_void_p(1)
+        assert lib.hicache_group_plan_create(pools, n, None, None, 0, 8, ctypes.byref(out)) == -1
+        assert out.value is None and lib.hicache_last_error()
+    for call in (lambda: lib.hicache_group_plan_execute(None, kvs, -1, -1, None),
+                 lambda: lib.hicache_group_plan_load_layers(None, kvs, -1, None)):
+        assert call() == -1
+    assert lib.hicache_group_plan_destroy(None) == 0
     with pytest.raises(ValueError):
         hc.group_transfer([object()], [], [0], [0], hc.LOAD)
     with pytest.raises(ValueError):

@@ -94,6 +94,10 @@ def _bind(lib):
                                                   _i32, _i32, _vp]),
         "hicache_group_load_pipelined": (ctypes.c_int, [_P(_vp), _P(_DeviceKVStruct), _i32, _vp, _vp, _i64,
                                                         _i32, _vp]),
+        "hicache_group_plan_create": (ctypes.c_int, [_P(_vp), _i32, _vp, _vp, _i64, _i64, _P(_vp)]),
+        "hicache_group_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
+        "hicache_group_plan_load_layers": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
+        "hicache_group_plan_destroy": (ctypes.c_int, [_vp]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
@@ -290,6 +294,57 @@ def group_load_pipelined(pools, kvs, device_pages, host_pages, layout=LAYOUT_POO
     structs = (_DeviceKVStruct * len(kvs))(*[k.struct for k in kvs])
     _check(library().hicache_group_load_pipelined(handles, structs, len(pools), _ptr(dp), _ptr(hp), dp.size,
                                                   layout, _stream(stream)))
+
+
+class GroupPlan:
+    """A load plan for a buffer group: the page pairs pre-passed once for
+    pools that share the page numbering, then loaded every layer at once, one
+    layer, or layer by layer from a CUDA graph."""
+
+    def __init__(self, pools, device_pages, host_pages, device_num_pages: int):
+        dp, hp = _idx(device_pages), _idx(host_pages)
+        if dp.size != hp.size:
+            raise ValueError("device_pages and host_pages differ in length")
+        handles = (ctypes.c_void_p * len(pools))(*[p.handle for p in pools])
+        h = ctypes.c_void_p()
+        _check(library().hicache_group_plan_create(handles, len(pools), _ptr(dp), _ptr(hp), dp.size,
+                                                   device_num_pages, ctypes.byref(h)))
+        self.pools = list(pools)
+        self.handle = h.value
+
+    def _kvs(self, kvs):
+        if len(kvs) != len(self.pools):
+            raise ValueError("one DeviceKV per pool of the plan")
+        return (_DeviceKVStruct * len(kvs))(*[k.struct for k in kvs])
+
+    def execute(self, kvs, layer: int = -1, layout=LAYOUT_POOL, stream=None):
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_group_plan_execute(self.handle, self._kvs(kvs), layout, layer,
+                                                    _stream(stream)))
+
+    def load_layers(self, kvs, layout=LAYOUT_POOL, stream=None):
+        """Every layer, layer by layer, each followed by its event in every
+        pool, replayed from a CUDA graph the plan captures on first use."""
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_group_plan_load_layers(self.handle, self._kvs(kvs), layout,
+                                                        _stream(stream)))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            library().hicache_group_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def group_plan(pools, device_pages, host_pages, device_num_pages: int) -> GroupPlan:
+    return GroupPlan(pools, device_pages, host_pages, device_num_pages)
 
 
 class PinnedHost:

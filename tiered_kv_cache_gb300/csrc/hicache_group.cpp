@@ -1,12 +1,15 @@
 // hicache_group.cpp -- buffer groups: up to HICACHE_MAX_GROUP pools (buffer
 // kinds with different rows) moved by one index set in one launch per chunk,
-// all layers, one layer, or pipelined with per-layer counters for every pool.
+// all layers, one layer, or pipelined with per-layer counters for every pool;
+// and group plans, whose per-layer loads replay from one CUDA graph.
 
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <climits>
 #include <mutex>
+#include <new>
+#include <utility>
 #include <vector>
 
 #include "hicache.h"
@@ -16,10 +19,12 @@
 namespace hicache {
 
 // Enqueue validated runs for every pool of a group, one launch per chunk of
-// runs that fits the parameters of all of them.
+// runs that fits the parameters of all of them.  pdl_first: the first launch
+// may start while the kernel before it on the stream drains; that kernel must
+// be a one-layer group load of another layer.
 int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t np,
                   const std::vector<RunRec> &runs, int32_t layout, int32_t layer, bool to_host,
-                  void *stream) {
+                  void *stream, bool pdl_first = false) {
   if (runs.empty()) return HICACHE_OK;
   const bool all = layer < 0;
   thread_local hicache::GroupParams params;
@@ -68,7 +73,7 @@ int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int3
     x.to_host = to_host;
     x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : all ? p0->ctas : p0->layer_ctas));
     x.stream = stream;
-    x.pdl = next > 0;                  // disjoint destinations: overlap the previous launch's drain
+    x.pdl = next > 0 ? true : pdl_first;  // disjoint destinations: overlap the previous launch's drain
     const int e = hicache::launch_group(x);
     if (e != 0) return cuda_error(cudaError_t(e), "group transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -142,19 +147,22 @@ int enqueue_group_pipelined(hicache_pool *const *pools, const hicache_device_kv 
 }
 
 // The checks every group call shares: 1..HICACHE_MAX_GROUP distinct pools on
-// one device with equal layers, page size and resolved layout, valid device KV
-// for each, at most kMaxBufs buffers, no buffer named twice.  Returns the
-// resolved layout and the bounds the pre-pass must apply to every pool.
+// one device with equal layers and page size; with kvs, also the same resolved
+// layout, valid device KV for each (at least min_pages pages), at most
+// kMaxBufs buffers and no buffer named twice.  Returns the resolved layout
+// (with kvs) and the bounds the pre-pass must apply to every pool (Dp only
+// with kvs).
 int check_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t npools, int32_t layout,
-                int32_t *lay, int64_t *Hp, int64_t *Dp, int64_t *max_run) {
-  if (!pools || !kvs) return set_error(HICACHE_ERR_INVALID_ARG, "pools or kvs is NULL");
+                int32_t *lay, int64_t *Hp, int64_t *Dp, int64_t *max_run, bool with_kvs = true,
+                int64_t min_pages = 0) {
+  if (!pools || (with_kvs && !kvs)) return set_error(HICACHE_ERR_INVALID_ARG, "pools or kvs is NULL");
   if (npools < 1 || npools > HICACHE_MAX_GROUP)
     return set_error(HICACHE_ERR_INVALID_ARG, "npools = %d outside [1, %d]", npools, HICACHE_MAX_GROUP);
   for (int32_t i = 0; i < npools; ++i)
     if (!pools[i]) return set_error(HICACHE_ERR_INVALID_ARG, "pool %d is NULL", i);
   const hicache_pool *p0 = pools[0];
-  int rc = resolve_layout(layout, p0->shape.layout, lay);
-  if (rc) return rc;
+  int rc = HICACHE_OK;
+  if (with_kvs && (rc = resolve_layout(layout, p0->shape.layout, lay))) return rc;
   *Hp = INT64_MAX;
   *Dp = INT64_MAX;
   *max_run = INT64_MAX;
@@ -172,14 +180,15 @@ int check_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_
                        "pool %d has %lld layers of %lld-token pages; pool 0 has %lld of %lld", i,
                        (long long)p->shape.L, (long long)p->shape.P, (long long)p0->shape.L,
                        (long long)p0->shape.P);
+    *Hp = std::min(*Hp, p->shape.Hp);
+    *max_run = std::min(*max_run, max_run_pages(p->shape));
+    if (!with_kvs) continue;
     int32_t li = 0;
     if ((rc = resolve_layout(layout, p->shape.layout, &li))) return rc;
     if (li != *lay)
       return set_error(HICACHE_ERR_INVALID_ARG, "pool %d resolves to layout %d, pool 0 to %d", i, li, *lay);
-    if ((rc = check_kv(p, &kvs[i], 0))) return rc;
-    *Hp = std::min(*Hp, p->shape.Hp);
+    if ((rc = check_kv(p, &kvs[i], min_pages))) return rc;
     *Dp = std::min(*Dp, kvs[i].device_num_pages);
-    *max_run = std::min(*max_run, max_run_pages(p->shape));
     bufs += p->shape.B * p->shape.L;
     for (int64_t b = 0; b < p->shape.B * p->shape.L; ++b)
       ptrs.push_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]));
@@ -272,6 +281,205 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
     const cudaError_t e = cudaEventRecord(p->pipeline_last, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
   }
+  return HICACHE_OK;
+}
+
+
+}  // extern "C"
+
+// ---- group plans -----------------------------------------------------------------
+
+struct hicache_group_plan {
+  std::vector<hicache_pool *> pools;
+  int64_t n = 0;
+  int64_t device_num_pages = 0;
+  int64_t Hp = 0;
+  std::vector<hicache::RunRec> runs;
+  // hicache_group_plan_load_layers: the per-layer group launches and every
+  // pool's layer events, captured once per device buffers and layout
+  std::mutex graph_mu;
+  cudaGraphExec_t graph = nullptr;
+  std::vector<void *> graph_bufs;        // every pool's buffer pointers, pool by pool
+  std::vector<int64_t> graph_pages;      // every pool's device_num_pages
+  int32_t graph_layout = -1;
+  int64_t graph_launches = 0;
+};
+
+namespace {
+
+// The checks of a group plan's call: the plan's pools with these kvs and
+// layout, and kvs holding at least the plan's device pages.
+int check_plan_call(const hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
+                    int32_t *lay) {
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  int64_t Hp = 0, Dp = 0, max_run = 0;
+  int rc = check_group(plan->pools.data(), kvs, int32_t(plan->pools.size()), layout, lay, &Hp, &Dp, &max_run,
+                       true, plan->device_num_pages);
+  if (rc) return rc;
+  return check_device(plan->pools[0]);
+}
+
+// No two device buffers of the group may share a byte: the layers' launches
+// of a replay may run at the same time.
+int check_no_overlap(const hicache_group_plan *plan, const hicache_device_kv *kvs) {
+  std::vector<std::pair<uintptr_t, uint64_t>> spans;
+  for (size_t i = 0; i < plan->pools.size(); ++i) {
+    const Shape &s = plan->pools[i]->shape;
+    const uint64_t bytes = uint64_t(kvs[i].device_num_pages) * uint64_t(s.PV) * 16u;
+    for (int64_t b = 0; b < s.B * s.L; ++b)
+      spans.emplace_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]), bytes);
+  }
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first - spans[i - 1].first < spans[i - 1].second)
+      return set_error(HICACHE_ERR_INVALID_ARG, "device buffers of the group overlap");
+  return HICACHE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hicache_group_plan_create(hicache_pool *const *pools, int32_t npools, const int64_t *device_pages,
+                              const int64_t *host_pages, int64_t n, int64_t device_num_pages,
+                              hicache_group_plan **out) {
+  clear_error();
+  if (!out) return set_error(HICACHE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int32_t lay = 0;
+  int64_t Hp = 0, Dp = 0, max_run = 0;
+  int rc = check_group(pools, nullptr, npools, HICACHE_LAYOUT_POOL, &lay, &Hp, &Dp, &max_run, false);
+  if (rc) return rc;
+  std::vector<RunRec> runs;
+  if ((rc = prepass(Hp, device_num_pages, device_pages, host_pages, n, HICACHE_DIR_LOAD, max_run, &runs)))
+    return rc;
+  hicache_group_plan *p = new (std::nothrow) hicache_group_plan();
+  if (!p) return set_error(HICACHE_ERR_NOMEM, "out of host memory");
+  p->pools.assign(pools, pools + npools);
+  p->n = n;
+  p->device_num_pages = device_num_pages;
+  p->Hp = Hp;
+  p->runs = std::move(runs);
+  *out = p;
+  return HICACHE_OK;
+}
+
+int hicache_group_plan_execute(const hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
+                               int32_t layer_id, void *stream) {
+  clear_error();
+  int32_t lay = 0;
+  int rc = check_plan_call(plan, kvs, layout, &lay);
+  if (rc) return rc;
+  hicache_pool *const *pools = plan->pools.data();
+  const int32_t np = int32_t(plan->pools.size());
+  if (layer_id >= pools[0]->shape.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id,
+                     (long long)pools[0]->shape.L);
+  if ((rc = enqueue_group(pools, kvs, np, plan->runs, lay, layer_id < 0 ? -1 : layer_id, false, stream)))
+    return rc;
+  if (layer_id >= 0) {
+    for (int32_t i = 0; i < np; ++i) {
+      hicache_pool *p = pools[i];
+      const cudaError_t e = cudaEventRecord(p->events[size_t(layer_id)], static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+      std::lock_guard<std::mutex> g(p->signal_mu);
+      p->layer_signal[size_t(layer_id)] = 0;
+    }
+  }
+  return HICACHE_OK;
+}
+
+int hicache_group_plan_load_layers(hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
+                                   void *stream) {
+  clear_error();
+  int32_t lay = 0;
+  int rc = check_plan_call(plan, kvs, layout, &lay);
+  if (rc) return rc;
+  hicache_pool *const *pools = plan->pools.data();
+  const int32_t np = int32_t(plan->pools.size());
+  const int64_t L = pools[0]->shape.L;
+  std::lock_guard<std::mutex> g(plan->graph_mu);
+  std::vector<void *> bufs;
+  std::vector<int64_t> pages;
+  for (int32_t i = 0; i < np; ++i) {
+    bufs.insert(bufs.end(), kvs[i].buf_ptrs, kvs[i].buf_ptrs + pools[i]->shape.B * L);
+    pages.push_back(kvs[i].device_num_pages);
+  }
+  if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != pages || plan->graph_layout != lay) {
+    if ((rc = check_no_overlap(plan, kvs))) return rc;
+    if (plan->graph) {
+      cudaGraphExecDestroy(plan->graph);
+      plan->graph = nullptr;
+    }
+    // As hicache_plan_load_layers: the layers' group launches one after
+    // another on a private stream, every launch after the first programmatic,
+    // and each layer's events (one per pool) recorded on a side branch that
+    // forks off after that layer's launch.
+    cudaStream_t cap = nullptr, side = nullptr;
+    std::vector<cudaEvent_t> forks(size_t(L) + 1, nullptr);
+    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+    for (auto &f : forks)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    auto release = [&] {
+      for (auto f : forks)
+        if (f) cudaEventDestroy(f);
+      if (side) cudaStreamDestroy(side);
+      if (cap) cudaStreamDestroy(cap);
+    };
+    if (e != cudaSuccess) {
+      release();
+      return cuda_error(e, "setting up the layer-load capture");
+    }
+    const int64_t before = g_launches.load();
+    for (int64_t l = 0; l < L && rc == HICACHE_OK; ++l) {
+      rc = enqueue_group(pools, kvs, np, plan->runs, lay, int32_t(l), false, cap, l > 0);
+      if (rc != HICACHE_OK) break;
+      e = cudaEventRecord(forks[size_t(l)], cap);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
+      for (int32_t i = 0; i < np && e == cudaSuccess; ++i)
+        e = cudaEventRecordWithFlags(pools[i]->events[size_t(l)], side, cudaEventRecordExternal);
+      if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer events");
+    }
+    if (rc == HICACHE_OK) {                // join the side branch back
+      e = cudaEventRecord(forks[size_t(L)], side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(L)], 0);
+      if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
+    }
+    const int64_t captured = g_launches.load() - before;
+    g_launches.fetch_sub(captured);      // counted when replayed
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(cap, &graph);
+    release();
+    if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
+    if (rc == HICACHE_OK) {
+      e = cudaGraphInstantiate(&plan->graph, graph, 0);
+      if (e != cudaSuccess) {
+        plan->graph = nullptr;
+        rc = cuda_error(e, "cudaGraphInstantiate");
+      }
+    }
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != HICACHE_OK) return rc;
+    plan->graph_bufs = bufs;
+    plan->graph_pages = pages;
+    plan->graph_layout = lay;
+    plan->graph_launches = captured;
+  }
+  const cudaError_t e = cudaGraphLaunch(plan->graph, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
+  g_launches.fetch_add(plan->graph_launches, std::memory_order_relaxed);
+  for (int32_t i = 0; i < np; ++i) {
+    std::lock_guard<std::mutex> gs(pools[i]->signal_mu);
+    for (int64_t l = 0; l < L; ++l) pools[i]->layer_signal[size_t(l)] = 0;
+  }
+  return HICACHE_OK;
+}
+
+int hicache_group_plan_destroy(hicache_group_plan *plan) {
+  if (plan && plan->graph) cudaGraphExecDestroy(plan->graph);
+  delete plan;
   return HICACHE_OK;
 }
 
