@@ -319,23 +319,6 @@ int check_plan_call(const hicache_group_plan *plan, const hicache_device_kv *kvs
   return check_device(plan->pools[0]);
 }
 
-// No two device buffers of the group may share a byte: the layers' launches
-// of a replay may run at the same time.
-int check_no_overlap(const hicache_group_plan *plan, const hicache_device_kv *kvs) {
-  std::vector<std::pair<uintptr_t, uint64_t>> spans;
-  for (size_t i = 0; i < plan->pools.size(); ++i) {
-    const Shape &s = plan->pools[i]->shape;
-    const uint64_t bytes = uint64_t(kvs[i].device_num_pages) * uint64_t(s.PV) * 16u;
-    for (int64_t b = 0; b < s.B * s.L; ++b)
-      spans.emplace_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]), bytes);
-  }
-  std::sort(spans.begin(), spans.end());
-  for (size_t i = 1; i < spans.size(); ++i)
-    if (spans[i].first - spans[i - 1].first < spans[i - 1].second)
-      return set_error(HICACHE_ERR_INVALID_ARG, "device buffers of the group overlap");
-  return HICACHE_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -406,75 +389,32 @@ int hicache_group_plan_load_layers(hicache_group_plan *plan, const hicache_devic
     pages.push_back(kvs[i].device_num_pages);
   }
   if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != pages || plan->graph_layout != lay) {
-    if ((rc = check_no_overlap(plan, kvs))) return rc;
+    std::vector<std::pair<uintptr_t, uint64_t>> spans;
+    for (int32_t i = 0; i < np; ++i) {
+      const Shape &s = pools[i]->shape;
+      const uint64_t bytes = uint64_t(kvs[i].device_num_pages) * uint64_t(s.PV) * 16u;
+      for (int64_t b = 0; b < s.B * s.L; ++b)
+        spans.emplace_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]), bytes);
+    }
+    if ((rc = check_disjoint(spans))) return rc;
     if (plan->graph) {
       cudaGraphExecDestroy(plan->graph);
       plan->graph = nullptr;
     }
-    // As hicache_plan_load_layers: the layers' group launches one after
-    // another on a private stream, every launch after the first programmatic,
-    // and each layer's events (one per pool) recorded on a side branch that
-    // forks off after that layer's launch.
-    cudaStream_t cap = nullptr, side = nullptr;
-    std::vector<cudaEvent_t> forks(size_t(L) + 1, nullptr);
-    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
-    for (auto &f : forks)
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
-    auto release = [&] {
-      for (auto f : forks)
-        if (f) cudaEventDestroy(f);
-      if (side) cudaStreamDestroy(side);
-      if (cap) cudaStreamDestroy(cap);
-    };
-    if (e != cudaSuccess) {
-      release();
-      return cuda_error(e, "setting up the layer-load capture");
-    }
-    const int64_t before = g_launches.load();
-    for (int64_t l = 0; l < L && rc == HICACHE_OK; ++l) {
-      rc = enqueue_group(pools, kvs, np, plan->runs, lay, int32_t(l), false, cap, l > 0);
-      if (rc != HICACHE_OK) break;
-      e = cudaEventRecord(forks[size_t(l)], cap);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
-      for (int32_t i = 0; i < np && e == cudaSuccess; ++i)
-        e = cudaEventRecordWithFlags(pools[i]->events[size_t(l)], side, cudaEventRecordExternal);
-      if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer events");
-    }
-    if (rc == HICACHE_OK) {                // join the side branch back
-      e = cudaEventRecord(forks[size_t(L)], side);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(L)], 0);
-      if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
-    }
-    const int64_t captured = g_launches.load() - before;
-    g_launches.fetch_sub(captured);      // counted when replayed
-    cudaGraph_t graph = nullptr;
-    e = cudaStreamEndCapture(cap, &graph);
-    release();
-    if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
-    if (rc == HICACHE_OK) {
-      e = cudaGraphInstantiate(&plan->graph, graph, 0);
-      if (e != cudaSuccess) {
-        plan->graph = nullptr;
-        rc = cuda_error(e, "cudaGraphInstantiate");
-      }
-    }
-    if (graph) cudaGraphDestroy(graph);
+    int64_t launches = 0;
+    rc = capture_layer_graph(
+        pools, np, L,
+        [&](int64_t l, void *cap) {
+          return enqueue_group(pools, kvs, np, plan->runs, lay, int32_t(l), false, cap, l > 0);
+        },
+        &plan->graph, &launches);
     if (rc != HICACHE_OK) return rc;
     plan->graph_bufs = bufs;
     plan->graph_pages = pages;
     plan->graph_layout = lay;
-    plan->graph_launches = captured;
+    plan->graph_launches = launches;
   }
-  const cudaError_t e = cudaGraphLaunch(plan->graph, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
-  g_launches.fetch_add(plan->graph_launches, std::memory_order_relaxed);
-  for (int32_t i = 0; i < np; ++i) {
-    std::lock_guard<std::mutex> gs(pools[i]->signal_mu);
-    for (int64_t l = 0; l < L; ++l) pools[i]->layer_signal[size_t(l)] = 0;
-  }
-  return HICACHE_OK;
+  return launch_layer_graph(plan->graph, plan->graph_launches, pools, np, stream);
 }
 
 int hicache_group_plan_destroy(hicache_group_plan *plan) {

@@ -9,7 +9,9 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <functional>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "hicache.h"
@@ -114,5 +116,19 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
 // (hicache_pipeline.cpp).
 int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
                       int32_t layout, void *stream);
+
+// hicache_plan.cpp: per-layer graphs.
+// INVALID_ARG unless the (address, bytes) spans are pairwise disjoint.
+int check_disjoint(std::vector<std::pair<uintptr_t, uint64_t>> spans);
+// Capture L layers into an executable graph: enqueue_layer(l, stream) enqueues
+// layer l's launches (every launch after the very first programmatic), and
+// each pool's event of layer l is recorded after them; *launches = the kernel
+// launches of one replay.
+int capture_layer_graph(hicache_pool *const *pools, int32_t np, int64_t L,
+                        const std::function<int(int64_t, void *)> &enqueue_layer, cudaGraphExec_t *out,
+                        int64_t *launches);
+// Replay such a graph on `stream`; the pools' per-layer waits use the events.
+int launch_layer_graph(cudaGraphExec_t graph, int64_t launches, hicache_pool *const *pools, int32_t np,
+                       void *stream);
 
 }  // namespace hicache

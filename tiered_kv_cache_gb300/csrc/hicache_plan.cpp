@@ -6,8 +6,10 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <functional>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "hicache.h"
@@ -31,6 +33,96 @@ struct hicache_plan {
   int32_t graph_layout = -1;
   int64_t graph_launches = 0;         // kernel launches one replay makes
 };
+
+namespace hicache {
+
+int check_disjoint(std::vector<std::pair<uintptr_t, uint64_t>> spans) {
+  std::sort(spans.begin(), spans.end());
+  for (size_t i = 1; i < spans.size(); ++i)
+    if (spans[i].first - spans[i - 1].first < spans[i - 1].second)
+      return set_error(HICACHE_ERR_INVALID_ARG,
+                       "device buffers overlap: each of the %zu buffers needs its own bytes", spans.size());
+  return HICACHE_OK;
+}
+
+int capture_layer_graph(hicache_pool *const *pools, int32_t np, int64_t L,
+                        const std::function<int(int64_t, void *)> &enqueue_layer, cudaGraphExec_t *out,
+                        int64_t *launches) {
+  // Capture the L layers' launches on a private stream, one after another.
+  // Each layer's events are recorded (as external event nodes) on a side
+  // branch that forks off after that layer's launches, so the kernel chain
+  // itself has no node between consecutive launches.  Every kernel after the
+  // first is a programmatic dependent launch: it may start as the previous
+  // kernel moves its last tiles (the layers write different buffers and only
+  // read the host pool) and ends after it.  A layer's event nodes follow that
+  // layer's last kernel and the event nodes before them, so event l means
+  // layers 0..l have landed.
+  *out = nullptr;
+  *launches = 0;
+  cudaStream_t cap = nullptr, side = nullptr;
+  std::vector<cudaEvent_t> forks(size_t(L) + 1, nullptr);
+  cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
+  for (auto &f : forks)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  auto release = [&] {
+    for (auto f : forks)
+      if (f) cudaEventDestroy(f);
+    if (side) cudaStreamDestroy(side);
+    if (cap) cudaStreamDestroy(cap);
+  };
+  if (e != cudaSuccess) {
+    release();
+    return cuda_error(e, "setting up the layer-load capture");
+  }
+  int rc = HICACHE_OK;
+  const int64_t before = g_launches.load();
+  for (int64_t l = 0; l < L && rc == HICACHE_OK; ++l) {
+    rc = enqueue_layer(l, cap);
+    if (rc != HICACHE_OK) break;
+    e = cudaEventRecord(forks[size_t(l)], cap);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
+    for (int32_t i = 0; i < np && e == cudaSuccess; ++i)
+      e = cudaEventRecordWithFlags(pools[i]->events[size_t(l)], side, cudaEventRecordExternal);
+    if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer events");
+  }
+  if (rc == HICACHE_OK) {                // join the side branch back
+    e = cudaEventRecord(forks[size_t(L)], side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(L)], 0);
+    if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
+  }
+  const int64_t captured = g_launches.load() - before;
+  g_launches.fetch_sub(captured);        // counted when replayed
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cap, &graph);
+  release();
+  if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
+  if (rc == HICACHE_OK) {
+    e = cudaGraphInstantiate(out, graph, 0);
+    if (e != cudaSuccess) {
+      *out = nullptr;
+      rc = cuda_error(e, "cudaGraphInstantiate");
+    }
+  }
+  if (graph) cudaGraphDestroy(graph);
+  if (rc == HICACHE_OK) *launches = captured;
+  return rc;
+}
+
+int launch_layer_graph(cudaGraphExec_t graph, int64_t launches, hicache_pool *const *pools, int32_t np,
+                       void *stream) {
+  const cudaError_t e = cudaGraphLaunch(graph, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
+  g_launches.fetch_add(launches, std::memory_order_relaxed);
+  for (int32_t i = 0; i < np; ++i) {     // hicache_wait_layer uses the events
+    std::lock_guard<std::mutex> g(pools[i]->signal_mu);
+    for (auto &sig : pools[i]->layer_signal) sig = 0;
+  }
+  return HICACHE_OK;
+}
+
+}  // namespace hicache
 
 extern "C" {
 
@@ -126,87 +218,26 @@ int hicache_plan_load_layers(hicache_plan *plan, const hicache_device_kv *kv, in
   const std::vector<void *> bufs(kv->buf_ptrs, kv->buf_ptrs + s.B * s.L);
   if (!plan->graph || plan->graph_bufs != bufs || plan->graph_pages != kv->device_num_pages ||
       plan->graph_layout != lay) {
-    // consecutive layers' kernels may run at the same time: no two buffers
-    // may share a byte
+    std::vector<std::pair<uintptr_t, uint64_t>> spans;
     const uint64_t buf_bytes = uint64_t(kv->device_num_pages) * uint64_t(s.PV) * 16u;
-    std::vector<uintptr_t> starts;
-    for (void *b : bufs) starts.push_back(reinterpret_cast<uintptr_t>(b));
-    std::sort(starts.begin(), starts.end());
-    for (size_t i = 1; i < starts.size(); ++i)
-      if (starts[i] - starts[i - 1] < buf_bytes)
-        return set_error(HICACHE_ERR_INVALID_ARG,
-                         "device buffers overlap: each of the %lld buffers must be %llu bytes of its own",
-                         (long long)bufs.size(), (unsigned long long)buf_bytes);
+    for (void *b : bufs) spans.emplace_back(reinterpret_cast<uintptr_t>(b), buf_bytes);
+    if ((rc = check_disjoint(spans))) return rc;
     if (plan->graph) {
       cudaGraphExecDestroy(plan->graph);
       plan->graph = nullptr;
     }
-    // Capture the L per-layer launches on a private stream, the kernels one
-    // after another.  Each layer's event is recorded (as an external event
-    // node) on a side branch that forks off after that layer's kernel, so the
-    // kernel chain itself has no node between consecutive launches.  Every
-    // kernel after the first is a programmatic dependent launch: it may start
-    // as the previous kernel moves its last tiles (the layers write different
-    // buffers and only read the host pool) and ends after it.  A layer's event
-    // node follows that layer's last kernel and the event node before it, so
-    // event l means layers 0..l have landed.
-    cudaStream_t cap = nullptr, side = nullptr;
-    std::vector<cudaEvent_t> forks(size_t(s.L) + 1, nullptr);
-    cudaError_t e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
-    for (auto &f : forks)
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
-    auto release = [&] {
-      for (auto f : forks)
-        if (f) cudaEventDestroy(f);
-      if (side) cudaStreamDestroy(side);
-      if (cap) cudaStreamDestroy(cap);
-    };
-    if (e != cudaSuccess) {
-      release();
-      return cuda_error(e, "setting up the layer-load capture");
-    }
-    const int64_t before = g_launches.load();
-    for (int64_t l = 0; l < s.L && rc == HICACHE_OK; ++l) {
-      rc = enqueue(pool, kv, plan->runs, nullptr, lay, int32_t(l), false, cap, l > 0);
-      if (rc != HICACHE_OK) break;
-      e = cudaEventRecord(forks[size_t(l)], cap);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(side, forks[size_t(l)], 0);
-      if (e == cudaSuccess) e = cudaEventRecordWithFlags(pool->events[size_t(l)], side, cudaEventRecordExternal);
-      if (e != cudaSuccess) rc = cuda_error(e, "capturing the layer event");
-    }
-    if (rc == HICACHE_OK) {                // join the side branch back
-      e = cudaEventRecord(forks[size_t(s.L)], side);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, forks[size_t(s.L)], 0);
-      if (e != cudaSuccess) rc = cuda_error(e, "joining the capture");
-    }
-    const int64_t captured = g_launches.load() - before;
-    g_launches.fetch_sub(captured);      // counted when replayed
-    cudaGraph_t graph = nullptr;
-    e = cudaStreamEndCapture(cap, &graph);
-    release();
-    if (rc == HICACHE_OK && e != cudaSuccess) rc = cuda_error(e, "cudaStreamEndCapture");
-    if (rc == HICACHE_OK) {
-      e = cudaGraphInstantiate(&plan->graph, graph, 0);
-      if (e != cudaSuccess) {
-        plan->graph = nullptr;
-        rc = cuda_error(e, "cudaGraphInstantiate");
-      }
-    }
-    if (graph) cudaGraphDestroy(graph);
+    int64_t launches = 0;
+    rc = capture_layer_graph(
+        &pool, 1, s.L,
+        [&](int64_t l, void *cap) { return enqueue(pool, kv, plan->runs, nullptr, lay, int32_t(l), false, cap, l > 0); },
+        &plan->graph, &launches);
     if (rc != HICACHE_OK) return rc;
     plan->graph_bufs = bufs;
     plan->graph_pages = kv->device_num_pages;
     plan->graph_layout = lay;
-    plan->graph_launches = captured;
+    plan->graph_launches = launches;
   }
-  const cudaError_t e = cudaGraphLaunch(plan->graph, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_error(e, "cudaGraphLaunch");
-  g_launches.fetch_add(plan->graph_launches, std::memory_order_relaxed);
-  std::lock_guard<std::mutex> gs(pool->signal_mu);
-  for (int64_t l = 0; l < s.L; ++l) pool->layer_signal[size_t(l)] = 0;
-  return HICACHE_OK;
+  return launch_layer_graph(plan->graph, plan->graph_launches, &pool, 1, stream);
 }
 
 int hicache_plan_destroy(hicache_plan *plan) {
