@@ -181,9 +181,10 @@ int hicache_pool_destroy(hicache_pool *pool);
  * host_num_pages (INDEX_RANGE); a backup may not name a host page twice and a
  * load may not name a device page twice (DUPLICATE_INDEX: the result would
  * depend on execution order); a source page may repeat.
- * Each call enqueues ceil(runs / 1536) kernel launches, where runs is the number
- * of maximal page runs contiguous on both sides; calls of up to 1536 pages are
- * exactly one launch. */
+ * Each call enqueues ceil(runs / ((3584 - B*L) / 2)) kernel launches, at most
+ * ceil(runs / 1536), where runs is the number of maximal page runs contiguous
+ * on both sides (a run is also cut where one buffer-layer slice of it would
+ * reach 32 GiB); calls of up to 1536 pages are exactly one launch. */
 
 /* L1 -> L2: every layer and buffer of the given device pages into the given
  * host pages. */
