@@ -183,8 +183,8 @@ int hicache_pool_destroy(hicache_pool *pool);
  * depend on execution order); a source page may repeat.
  * Each call enqueues ceil(runs / ((3584 - B*L) / 2)) kernel launches, at most
  * ceil(runs / 1536), where runs is the number of maximal page runs contiguous
- * on both sides (a run is also cut where one buffer-layer slice of it would
- * reach 32 GiB); calls of up to 1536 pages are exactly one launch. */
+ * on both sides (a run is also cut before its pages, counting every buffer
+ * and layer, reach 32 GiB); calls of up to 1536 pages are exactly one launch. */
 
 /* L1 -> L2: every layer and buffer of the given device pages into the given
  * host pages. */
