@@ -197,7 +197,10 @@ int hicache_load(hicache_pool *pool, const hicache_device_kv *kv, const int64_t 
                  const int64_t *host_pages, int64_t n, int32_t layout, void *stream);
 
 /* L2 -> L1 for one layer (every buffer of layer_id), then records the pool's
- * event for that layer on `stream`. */
+ * event for that layer on `stream`.  To load every layer of one set of pages
+ * this way, a plan's hicache_plan_load_layers does the same with one graph
+ * launch and overlaps consecutive layers (about 209 against 165 GB/s for
+ * 4K-token MLA loads on GB300). */
 int hicache_load_layer(hicache_pool *pool, const hicache_device_kv *kv,
                        const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                        int32_t layout, int32_t layer_id, void *stream);
