@@ -163,11 +163,20 @@ def _stream(stream) -> int:
 
 
 def _idx(a) -> np.ndarray:
+    if type(a) is np.ndarray and a.dtype == np.int64 and a.ndim == 1 and a.flags.c_contiguous:
+        return a
     return np.ascontiguousarray(np.asarray(a, dtype=np.int64).reshape(-1))
 
 
 def _ptr(a: np.ndarray):
-    return a.ctypes.data if a.size else None
+    """Address of a contiguous array's data (None when empty).  Through the
+    buffer protocol where the array is writable: a third of the cost of
+    ndarray.ctypes, which a small call pays twice."""
+    if not a.size:
+        return None
+    if a.flags.writeable:
+        return ctypes.addressof(ctypes.c_char.from_buffer(a))
+    return a.ctypes.data
 
 
 def version() -> int:
@@ -206,6 +215,7 @@ class DeviceKV:
         self._tensors = tensors
         self.struct = _DeviceKVStruct(ctypes.cast(self._arr, ctypes.POINTER(ctypes.c_void_p)),
                                       device_num_pages)
+        self.ref = ctypes.byref(self.struct)      # made once: every call passes it
         self.device_num_pages = device_num_pages
         self.num_buffers_total = len(ptrs)
 
@@ -255,7 +265,7 @@ def layer_checksum(kv: DeviceKV, pool_or_desc, device_pages, layer: int, out_ptr
     pages (every buffer, `reps` passes) into the device uint64 at out_ptr."""
     desc = pool_or_desc.desc if isinstance(pool_or_desc, Pool) else pool_or_desc
     dp = _idx(device_pages)
-    _check(library().hicache_layer_checksum(ctypes.byref(kv.struct), ctypes.byref(desc), _ptr(dp),
+    _check(library().hicache_layer_checksum(kv.ref, ctypes.byref(desc), _ptr(dp),
                                             dp.size, layer, reps, out_ptr, _stream(stream)))
 
 
@@ -404,8 +414,9 @@ class Pool:
             raise ValueError("device_pages and host_pages differ in length")
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        args = [self.handle, ctypes.byref(kv.struct), _ptr(dp), _ptr(hp), dp.size, layout]
-        _check(fn(*args, *extra, _stream(stream)))
+        rc = fn(self.handle, kv.ref, _ptr(dp), _ptr(hp), dp.size, layout, *extra, _stream(stream))
+        if rc:
+            _check(rc)
 
     def backup(self, kv: DeviceKV, device_pages, host_pages, layout=LAYOUT_POOL, stream=None):
         self._xfer(library().hicache_backup, kv, device_pages, host_pages, layout, stream)
@@ -431,7 +442,7 @@ class Pool:
             raise ValueError("device and host page lists differ in length")
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        _check(library().hicache_backup_load(self.handle, ctypes.byref(kv.struct), _ptr(bd), _ptr(bh), bd.size,
+        _check(library().hicache_backup_load(self.handle, kv.ref, _ptr(bd), _ptr(bh), bd.size,
                                              _ptr(ld), _ptr(lh), ld.size, layout, _stream(stream)))
 
     def page_span(self, host_page: int, buffer: int = -1):
@@ -498,7 +509,7 @@ class Engine:
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
         t = ctypes.c_uint64()
-        _check(library().hicache_engine_submit(self.handle, ctypes.byref(kv.struct), _ptr(dp), _ptr(hp), dp.size,
+        _check(library().hicache_engine_submit(self.handle, kv.ref, _ptr(dp), _ptr(hp), dp.size,
                                                direction, layout, 0 if after_stream is None else 1,
                                                _stream(after_stream), ctypes.byref(t)))
         return t.value
@@ -586,7 +597,7 @@ class Plan:
     def execute(self, kv: DeviceKV, layer: int = -1, layout=LAYOUT_POOL, stream=None):
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        _check(library().hicache_plan_execute(self.handle, ctypes.byref(kv.struct), layout, layer,
+        _check(library().hicache_plan_execute(self.handle, kv.ref, layout, layer,
                                               _stream(stream)))
 
     def load_layers(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
@@ -594,20 +605,20 @@ class Plan:
         from a CUDA graph the plan captures on first use."""
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        _check(library().hicache_plan_load_layers(self.handle, ctypes.byref(kv.struct), layout,
+        _check(library().hicache_plan_load_layers(self.handle, kv.ref, layout,
                                                   _stream(stream)))
 
     def load_layer(self, kv: DeviceKV, layer: int, layout=LAYOUT_POOL, stream=None):
         """Load one layer of a load plan and record that layer's event."""
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        _check(library().hicache_plan_load_layer(self.handle, ctypes.byref(kv.struct), layout, layer,
+        _check(library().hicache_plan_load_layer(self.handle, kv.ref, layout, layer,
                                                  _stream(stream)))
 
     def load_pipelined(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
         if isinstance(layout, str):
             layout = LAYOUTS[layout]
-        _check(library().hicache_plan_load_pipelined(self.handle, ctypes.byref(kv.struct), layout,
+        _check(library().hicache_plan_load_pipelined(self.handle, kv.ref, layout,
                                                      _stream(stream)))
 
     def info(self):
