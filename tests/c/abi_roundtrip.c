@@ -1,8 +1,8 @@
 /* A plain C caller of libhicache: a pool on huge-page pinned memory, a backup,
  * per-layer loads into fresh device pages with a compute stream waiting on the
  * layer events, a fused backup + load, a buffer group (a second pool with
- * 32-byte fp32 rows) backed up and then loaded back by one pipelined launch,
- * and the error path.  Every element is checked against a position pattern
+ * 32-byte fp32 rows) backed up and then loaded back by one pipelined launch
+ * and by a group plan's graph replay, and the error path.  Every element is checked against a position pattern
  * (round trip = identity).  Prints "ok". */
 #include <stdint.h>
 #include <stdio.h>
@@ -134,23 +134,37 @@ int main(void) {
     CHECK(hicache_wait_layer(pool, l, comp));
     CHECK(hicache_wait_layer(pool2, l, comp));
   }
+  /* the same host pages once more through a group plan: layer by layer,
+   * replayed from one CUDA graph, each layer's event in both pools */
+  const int64_t dst4[N] = {0, 1, 2, 6, 7, 8, 10, 11};
+  hicache_group_plan *gplan = NULL;
+  CHECK(hicache_group_plan_create(group, 2, dst4, hp3, N, Dp, &gplan));
+  CHECK(hicache_group_plan_load_layers(gplan, kvs, HICACHE_LAYOUT_POOL, xfer));
+  for (int l = 0; l < L; ++l) {
+    CHECK(hicache_wait_layer(pool, l, comp));
+    CHECK(hicache_wait_layer(pool2, l, comp));
+  }
   CHECK(hicache_wait(comp, -1));
   CHECK(hicache_wait(xfer, -1));
-  for (int k = 0; k < NB; ++k) {
-    if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
-    for (int i = 0; i < N; ++i)
-      for (int64_t t = 0; t < P; ++t)
-        for (int64_t e = 0; e < R; ++e)
-          if (h[(dst3[i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 6;
-  }
-  for (int l = 0; l < L; ++l) {
-    if (cudaMemcpy(h2, bufs2[l], buf2_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
-    for (int i = 0; i < N; ++i)
-      for (int64_t t = 0; t < P; ++t)
-        for (int64_t e = 0; e < R2; ++e) {
-          const uint32_t want = 0x9E3779B9u * (uint32_t)(l + 1) + (uint32_t)((src[i] * P + t) * R2 + e);
-          if (h2[(dst3[i] * P + t) * R2 + e] != want) return 7;
-        }
+  CHECK(hicache_group_plan_destroy(gplan));
+  const int64_t *dsts[2] = {dst3, dst4};
+  for (int v = 0; v < 2; ++v) {
+    for (int k = 0; k < NB; ++k) {
+      if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+      for (int i = 0; i < N; ++i)
+        for (int64_t t = 0; t < P; ++t)
+          for (int64_t e = 0; e < R; ++e)
+            if (h[(dsts[v][i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 6;
+    }
+    for (int l = 0; l < L; ++l) {
+      if (cudaMemcpy(h2, bufs2[l], buf2_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+      for (int i = 0; i < N; ++i)
+        for (int64_t t = 0; t < P; ++t)
+          for (int64_t e = 0; e < R2; ++e) {
+            const uint32_t want = 0x9E3779B9u * (uint32_t)(l + 1) + (uint32_t)((src[i] * P + t) * R2 + e);
+            if (h2[(dsts[v][i] * P + t) * R2 + e] != want) return 7;
+          }
+    }
   }
   CHECK(hicache_pool_destroy(pool2));
   CHECK(hicache_host_free(host2));
