@@ -1,6 +1,7 @@
 """Seeded random buffer groups: 1-4 pools with random buffer counts, row sizes
-and element sizes, random pages and operations; every pool compared byte for
-byte with the oracle's transfer of that pool (GB300)."""
+and element sizes, random pages and operations (group calls and group plans);
+every pool compared byte for byte with the oracle's transfer of that pool
+(GB300)."""
 import numpy as np
 import pytest
 import torch
@@ -34,7 +35,8 @@ def draw(seed):
         dp = rng.choice(Dp, n, replace=False)
     hp = rng.choice(min(Hps), n, replace=False)
     return dict(L=L, P=P, Dp=Dp, Hps=Hps, kinds=kinds, dp=dp, hp=hp, layout=int(rng.integers(0, 4)),
-                op=str(rng.choice(["backup", "load", "load_layer", "pipelined"])),
+                op=str(rng.choice(["backup", "load", "load_layer", "pipelined", "plan_all", "plan_layer",
+                                   "plan_graph"])),
                 layer=int(rng.integers(0, L)))
 
 
@@ -63,8 +65,18 @@ def test_random_group(seed):
         hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, layout=layout, stream=s)
     elif c["op"] == "load_layer":
         hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, layer=c["layer"], layout=layout, stream=s)
-    else:
+    elif c["op"] == "pipelined":
         hc.group_load_pipelined(pools, kvs, dp, hp, layout=layout, stream=s)
+    else:
+        plan = hc.group_plan(pools, dp, hp, Dp)
+        if c["op"] == "plan_all":
+            plan.execute(kvs, layout=layout, stream=s)
+        elif c["op"] == "plan_layer":
+            plan.execute(kvs, layer=c["layer"], layout=layout, stream=s)
+        else:
+            plan.load_layers(kvs, layout=layout, stream=s)
+        hc.wait(s, TEN_S)
+        plan.close()
     hc.wait(s, TEN_S)
     for i, (pool, bufs, (B, R, es), h) in enumerate(zip(pools, bufsets, c["kinds"], c["Hps"])):
         want_host = host0[i].view(gh.NP_DT[es]).copy()
@@ -72,7 +84,7 @@ def test_random_group(seed):
         if c["op"] == "backup":
             gh.orc().backup(dev0[i], want_host, B, L, P, R, h, dp, hp, layout)
         else:
-            layer = c["layer"] if c["op"] == "load_layer" else -1
+            layer = c["layer"] if c["op"] in ("load_layer", "plan_layer") else -1
             gh.orc().load(want_dev, host0[i].view(gh.NP_DT[es]), B, L, P, R, h, dp, hp, layout, layer)
         assert np.array_equal(pool.host_array(gh.NP_DT[es]), want_host), (c, i)
         got = gh.to_np(bufs, es)
