@@ -147,6 +147,7 @@ void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, hicache::X
   h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
   h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
   h.job[1] = hicache::Job{0, nb, 0, 0, 0u, 0u};
+  h.wait_previous = 0;
 }
 
 // Header fields shared by every launch of a pool, and its buffer pointers.
@@ -217,9 +218,17 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
                                    : pool->layer_ctas;
     x.grid = int(std::min<int64_t>(tiles, ctas));
     x.stream = stream;
-    // the launches of one call move disjoint destinations: each after the
-    // first may start as the one before it drains
-    x.pdl = (next0 == 0 && next1 == 0) ? pdl_first : true;
+    // The launches of one call move disjoint destinations: each after the
+    // first is programmatic and starts work as the one before it drains.  The
+    // first launch of a one-layer load is programmatic too: it follows work
+    // it may depend on and waits for it before touching memory, unless the
+    // caller knows that work is a one-layer load of another layer
+    // (pdl_first); that hides the launch of a short per-layer kernel.  The
+    // first launch of any other call is plain (it runs long enough that its
+    // launch does not show, and a plain launch places its CTAs on an idle GPU).
+    const bool first = next0 == 0 && next1 == 0;
+    x.pdl = !first || !all;
+    h.wait_previous = first && !all && !pdl_first ? 1 : 0;
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

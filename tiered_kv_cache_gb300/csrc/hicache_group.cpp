@@ -73,7 +73,8 @@ int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int3
     x.to_host = to_host;
     x.grid = int(std::min<int64_t>(tiles, to_host ? p0->backup_ctas : all ? p0->ctas : p0->layer_ctas));
     x.stream = stream;
-    x.pdl = next > 0 ? true : pdl_first;  // disjoint destinations: overlap the previous launch's drain
+    x.pdl = next > 0 || !all;          // as enqueue
+    g.h[0].wait_previous = next == 0 && !all && !pdl_first ? 1 : 0;
     const int e = hicache::launch_group(x);
     if (e != 0) return cuda_error(cudaError_t(e), "group transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -116,6 +116,9 @@ struct XferHeader {
   FastDiv fd_V, fd_PV, fd_LV, fd_LPV, fd_BLPV;
   Job job[2];                 // [0]: the transfer (the backup of a bidirectional
                               // launch); [1]: the load of a bidirectional launch
+  int32_t wait_previous;      // nonzero: the launch was started early behind work
+                              // it may depend on; it waits for that work to finish
+                              // before it touches memory
 };
 
 template <int WORDS>

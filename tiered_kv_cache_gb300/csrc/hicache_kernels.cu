@@ -60,13 +60,17 @@ namespace {
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
 
-// Programmatic dependent launch.  Consecutive launches of one call (a run
+// Programmatic dependent launch.  Each CTA allows the next launch on the
+// stream on reaching its last tile.  Consecutive launches of one call (a run
 // table larger than one parameter block, or one layer after another in a
-// per-layer graph) move disjoint destinations, so the next may start while
-// this one drains: each CTA allows it on reaching its last tile.  A launch
-// started that way finishes only after the one before it has (the wait at the
-// end of the kernel), so whatever follows the call on the stream still sees
-// every launch of it complete.  Both are no-ops for a kernel launched plainly.
+// per-layer graph) move disjoint destinations, so the next starts work while
+// this one drains.  A launch started that way finishes only after the one
+// before it has (the wait at the end of the kernel), so whatever follows the
+// call on the stream still sees every launch of it complete.  The first
+// launch of a one-layer load is programmatic as well, behind work it may
+// depend on: it waits for that work before touching memory (wait_previous),
+// which keeps plain stream order and hides only the launch itself.  The waits
+// are no-ops for a kernel launched plainly.
 __device__ __forceinline__ void allow_next_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -225,6 +229,7 @@ template <int LAYOUT, bool ALL, bool TO_HOST, class Params>
 __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ Params p) {
   __shared__ uint4 *s_bufs[kMaxBufs];
   load_buffer_table(p, s_bufs);
+  if (p.h.wait_previous) finish_after_previous_launch();
   const Job &job = p.h.job[0];
   const Run *runs = job_runs(p, 0);
   for (int32_t g = blockIdx.x; g < job.total_tiles; g += gridDim.x) {
@@ -242,6 +247,7 @@ template <int LAYOUT, class Params>
 __global__ void __launch_bounds__(kThreads) bidir_kernel(const __grid_constant__ Params p) {
   __shared__ uint4 *s_bufs[kMaxBufs];
   load_buffer_table(p, s_bufs);
+  if (p.h.wait_previous) finish_after_previous_launch();
   const Job &jb = p.h.job[0];
   const Job &jl = p.h.job[1];
   const Run *rb = job_runs(p, 0);
@@ -276,6 +282,7 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__
   for (int i = threadIdx.x; i < p.g.num_bufs; i += kThreads)
     s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
   __syncthreads();
+  if (p.g.h[0].wait_previous) finish_after_previous_launch();
   const int32_t total = p.g.tile_start[p.g.njobs];
   for (int32_t g = blockIdx.x; g < total; g += gridDim.x) {
     if (g + int32_t(gridDim.x) >= total) allow_next_launch();
