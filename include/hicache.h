@@ -57,7 +57,8 @@
  *     (more page runs than one launch's parameters hold) and the layers of a
  *     per-layer graph replay start each launch as the one before it drains;
  *     the call still completes, for whatever follows it on the stream, only
- *     once every launch of it has.  A kernel of the caller's that is launched
+ *     once every launch of it has.  A one-layer load is launched early behind
+ *     the work before it and waits for that work before touching memory.  A kernel of the caller's that is launched
  *     programmatically (programmatic stream serialization) right behind a
  *     transfer may likewise start while the transfer's last tiles move: as
  *     for any programmatic launch, it must call cudaGridDependencySynchronize
