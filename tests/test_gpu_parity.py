@@ -740,3 +740,38 @@ def test_split_call_is_complete_for_the_next_work_on_the_stream(op):
             hc.wait(s, 10_000_000)
             got = [int(v) & (2**64 - 1) for v in sums.tolist()]
             assert got == expect, rep
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
+def test_layer_load_right_after_a_backup_of_the_same_pages(layout):
+    """A one-layer load starts early behind the kernel before it and must wait
+    for it before touching memory.  Here that kernel is a backup that reads the
+    very device pages the load overwrites (and lets the next launch in during
+    its last tiles): the backup must still see the old contents, and every
+    layer load must land, for each layer in turn, on one stream."""
+    B, L, P, R, Dp, Hp, n = 2, 4, 16, 128, 64, 96, 40
+    rng = np.random.default_rng(130 + layout)
+    dp = rng.permutation(Dp)[:n]
+    h_old = rng.permutation(Hp)[:n]
+    h_new = np.setdiff1d(np.arange(Hp), h_old)[:n]
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=131 + layout)
+    with hc.Pool(L, B, P, R, Hp, layout) as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        kv = hc.DeviceKV(bufs, Dp)
+        s = torch.cuda.Stream()
+        for layer in range(L):
+            torch.cuda.synchronize()
+            dev0 = gh.to_np(bufs, 2)
+            host0 = host.view(np.uint16).copy()
+            pool.backup(kv, dp, h_old, stream=s)            # reads pages dp of every layer
+            pool.load_layer(kv, dp, h_new, layer, stream=s)  # overwrites pages dp of one layer
+            hc.wait(s, 10_000_000)
+            want_host = host0.copy()
+            gh.orc().backup(dev0, want_host, B, L, P, R, Hp, dp, h_old, layout)
+            assert np.array_equal(host.view(np.uint16), want_host), layer
+            want_dev = [x.copy() for x in dev0]
+            gh.orc().load(want_dev, want_host, B, L, P, R, Hp, dp, h_new, layout, layer)
+            got = gh.to_np(bufs, 2)
+            for k in range(B * L):
+                assert np.array_equal(got[k], want_dev[k]), (layer, k)
