@@ -309,3 +309,21 @@ def test_prepass_duplicate_check_beyond_the_bitmap():
     ok = np.array([(1 << 28) + 4 - k for k in range(41)], np.int64)
     runs = hc.prepass(100, Dp, ok, np.arange(41), hc.LOAD)
     assert np.array_equal(runs, py_runs(ok, np.arange(41, dtype=np.int64)))
+
+
+def test_index_marshalling_fast_paths():
+    """1-D contiguous int64 arrays pass through unchanged; anything else is
+    converted; pointers come from the buffer protocol or, for a read-only
+    array, from ndarray.ctypes, and are the array's own data address."""
+    a = np.arange(5, dtype=np.int64)
+    assert hc._idx(a) is a
+    for other in ([1, 2, 3], np.arange(4, dtype=np.int32), np.arange(6, dtype=np.int64).reshape(2, 3),
+                  np.arange(10, dtype=np.int64)[::2]):
+        out = hc._idx(other)
+        assert out.dtype == np.int64 and out.ndim == 1 and out.flags.c_contiguous
+        assert np.array_equal(out, np.asarray(other).reshape(-1))
+    assert hc._ptr(a) == a.ctypes.data
+    ro = np.arange(3, dtype=np.int64)
+    ro.flags.writeable = False
+    assert hc._ptr(ro) == ro.ctypes.data
+    assert hc._ptr(a[:0]) is None
