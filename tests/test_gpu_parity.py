@@ -631,8 +631,8 @@ def test_plan_load_layers_of_an_empty_plan_records_every_event():
 @pytest.mark.parametrize("layout", LAYOUTS, ids=list(hc.LAYOUTS))
 def test_plan_load_layers_graph_with_split_layers(layout):
     """A plan of 4,000 scattered one-token pages needs several launches per
-    layer.  In the graph only the first launch of each layer may start while
-    the previous layer drains; the chunks of one layer follow one another.  The
+    layer.  In the graph every launch may start while the one before it drains
+    (the next chunk of a layer, or the next layer) and ends after it.  The
     replay must equal the oracle's load, three times over."""
     B, L, P, R, Dp, Hp, n = 2, 3, 1, 8, 9000, 9000, 4000
     rng = np.random.default_rng(80 + layout)
