@@ -6,9 +6,12 @@ pre-pass, kernels) runs in the C/CUDA library.  There is no fallback: if the
 library is not built, importing works but every call raises.
 
 Names follow the C ABI in ``include/hicache.h``:
-    Pool.backup / Pool.load / Pool.load_layer / Pool.wait_layer
-    Pool.plan(...) -> Plan.execute(...)
-    host_alloc / host_free, wait, prepass, segment_count, layer_checksum
+    Pool.backup / Pool.load / Pool.load_layer / Pool.load_pipelined / Pool.backup_load
+    Pool.wait_layer / Pool.layer_event
+    Pool.plan(...) -> Plan.execute / load_layer / load_layers / load_pipelined
+    group_transfer / group_load_pipelined / group_plan(...) -> GroupPlan
+    Engine (submission engine), PageAllocator (host pages)
+    host_alloc / host_free, wait, prepass, segment_count, page_span, layer_checksum
 """
 from __future__ import annotations
 
@@ -21,7 +24,8 @@ import numpy as np
 __all__ = [
     "HiCacheError", "LAYER_FIRST", "PAGE_FIRST", "PAGE_FIRST_DIRECT", "LAYOUT_POOL", "LAYOUTS",
     "BACKUP", "LOAD", "library", "library_path", "PoolDesc", "DeviceKV", "Pool", "Plan", "PinnedHost",
-    "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "MAX_GROUP",
+    "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "group_plan", "GroupPlan",
+    "MAX_GROUP", "PAGE_FIRST_DIRECT_KV",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
     "launch_count", "version",
 ]
