@@ -237,8 +237,14 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
  * recorded too, once the whole load is in.  Checks as hicache_load.  A
  * pipelined load may only go on another stream than the pool's previous one
  * once that one's pipelined loads have finished (INVALID_ARG otherwise): the
- * per-layer counts must rise in load order.  CUDA if the driver offers no
- * stream memory wait. */
+ * per-layer counts must rise in load order.  A stream that is being captured
+ * into a CUDA graph is refused (INVALID_ARG, nothing enqueued): the value each
+ * layer's counter must reach is raised on the host when the call is enqueued,
+ * so a graph replayed twice, or never, would leave hicache_wait_layer passing
+ * early or waiting forever.  If a call split over several launches fails on a
+ * launch after the first, the launches before it stay enqueued and
+ * hicache_wait_layer waits for them.  CUDA if the driver offers no stream
+ * memory wait. */
 int hicache_load_pipelined(hicache_pool *pool, const hicache_device_kv *kv,
                            const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                            int32_t layout, void *stream);
@@ -286,6 +292,11 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
  *   - More than 256 layers: INVALID_ARG, nothing enqueued.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     A capturing stream is refused, as for hicache_load_pipelined.
+ *   - The address and the counts belong to the device's context: after a
+ *     cudaDeviceReset in the same process the counts start again from zero
+ *     while the library's targets keep their values, so do not use this entry
+ *     point on a device after resetting it.
  *   - Every call on a device shares the array and leaves its counts there;
  *     the library tracks the values they reach, so nothing needs clearing
  *     between calls.  Calls whose loads overlap on the GPU (e.g. on two

@@ -187,3 +187,44 @@ def test_tile_counter_covers_every_tile_and_resets(ctas):
             for layer in range(L):
                 done, target = pool.pipeline_status(layer)
                 assert done == target
+
+
+def test_pipelined_loads_refuse_a_capturing_stream():
+    """A pipelined load raises each layer's target on the host when it is
+    enqueued, so a captured call (replayed any number of times, or never) would
+    leave the per-layer waits wrong.  Every pipelined entry point refuses a
+    capturing stream with INVALID_ARG and enqueues nothing."""
+    B, L, P, R, Dp, Hp, n = 1, 3, 16, 64, 32, 32, 8
+    rng = np.random.default_rng(330)
+    dp = rng.choice(Dp, n, replace=False)
+    hp = rng.choice(Hp, n, replace=False)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=330)
+    kv = hc.DeviceKV(bufs, Dp)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        s = torch.cuda.Stream()
+        pool.load_pipelined(kv, dp, hp, stream=s)          # a plain call first
+        s.synchronize()
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        before = [pool.pipeline_status(layer) for layer in range(L)]
+        marker = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        codes = []
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for call in (lambda: pool.load_pipelined(kv, dp, hp, stream=s),
+                         lambda: plan.load_pipelined(kv, stream=s),
+                         lambda: hc.group_load_pipelined([pool], [kv], dp, hp, stream=s)):
+                try:
+                    call()
+                    codes.append(0)
+                except hc.HiCacheError as e:
+                    codes.append(e.code)
+            marker.add_(1)                                 # keeps the captured graph non-empty
+        assert codes == [-1, -1, -1]
+        assert hc.launch_count() == c0
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(marker.item()) == 1
+        assert [pool.pipeline_status(layer) for layer in range(L)] == before
+        plan.close()

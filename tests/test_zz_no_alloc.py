@@ -109,3 +109,38 @@ def test_noalloc_load_refuses_more_layers_than_it_holds():
         assert rc == -1
         assert "256" in hc.library().hicache_last_error().decode()
         assert hc.launch_count() == c0
+
+
+def test_noalloc_load_refuses_a_capturing_stream():
+    """Its per-layer targets are raised on the host when the call is enqueued,
+    so a captured call would leave the per-layer waits wrong: a capturing
+    stream gets INVALID_ARG and nothing is enqueued.  (The first call on the
+    device, which looks up the array's address, comes before the capture.)"""
+    B, L, P, R, Dp, Hp, n = 1, 3, 16, 64, 32, 32, 8
+    rng = np.random.default_rng(530)
+    dp = rng.choice(Dp, n, replace=False)
+    hp = rng.choice(Hp, n, replace=False)
+    bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]
+    kv = hc.DeviceKV(bufs, Dp)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        s = torch.cuda.Stream()
+        assert noalloc_load(pool, kv, dp, hp, s) == 0, hc.library().hicache_last_error()
+        hc.wait(s, TEN_S)
+        marker = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rc = noalloc_load(pool, kv, dp, hp, s)
+            marker.add_(1)
+        assert rc == -1
+        assert b"captur" in hc.library().hicache_last_error()
+        assert hc.launch_count() == c0
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(marker.item()) == 1
+        # the waits still match the plain call that ran
+        comp = torch.cuda.Stream()
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+        hc.wait(comp, TEN_S)

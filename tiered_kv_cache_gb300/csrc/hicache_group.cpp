@@ -252,6 +252,7 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
   thread_local std::vector<RunRec> runs;
   if ((rc = prepass(Hp, Dp, device_pages, host_pages, n, HICACHE_DIR_LOAD, max_run, &runs))) return rc;
   if ((rc = check_device(pools[0]))) return rc;
+  if ((rc = refuse_capture(stream))) return rc;
   if (!wait_value32())
     return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
   // every pool's signal lock, in address order (the pools are distinct)

@@ -116,6 +116,9 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
 // (hicache_pipeline.cpp).
 int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
                       int32_t layout, void *stream);
+// INVALID_ARG if `stream` is capturing (pipelined loads keep their per-layer
+// targets on the host, raised at enqueue time), CUDA if that cannot be told.
+int refuse_capture(void *stream);
 
 // hicache_plan.cpp: per-layer graphs.
 // INVALID_ARG unless the (address, bytes) spans are pairwise disjoint.

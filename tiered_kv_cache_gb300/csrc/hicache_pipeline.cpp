@@ -32,9 +32,25 @@ WaitValue32Fn wait_value32() {
   return fn;
 }
 
+// Pipelined loads raise each layer's target on the host when the call is
+// enqueued, while the device counters rise each time the kernel runs.  A call
+// captured into a graph would raise the targets once however often the graph
+// is replayed (and never catch up if it is not launched), so hicache_wait_layer
+// would pass too early or wait forever.  They refuse a capturing stream.
+int refuse_capture(void *stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &st);
+  if (e != cudaSuccess) return cuda_error(e, "cudaStreamIsCapturing");
+  if (st != cudaStreamCaptureStatusNone)
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "pipelined loads cannot be captured: their per-layer targets are kept on the host");
+  return HICACHE_OK;
+}
+
 int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
                       int32_t layout, void *stream) {
   if (int rc = check_device(pool)) return rc;
+  if (int rc = refuse_capture(stream)) return rc;
   if (!wait_value32())
     return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
   std::lock_guard<std::mutex> g(pool->signal_mu);
@@ -148,6 +164,7 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
                     max_run_pages(s), &runs)))
     return rc;
   if ((rc = check_device(pool))) return rc;
+  if ((rc = refuse_capture(stream))) return rc;
   if (!wait_value32())
     return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
   unsigned int *counters = nullptr;
@@ -159,6 +176,8 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
   std::lock_guard<std::mutex> gg(g_noalloc_mu);
   std::lock_guard<std::mutex> g(pool->signal_mu);
   uint32_t *target = g_noalloc_target[pool->device];
+  pool->noalloc_done = counters;
+  if (pool->noalloc_target.size() != size_t(s.L)) pool->noalloc_target.assign(size_t(s.L), 0);
   size_t next = 0;
   while (next < runs.size()) {
     const int32_t c = fill_job(runs, next, s.PV, s.B, (hicache::kBlobWords - nb) / 2, params, nb, 0, s.L);
@@ -177,14 +196,14 @@ int hicache_load_pipelined_noalloc(hicache_pool *pool, const hicache_device_kv *
     const int e = hicache::launch_pipelined_load(x, counters, sched);
     if (e != 0) return cuda_error(cudaError_t(e), "pipelined load kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    for (int64_t l = 0; l < s.L; ++l) target[l] += uint32_t(params.h.job[0].total_tiles);
+    // the targets follow every launch that went out, so that a launch error
+    // later in a split call leaves waits that cover the launches before it
+    for (int64_t l = 0; l < s.L; ++l) {
+      target[l] += uint32_t(params.h.job[0].total_tiles);
+      pool->noalloc_target[size_t(l)] = target[l];
+      pool->layer_signal[size_t(l)] = 2;
+    }
     next += size_t(c);
-  }
-  pool->noalloc_done = counters;
-  if (pool->noalloc_target.size() != size_t(s.L)) pool->noalloc_target.assign(size_t(s.L), 0);
-  for (int64_t l = 0; l < s.L; ++l) {
-    pool->noalloc_target[size_t(l)] = target[l];
-    pool->layer_signal[size_t(l)] = 2;
   }
   for (int64_t l = 0; l < s.L; ++l) {
     const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
