@@ -12,6 +12,7 @@ import tiered_kv_cache_gb300 as hc
 from tiered_kv_cache_gb300 import build as hc_build
 from tiered_kv_cache_gb300 import workloads as wl
 
+import fullsize as fs
 import gpu_helpers as gh
 
 pytestmark = pytest.mark.gpu
@@ -677,11 +678,15 @@ def test_plan_load_layers_last_event_means_every_layer():
         s, comp = torch.cuda.Stream(), torch.cuda.Stream()
         sums = torch.zeros(L, dtype=torch.int64, device="cuda")
         # the expected per-layer sums, from a plain all-layer load checked
-        # against the oracle on sampled elements
+        # against the oracle in every device buffer
+        mirror = fs.DeviceMirror(bufs)
+        mirror.pull(bufs)
         pool.load(kv, t.device_pages, t.host_pages)
         torch.cuda.synchronize()
-        assert gh.sampled_host_check(host.view(np.uint16), bufs, t.device_pages, t.host_pages, hc.PAGE_FIRST,
-                                     B, L, P, R, Hp, 20000, 92)
+        fs.oracle_load(mirror.np, host.view(np.uint16), B, L, P, R, Hp, t.device_pages, t.host_pages,
+                       hc.PAGE_FIRST)
+        mirror.compare(bufs, "all-layer load of 64K tokens")
+        mirror.close()
         for layer in range(L):
             hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer)
         torch.cuda.synchronize()

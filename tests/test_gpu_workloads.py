@@ -1,11 +1,12 @@
-"""The four large workload shapes at their full sizes, on the GPU, in the launch
+"""The large workload shapes at their full sizes, on the GPU, in the launch
 configuration the benchmark times (automatic grid).
 
-Full pools are too large for the oracle to redo in seconds, so each transfer is
-checked on sampled elements whose host and device offsets come from the oracle
-one by one, plus properties that hold at any size: untouched pages keep their
-sentinel, a backup followed by a load is the identity, every call of up to
-1536 pages is one launch."""
+Every transfer is compared with the oracle element by element over the WHOLE
+host pool and EVERY device buffer: the oracle runs over disjoint groups of the
+call's page pairs on all host cores (tests/fullsize.py), so untouched bytes are
+checked as well as moved ones.  On top of that: a backup followed by a load is
+the identity, per-layer checksums taken behind each layer's signal equal those
+of the oracle's result, and every call of up to 1536 pages is one launch."""
 import numpy as np
 import pytest
 import torch
@@ -14,11 +15,12 @@ import tiered_kv_cache_gb300 as hc
 from tiered_kv_cache_gb300 import build as hc_build
 from tiered_kv_cache_gb300 import workloads as wl
 
+import fullsize as fs
 import gpu_helpers as gh
 
 pytestmark = pytest.mark.gpu
 
-SENT16 = 0xC3C3          # never a normal(0,1) bf16 (it is about -390)
+SENT8 = 0xC3             # 0xC3C3 is never a normal(0,1) bf16 (it is about -390)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,62 +33,45 @@ def gpu():
     torch.cuda.empty_cache()
 
 
-def position_fill(words: np.ndarray, chunk=1 << 26):
-    """Host pool words = their own index mod 2^32: a misplaced copy is visible."""
-    for off in range(0, words.size, chunk):
-        m = min(chunk, words.size - off)
-        words[off:off + m] = np.arange(off, off + m, dtype=np.uint64).astype(np.uint32)
-
-
-def count_equal(a: np.ndarray, value, chunk=1 << 27) -> int:
-    return sum(int(np.count_nonzero(a[o:o + chunk] == value)) for o in range(0, a.size, chunk))
-
-
 def device_pool(shape: wl.KVShape):
     vals = wl.kv_values(shape, device="cuda")
     return [v.view(torch.int16) for v in vals]
 
 
-def untouched_pages_ok(bufs, P, moved, sentinel16):
-    Dp = bufs[0].shape[0] // P
-    mask = torch.ones(Dp, dtype=torch.bool, device="cuda")
-    mask[torch.as_tensor(np.asarray(moved), device="cuda")] = False
-    s = torch.tensor(sentinel16, dtype=torch.int32).to(torch.int16).item()
-    for b in bufs:
-        rows = b.view(Dp, -1)[mask]
-        if rows.numel() and not bool((rows == s).all()):
-            return False
-    return True
+def dims(s: wl.KVShape):
+    return s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
 
 
-def run_backup_load(pool, bufs, shape, dp, hp, layout, samples=20000, seed=0):
-    B, L, P, R, Hp = shape.num_buffers, shape.num_layers, shape.page_size, shape.row_elems, shape.host_pages
-    Dp = bufs[0].shape[0] // P
-    kv = hc.DeviceKV(bufs, Dp)
+def check_backup(pool, bufs, mirror, exp_host, s, dp, hp, layout):
+    """Backup over a sentinel host pool; the whole pool against the oracle."""
+    B, L, P, R, Hp = dims(s)
     host = pool.host_array(np.uint16)
-    # backup
-    host.view(np.uint8)[:] = 0xC3
+    fs.fill(host.view(np.uint8), SENT8)
+    fs.fill(exp_host.view(np.uint8), SENT8)
     c0 = hc.launch_count()
-    pool.backup(kv, dp, hp, layout)
+    pool.backup(hc.DeviceKV(bufs, s.device_pages), dp, hp, layout)
     torch.cuda.synchronize()
     assert hc.launch_count() - c0 == 1
-    assert gh.sampled_host_check(host, bufs, dp, hp, layout, B, L, P, R, Hp, samples, seed)
-    moved_words = len(dp) * B * L * P * R
-    assert count_equal(host, SENT16) == host.size - moved_words
-    # load into sentinel-filled device pages from a position-coded host pool
-    keep = [b.clone() for b in bufs]
-    position_fill(host.view(np.uint32))
-    gh.sentinel_fill(bufs, 0xC3)
+    mirror.pull(bufs)
+    fs.oracle_backup(mirror.np, exp_host, B, L, P, R, Hp, dp, hp, layout)
+    fs.assert_equal(host, exp_host, f"backup, layout {layout}")
+
+
+def check_load(pool, bufs, mirror, s, dp, hp, layout, salt):
+    """Load from a position-coded host pool into sentinel device buffers;
+    every device buffer against the oracle."""
+    B, L, P, R, Hp = dims(s)
+    host = pool.host_array(np.uint16)
+    fs.position_fill(host.view(np.uint32), salt)
+    gh.sentinel_fill(bufs, SENT8)
     torch.cuda.synchronize()
     c0 = hc.launch_count()
-    pool.load(kv, dp, hp, layout)
+    pool.load(hc.DeviceKV(bufs, s.device_pages), dp, hp, layout)
     torch.cuda.synchronize()
     assert hc.launch_count() - c0 == 1
-    assert gh.sampled_host_check(host, bufs, dp, hp, layout, B, L, P, R, Hp, samples, seed + 1)
-    assert untouched_pages_ok(bufs, P, dp, SENT16)
-    for b, k in zip(bufs, keep):
-        b.copy_(k)
-    del keep
+    mirror.fill(SENT8)
+    fs.oracle_load(mirror.np, host, B, L, P, R, Hp, dp, hp, layout)
+    mirror.compare(bufs, f"load, layout {layout}")
 
 
 @pytest.mark.parametrize("shuffled_host", [False, True], ids=["host_contiguous", "host_shuffled"])
@@ -94,10 +79,17 @@ def test_llama3_8b_32k_all_layouts(shuffled_host):
     s = wl.LLAMA3_8B
     t = wl.llama_transfer(s, 512, shuffled_host=shuffled_host)
     bufs = device_pool(s)
-    with hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
-                 "layer_first") as pool:
+    keep = [b.clone() for b in bufs]
+    mirror = fs.DeviceMirror(bufs)
+    B, L, P, R, Hp = dims(s)
+    with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
+        exp_host = np.empty_like(pool.host_array(np.uint16))
         for layout in hc.LAYOUTS.values():
-            run_backup_load(pool, bufs, s, t.device_pages, t.host_pages, layout, seed=layout)
+            check_backup(pool, bufs, mirror, exp_host, s, t.device_pages, t.host_pages, layout)
+            check_load(pool, bufs, mirror, s, t.device_pages, t.host_pages, layout, salt=layout)
+            for b, k in zip(bufs, keep):
+                b.copy_(k)
+        del exp_host
         # round trip through the host into other device pages is the identity
         src = t.device_pages
         rest = np.setdiff1d(np.arange(s.device_pages), src)[: len(src)]
@@ -106,65 +98,91 @@ def test_llama3_8b_32k_all_layouts(shuffled_host):
             pool.backup(kv, src, t.host_pages, layout)
             pool.load(kv, rest, t.host_pages, layout)
             torch.cuda.synchronize()
-            P = s.page_size
             si = torch.as_tensor(src, device="cuda")
             di = torch.as_tensor(rest, device="cuda")
             for b in bufs:
                 v = b.view(s.device_pages, -1)
                 assert torch.equal(v[si], v[di])
-    del bufs
+    mirror.close()
+    del bufs, keep
     torch.cuda.empty_cache()
 
 
 def test_deep78_32k_bidirectional():
+    """Backup of request A and load of request B at the same time, on two
+    streams and as one fused launch, in every layout: the whole host pool and
+    every device buffer against the oracle applying both (they commute: the
+    requests are disjoint on both sides)."""
     s = wl.DEEP_STRESS
     a, b_req = wl.deep_bidir_transfers(s, 512)
     bufs = device_pool(s)
-    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    B, L, P, R, Hp = dims(s)
     kv = hc.DeviceKV(bufs, s.device_pages)
+    mirror = fs.DeviceMirror(bufs)
     with hc.Pool(L, B, P, R, Hp, "page_first_direct") as pool:
         host = pool.host_array(np.uint16)
+        exp_host = np.empty_like(host)
+        run = 0
         for layout in hc.LAYOUTS.values():
-            position_fill(host.view(np.uint32))
-            s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-            c0 = hc.launch_count()
-            pool.backup(kv, a.device_pages, a.host_pages, layout, stream=s1)
-            pool.load(kv, b_req.device_pages, b_req.host_pages, layout, stream=s2)
-            torch.cuda.synchronize()
-            assert hc.launch_count() - c0 == 2
-            assert gh.sampled_host_check(host, bufs, a.device_pages, a.host_pages, layout, B, L, P, R, Hp,
-                                         20000, 10 + layout)
-            assert gh.sampled_host_check(host, bufs, b_req.device_pages, b_req.host_pages, layout, B, L, P,
-                                         R, Hp, 20000, 20 + layout)
-            # the same two requests as one fused launch
-            position_fill(host.view(np.uint32))
-            c0 = hc.launch_count()
-            pool.backup_load(kv, a.device_pages, a.host_pages, b_req.device_pages, b_req.host_pages, layout)
-            torch.cuda.synchronize()
-            assert hc.launch_count() - c0 == 1
-            assert gh.sampled_host_check(host, bufs, a.device_pages, a.host_pages, layout, B, L, P, R, Hp,
-                                         20000, 30 + layout)
-            assert gh.sampled_host_check(host, bufs, b_req.device_pages, b_req.host_pages, layout, B, L, P,
-                                         R, Hp, 20000, 40 + layout)
+            for fused in (False, True):
+                run += 1
+                fs.normal_fill(bufs, 300 + run)          # fresh values, unlike what B loads
+                fs.position_fill(host.view(np.uint32), run)
+                mirror.pull(bufs)
+                fs.copy(exp_host, host)
+                c0 = hc.launch_count()
+                if fused:
+                    pool.backup_load(kv, a.device_pages, a.host_pages, b_req.device_pages, b_req.host_pages,
+                                     layout)
+                else:
+                    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+                    pool.backup(kv, a.device_pages, a.host_pages, layout, stream=s1)
+                    pool.load(kv, b_req.device_pages, b_req.host_pages, layout, stream=s2)
+                torch.cuda.synchronize()
+                assert hc.launch_count() - c0 == (1 if fused else 2)
+                fs.oracle_backup(mirror.np, exp_host, B, L, P, R, Hp, a.device_pages, a.host_pages, layout)
+                fs.oracle_load(mirror.np, exp_host, B, L, P, R, Hp, b_req.device_pages, b_req.host_pages,
+                               layout)
+                what = f"layout {layout}, {'fused' if fused else 'two streams'}"
+                fs.assert_equal(host, exp_host, what)
+                mirror.compare(bufs, what)
+        del exp_host, host
+    mirror.close()
     del bufs, kv
     torch.cuda.empty_cache()
 
 
+def layer_sums(mirror, dp, L, Dp):
+    """Per-layer sums of the 32-bit words of the given pages (one buffer per
+    layer), from the oracle's device buffers: what the stand-in attention adds."""
+    out = np.zeros(L, np.uint64)
+    for layer in range(L):
+        rows = mirror.np[layer].reshape(Dp, -1)[dp]
+        out[layer] = rows.view(np.uint32).astype(np.uint64).sum(dtype=np.uint64)
+    return out
+
+
 @pytest.mark.parametrize("tokens", [4096, 16384, 65536])
-def test_mla61_per_layer_load_with_events(tokens):
+def test_mla61_per_layer_and_pipelined_loads(tokens):
+    """61 per-layer loads, each gating the stand-in attention of its layer
+    through the layer's event, then the same load as one pipelined launch
+    gated per layer on the device counters: every device buffer against the
+    oracle's per-layer loads applied in the same order."""
     s = wl.MLA_LATENT
     t = wl.mla_transfer(s, tokens)
-    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    B, L, P, R, Hp = dims(s)
+    Dp = s.device_pages
     bufs = device_pool(s)
-    kv = hc.DeviceKV(bufs, s.device_pages)
+    kv = hc.DeviceKV(bufs, Dp)
+    mirror = fs.DeviceMirror(bufs)
     with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
         host = pool.host_array(np.uint16)
-        position_fill(host.view(np.uint32))
-        gh.sentinel_fill(bufs, 0xC3)
+        fs.position_fill(host.view(np.uint32), tokens)
+        gh.sentinel_fill(bufs, SENT8)
         torch.cuda.synchronize()
         xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
         sums = torch.zeros(L, dtype=torch.int64, device="cuda")
-        plan = pool.plan(t.device_pages, t.host_pages, s.device_pages, hc.LOAD)
+        plan = pool.plan(t.device_pages, t.host_pages, Dp, hc.LOAD)
         c0 = hc.launch_count()
         for layer in range(L):
             plan.execute(kv, layer=layer, stream=xfer)
@@ -172,67 +190,82 @@ def test_mla61_per_layer_load_with_events(tokens):
             hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, stream=comp)
         torch.cuda.synchronize()
         assert hc.launch_count() - c0 == 2 * L
-        assert gh.sampled_host_check(host, bufs, t.device_pages, t.host_pages, 1, B, L, P, R, Hp, 30000, 4)
-        assert untouched_pages_ok(bufs, P, t.device_pages, SENT16)
-        # the checksums taken behind each layer event equal those taken after
-        # everything finished
-        after = torch.zeros(L, dtype=torch.int64, device="cuda")
+        mirror.fill(SENT8)
         for layer in range(L):
-            hc.layer_checksum(kv, pool, t.device_pages, layer, after.data_ptr() + 8 * layer)
+            fs.oracle_load(mirror.np, host, B, L, P, R, Hp, t.device_pages, t.host_pages, hc.PAGE_FIRST, layer)
+        mirror.compare(bufs, f"per-layer loads of {tokens} tokens")
+        # the checksums taken behind each layer's event are those of the oracle's result
+        want = layer_sums(mirror, t.device_pages, L, Dp)
+        assert np.array_equal(sums.cpu().numpy().view(np.uint64), want)
+        # the same load in one pipelined launch, each layer waited for on the device
+        gh.sentinel_fill(bufs, SENT8)
+        sums.zero_()
         torch.cuda.synchronize()
-        assert torch.equal(sums, after)
-        if tokens <= 16384:
-            # and both equal the sums of what the oracle loads
-            n = len(t.device_pages)
-            want = [np.zeros((n * P, R), np.uint16) for _ in range(L)]
-            gh.orc().load(want, host, B, L, P, R, Hp, np.arange(n), t.host_pages, 1)
-            exp = np.array([w.view(np.uint32).astype(np.uint64).sum() for w in want], np.uint64)
-            assert np.array_equal(after.cpu().numpy().view(np.uint64), exp)
+        c0 = hc.launch_count()
+        pool.load_pipelined(kv, t.device_pages, t.host_pages, stream=xfer)
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        hc.wait(comp, 30_000_000)
+        hc.wait(xfer, 30_000_000)
+        assert hc.launch_count() - c0 == 1 + L
+        mirror.compare(bufs, f"pipelined load of {tokens} tokens")
+        assert np.array_equal(sums.cpu().numpy().view(np.uint64), want)
         plan.close()
+        del host
+    mirror.close()
     del bufs, kv
     torch.cuda.empty_cache()
 
 
-def test_small_mix_one_launch_per_call():
+def test_small_mix_all_requests_against_an_oracle_shadow():
+    """All 10,000 requests of the mix (1-256 pages, 30% backups) on one stream,
+    one launch each.  An oracle shadow of the device pool and the host pool
+    applies the same requests in the same order; at five checkpoints (the
+    last after every request) the whole host pool and every device buffer are
+    compared with the shadow."""
     s = wl.SMALL_MIX
-    reqs = wl.small_mix_requests(s)[:300]
-    B, L, P, R, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.host_pages
+    reqs = wl.small_mix_requests(s)
+    assert len(reqs) == 10_000
+    B, L, P, R, Hp = dims(s)
     bufs = device_pool(s)
     kv = hc.DeviceKV(bufs, s.device_pages)
+    mirror = fs.DeviceMirror(bufs)
+    mirror.pull(bufs)
+    stream = torch.cuda.Stream()
     with hc.Pool(L, B, P, R, Hp, "layer_first") as pool:
         host = pool.host_array(np.uint16)
-        position_fill(host.view(np.uint32))
+        fs.position_fill(host.view(np.uint32), 5)
+        shadow_host = np.empty_like(host)
+        fs.copy(shadow_host, host)
+        checkpoints = {1999, 3999, 5999, 7999, len(reqs) - 1}
         for k, r in enumerate(reqs):
             c0 = hc.launch_count()
             if r.direction == "backup":
-                pool.backup(kv, r.device_pages, r.host_pages)
+                pool.backup(kv, r.device_pages, r.host_pages, stream=stream)
+                fs.oracle_backup(mirror.np, shadow_host, B, L, P, R, Hp, r.device_pages, r.host_pages,
+                                 hc.LAYER_FIRST)
             else:
-                pool.load(kv, r.device_pages, r.host_pages)
-            torch.cuda.synchronize()
-            assert hc.launch_count() - c0 == 1
-            assert gh.sampled_host_check(host, bufs, r.device_pages, r.host_pages, 0, B, L, P, R, Hp,
-                                         1000, k), k
+                pool.load(kv, r.device_pages, r.host_pages, stream=stream)
+                fs.oracle_load(mirror.np, shadow_host, B, L, P, R, Hp, r.device_pages, r.host_pages,
+                               hc.LAYER_FIRST)
+            assert hc.launch_count() - c0 == 1, k
+            if k in checkpoints:
+                hc.wait(stream, 60_000_000)
+                fs.assert_equal(host, shadow_host, f"host pool after request {k}")
+                mirror.compare(bufs, f"device pool after request {k}")
+        del host, shadow_host
+    mirror.close()
     del bufs, kv
     torch.cuda.empty_cache()
-
-
-def untouched_bytes_ok(bufs, P, moved, sentinel8):
-    """Every device page not in `moved` still holds the sentinel byte (any dtype)."""
-    Dp = bufs[0].shape[0] // P
-    mask = torch.ones(Dp, dtype=torch.bool, device="cuda")
-    mask[torch.as_tensor(np.asarray(moved), device="cuda")] = False
-    for b in bufs:
-        rows = b.view(torch.uint8).view(Dp, -1)[mask]
-        if rows.numel() and not bool((rows == sentinel8).all()):
-            return False
-    return True
 
 
 def test_nsa_group_full_size_per_layer_and_all_layers():
     """An MLA latent (576 bf16), an fp8 indexer key (128) and fp32 scales (4)
     as three pools of one pinned allocation, at 64K tokens: 61 per-layer group
     loads, each gating per-pool checksums through the pools' layer events, then
-    one all-layer group backup; every pool checked on sampled oracle offsets."""
+    one all-layer group backup over sentinel host pools.  Every device buffer
+    and every host pool against the oracle's transfer of that pool."""
     s = wl.MLA_LATENT
     L, P, Dp, Hp = s.num_layers, s.page_size, s.device_pages, s.host_pages
     kinds = [(576, 2), (128, 1), (4, 4)]
@@ -244,11 +277,11 @@ def test_nsa_group_full_size_per_layer_and_all_layers():
     for (R, es), nbytes in zip(kinds, sizes):
         pools.append(hc.Pool(L, 1, P, R, Hp, "page_first", elem_bytes=es, host_ptr=mem.ptr + off,
                              host_bytes=nbytes))
-        bufs = [torch.full((Dp * P, R * es), 0xC3, dtype=torch.uint8, device="cuda").view(gh.TORCH_DT[es])
+        bufs = [torch.full((Dp * P, R * es), SENT8, dtype=torch.uint8, device="cuda").view(gh.TORCH_DT[es])
                 for _ in range(L)]
         bufsets.append(bufs)
         kvs.append(hc.DeviceKV(bufs, Dp))
-        position_fill(pools[-1].host_array(np.uint32))
+        fs.position_fill(pools[-1].host_array(np.uint32), len(pools))
         off += nbytes
     xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
     sums = torch.zeros((len(kinds), L), dtype=torch.int64, device="cuda")
@@ -261,29 +294,30 @@ def test_nsa_group_full_size_per_layer_and_all_layers():
             hc.layer_checksum(kv, pool, dp, layer, sums[i].data_ptr() + 8 * layer, stream=comp)
     torch.cuda.synchronize()
     assert hc.launch_count() - c0 == L + len(kinds) * L
-    after = torch.zeros_like(sums)
-    for i, (pool, kv) in enumerate(zip(pools, kvs)):
-        for layer in range(L):
-            hc.layer_checksum(kv, pool, dp, layer, after[i].data_ptr() + 8 * layer)
-    torch.cuda.synchronize()
-    assert torch.equal(sums, after)
+    mirrors = []
     for i, (pool, bufs, (R, es)) in enumerate(zip(pools, bufsets, kinds)):
+        m = fs.DeviceMirror(bufs)
+        m.fill(SENT8)
         host = pool.host_array(gh.NP_DT[es])
-        assert gh.sampled_host_check(host, bufs, dp, hp, 1, 1, L, P, R, Hp, 20000, 10 + i), (R, es)
-        assert untouched_bytes_ok(bufs, P, dp, 0xC3), (R, es)
-    # every layer back to the host in one launch, over a sentinel-filled pool
+        for layer in range(L):
+            fs.oracle_load(m.np, host, 1, L, P, R, Hp, dp, hp, hc.PAGE_FIRST, layer)
+        m.compare(bufs, f"per-layer group loads, pool {i}")
+        assert np.array_equal(sums[i].cpu().numpy().view(np.uint64), layer_sums(m, dp, L, Dp)), i
+        mirrors.append(m)
+    # every layer back to the host in one launch, over sentinel host pools
     for pool in pools:
-        pool.host_array(np.uint8)[:] = 0xC3
+        fs.fill(pool.host_array(np.uint8), SENT8)
     c0 = hc.launch_count()
     hc.group_transfer(pools, kvs, dp, hp, hc.BACKUP)
     torch.cuda.synchronize()
     assert hc.launch_count() - c0 == 1
-    for i, (pool, bufs, (R, es)) in enumerate(zip(pools, bufsets, kinds)):
-        host = pool.host_array(np.uint8)
-        assert gh.sampled_host_check(pool.host_array(gh.NP_DT[es]), bufs, dp, hp, 1, 1, L, P, R, Hp, 20000,
-                                     20 + i), (R, es)
-        moved = len(dp) * L * P * R * es
-        assert count_equal(host, 0xC3) >= host.size - moved
+    for i, (pool, m, (R, es)) in enumerate(zip(pools, mirrors, kinds)):
+        host = pool.host_array(gh.NP_DT[es])
+        want = np.empty_like(host)
+        fs.fill(want.view(np.uint8), SENT8)
+        fs.oracle_backup(m.np, want, 1, L, P, R, Hp, dp, hp, hc.PAGE_FIRST)
+        fs.assert_equal(host, want, f"group backup, pool {i}")
+        m.close()
     for pool in pools:
         pool.close()
     del bufsets, kvs
