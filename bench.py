@@ -187,25 +187,12 @@ def build_workload(device, pages=512, launch_ctas=0, name="llama3_8b_32k"):
     deep78_32k    -- 78 layers, fully scattered device pages, contiguous host.
     (1024 device and 1024 host pages at 512 pages per transfer; 2x `pages`
     each for a scaled-down case.)"""
-    import dataclasses
     import torch
     import tiered_kv_cache_gb300 as hc
     from tiered_kv_cache_gb300 import workloads as wl
 
-    s = wl.LLAMA3_8B if name == "llama3_8b_32k" else wl.DEEP_STRESS
-    if pages != 512:
-        s = dataclasses.replace(s, device_pages=2 * pages, host_pages=2 * pages)
+    s, a_dev, b_dev, a_host, b_host = workload_indices(name, pages)
     vals = [v.view(torch.int16) for v in wl.kv_values(s, device=device)]
-    if name == "llama3_8b_32k":
-        t = wl.llama_transfer(s, pages)
-        a_dev = t.device_pages
-        rng = wl.index_rng(s.seed + 1)
-        b_dev = wl.fragmented_pages(rng, s.device_pages, pages, exclude=a_dev)
-    else:
-        a, b = wl.deep_bidir_transfers(s, pages)
-        a_dev, b_dev = a.device_pages, b.device_pages
-    a_host = wl.contiguous_pages(pages, 0)
-    b_host = wl.contiguous_pages(pages, pages)
     pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first",
                    launch_ctas=launch_ctas)
     kv = hc.DeviceKV(vals, s.device_pages)
@@ -213,7 +200,7 @@ def build_workload(device, pages=512, launch_ctas=0, name="llama3_8b_32k"):
                 b_host=b_host, bytes_per_xfer=pages * s.page_bytes, pages=pages)
 
 
-def link_peaks(torch, nbytes=1 << 30, reps=5):
+def link_peaks(torch, nbytes=1 << 30, reps=5, hc=None):
     """Pinned cudaMemcpyAsync of 1 GiB: H2D, D2H, and both at once."""
     host_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     host_b = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
@@ -264,8 +251,67 @@ def link_peaks(torch, nbytes=1 << 30, reps=5):
     t_dd = timed(d2d)
     res["d2d_gbs"] = 2 * nbytes / t_dd / GB      # bytes read + written
     res["d2d_how"] = "device-to-device copy of 1 GiB on the same stream, bytes read + written, best of 5"
+    if hc is not None:
+        res["zero_copy_kernel"] = link_probe_kernel(torch, hc, timed, s1, s2, host_a, host_b, dev_a, dev_b,
+                                                    nbytes)
+    res["host_dram"] = host_copy_rate()
     del host_a, host_b, dev_a, dev_b, dev_d
     return res
+
+
+def link_probe_kernel(torch, hc, timed, s1, s2, host_a, host_b, dev_a, dev_b, nbytes):
+    """The same 1 GiB moves by the library's plain streaming-copy kernel (SM
+    loads and stores to mapped pinned memory, no index decode), over a sweep of
+    grids and bytes in flight; and a load whose 32 MiB host source is read 32
+    times over, so that it can sit in the host's last-level cache instead of
+    its DRAM."""
+    grids = (38, 76, 152, 304, 608)
+    h2d, d2h = {}, {}
+    for unroll in (4, 8):
+        for g in grids:
+            t = timed(lambda: hc.stream_copy(dev_a.data_ptr(), host_a.data_ptr(), nbytes, g, unroll, s1))
+            h2d[f"{g}x{unroll}"] = round(nbytes / t / GB, 1)
+            t = timed(lambda: hc.stream_copy(host_b.data_ptr(), dev_b.data_ptr(), nbytes, g, unroll, s1))
+            d2h[f"{g}x{unroll}"] = round(nbytes / t / GB, 1)
+
+    def both():
+        hc.stream_copy(dev_a.data_ptr(), host_a.data_ptr(), nbytes, 152, 4, s1)
+        hc.stream_copy(host_b.data_ptr(), dev_b.data_ptr(), nbytes, 95, 4, s2)
+    t_bi = timed(both)
+    small = 32 << 20
+
+    def cached():
+        for k in range(nbytes // small):
+            hc.stream_copy(dev_a.data_ptr() + k * small, host_a.data_ptr(), small, 152, 4, s1)
+    t_c = timed(cached)
+    return {"h2d_gbs": max(h2d.values()), "d2h_gbs": max(d2h.values()),
+            "bidir_gbs": round(2 * nbytes / t_bi / GB, 1),
+            "h2d_32mib_source_gbs": round(nbytes / t_c / GB, 1),
+            "h2d_by_grid_x_vecs_per_thread": h2d, "d2h_by_grid_x_vecs_per_thread": d2h,
+            "how": "hicache_stream_copy of 1 GiB, best of 5 per setting; bidir = 152-CTA load and 95-CTA "
+                   "backup on two streams; the 32 MiB source case copies one 32 MiB host range into 32 "
+                   "device ranges"}
+
+
+def host_copy_rate(nbytes=1 << 30, reps=3):
+    """The host's own memory bandwidth: numpy copies of 1 GiB split over every
+    core (bytes read + written)."""
+    import threading
+    n = os.cpu_count() or 1
+    a = np.ones(nbytes, np.uint8)
+    b = np.zeros(nbytes, np.uint8)
+    parts = [(nbytes * k // n, nbytes * (k + 1) // n) for k in range(n)]
+    best = float("inf")
+    for _ in range(reps):
+        ts = [threading.Thread(target=np.copyto, args=(b[x:y], a[x:y])) for x, y in parts]
+        t0 = time.perf_counter()
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        best = min(best, time.perf_counter() - t0)
+    return {"copy_gbs_read_plus_write": round(2 * nbytes / best / GB, 1), "threads": n,
+            "how": "numpy copy of 1 GiB split over every core, best of 3"}
 
 
 def run_step(torch, w, s1, s2, ev=None):
@@ -380,30 +426,62 @@ def step_config(args, npages, bpx):
             "launch_ctas": args.ctas or "auto"}
 
 
+def workload_indices(name, pages):
+    """Shape and page indices of requests A and B of a step workload (the
+    same draws build_workload makes)."""
+    import dataclasses
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B if name == "llama3_8b_32k" else wl.DEEP_STRESS
+    if pages != 512:
+        s = dataclasses.replace(s, device_pages=2 * pages, host_pages=2 * pages)
+    if name == "llama3_8b_32k":
+        a_dev = wl.llama_transfer(s, pages).device_pages
+        b_dev = wl.fragmented_pages(wl.index_rng(s.seed + 1), s.device_pages, pages, exclude=a_dev)
+    else:
+        a, b = wl.deep_bidir_transfers(s, pages)
+        a_dev, b_dev = a.device_pages, b.device_pages
+    return s, a_dev, b_dev, wl.contiguous_pages(pages, 0), wl.contiguous_pages(pages, pages)
+
+
 def reference_arm(args):
-    """`--impl reference`: the oracle on the host cores, timed on the same
-    workload shape, a bounded sample per step."""
+    """`--impl reference`: the oracle (single-threaded C, as written) on one
+    host core, on the same workload as the step: the same pools, pages and
+    layouts, at full transfer size.  One oracle transfer of a full request
+    takes seconds, so a reference step is ONE of the step's transfers, taken in
+    the step's order (per layout: backup A, load A, backup A with load B,
+    fused backup A + load B), and GB/s = bytes moved / time."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     import oracle
-    from tiered_kv_cache_gb300 import workloads as wl
-    s = wl.LLAMA3_8B
+    s, a_dev, b_dev, a_host, b_host = workload_indices(args.workload, args.pages)
     o = oracle.Oracle()
-    pages = 4
-    rng = np.random.default_rng(0)
-    Dp = Hp = 16
-    B, L, P, R = s.num_buffers, s.num_layers, s.page_size, s.row_elems
-    dev = [rng.integers(0, 65535, (Dp * P, R), dtype=np.uint16) for _ in range(B * L)]
-    host = np.zeros(B * L * Hp * P * R, np.uint16)
-    dp = wl.fragmented_pages(rng, Dp, pages)
-    hp = np.arange(pages)
+    B, L, P, R, Dp, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.device_pages, s.host_pages
+    block = np.random.default_rng(0).integers(0, 1 << 16, 1 << 20, dtype=np.uint16)
+
+    def filled(n):
+        a = np.empty(n, np.uint16)
+        for off in range(0, n, block.size):
+            m = min(block.size, n - off)
+            a[off:off + m] = block[:m]
+        return a
+    dev = [filled(Dp * P * R).reshape(Dp * P, R) for _ in range(B * L)]
+    host = filled(B * L * Hp * P * R)
+    ops = []
+    for lay in LAYOUT_NAMES:
+        lid = LAYOUT_IDS[lay]
+        ops += [(o.backup, a_dev, a_host, lid), (o.load, a_dev, a_host, lid),
+                (o.backup, a_dev, a_host, lid), (o.load, b_dev, b_host, lid),
+                (o.backup, a_dev, a_host, lid), (o.load, b_dev, b_host, lid)]
+    bpx = args.pages * s.page_bytes
+    k = 0
 
     def step():
-        for lid in (0, 1, 2):
-            o.backup(dev, host, B, L, P, R, Hp, dp, hp, lid)
-            o.load(dev, host, B, L, P, R, Hp, dp, hp, lid)
-        return 6 * pages * s.page_bytes
+        nonlocal k
+        fn, d, h, lid = ops[k % len(ops)]
+        k += 1
+        fn(dev, host, B, L, P, R, Hp, d, h, lid)
+        return bpx
 
     for _ in range(args.warmup):
         step()
@@ -411,14 +489,15 @@ def reference_arm(args):
     moved = sum(step() for _ in range(args.steps))
     el = time.perf_counter() - t0
     v = moved / el / GB
-    sample = (f"per step: backup+load of {pages} pages ({pages * s.page_bytes / 2**20:.0f} MiB) in each of "
-              "layer_first, page_first and page_first_direct, on host arrays")
+    sample = (f"each step one of the GPU step's {len(ops)} transfers of {args.pages} pages "
+              f"({bpx / 2**30:.3g} GiB), in the step's order; {args.steps} steps after {args.warmup} "
+              f"warm-up steps; host arrays; {el:.1f} s timed")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": step_config(args, args.pages, args.pages * s.page_bytes),
+        "config": step_config(args, args.pages, bpx),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -426,6 +505,124 @@ def reference_arm(args):
 
 def _elapsed(torch, e0, e1):
     return e0.elapsed_time(e1) / 1e3
+
+
+def breakdown_from_events(ev, bpx, link):
+    """Per-layout, per-operation GB/s (from the mean launch time) and their
+    fraction of the in-run link peak, from (name, start, end) event triples."""
+    per = {}
+    for name, a, b in ev:
+        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    breakdown = {}
+    for lay in LAYOUT_NAMES:
+        bk = bpx / statistics.mean(per[f"{lay}/backup"]) / GB
+        ld = bpx / statistics.mean(per[f"{lay}/load"]) / GB
+        bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
+        bf = 2 * bpx / statistics.mean(per[f"{lay}/bidir_fused"]) / GB
+        breakdown[lay] = {
+            "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1),
+            "bidir_streams_gbs": round(bi, 1), "bidir_fused_gbs": round(bf, 1),
+            "backup_frac_of_link": frac(bk, link["d2h_gbs"]),
+            "load_frac_of_link": frac(ld, link["h2d_gbs"]),
+            "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
+            "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
+            # per-op launch times (GB/s above are from the mean)
+            "ms": {op: {"median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
+                        "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"])}
+                   for op in ("backup", "load", "bidir", "bidir_fused")},
+        }
+    return per, breakdown
+
+
+def bench_deep78(torch, hc, args, link, steps=3):
+    """The deep-model segment-count stress: 78 layers, K+V, 512 fully scattered
+    device pages per request (39,936 page x layer segments per buffer under
+    page_first_direct), the same four operations per layout as the headline
+    step, timed with events over `steps` steps after one warm-up step."""
+    w = build_workload("cuda", 512, args.ctas, "deep78_32k")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    run_step(torch, w, s1, s2)
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(steps):
+        run_step(torch, w, s1, s2, ev)
+    torch.cuda.synchronize()
+    s = w["shape"]
+    seg = {lay: hc.segment_count(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
+                                 LAYOUT_IDS[lay], w["a_dev"], w["a_host"]) // s.num_buffers
+           for lay in LAYOUT_NAMES}
+    _, br = breakdown_from_events(ev, w["bytes_per_xfer"], link)
+    w["pool"].close()
+    del w
+    torch.cuda.empty_cache()
+    return {"bytes_per_transfer": 512 * s.page_bytes, "segments_per_buffer": seg, "steps": steps,
+            "breakdown": br}
+
+
+def bench_host_shuffled(torch, hc, args, link, reps=3):
+    """The Llama-3-8B transfer of the headline with the host pages shuffled
+    (a random permutation sample of the host pool instead of a contiguous
+    range): backup and load of 512 pages per layout, event-timed."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.LLAMA3_8B
+    t = wl.llama_transfer(s, 512, shuffled_host=True)
+    vals = [v.view(torch.int16) for v in wl.kv_values(s, device="cuda")]
+    kv = hc.DeviceKV(vals, s.device_pages)
+    pool = hc.Pool(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages, "layer_first",
+                   launch_ctas=args.ctas)
+    st = torch.cuda.Stream()
+    bpx = 512 * s.page_bytes
+    out = {}
+    for lay in LAYOUT_NAMES:
+        lid = LAYOUT_IDS[lay]
+        res = {}
+        for op, fn in (("backup", pool.backup), ("load", pool.load)):
+            fn(kv, t.device_pages, t.host_pages, lid, stream=st)
+            times = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                fn(kv, t.device_pages, t.host_pages, lid, stream=st)
+                e1.record(st)
+                torch.cuda.synchronize()
+                times.append(_elapsed(torch, e0, e1))
+            gbs = bpx / statistics.mean(times) / GB
+            res[f"{op}_gbs"] = round(gbs, 1)
+            res[f"{op}_frac_of_link"] = frac(gbs, link["d2h_gbs"] if op == "backup" else link["h2d_gbs"])
+        out[lay] = res
+    pool.close()
+    del vals, kv
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_extras(torch, hc, args, link):
+    """The other workload shapes, measured after the headline step of the
+    default run so that one bench line carries them all."""
+    import types
+    out = {}
+    t0 = time.perf_counter()
+    out["llama3_8b_32k_host_shuffled"] = bench_host_shuffled(torch, hc, args, link)
+    out["llama3_8b_32k_host_shuffled"]["wall_s"] = round(time.perf_counter() - t0, 1)
+    t0 = time.perf_counter()
+    out["deep78_32k"] = bench_deep78(torch, hc, args, link)
+    out["deep78_32k"]["wall_s"] = round(time.perf_counter() - t0, 1)
+    t0 = time.perf_counter()
+    mla_args = types.SimpleNamespace(ctas=args.ctas, tokens="4096,16384,65536", steps=min(args.steps, 10),
+                                     warmup=3)
+    res, launches = bench_mla_overlap(torch, hc, mla_args)
+    out["mla61"] = {"results": res, "gpu_launches": launches, "wall_s": round(time.perf_counter() - t0, 1),
+                    "how": "61 per-layer loads with an event each (per_layer), the same replayed from a "
+                           "plan's graph (graph), one pipelined launch (pipelined), one all-layer launch; "
+                           "alone and overlapped with a stand-in attention on a second stream; overlap "
+                           "efficiency = (load + compute - overlapped) / min(load, compute)"}
+    torch.cuda.empty_cache()
+    t0 = time.perf_counter()
+    out["small_mix"] = bench_small_mix(torch, hc, args)
+    out["small_mix"]["wall_s"] = round(time.perf_counter() - t0, 1)
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_mla_overlap(torch, hc, args):
@@ -899,6 +1096,8 @@ def main():
     ap.add_argument("--ctas", type=int, default=0, help="CTAs per transfer launch (0 = automatic)")
     ap.add_argument("--pages", type=int, default=512,
                     help="pages per transfer (512 = the 32K-token workload; smaller for profiling)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workload shapes that the default run measures after the step")
     ap.add_argument("--no-link-probe", action="store_true",
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
@@ -933,7 +1132,7 @@ def main():
     if args.no_link_probe:
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
-        link = link_peaks(torch)
+        link = link_peaks(torch, hc=hc)
     if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group", "shapes"):
         t0 = time.perf_counter()
         if args.workload == "shapes":
@@ -1020,27 +1219,7 @@ def main():
     npages = w["pages"]
     value = whole_job_gbs(args.steps * step_bytes, elapsed, world)
 
-    per = {}
-    for name, a, b in ev:
-        per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
-    breakdown = {}
-    for lay in LAYOUT_NAMES:
-        bk = bpx / statistics.mean(per[f"{lay}/backup"]) / GB
-        ld = bpx / statistics.mean(per[f"{lay}/load"]) / GB
-        bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
-        bf = 2 * bpx / statistics.mean(per[f"{lay}/bidir_fused"]) / GB
-        breakdown[lay] = {
-            "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1),
-            "bidir_streams_gbs": round(bi, 1), "bidir_fused_gbs": round(bf, 1),
-            "backup_frac_of_link": frac(bk, link["d2h_gbs"]),
-            "load_frac_of_link": frac(ld, link["h2d_gbs"]),
-            "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
-            "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
-            # per-op launch times over the timed steps (GB/s above are from the mean)
-            "ms": {op: {"median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
-                        "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"])}
-                   for op in ("backup", "load", "bidir", "bidir_fused")},
-        }
+    per, breakdown = breakdown_from_events(ev, bpx, link)
     # dominant single-direction kernel: the largest total time
     singles = {k: sum(v) for k, v in per.items() if "bidir" not in k}
     dom = max(singles, key=singles.get)
@@ -1095,9 +1274,13 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
     }
+    w["pool"].close()
+    del w
+    torch.cuda.empty_cache()
+    if not args.no_extras and args.workload == "llama3_8b_32k" and args.pages == 512:
+        out["workloads"] = bench_extras(torch, hc, args, link)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
-    w["pool"].close()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

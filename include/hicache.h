@@ -529,6 +529,24 @@ int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc 
                            const int64_t *device_pages, int64_t n, int32_t layer_id,
                            int32_t reps, uint64_t *out_sum_dev, void *stream);
 
+/* ---- roofline probe -----------------------------------------------------------
+ * A plain streaming copy of `bytes` from src to dst with no index decode: each
+ * CTA of `grid` (0 = one per SM) moves tiles of 256 threads x vecs_per_thread
+ * (4 or 8; 0 = 4) consecutive 16-byte vectors, all loads of a tile in flight
+ * before its stores, CTAs in address order -- the transfer kernels' access
+ * pattern without their address arithmetic.  It is the zero-copy counterpart
+ * of the copy-engine baseline (cudaMemcpyAsync) that "HiCache 시스템 설계와
+ * 최적화", section "CPU→GPU 전송 최적화", measures its GPU I/O kernels against,
+ * and serves to tell which resource caps the host link.  dst and src are
+ * device memory of the current device or pinned, device-mapped host memory
+ * (each checked up to its last byte with cudaPointerGetAttributes; host
+ * memory is addressed through its device alias), 16-byte aligned, not
+ * overlapping; bytes a multiple of 16 (0: nothing enqueued).  Enqueues one
+ * launch on `stream`.  Errors: INVALID_ARG, ALIGNMENT, NOT_PINNED (pageable
+ * or unknown memory), CUDA; on error nothing is enqueued. */
+int hicache_stream_copy(void *dst, const void *src, size_t bytes, int32_t grid, int32_t vecs_per_thread,
+                        void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -12,6 +12,7 @@ Names follow the C ABI in ``include/hicache.h``:
     group_transfer / group_load_pipelined / group_plan(...) -> GroupPlan
     Engine (submission engine), PageAllocator (host pages)
     host_alloc / host_free, wait, prepass, segment_count, page_span, layer_checksum
+    stream_copy (roofline probe: plain zero-copy streaming copy)
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ __all__ = [
     "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "group_plan", "GroupPlan",
     "MAX_GROUP", "PAGE_FIRST_DIRECT_KV",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
-    "launch_count", "version",
+    "launch_count", "version", "stream_copy",
 ]
 
 LAYOUT_POOL = -1
@@ -111,6 +112,7 @@ def _bind(lib):
         "hicache_layer_event": (ctypes.c_int, [_vp, _i32, _P(_vp)]),
         "hicache_wait_layer": (ctypes.c_int, [_vp, _i32, _vp]),
         "hicache_wait": (ctypes.c_int, [_vp, _i64]),
+        "hicache_stream_copy": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp]),
         "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
         "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
         "hicache_page_span": (ctypes.c_int, [_P(PoolDesc), _i64, _i32, _P(_i64), _P(_i64)]),
@@ -206,6 +208,13 @@ def host_free(ptr: int):
 def wait(stream=None, timeout_us: int = -1):
     """Block until `stream` is idle, for at most timeout_us (raises TIMEOUT)."""
     _check(library().hicache_wait(_stream(stream), timeout_us))
+
+
+def stream_copy(dst_ptr: int, src_ptr: int, nbytes: int, grid: int = 0, vecs_per_thread: int = 4,
+                stream=None):
+    """Roofline probe: a plain zero-copy streaming copy of nbytes (no index
+    decode) between device memory and/or pinned, mapped host memory."""
+    _check(library().hicache_stream_copy(dst_ptr, src_ptr, nbytes, grid, vecs_per_thread, _stream(stream)))
 
 
 class DeviceKV:

@@ -516,6 +516,59 @@ int hicache_wait(void *stream, int64_t timeout_us) {
   }
 }
 
+// The device address of [p, p + bytes): device memory as it is, pinned host
+// memory through its device alias; anything else (pageable memory, a range
+// that leaves its allocation) is refused before any launch.
+static int device_range(const void *p, size_t bytes, const char *what, void **out) {
+  cudaPointerAttributes a, b;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e == cudaSuccess) e = cudaPointerGetAttributes(&b, static_cast<const char *>(p) + bytes - 1);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return set_error(HICACHE_ERR_NOT_PINNED, "%s is not CUDA memory", what);
+  }
+  const bool ok_a = a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+                    (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+  if (!ok_a || b.type != a.type || b.devicePointer == nullptr)
+    return set_error(HICACHE_ERR_NOT_PINNED, "%s is not device memory or pinned, device-mapped host memory "
+                     "up to its last byte", what);
+  int dev = -1;
+  if (a.type == cudaMemoryTypeDevice && (cudaGetDevice(&dev) != cudaSuccess || dev != a.device))
+    return set_error(HICACHE_ERR_INVALID_ARG, "%s is on device %d, not the current device", what, a.device);
+  *out = a.devicePointer;
+  return HICACHE_OK;
+}
+
+int hicache_stream_copy(void *dst, const void *src, size_t bytes, int32_t grid, int32_t vecs_per_thread,
+                        void *stream) {
+  g_last_error.clear();
+  if (bytes == 0) return HICACHE_OK;
+  if (!dst || !src) return set_error(HICACHE_ERR_INVALID_ARG, "dst or src is NULL");
+  if (reinterpret_cast<uintptr_t>(dst) % 16 || reinterpret_cast<uintptr_t>(src) % 16 || bytes % 16)
+    return set_error(HICACHE_ERR_ALIGNMENT, "dst, src and bytes must be multiples of 16 bytes");
+  if (vecs_per_thread == 0) vecs_per_thread = 4;
+  if (vecs_per_thread != 4 && vecs_per_thread != 8)
+    return set_error(HICACHE_ERR_INVALID_ARG, "vecs_per_thread must be 4 or 8");
+  const char *d = static_cast<const char *>(dst);
+  const char *s = static_cast<const char *>(src);
+  if (d < s + bytes && s < d + bytes) return set_error(HICACHE_ERR_INVALID_ARG, "dst and src overlap");
+  void *dd = nullptr, *sd = nullptr;
+  if (int rc = device_range(dst, bytes, "dst", &dd)) return rc;
+  if (int rc = device_range(src, bytes, "src", &sd)) return rc;
+  if (grid == 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaDeviceGetAttribute");
+    grid = sms;
+  }
+  if (grid < 1 || grid > 65536) return set_error(HICACHE_ERR_INVALID_ARG, "grid %d outside [1, 65536]", grid);
+  const int e = hicache::launch_stream_copy(dd, sd, uint64_t(bytes / 16), grid, vecs_per_thread, stream);
+  if (e != 0) return cuda_error(cudaError_t(e), "stream copy kernel launch");
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return HICACHE_OK;
+}
+
 int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc *desc,
                            const int64_t *device_pages, int64_t n, int32_t layer_id,
                            int32_t reps, uint64_t *out_sum_dev, void *stream) {

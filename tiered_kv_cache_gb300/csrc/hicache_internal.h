@@ -224,5 +224,8 @@ int noalloc_layer_counters(unsigned int **out);
 // Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).
 int set_error_text(int code, const char *msg);
 int launch_checksum(const ChecksumParams &p, int grid, void *stream);
+// Roofline probe: copy nvec 16-byte vectors from src to dst (both
+// device-addressable), `unroll` (4 or 8) vectors in flight per thread.
+int launch_stream_copy(void *dst, const void *src, uint64_t nvec, int grid, int unroll, void *stream);
 
 }  // namespace hicache

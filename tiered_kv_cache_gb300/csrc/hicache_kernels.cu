@@ -412,6 +412,30 @@ __global__ void __launch_bounds__(kThreads) checksum_kernel(const __grid_constan
   if ((threadIdx.x & 31) == 0 && acc != 0) atomicAdd(p.out, acc);
 }
 
+// Roofline probe: a plain streaming copy of nvec 16-byte vectors, with no
+// index decode.  Each CTA moves tiles of kThreads * UNROLL consecutive vectors,
+// UNROLL loads in flight per thread before the first store, CTAs grid-stride in
+// address order: the transfer kernels' access pattern on both sides, without
+// their address arithmetic.
+template <int UNROLL>
+__global__ void __launch_bounds__(kThreads)
+    stream_copy_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, uint64_t nvec) {
+  const uint64_t tile = uint64_t(kThreads) * UNROLL;
+  for (uint64_t t = uint64_t(blockIdx.x) * tile; t < nvec; t += uint64_t(gridDim.x) * tile) {
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint64_t i = t + uint64_t(k) * kThreads + threadIdx.x;
+      if (i < nvec) v[k] = ld_stream(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint64_t i = t + uint64_t(k) * kThreads + threadIdx.x;
+      if (i < nvec) st_stream(dst + i, v[k]);
+    }
+  }
+}
+
 template <class Params>
 const Params &params_for(const XferLaunch &x, Params &small) {
   small.h = x.params->h;
@@ -594,6 +618,19 @@ int launch_xfer(const XferLaunch &x) {
     case kPageFirstDirectKV: return int(launch_layout<kPageFirstDirectKV>(x));
     default: return int(cudaErrorInvalidValue);
   }
+}
+
+int launch_stream_copy(void *dst, const void *src, uint64_t nvec, int grid, int unroll, void *stream) {
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint4 *d = static_cast<uint4 *>(dst);
+  const uint4 *s = static_cast<const uint4 *>(src);
+  if (unroll == 8)
+    stream_copy_kernel<8><<<grid, kThreads, 0, st>>>(d, s, nvec);
+  else if (unroll == 4)
+    stream_copy_kernel<4><<<grid, kThreads, 0, st>>>(d, s, nvec);
+  else
+    return int(cudaErrorInvalidValue);
+  return int(cudaGetLastError());
 }
 
 int launch_checksum(const ChecksumParams &p, int grid, void *stream) {
