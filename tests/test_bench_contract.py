@@ -10,7 +10,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_reference_arm_prints_one_contract_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                        "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+                        "--warmup", "1", "--pages", "32"], capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -24,6 +24,6 @@ def test_reference_arm_prints_one_contract_line():
     sys.path.insert(0, ROOT)
     import bench
     import argparse
-    args = argparse.Namespace(workload="llama3_8b_32k", ctas=0, pages=512)
+    args = argparse.Namespace(workload="llama3_8b_32k", ctas=0, pages=32)
     from tiered_kv_cache_gb300 import workloads as wl
-    assert d["config"] == bench.step_config(args, 512, 512 * wl.LLAMA3_8B.page_bytes)
+    assert d["config"] == bench.step_config(args, 32, 32 * wl.LLAMA3_8B.page_bytes)
