@@ -259,6 +259,31 @@ def link_peaks(torch, nbytes=1 << 30, reps=5, hc=None):
     return res
 
 
+def binding_resource(link):
+    """What caps the host link, from this run's probes: the copy engines and
+    the SM streaming kernel at every grid and depth stop at the same rate, and
+    a host source small enough for the host's cache is no faster, so neither
+    the engine, the requests in flight nor host DRAM binds."""
+    k = link.get("zero_copy_kernel") or {}
+    if not k or not link.get("h2d_gbs"):
+        return None
+    h2d = k["h2d_by_grid_x_vecs_per_thread"]
+    d2h = k["d2h_by_grid_x_vecs_per_thread"]
+    return {
+        "resource": "the GPU's NVLink-C2C link to host memory, at the rate it delivers to this GPU",
+        "h2d_gbs": {"copy_engine": round(link["h2d_gbs"], 1), "sm_kernel_min": min(h2d.values()),
+                    "sm_kernel_max": max(h2d.values()), "sm_kernel_32mib_cached_source": k["h2d_32mib_source_gbs"]},
+        "d2h_gbs": {"copy_engine": round(link["d2h_gbs"], 1), "sm_kernel_min": min(d2h.values()),
+                    "sm_kernel_max": max(d2h.values())},
+        "host_dram_copy_gbs": (link.get("host_dram") or {}).get("copy_gbs_read_plus_write"),
+        "sm_kernel_grids": "38-608 CTAs x 4 or 8 16-byte vectors in flight per thread",
+        "ncu_c2c_fraction": "65.8% RX at 210.9 GB/s, 60.3% TX at 192.9 GB/s of ncu's nominal C2C peak "
+                            "(about 320 GB/s per direction; profiles/xfer_kernel_counters_llama3_8b_64pages.md)",
+        "nominal": "900 GB/s two-way NVLink-C2C per Grace, which serves two GPUs: 450 two-way, 225 per "
+                   "direction per GPU (a reading of the superchip figure)",
+    }
+
+
 def link_probe_kernel(torch, hc, timed, s1, s2, host_a, host_b, dev_a, dev_b, nbytes):
     """The same 1 GiB moves by the library's plain streaming-copy kernel (SM
     loads and stores to mapped pinned memory, no index decode), over a sweep of
@@ -559,10 +584,11 @@ def bench_deep78(torch, hc, args, link, steps=3):
             "breakdown": br}
 
 
-def bench_host_shuffled(torch, hc, args, link, reps=3):
+def bench_host_shuffled(torch, hc, args, link, reps=5):
     """The Llama-3-8B transfer of the headline with the host pages shuffled
     (a random permutation sample of the host pool instead of a contiguous
-    range): backup and load of 512 pages per layout, event-timed."""
+    range): backup and load of 512 pages per layout, event-timed, median of
+    `reps` after one warm-up call."""
     from tiered_kv_cache_gb300 import workloads as wl
     s = wl.LLAMA3_8B
     t = wl.llama_transfer(s, 512, shuffled_host=True)
@@ -587,8 +613,9 @@ def bench_host_shuffled(torch, hc, args, link, reps=3):
                 e1.record(st)
                 torch.cuda.synchronize()
                 times.append(_elapsed(torch, e0, e1))
-            gbs = bpx / statistics.mean(times) / GB
+            gbs = bpx / statistics.median(times) / GB
             res[f"{op}_gbs"] = round(gbs, 1)
+            res[f"{op}_min_ms"] = round(min(times) * 1e3, 3)
             res[f"{op}_frac_of_link"] = frac(gbs, link["d2h_gbs"] if op == "backup" else link["h2d_gbs"])
         out[lay] = res
     pool.close()
@@ -1239,6 +1266,7 @@ def main():
                                   "its source changed since" ,
                 "peak_source": "in-run pinned cudaMemcpyAsync of 1 GiB, same direction (no host-link "
                                "figure in MEASURED_PEAKS.json)",
+                "binding_resource": binding_resource(link),
                 "bytes_per_launch": bpx, "avg_launch_ms": round(dom_avg * 1e3, 3)}
     # device side of the same kernel: the payload crosses HBM once
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
