@@ -789,6 +789,64 @@ def bench_mla_overlap(torch, hc, args):
     return out, launches
 
 
+def bench_tp_mla(torch, hc, args):
+    """The tensor-parallel load of the MLA latent (61 layers, 576 bf16, page 64,
+    page_first) with tp ranks stood in for by tp pools on this one GPU over the
+    same host memory, each rank's launch on its own stream: every rank reads
+    1/tp of the pages and stores them into all tp ranks' buffers.  On one GPU
+    all ranks share one host link, so the whole group moves the request's bytes
+    over it once; the rates show what the fan-out stores cost the host reads
+    (compare tp = 1, a plain pipelined load)."""
+    from tiered_kv_cache_gb300 import workloads as wl
+    s = wl.MLA_LATENT
+    B, L, P, R, Dp, Hp = s.num_buffers, s.num_layers, s.page_size, s.row_elems, s.device_pages, s.host_pages
+    mem = hc.PinnedHost(B * L * Hp * P * R * 2)
+    out = {}
+    for tp in (1, 2, 4, 8):
+        pools = [hc.Pool(L, B, P, R, Hp, "page_first", host_ptr=mem.ptr, host_bytes=mem.nbytes,
+                         launch_ctas=args.ctas) for _ in range(tp)]
+        bufs = [[torch.empty((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(L)] for _ in range(tp)]
+        kvs = [hc.DeviceKV(b, Dp) for b in bufs]
+        counters = [p.layer_counters() for p in pools]
+        streams = [torch.cuda.Stream() for _ in range(tp)]
+        gate = torch.cuda.Stream()
+        for tokens in (4096, 16384, 65536):
+            t = wl.mla_transfer(s, tokens)
+            nbytes = len(t.device_pages) * s.page_bytes
+
+            def once():
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                torch.cuda._sleep(2_000_000)               # host enqueues every rank before the GPU starts
+                e0.record()
+                for st in streams:
+                    st.wait_event(e0)
+                for r, pool in enumerate(pools):
+                    hc.tp_load_pipelined(pool, kvs, counters, r, t.device_pages, t.host_pages, stream=streams[r])
+                for st in streams:
+                    j = torch.cuda.Event()
+                    j.record(st)
+                    torch.cuda.current_stream().wait_event(j)
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / 1e3
+            for _ in range(3):
+                once()
+            ts = [once() for _ in range(max(3, min(args.steps, 10)))]
+            el = statistics.median(ts)
+            out[f"tp{tp}/{tokens // 1024}k"] = {
+                "ms": round(el * 1e3, 3), "host_read_gbs": round(nbytes / el / GB, 1),
+                "device_write_gbs": round(tp * nbytes / el / GB, 1),
+                "host_bytes_per_rank": nbytes // tp}
+        for p in pools:
+            p.close()
+        del bufs, kvs
+        torch.cuda.empty_cache()
+    mem.free()
+    return out
+
+
 def bench_nsa_group(torch, hc, args):
     """A buffer group: an MLA latent (576 bf16) beside an fp8 indexer key (128)
     and its fp32 scales (4 per row), 61 layers, page 64, three page_first pools
@@ -1129,7 +1187,7 @@ def main():
                     help="skip the cudaMemcpyAsync host-link probe (profiling runs)")
     ap.add_argument("--workload", default="llama3_8b_32k",
                     choices=["llama3_8b_32k", "deep78_32k", "mla61_overlap", "small_mix", "host_alloc",
-                             "engine_bidir", "nsa_group", "shapes"],
+                             "engine_bidir", "nsa_group", "shapes", "tp_mla61"],
                     help="llama3_8b_32k is the headline step; the others measure the remaining "
                          "workload shapes")
     ap.add_argument("--tokens", default="",
@@ -1160,9 +1218,20 @@ def main():
         link = {"h2d_gbs": None, "d2h_gbs": None, "bidir_gbs": None, "how": "skipped"}
     else:
         link = link_peaks(torch, hc=hc)
-    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group", "shapes"):
+    if args.workload in ("mla61_overlap", "small_mix", "host_alloc", "engine_bidir", "nsa_group", "shapes",
+                         "tp_mla61"):
         t0 = time.perf_counter()
-        if args.workload == "shapes":
+        if args.workload == "tp_mla61":
+            res = bench_tp_mla(torch, hc, args)
+            launches = None
+            value = res["tp8/64k"]["host_read_gbs"]
+            what = {"workload": "tp_mla61: tensor-parallel load of the MLA latent (61 layers, 576 bf16, page "
+                                "64, page_first), tp = 1/2/4/8 ranks stood in for by pools on one GPU over one "
+                                "host memory; each rank reads 1/tp of the pages and stores them into every "
+                                "rank's buffers; 4K/16K/64K tokens",
+                    "value": "host-read GB/s of the whole group at tp = 8, 64K tokens (one GPU: the ranks "
+                             "share one host link)"}
+        elif args.workload == "shapes":
             res = bench_shapes(torch, hc, args)
             launches = None
             value = next(r["load_layer_first_gbs"] for r in res if r["row_bytes"] == 1152 and r["page_size"] == 1)

@@ -529,6 +529,56 @@ int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc 
                            const int64_t *device_pages, int64_t n, int32_t layer_id,
                            int32_t reps, uint64_t *out_sum_dev, void *stream);
 
+/* ---- tensor-parallel load of a replicated latent ---------------------------------
+ * "Baidu's KVCache Overhaul", section "MLA-class cache optimization": with MLA
+ * latents (and the CSA/HCA caches named there) every rank of a tensor-parallel
+ * group of tp GPUs holds the same KV, so each GPU reads only its part of the
+ * pages over its host link and the parts reach every GPU over NVLink, the host
+ * reads and the NVLink traffic running side by side, layer by layer.
+ *
+ * hicache_tp_share: the pairs [*first, *first + *count) of rank `rank` when n
+ * pairs are split into tp contiguous parts in the caller's order:
+ * [floor(n*rank/tp), floor(n*(rank+1)/tp)).  1 <= tp <= 16, 0 <= rank < tp,
+ * 0 <= n < 2^40.  Host-only.  Errors: INVALID_ARG. */
+int hicache_tp_share(int64_t n, int32_t tp, int32_t rank, int64_t *first, int64_t *count);
+/* The device address of the pool's num_layers per-layer counters (uint32, in
+ * device memory the pool owns), which hicache_tp_load_pipelined of any rank
+ * raises.  Export it to the other ranks of the group (e.g. with
+ * cudaIpcGetMemHandle on the allocation) so that their loads can count into
+ * it.  Errors: INVALID_ARG. */
+int hicache_pool_layer_counters(hicache_pool *pool, void **counters_out);
+/* This rank's part of a tensor-parallel load: the pairs of hicache_tp_share(n,
+ * tp, rank) are read from `pool`'s host memory (the group's replicated latent,
+ * e.g. one host buffer the ranks share) and every vector is stored into the
+ * same device page of each rank's buffers, rank_kvs[0..tp) (rank_kvs[rank] is
+ * this rank's own; the others are peers' buffers mapped into this GPU's
+ * address space with peer access enabled), layer by layer in one launch like
+ * hicache_load_pipelined.  Every finished tile of layer l adds one to word l
+ * of every rank's counters, rank_counters[0..tp) (hicache_pool_layer_counters
+ * of each rank, device-addressable from here), behind a system-wide fence; a
+ * CTA adds its tiles of a layer at once, when it moves past that layer.  This
+ * pool's per-layer targets rise by the tiles of ALL ranks' parts, so once
+ * every rank of the group has made the same call, hicache_wait_layer(pool, l,
+ * stream) waits until every part of layer l has landed in this rank's
+ * buffers.
+ *   - Every rank validates the whole request (range, duplicate device pages)
+ *     and accepts or refuses it alike; each rank's buffers hold the same
+ *     device_num_pages; tp * num_buffers * num_layers <= 1024.
+ *   - The ranks must make the same calls in the same order, and a rank must
+ *     not start the next tensor-parallel load of a pool until every rank's
+ *     waits for the previous one are satisfied: the counters add up tiles
+ *     from every rank and cannot tell two loads apart.
+ *   - No kernel waits for another rank; a rank that never makes its call
+ *     leaves the other ranks' waits unsatisfied.
+ *   - Stream rules and errors as hicache_load_pipelined (a capturing stream is
+ *     refused); on a refused call nothing is enqueued and no target changes.
+ * One GPU can stand in for the group: tp pools on the same device, each with
+ * its own device KV, all over the same host memory. */
+int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_kvs,
+                              void *const *rank_counters, int32_t tp, int32_t rank,
+                              const int64_t *device_pages, const int64_t *host_pages, int64_t n,
+                              int32_t layout, void *stream);
+
 /* ---- roofline probe -----------------------------------------------------------
  * A plain streaming copy of `bytes` from src to dst with no index decode: each
  * CTA of `grid` (0 = one per SM) moves tiles of 256 threads x vecs_per_thread

@@ -12,6 +12,7 @@ Names follow the C ABI in ``include/hicache.h``:
     group_transfer / group_load_pipelined / group_plan(...) -> GroupPlan
     Engine (submission engine), PageAllocator (host pages)
     host_alloc / host_free, wait, prepass, segment_count, page_span, layer_checksum
+    tp_share / tp_load_pipelined / Pool.layer_counters (tensor-parallel load of a replicated latent)
     stream_copy (roofline probe: plain zero-copy streaming copy)
 """
 from __future__ import annotations
@@ -28,7 +29,7 @@ __all__ = [
     "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "group_plan", "GroupPlan",
     "MAX_GROUP", "PAGE_FIRST_DIRECT_KV",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
-    "launch_count", "version", "stream_copy",
+    "launch_count", "version", "stream_copy", "tp_share", "tp_load_pipelined",
 ]
 
 LAYOUT_POOL = -1
@@ -113,6 +114,10 @@ def _bind(lib):
         "hicache_wait_layer": (ctypes.c_int, [_vp, _i32, _vp]),
         "hicache_wait": (ctypes.c_int, [_vp, _i64]),
         "hicache_stream_copy": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp]),
+        "hicache_tp_share": (ctypes.c_int, [_i64, _i32, _i32, _P(_i64), _P(_i64)]),
+        "hicache_pool_layer_counters": (ctypes.c_int, [_vp, _P(_vp)]),
+        "hicache_tp_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _P(_vp), _i32, _i32, _vp, _vp,
+                                                     _i64, _i32, _vp]),
         "hicache_prepass": (ctypes.c_int, [_i64, _i64, _vp, _vp, _i64, _i32, _P(_i64), _vp, _i64]),
         "hicache_segment_count": (_i64, [_P(PoolDesc), _vp, _vp, _i64, _i32, _i32]),
         "hicache_page_span": (ctypes.c_int, [_P(PoolDesc), _i64, _i32, _P(_i64), _P(_i64)]),
@@ -208,6 +213,32 @@ def host_free(ptr: int):
 def wait(stream=None, timeout_us: int = -1):
     """Block until `stream` is idle, for at most timeout_us (raises TIMEOUT)."""
     _check(library().hicache_wait(_stream(stream), timeout_us))
+
+def tp_share(n: int, tp: int, rank: int):
+    """(first, count): the pairs rank `rank` of a tensor-parallel group of tp
+    loads out of n, a contiguous part in the caller's order."""
+    first, count = ctypes.c_int64(), ctypes.c_int64()
+    _check(library().hicache_tp_share(n, tp, rank, ctypes.byref(first), ctypes.byref(count)))
+    return first.value, count.value
+
+
+def tp_load_pipelined(pool, rank_kvs, rank_counters, rank: int, device_pages, host_pages,
+                      layout=LAYOUT_POOL, stream=None):
+    """This rank's part of a tensor-parallel load of a replicated latent: its
+    share of the pages, read from ``pool``'s host memory and stored into every
+    rank's buffers (``rank_kvs``), counted into every rank's per-layer
+    counters (``rank_counters``: each rank's Pool.layer_counters())."""
+    if len(rank_kvs) != len(rank_counters):
+        raise ValueError("rank_kvs and rank_counters differ in length")
+    dp, hp = _idx(device_pages), _idx(host_pages)
+    if dp.size != hp.size:
+        raise ValueError("device_pages and host_pages differ in length")
+    if isinstance(layout, str):
+        layout = LAYOUTS[layout]
+    structs = (_DeviceKVStruct * len(rank_kvs))(*[k.struct for k in rank_kvs])
+    counters = (ctypes.c_void_p * len(rank_counters))(*rank_counters)
+    _check(library().hicache_tp_load_pipelined(pool.handle, structs, counters, len(rank_kvs), rank, _ptr(dp),
+                                               _ptr(hp), dp.size, layout, _stream(stream)))
 
 
 def stream_copy(dst_ptr: int, src_ptr: int, nbytes: int, grid: int = 0, vecs_per_thread: int = 4,
@@ -471,6 +502,13 @@ class Pool:
         d, t = ctypes.c_uint32(), ctypes.c_uint32()
         _check(library().hicache_pipeline_status(self.handle, layer, ctypes.byref(d), ctypes.byref(t)))
         return d.value, t.value
+
+    def layer_counters(self) -> int:
+        """Device address of the pool's per-layer counters (for the other ranks
+        of a tensor-parallel load)."""
+        out = ctypes.c_void_p()
+        _check(library().hicache_pool_layer_counters(self.handle, ctypes.byref(out)))
+        return out.value
 
     def wait_layer(self, layer: int, compute_stream=None):
         _check(library().hicache_wait_layer(self.handle, layer, _stream(compute_stream)))

@@ -1,6 +1,6 @@
 """Build libhicache.so in-tree with nvcc for sm_103a (GB300).
 
-Eight translation units, compiled in parallel, linked with the static CUDA
+Nine translation units, compiled in parallel, linked with the static CUDA
 runtime so the library loads on a machine without a GPU driver:
   csrc/hicache_kernels.cu    transfer and stand-in compute kernels
   csrc/hicache_api.cpp       errors, pinned memory, pools, transfers, events
@@ -10,6 +10,7 @@ runtime so the library loads on a machine without a GPU driver:
   csrc/hicache_group.cpp     buffer groups
   csrc/hicache_alloc.cpp     LIFO host-page allocator
   csrc/hicache_engine.cpp    submission engine (queue + worker thread)
+  csrc/hicache_tp.cpp        tensor-parallel load of a replicated latent
 """
 from __future__ import annotations
 
@@ -29,7 +30,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{INCLUDE}", f"-I{CSRC}"]
 SOURCES = ["hicache_kernels.cu", "hicache_api.cpp", "hicache_index.cpp", "hicache_pipeline.cpp",
-           "hicache_plan.cpp", "hicache_group.cpp", "hicache_alloc.cpp", "hicache_engine.cpp"]
+           "hicache_plan.cpp", "hicache_group.cpp", "hicache_alloc.cpp", "hicache_engine.cpp",
+           "hicache_tp.cpp"]
 
 
 def _nvcc() -> str:

@@ -213,6 +213,18 @@ int launch_pipelined_group(const GroupLaunch &x);
 // tile counter and exit count); launches that may overlap on the GPU need
 // their own.
 int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done, unsigned int *sched);
+// A rank's share of a tensor-parallel load of a replicated latent: every
+// vector goes to the same place in each of `tp` ranks' buffers (the launch's
+// blob holds tp * num_bufs pointers, rank-major, then the run table), and each
+// finished tile of layer l adds one to counters[r][l] for every rank r.
+constexpr int kMaxTp = 16;
+constexpr int kMaxTpBufs = 1024;   // tp * B * L device buffer pointers
+struct TpFanout {
+  int32_t tp;
+  int32_t pad;
+  unsigned int *counters[kMaxTp];
+};
+int launch_tp_pipelined_load(const XferLaunch &x, const TpFanout &f, unsigned int *sched);
 // Counters of allocation-free pipelined loads: a static device array of
 // kNoAllocMaxLayers layer counters followed by kNoAllocSchedSlots scheduler
 // pairs; *out receives its device address on the current device (looked up

@@ -157,9 +157,15 @@ __device__ __forceinline__ int find_run(const Run *runs, int n_runs, uint32_t w)
 // finds the run of its first vector (the same address in every lane) and each
 // lane then steps forward from it to its own run: no step where runs are
 // longer than a warp's span, one or two where they are a few rows long.
-template <int LAYOUT, bool ALL, bool TO_HOST>
+//
+// FANOUT (loads of one layer only): every vector is stored to the same place
+// in `fan` sets of device buffers, bufs[r * nb + i] for r < fan -- the ranks of
+// a tensor-parallel group that each hold the whole replicated latent.  One
+// layer's tile lies in one buffer, so only that buffer's base changes per rank.
+template <int LAYOUT, bool ALL, bool TO_HOST, bool FANOUT = false>
 __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, const Run *runs,
-                                          uint4 *const *bufs, int32_t g, int layer) {
+                                          uint4 *const *bufs, int32_t g, int layer, int fan = 1,
+                                          int nb = 0) {
   const int32_t outer = g / job.tiles_per_outer;
   const int32_t inner = g - outer * job.tiles_per_outer;
   int b, l;
@@ -206,6 +212,18 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
         }
       }
     }
+  }
+  if constexpr (FANOUT) {
+    static_assert(!ALL && !TO_HOST, "fan-out is for loads of one layer");
+    const int idx = b * h.L + l;
+    uint4 *const base0 = bufs[idx];
+    for (int r = 0; r < fan; ++r) {
+      uint4 *const base = bufs[r * nb + idx];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k)
+        if (dst[k] != nullptr) st_stream(base + (dst[k] - base0), v[k]);
+    }
+    return;
   }
 #pragma unroll
   for (int k = 0; k < kUnroll; ++k)
@@ -346,6 +364,65 @@ __global__ void __launch_bounds__(kThreads)
       atomicAdd(&layer_done[layer], 1u);
       s_next = int32_t(atomicAdd(&sched[0], 1u));
     }
+    __syncthreads();
+  }
+  release_schedule(sched);
+}
+
+// The share of one rank of a tensor-parallel group in a load of a replicated
+// latent ("Baidu's KVCache Overhaul", section "MLA-class cache optimization":
+// each GPU reads only its part of the pages over the host link, and the parts
+// are spread to every GPU over NVLink, layer by layer, alongside the loads).
+// Like pipelined_load_kernel -- every layer in one launch, in layer order,
+// tiles taken from a counter -- except that each vector read from the host is
+// stored into every rank's buffers (the blob holds f.tp sets of num_bufs
+// pointers, rank-major; a peer's buffers are reached over NVLink), and each
+// finished tile adds one to that layer's counter of every rank, behind a
+// system-wide fence, so a rank's counter of layer l reaches the tiles of all
+// ranks' shares once every share of that layer has landed in its buffers.
+// No CTA waits for another rank: a launch only stores and counts.
+template <int LAYOUT, class Params>
+__global__ void __launch_bounds__(kThreads)
+    tp_pipelined_load_kernel(const __grid_constant__ Params p, const __grid_constant__ TpFanout f,
+                             unsigned int *sched) {
+  __shared__ uint4 *s_bufs[kMaxTpBufs];
+  __shared__ int32_t s_next;
+  const int nb = p.h.num_bufs;
+  for (int i = threadIdx.x; i < f.tp * nb; i += kThreads) s_bufs[i] = reinterpret_cast<uint4 *>(p.blob[i]);
+  const Job &job = p.h.job[0];
+  const Run *runs = job_runs(p, 0);
+  const int32_t per_layer = job.total_tiles;            // tiles of one layer
+  const int32_t total = per_layer * p.h.L;
+  if (threadIdx.x == 0) s_next = int32_t(atomicAdd(&sched[0], 1u));
+  __syncthreads();
+  // A system-wide fence per tile would hold the loads back (a tile's stores
+  // must reach every GPU before the next tile starts), so the CTA holds the
+  // count of its finished tiles of one layer and fences and counts them once,
+  // when its next tile is in another layer or it has none left.  Tiles come
+  // in layer order, so that is as soon as its last tile of the layer is done.
+  int32_t held_layer = 0;                               // CTA-uniform, as g is
+  uint32_t held = 0;
+  for (int32_t g = s_next;; g = s_next) {
+    const bool done = g >= total;
+    const int32_t layer = done ? -1 : g / per_layer;
+    if (held != 0 && layer != held_layer) {
+      // The barrier orders every thread's stores before thread 0's fence, and
+      // the fence is cumulative: one system-wide fence by thread 0 makes the
+      // whole CTA's stores visible to every GPU before the counts (the
+      // pattern of a cooperative grid barrier).
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence_system();
+        for (int r = 0; r < f.tp; ++r) atomicAdd_system(&f.counters[r][held_layer], held);
+      }
+      held = 0;
+    }
+    if (done) break;
+    move_tile<LAYOUT, false, false, true>(p.h, job, runs, s_bufs, g - layer * per_layer, layer, f.tp, nb);
+    held_layer = layer;
+    ++held;
+    __syncthreads();                                    // every thread has read s_next
+    if (threadIdx.x == 0) s_next = int32_t(atomicAdd(&sched[0], 1u));
     __syncthreads();
   }
   release_schedule(sched);
@@ -507,7 +584,29 @@ cudaError_t launch_pipelined_layout(const XferLaunch &x, unsigned int *layer_don
   return cudaGetLastError();
 }
 
+template <int LAYOUT>
+cudaError_t launch_tp_layout(const XferLaunch &x, const TpFanout &f, unsigned int *sched) {
+  const cudaStream_t st = static_cast<cudaStream_t>(x.stream);
+  if (x.words <= kBlobWordsSmall) {
+    XferParamsSmall small;
+    tp_pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(params_for(x, small), f, sched);
+  } else {
+    tp_pipelined_load_kernel<LAYOUT><<<x.grid, kThreads, 0, st>>>(*x.params, f, sched);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+int launch_tp_pipelined_load(const XferLaunch &x, const TpFanout &f, unsigned int *sched) {
+  switch (x.layout) {
+    case kLayerFirst: return int(launch_tp_layout<kLayerFirst>(x, f, sched));
+    case kPageFirst: return int(launch_tp_layout<kPageFirst>(x, f, sched));
+    case kPageFirstDirect: return int(launch_tp_layout<kPageFirstDirect>(x, f, sched));
+    case kPageFirstDirectKV: return int(launch_tp_layout<kPageFirstDirectKV>(x, f, sched));
+    default: return int(cudaErrorInvalidValue);
+  }
+}
 
 int launch_pipelined_load(const XferLaunch &x, unsigned int *layer_done, unsigned int *sched) {
   switch (x.layout) {
