@@ -579,6 +579,25 @@ int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_
                               const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                               int32_t layout, void *stream);
 
+/* ---- bounds-checked builds ----------------------------------------------------------
+ * libhicache_checked.so is this library built with HICACHE_CHECKED=1: every
+ * transfer kernel checks each decoded vector before it touches memory -- the
+ * device buffer index against B*L, the offset in the device buffer against
+ * device_num_pages * page_size * row, the offset in the host pool against the
+ * pool, the run index against the run table -- and instead of an access
+ * outside them it skips the access and records the failure in a device word
+ * (no trap, no fault).  With the host's validation in front, no check should
+ * ever fail; the checked build is the device-side evidence of that.
+ * hicache_checked_build: 1 for the checked build, 0 otherwise.
+ * hicache_check_status: the first failed check since the last clear (0 if
+ * none; else bit 63 set, the check in bits 60-62 -- 1 buffer index, 2 device
+ * offset, 3 host offset, 4 run index -- and the offending value in bits 0-59)
+ * and the number of failed checks, of the current device; clears both if
+ * `clear`.  Reads device memory synchronously (call it once the transfers are
+ * done); always 0 and 0 in the plain build.  Errors: INVALID_ARG, CUDA. */
+int32_t hicache_checked_build(void);
+int hicache_check_status(uint64_t *first, uint64_t *count, int32_t clear);
+
 /* ---- roofline probe -----------------------------------------------------------
  * A plain streaming copy of `bytes` from src to dst with no index decode: each
  * CTA of `grid` (0 = one per SM) moves tiles of 256 threads x vecs_per_thread

@@ -14,6 +14,7 @@ Names follow the C ABI in ``include/hicache.h``:
     host_alloc / host_free, wait, prepass, segment_count, page_span, layer_checksum
     tp_share / tp_load_pipelined / Pool.layer_counters (tensor-parallel load of a replicated latent)
     stream_copy (roofline probe: plain zero-copy streaming copy)
+    checked_build / check_status (the bounds-checked build, HICACHE_CHECKED=1)
 """
 from __future__ import annotations
 
@@ -29,7 +30,8 @@ __all__ = [
     "PageAllocator", "Engine", "group_transfer", "group_load_pipelined", "group_plan", "GroupPlan",
     "MAX_GROUP", "PAGE_FIRST_DIRECT_KV",
     "host_alloc", "host_free", "wait", "prepass", "segment_count", "layer_checksum", "page_span",
-    "launch_count", "version", "stream_copy", "tp_share", "tp_load_pipelined",
+    "launch_count", "version", "stream_copy", "tp_share", "tp_load_pipelined", "checked_build",
+    "check_status",
 ]
 
 LAYOUT_POOL = -1
@@ -50,6 +52,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def library_path() -> str:
+    """libhicache.so, or the bounds-checked build libhicache_checked.so when
+    the environment sets HICACHE_CHECKED=1 before the library is first loaded."""
+    if os.environ.get("HICACHE_CHECKED") == "1":
+        return os.path.join(_HERE, "libhicache_checked.so")
     return os.path.join(_HERE, "libhicache.so")
 
 
@@ -114,6 +120,8 @@ def _bind(lib):
         "hicache_wait_layer": (ctypes.c_int, [_vp, _i32, _vp]),
         "hicache_wait": (ctypes.c_int, [_vp, _i64]),
         "hicache_stream_copy": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp]),
+        "hicache_checked_build": (_i32, []),
+        "hicache_check_status": (ctypes.c_int, [_P(ctypes.c_uint64), _P(ctypes.c_uint64), _i32]),
         "hicache_tp_share": (ctypes.c_int, [_i64, _i32, _i32, _P(_i64), _P(_i64)]),
         "hicache_pool_layer_counters": (ctypes.c_int, [_vp, _P(_vp)]),
         "hicache_tp_load_pipelined": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _P(_vp), _i32, _i32, _vp, _vp,
@@ -213,6 +221,20 @@ def host_free(ptr: int):
 def wait(stream=None, timeout_us: int = -1):
     """Block until `stream` is idle, for at most timeout_us (raises TIMEOUT)."""
     _check(library().hicache_wait(_stream(stream), timeout_us))
+
+def checked_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(library().hicache_checked_build())
+
+
+def check_status(clear: bool = False):
+    """(first failed bounds check, number of failed checks) of the current
+    device since the last clear; (0, 0) when every check passed (and always in
+    the plain build)."""
+    first, count = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(library().hicache_check_status(ctypes.byref(first), ctypes.byref(count), int(clear)))
+    return first.value, count.value
+
 
 def tp_share(n: int, tp: int, rank: int):
     """(first, count): the pairs rank `rank` of a tensor-parallel group of tp

@@ -125,7 +125,8 @@ int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int6
 }
 
 // A pool's shape, host alias and dividers, as one launch header.
-void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, hicache::XferHeader &h) {
+void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, int64_t device_pages,
+                hicache::XferHeader &h) {
   const Shape &s = pool->shape;
   const int32_t nb = int32_t(s.B * s.L);
   h.host = pool->host_dev;
@@ -148,12 +149,14 @@ void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, hicache::X
   h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
   h.job[1] = hicache::Job{0, nb, 0, 0, 0u, 0u};
   h.wait_previous = 0;
+  h.Dp = int32_t(device_pages);
+  h.host_vecs = s.B * s.Hp * s.LPV;
 }
 
 // Header fields shared by every launch of a pool, and its buffer pointers.
 void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, hicache::XferParams &params,
                  int64_t upp, int32_t layer) {
-  fill_shape(pool, upp, layer, params.h);
+  fill_shape(pool, upp, layer, kv->device_num_pages, params.h);
   const int32_t nb = int32_t(pool->shape.B * pool->shape.L);
   for (int32_t i = 0; i < nb; ++i)
     params.blob[i] = uint64_t(reinterpret_cast<uintptr_t>(kv->buf_ptrs[i]));
@@ -566,6 +569,19 @@ int hicache_stream_copy(void *dst, const void *src, size_t bytes, int32_t grid, 
   const int e = hicache::launch_stream_copy(dd, sd, uint64_t(bytes / 16), grid, vecs_per_thread, stream);
   if (e != 0) return cuda_error(cudaError_t(e), "stream copy kernel launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  return HICACHE_OK;
+}
+
+int32_t hicache_checked_build(void) { return int32_t(hicache::checked_build()); }
+
+int hicache_check_status(uint64_t *first, uint64_t *count, int32_t clear) {
+  g_last_error.clear();
+  if (!first || !count) return set_error(HICACHE_ERR_INVALID_ARG, "first or count is NULL");
+  unsigned long long f = 0, c = 0;
+  const int e = hicache::check_status(&f, &c, clear != 0);
+  if (e != 0) return cuda_error(cudaError_t(e), "reading the bounds-check words");
+  *first = f;
+  *count = c;
   return HICACHE_OK;
 }
 

@@ -38,7 +38,7 @@ int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int3
     const bool kv_all = (layout == HICACHE_PAGE_FIRST_DIRECT_KV) && all;
     outers[j] = lf_all ? s.B * s.L : (kv_all ? 1 : s.B);
     upp[j] = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
-    fill_shape(pools[j], upp[j], all ? 0 : layer, g.h[j]);
+    fill_shape(pools[j], upp[j], all ? 0 : layer, kvs[j].device_num_pages, g.h[j]);
     g.bufs_word[j] = word;
     for (int64_t i = 0; i < s.B * s.L; ++i)
       params.blob[word++] = uint64_t(reinterpret_cast<uintptr_t>(kvs[j].buf_ptrs[i]));
@@ -95,7 +95,7 @@ int enqueue_group_pipelined(hicache_pool *const *pools, const hicache_device_kv 
   int32_t word = 0;
   for (int32_t j = 0; j < np; ++j) {
     const Shape &s = pools[j]->shape;
-    fill_shape(pools[j], s.PV, 0, g.h[j]);
+    fill_shape(pools[j], s.PV, 0, kvs[j].device_num_pages, g.h[j]);
     g.bufs_word[j] = word;
     for (int64_t i = 0; i < s.B * s.L; ++i)
       params.blob[word++] = uint64_t(reinterpret_cast<uintptr_t>(kvs[j].buf_ptrs[i]));

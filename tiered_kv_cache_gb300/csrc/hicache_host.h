@@ -99,8 +99,9 @@ int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int
                   int64_t max_runs, Job &job, Run *table, int32_t word, int64_t launch_factor);
 int32_t fill_job(const std::vector<RunRec> &runs, size_t next, int64_t upp, int64_t outers,
                  int64_t max_runs, XferParams &params, int32_t word, int j, int64_t launch_factor = 1);
-// A pool's shape, host alias and dividers, as one launch header.
-void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, XferHeader &h);
+// A pool's shape, host alias and dividers, as one launch header (device_pages:
+// the pages of each device buffer, for bounds-checked builds).
+void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, int64_t device_pages, XferHeader &h);
 // fill_shape plus the device buffer pointers at the start of the blob.
 void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, XferParams &params, int64_t upp,
                  int32_t layer);

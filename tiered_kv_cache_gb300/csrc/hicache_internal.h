@@ -119,7 +119,27 @@ struct XferHeader {
   int32_t wait_previous;      // nonzero: the launch was started early behind work
                               // it may depend on; it waits for that work to finish
                               // before it touches memory
+  int32_t Dp;                 // device pages per buffer (bounds-checked builds)
+  int64_t host_vecs;          // vectors of the whole host pool (bounds-checked builds)
 };
+
+// ---- bounds-checked builds (HICACHE_CHECKED) -------------------------------
+// A build with HICACHE_CHECKED=1 checks every decoded vector against the
+// extents before touching it: the buffer index within [0, num_bufs), the
+// vector offset within the device buffer [0, Dp * P * V), the vector offset
+// within the host pool [0, host_vecs), and the run index within the run
+// table.  A failed check skips the access and is recorded in a device word
+// (hicache_check_status); nothing traps.  The predicate, shared by the kernels
+// and a host-side test: 0 if the vector is inside every extent, else the kind
+// of the first failed check.
+enum CheckKind : int32_t { kCheckOk = 0, kCheckBuffer = 1, kCheckDevice = 2, kCheckHost = 3, kCheckRun = 4 };
+HC_HD int32_t check_vector(int64_t bi, int64_t num_bufs, int64_t doff, int64_t dev_vecs, int64_t hoff,
+                           int64_t host_vecs) {
+  if (bi < 0 || bi >= num_bufs) return kCheckBuffer;
+  if (doff < 0 || doff >= dev_vecs) return kCheckDevice;
+  if (hoff < 0 || hoff >= host_vecs) return kCheckHost;
+  return kCheckOk;
+}
 
 template <int WORDS>
 struct XferParamsT {
@@ -236,6 +256,11 @@ int noalloc_layer_counters(unsigned int **out);
 // Record `msg` as the calling thread's last error and return `code` (hicache_api.cpp).
 int set_error_text(int code, const char *msg);
 int launch_checksum(const ChecksumParams &p, int grid, void *stream);
+// 1 in a bounds-checked build (HICACHE_CHECKED), else 0.
+int checked_build();
+// The bounds-check words of the current device (first failure, count),
+// cleared afterwards if `clear`; returns a cudaError_t value.
+int check_status(unsigned long long *first, unsigned long long *count, bool clear);
 // Roofline probe: copy nvec 16-byte vectors from src to dst (both
 // device-addressable), `unroll` (4 or 8) vectors in flight per thread.
 int launch_stream_copy(void *dst, const void *src, uint64_t nvec, int grid, int unroll, void *stream);

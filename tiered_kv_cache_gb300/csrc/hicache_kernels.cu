@@ -78,33 +78,55 @@ __device__ __forceinline__ void finish_after_previous_launch() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+#ifndef HICACHE_CHECKED
+#define HICACHE_CHECKED 0
+#endif
+
+// Bounds-checked builds: the first failed check (bit 63 set, the check's kind
+// in bits 60-62, the offending value in bits 0-59) and the number of failed
+// checks, since the host last cleared them.
+__device__ unsigned long long g_check_words[2];
+
+__device__ __forceinline__ void report_check(int32_t kind, int64_t value) {
+  const unsigned long long code = (1ull << 63) | (static_cast<unsigned long long>(kind & 7) << 60) |
+                                  (static_cast<unsigned long long>(value) & ((1ull << 60) - 1));
+  atomicCAS(&g_check_words[0], 0ull, code);
+  atomicAdd(&g_check_words[1], 1ull);
+}
+
 // Address of vector w of the current unit.  `dev` and `host` receive vector
 // pointers; b, l, run describe the unit (l is ignored where the unit spans all
-// layers).
+// layers).  Each layout gives the device buffer index, the vector offset in
+// that buffer and the vector offset in the host pool; a bounds-checked build
+// checks the three against their extents and gives null pointers (and records
+// the failure) instead of an address outside them.
 template <int LAYOUT, bool ALL>
 __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bufs, int b, int l,
                                            const Run &r, uint32_t w, uint4 *&dev, uint4 *&host) {
-  uint4 *const hbase = static_cast<uint4 *>(h.host);
+  int64_t bi, doff, hoff;
   if (LAYOUT == kLayerFirst) {
     // host (B, L, size, R): unit (b, l, run) is contiguous on both sides
-    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
-    host = hbase + (int64_t(b * h.L + l) * h.Hp + r.h0) * h.PV + w;
+    bi = b * h.L + l;
+    doff = int64_t(r.d0) * h.PV + w;
+    hoff = (int64_t(b * h.L + l) * h.Hp + r.h0) * h.PV + w;
   } else if (LAYOUT == kPageFirstDirect && ALL) {
     // host (B, Hp, L, P, R): the unit is [page j][layer ll][token, elem]
     const uint32_t j = fast_div(w, h.fd_LPV);
     const uint32_t rem = w - j * h.LPV;
     const uint32_t ll = fast_div(rem, h.fd_PV);
     const uint32_t q = rem - ll * h.PV;
-    dev = bufs[b * h.L + ll] + int64_t(r.d0 + int32_t(j)) * h.PV + q;
-    host = hbase + (int64_t(b) * h.Hp + r.h0) * h.LPV + w;
+    bi = b * h.L + int32_t(ll);
+    doff = int64_t(r.d0 + int32_t(j)) * h.PV + q;
+    hoff = (int64_t(b) * h.Hp + r.h0) * h.LPV + w;
   } else if (LAYOUT == kPageFirst && ALL) {
     // host (B, size, L, R): the unit is [token][layer ll][elem]
     const uint32_t tok = fast_div(w, h.fd_LV);
     const uint32_t rem = w - tok * h.LV;
     const uint32_t ll = fast_div(rem, h.fd_V);
     const uint32_t v = rem - ll * h.V;
-    dev = bufs[b * h.L + ll] + (int64_t(r.d0) * h.P + tok) * h.V + v;
-    host = hbase + (int64_t(b) * h.Hp + r.h0) * h.P * h.LV + w;
+    bi = b * h.L + int32_t(ll);
+    doff = (int64_t(r.d0) * h.P + tok) * h.V + v;
+    hoff = (int64_t(b) * h.Hp + r.h0) * h.P * h.LV + w;
   } else if (LAYOUT == kPageFirstDirectKV && ALL) {
     // host (Hp, B, L, P, R): the unit is the whole run, every buffer:
     // [page j][buffer bb][layer ll][token, elem]
@@ -114,27 +136,41 @@ __device__ __forceinline__ void map_vector(const XferHeader &h, uint4 *const *bu
     rem -= bb * h.LPV;
     const uint32_t ll = fast_div(rem, h.fd_PV);
     const uint32_t q = rem - ll * h.PV;
-    dev = bufs[bb * h.L + ll] + int64_t(r.d0 + int32_t(j)) * h.PV + q;
-    host = hbase + int64_t(r.h0) * h.BLPV + w;
+    bi = int32_t(bb) * h.L + int32_t(ll);
+    doff = int64_t(r.d0 + int32_t(j)) * h.PV + q;
+    hoff = int64_t(r.h0) * h.BLPV + w;
   } else if (LAYOUT == kPageFirstDirect) {
     // one layer: device contiguous over the run, host one P*R block per page
     const uint32_t j = fast_div(w, h.fd_PV);
     const uint32_t q = w - j * h.PV;
-    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
-    host = hbase + ((int64_t(b) * h.Hp + r.h0 + j) * h.L + l) * h.PV + q;
+    bi = b * h.L + l;
+    doff = int64_t(r.d0) * h.PV + w;
+    hoff = ((int64_t(b) * h.Hp + r.h0 + j) * h.L + l) * h.PV + q;
   } else if (LAYOUT == kPageFirstDirectKV) {
     // one layer: device contiguous over the run, host one P*R block per page
     const uint32_t j = fast_div(w, h.fd_PV);
     const uint32_t q = w - j * h.PV;
-    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
-    host = hbase + ((int64_t(r.h0 + int32_t(j)) * h.B + b) * h.L + l) * h.PV + q;
+    bi = b * h.L + l;
+    doff = int64_t(r.d0) * h.PV + w;
+    hoff = ((int64_t(r.h0 + int32_t(j)) * h.B + b) * h.L + l) * h.PV + q;
   } else {
     // page_first, one layer: device contiguous over the run, host one row per token
     const uint32_t tok = fast_div(w, h.fd_V);
     const uint32_t v = w - tok * h.V;
-    dev = bufs[b * h.L + l] + int64_t(r.d0) * h.PV + w;
-    host = hbase + (((int64_t(b) * h.Hp + r.h0) * h.P + tok) * h.L + l) * h.V + v;
+    bi = b * h.L + l;
+    doff = int64_t(r.d0) * h.PV + w;
+    hoff = (((int64_t(b) * h.Hp + r.h0) * h.P + tok) * h.L + l) * h.V + v;
   }
+#if HICACHE_CHECKED
+  const int32_t kind = check_vector(bi, h.num_bufs, doff, int64_t(h.Dp) * h.PV, hoff, h.host_vecs);
+  if (kind != kCheckOk) {
+    report_check(kind, kind == kCheckBuffer ? bi : kind == kCheckDevice ? doff : hoff);
+    dev = host = nullptr;
+    return;
+  }
+#endif
+  dev = bufs[bi] + doff;
+  host = static_cast<uint4 *>(h.host) + hoff;
 }
 
 // The run holding vector w of an outer unit: the last run with vec0 <= w.
@@ -198,11 +234,23 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
         uint32_t end = rb_end;
         while (w >= end) {                                 // runs shorter than the warp's span
           ++r;
+#if HICACHE_CHECKED
+          if (r >= job.n_runs) break;
+#endif
           end = uint32_t(runs[r].vec0) + uint32_t(runs[r].len) * h.unit_per_page;
         }
+#if HICACHE_CHECKED
+        if (r >= job.n_runs) {
+          report_check(kCheckRun, r);
+          continue;
+        }
+#endif
         const Run cur = runs[r];
         uint4 *dev, *host;
         map_vector<LAYOUT, ALL>(h, bufs, b, l, cur, w - uint32_t(cur.vec0), dev, host);
+#if HICACHE_CHECKED
+        if (dev == nullptr) continue;
+#endif
         if (TO_HOST) {
           v[k] = ld_stream(dev);
           dst[k] = host;
@@ -730,6 +778,20 @@ int launch_stream_copy(void *dst, const void *src, uint64_t nvec, int grid, int 
   else
     return int(cudaErrorInvalidValue);
   return int(cudaGetLastError());
+}
+
+int checked_build() { return HICACHE_CHECKED; }
+
+int check_status(unsigned long long *first, unsigned long long *count, bool clear) {
+  unsigned long long w[2] = {0, 0};
+  cudaError_t e = cudaMemcpyFromSymbol(w, g_check_words, sizeof w);
+  if (e == cudaSuccess && clear) {
+    const unsigned long long z[2] = {0, 0};
+    e = cudaMemcpyToSymbol(g_check_words, z, sizeof z);
+  }
+  *first = w[0];
+  *count = w[1];
+  return int(e);
 }
 
 int launch_checksum(const ChecksumParams &p, int grid, void *stream) {

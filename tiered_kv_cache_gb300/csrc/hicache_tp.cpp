@@ -144,7 +144,7 @@ int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_
     pool->layer_signal[size_t(l)] = 1;
   }
   thread_local XferParams params;
-  fill_shape(pool, s.PV, 0, params.h);
+  fill_shape(pool, s.PV, 0, Dp, params.h);
   for (int32_t r = 0; r < tp; ++r)
     for (int32_t i = 0; i < nb; ++i)
       params.blob[r * nb + i] = uint64_t(reinterpret_cast<uintptr_t>(rank_kvs[r].buf_ptrs[i]));
