@@ -739,6 +739,17 @@ def bench_mla_overlap(torch, hc, args):
         def loads_graph():
             plan.load_layers(kv, stream=xfer)
 
+        def loads_chained():
+            for layer in range(L):
+                plan.load_layer_chained(kv, layer, stream=xfer)
+
+        def overlapped_chained(reps):
+            for layer in range(L):
+                plan.load_layer_chained(kv, layer, stream=xfer)
+                pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
         def overlapped_graph(reps):
             plan.load_layers(kv, stream=xfer)
             for layer in range(L):
@@ -765,6 +776,8 @@ def bench_mla_overlap(torch, hc, args):
         c2 = timed(lambda: overlapped_two_streams(reps))
         ag = timed(loads_graph)
         cg = timed(lambda: overlapped_graph(reps))
+        ach = timed(loads_chained)
+        cch = timed(lambda: overlapped_chained(reps))
         out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
             "pages": n, "bytes": nbytes,
             "per_layer_loads_ms": round(a * 1e3, 3), "per_layer_load_gbs": round(nbytes / a / GB, 1),
@@ -782,6 +795,10 @@ def bench_mla_overlap(torch, hc, args):
             "per_layer_graph_ms": round(ag * 1e3, 3), "per_layer_graph_gbs": round(nbytes / ag / GB, 1),
             "overlapped_graph_ms": round(cg * 1e3, 3),
             "overlap_efficiency_graph": round((ag + b - cg) / min(ag, b), 3),
+            "per_layer_chained_ms": round(ach * 1e3, 3),
+            "per_layer_chained_gbs": round(nbytes / ach / GB, 1),
+            "overlapped_chained_ms": round(cch * 1e3, 3),
+            "overlap_efficiency_chained": round((ach + b - cch) / min(ach, b), 3),
         }
         plan.close()
     launches = hc.launch_count() - launches0
@@ -855,7 +872,8 @@ def bench_nsa_group(torch, hc, args):
     pipelined group load (every layer of every pool in one launch, each
     pool's layers signalled as they land), and a group plan's per-layer
     launches replayed from one CUDA graph (its first, capturing call is a
-    warm-up).  Each
+    warm-up), and one chained call per layer (each layer's group launch
+    starting as the previous layer's drains).  Each
     variant is enqueued behind a sleep kernel on a gate stream, so the device
     time excludes the host's enqueue cost, which is reported beside it."""
     from tiered_kv_cache_gb300 import workloads as wl
@@ -913,6 +931,8 @@ def bench_nsa_group(torch, hc, args):
             "all_layers_group": lambda: hc.group_transfer(pools, kvs, dp, hp, hc.LOAD, stream=stream),
             "pipelined_group": lambda: hc.group_load_pipelined(pools, kvs, dp, hp, stream=stream),
             "per_layer_group_graph": lambda: plan.load_layers(kvs, stream=stream),
+            "per_layer_group_chained": lambda: [plan.load_layer_chained(kvs, layer, stream=stream)
+                                                for layer in range(L)],
         }
         plan = hc.group_plan(pools, dp, hp, Dp)
         r = {"pages": len(dp), "bytes": nbytes}

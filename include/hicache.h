@@ -277,6 +277,32 @@ int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, 
  * is enqueued. */
 int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                             int32_t layer_id, void *stream);
+/* One layer of a load plan, as hicache_plan_load_layer, chained to the plan's
+ * previous layer: the per-layer load of "Why compute, H2D, and D2H should stay
+ * in one GPU execution domain" ("Rethinking the SGLang HiCache Boundary"),
+ * one call per layer as the layers are needed, without the gap between
+ * per-layer kernels.  A call for layer l continues a chain when the plan's
+ * previous chained call loaded layer l - 1 on the same stream; its kernel is
+ * then a programmatic dependent launch that starts moving data while layer
+ * l - 1's kernel drains its last tiles.  The caller guarantees that nothing
+ * else is enqueued on that stream between the calls of a chain (compute goes
+ * on another stream); any other call -- layer 0, a layer out of order,
+ * another stream -- waits for all earlier work on the stream like a plain
+ * call.  Layers overlap, so no two device buffers may share bytes (checked
+ * once per set of buffers: INVALID_ARG).
+ *   - Each layer is signalled on the device, not by an event recorded between
+ *     kernels (which would stop them overlapping): every CTA counts itself into
+ *     the layer's pool counter once its tiles have landed, and
+ *     hicache_wait_layer(pool, l, stream) waits for that count.  The layer
+ *     events are recorded after the call for the last layer.
+ *   - A capturing stream is refused (INVALID_ARG): the count each layer must
+ *     reach is raised on the host when the call is enqueued.
+ *   - Calls of one plan's chain come from one thread, in layer order.
+ * Errors: INVALID_ARG (NULL plan, backup plan, layer_id outside [0,
+ * num_layers), bad layout or kv, overlapping buffers, capturing stream),
+ * CUDA; on a refused call nothing is enqueued. */
+int hicache_plan_load_layer_chained(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                                    int32_t layer_id, void *stream);
 /* hicache_load_pipelined without any allocation.  The pages have no
  * counterpart to this entry point: it serves callers that cannot allocate
  * device memory when they load -- for example an engine whose device memory is
@@ -402,6 +428,19 @@ int hicache_group_plan_execute(const hicache_group_plan *plan, const hicache_dev
  * is allowed. */
 int hicache_group_plan_load_layers(hicache_group_plan *plan, const hicache_device_kv *kvs, int32_t layout,
                                    void *stream);
+/* hicache_plan_load_layer_chained for a buffer group: one group launch for
+ * layer layer_id of every pool, chained to the plan's previous chained call
+ * when that loaded layer_id - 1 on the same stream (nothing else enqueued on
+ * the stream in between), and every CTA counted into each pool's counter of
+ * the layer, so hicache_wait_layer on any pool of the group waits for that
+ * pool's layer on the device.  Every pool's layer events are recorded after
+ * the call for the last layer.  No two device buffers of the group may
+ * overlap; a capturing stream is refused.  Errors as
+ * hicache_group_plan_execute, plus INVALID_ARG for layer_id outside [0,
+ * num_layers), overlapping buffers or a capturing stream; on a refused call
+ * nothing is enqueued. */
+int hicache_group_plan_load_layer_chained(hicache_group_plan *plan, const hicache_device_kv *kvs,
+                                          int32_t layout, int32_t layer_id, void *stream);
 int hicache_group_plan_destroy(hicache_group_plan *plan);
 
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */

@@ -165,9 +165,10 @@ def layer_sums(mirror, dp, L, Dp):
 @pytest.mark.parametrize("tokens", [4096, 16384, 65536])
 def test_mla61_per_layer_and_pipelined_loads(tokens):
     """61 per-layer loads, each gating the stand-in attention of its layer
-    through the layer's event, then the same load as one pipelined launch
-    gated per layer on the device counters: every device buffer against the
-    oracle's per-layer loads applied in the same order."""
+    through the layer's event, then the same load as one pipelined launch and
+    as 61 chained per-layer calls, both gated per layer on the device counters:
+    every device buffer against the oracle's per-layer loads applied in the
+    same order."""
     s = wl.MLA_LATENT
     t = wl.mla_transfer(s, tokens)
     B, L, P, R, Hp = dims(s)
@@ -210,6 +211,20 @@ def test_mla61_per_layer_and_pipelined_loads(tokens):
         hc.wait(xfer, 30_000_000)
         assert hc.launch_count() - c0 == 1 + L
         mirror.compare(bufs, f"pipelined load of {tokens} tokens")
+        assert np.array_equal(sums.cpu().numpy().view(np.uint64), want)
+        # and as 61 chained per-layer calls, each layer waited for on the device
+        gh.sentinel_fill(bufs, SENT8)
+        sums.zero_()
+        torch.cuda.synchronize()
+        c0 = hc.launch_count()
+        for layer in range(L):
+            plan.load_layer_chained(kv, layer, stream=xfer)
+            pool.wait_layer(layer, comp)
+            hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        hc.wait(comp, 30_000_000)
+        hc.wait(xfer, 30_000_000)
+        assert hc.launch_count() - c0 == 2 * L
+        mirror.compare(bufs, f"chained per-layer loads of {tokens} tokens")
         assert np.array_equal(sums.cpu().numpy().view(np.uint64), want)
         plan.close()
         del host

@@ -8,7 +8,7 @@ library is not built, importing works but every call raises.
 Names follow the C ABI in ``include/hicache.h``:
     Pool.backup / Pool.load / Pool.load_layer / Pool.load_pipelined / Pool.backup_load
     Pool.wait_layer / Pool.layer_event
-    Pool.plan(...) -> Plan.execute / load_layer / load_layers / load_pipelined
+    Pool.plan(...) -> Plan.execute / load_layer / load_layer_chained / load_layers / load_pipelined
     group_transfer / group_load_pipelined / group_plan(...) -> GroupPlan
     Engine (submission engine), PageAllocator (host pages)
     host_alloc / host_free, wait, prepass, segment_count, page_span, layer_checksum
@@ -109,11 +109,13 @@ def _bind(lib):
         "hicache_group_plan_create": (ctypes.c_int, [_P(_vp), _i32, _vp, _vp, _i64, _i64, _P(_vp)]),
         "hicache_group_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_group_plan_load_layers": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
+        "hicache_group_plan_load_layer_chained": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_group_plan_destroy": (ctypes.c_int, [_vp]),
         "hicache_plan_create": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _i32, _P(_vp)]),
         "hicache_plan_execute": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layer": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_load_layers": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _vp]),
+        "hicache_plan_load_layer_chained": (ctypes.c_int, [_vp, _P(_DeviceKVStruct), _i32, _i32, _vp]),
         "hicache_plan_info": (ctypes.c_int, [_vp, _P(_i64), _P(_i64)]),
         "hicache_plan_destroy": (ctypes.c_int, [_vp]),
         "hicache_layer_event": (ctypes.c_int, [_vp, _i32, _P(_vp)]),
@@ -407,6 +409,15 @@ class GroupPlan:
         _check(library().hicache_group_plan_load_layers(self.handle, self._kvs(kvs), layout,
                                                         _stream(stream)))
 
+    def load_layer_chained(self, kvs, layer: int, layout=LAYOUT_POOL, stream=None):
+        """One layer of every pool in one launch, chained to this plan's
+        previous layer on the same stream (nothing else on that stream in
+        between); each pool's wait_layer waits for it on the device."""
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_group_plan_load_layer_chained(self.handle, self._kvs(kvs), layout, layer,
+                                                               _stream(stream)))
+
     def close(self):
         if getattr(self, "handle", None):
             library().hicache_group_plan_destroy(self.handle)
@@ -687,6 +698,15 @@ class Plan:
             layout = LAYOUTS[layout]
         _check(library().hicache_plan_load_layer(self.handle, kv.ref, layout, layer,
                                                  _stream(stream)))
+
+    def load_layer_chained(self, kv: DeviceKV, layer: int, layout=LAYOUT_POOL, stream=None):
+        """Load one layer, chained to this plan's previous layer on the same
+        stream (nothing else may go on that stream in between); the pool's
+        wait_layer waits for it on the device."""
+        if isinstance(layout, str):
+            layout = LAYOUTS[layout]
+        _check(library().hicache_plan_load_layer_chained(self.handle, kv.ref, layout, layer,
+                                                         _stream(stream)))
 
     def load_pipelined(self, kv: DeviceKV, layout=LAYOUT_POOL, stream=None):
         if isinstance(layout, str):

@@ -151,6 +151,7 @@ void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, int64_t de
   h.wait_previous = 0;
   h.Dp = int32_t(device_pages);
   h.host_vecs = s.B * s.Hp * s.LPV;
+  h.signal = nullptr;
 }
 
 // Header fields shared by every launch of a pool, and its buffer pointers.
@@ -176,7 +177,7 @@ int check_device(const hicache_pool *pool) {
 // per chunk so the two directions share every CTA.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
-            void *stream, bool pdl_first) {
+            void *stream, bool pdl_first, unsigned int *signal, int64_t *signalled) {
   const bool bidir = load_runs != nullptr;
   if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
   if (int rc = check_device(pool)) return rc;
@@ -194,6 +195,7 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   thread_local hicache::XferParams params;
   hicache::XferHeader &h = params.h;
   fill_header(pool, kv, params, upp, all ? 0 : layer);
+  if (!bidir) h.signal = signal;
 
   size_t next0 = 0, next1 = 0;
   const size_t n1 = bidir ? load_runs->size() : 0;
@@ -235,6 +237,7 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     const int e = hicache::launch_xfer(x);
     if (e != 0) return cuda_error(cudaError_t(e), "transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (signalled && h.signal) *signalled += x.grid;
     next0 += size_t(c0);
     next1 += size_t(c1);
   }

@@ -22,14 +22,19 @@ namespace hicache {
 // runs that fits the parameters of all of them.  pdl_first: the first launch
 // may start while the kernel before it on the stream drains; that kernel must
 // be a one-layer group load of another layer.
+// signal (one-layer loads): every CTA of every launch adds one to each pool's
+// counter of that layer once its last tile has landed; *signalled grows by
+// the CTAs launched.
 int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int32_t np,
                   const std::vector<RunRec> &runs, int32_t layout, int32_t layer, bool to_host,
-                  void *stream, bool pdl_first = false) {
+                  void *stream, bool pdl_first = false, bool signal = false, int64_t *signalled = nullptr) {
   if (runs.empty()) return HICACHE_OK;
   const bool all = layer < 0;
   thread_local hicache::GroupParams params;
   hicache::GroupHeader &g = params.g;
   g.njobs = np;
+  for (int32_t j = 0; j < hicache::kMaxGroup; ++j)
+    g.signal[j] = signal && !all && j < np ? pools[j]->layer_done + layer : nullptr;
   int32_t word = 0;
   int64_t outers[hicache::kMaxGroup], upp[hicache::kMaxGroup];
   for (int32_t j = 0; j < np; ++j) {
@@ -78,6 +83,7 @@ int enqueue_group(hicache_pool *const *pools, const hicache_device_kv *kvs, int3
     const int e = hicache::launch_group(x);
     if (e != 0) return cuda_error(cudaError_t(e), "group transfer kernel launch");
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (signalled && g.signal[0]) *signalled += x.grid;
     next += size_t(c);
   }
   return HICACHE_OK;
@@ -92,6 +98,7 @@ int enqueue_group_pipelined(hicache_pool *const *pools, const hicache_device_kv 
   thread_local hicache::GroupParams params;
   hicache::GroupHeader &g = params.g;
   g.njobs = np;
+  for (int32_t j = 0; j < hicache::kMaxGroup; ++j) g.signal[j] = nullptr;
   int32_t word = 0;
   for (int32_t j = 0; j < np; ++j) {
     const Shape &s = pools[j]->shape;
@@ -305,6 +312,13 @@ struct hicache_group_plan {
   std::vector<int64_t> graph_pages;      // every pool's device_num_pages
   int32_t graph_layout = -1;
   int64_t graph_launches = 0;
+  // hicache_group_plan_load_layer_chained: the stream and layer of the last
+  // chained call, and the buffers found disjoint
+  std::mutex chain_mu;
+  void *chain_stream = nullptr;
+  int32_t chain_layer = -1;
+  std::vector<void *> chain_bufs;
+  std::vector<int64_t> chain_pages;
 };
 
 namespace {
@@ -370,6 +384,63 @@ int hicache_group_plan_execute(const hicache_group_plan *plan, const hicache_dev
       std::lock_guard<std::mutex> g(p->signal_mu);
       p->layer_signal[size_t(layer_id)] = 0;
     }
+  }
+  return HICACHE_OK;
+}
+
+int hicache_group_plan_load_layer_chained(hicache_group_plan *plan, const hicache_device_kv *kvs,
+                                          int32_t layout, int32_t layer_id, void *stream) {
+  clear_error();
+  int32_t lay = 0;
+  int rc = check_plan_call(plan, kvs, layout, &lay);
+  if (rc) return rc;
+  hicache_pool *const *pools = plan->pools.data();
+  const int32_t np = int32_t(plan->pools.size());
+  const int64_t L = pools[0]->shape.L;
+  if (layer_id < 0 || layer_id >= L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id, (long long)L);
+  if ((rc = refuse_capture(stream))) return rc;
+  if (!wait_value32())
+    return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no chained loads");
+  std::lock_guard<std::mutex> g(plan->chain_mu);
+  std::vector<void *> bufs;
+  std::vector<int64_t> pages;
+  for (int32_t i = 0; i < np; ++i) {
+    bufs.insert(bufs.end(), kvs[i].buf_ptrs, kvs[i].buf_ptrs + pools[i]->shape.B * L);
+    pages.push_back(kvs[i].device_num_pages);
+  }
+  if (plan->chain_bufs != bufs || plan->chain_pages != pages) {
+    // consecutive layers' launches overlap: no two buffers of the group may share bytes
+    std::vector<std::pair<uintptr_t, uint64_t>> spans;
+    for (int32_t i = 0; i < np; ++i) {
+      const Shape &s = pools[i]->shape;
+      const uint64_t bytes = uint64_t(kvs[i].device_num_pages) * uint64_t(s.PV) * 16u;
+      for (int64_t b = 0; b < s.B * s.L; ++b)
+        spans.emplace_back(reinterpret_cast<uintptr_t>(kvs[i].buf_ptrs[b]), bytes);
+    }
+    if ((rc = check_disjoint(spans))) return rc;
+    plan->chain_bufs = bufs;
+    plan->chain_pages = pages;
+    plan->chain_layer = -1;
+  }
+  const bool chained = plan->chain_layer >= 0 && plan->chain_stream == stream &&
+                       layer_id == plan->chain_layer + 1;
+  int64_t signalled = 0;
+  rc = enqueue_group(pools, kvs, np, plan->runs, lay, layer_id, false, stream, chained, true, &signalled);
+  plan->chain_stream = stream;
+  plan->chain_layer = rc == HICACHE_OK && layer_id + 1 < L ? layer_id : -1;
+  for (int32_t i = 0; i < np; ++i) {
+    std::lock_guard<std::mutex> gs(pools[i]->signal_mu);
+    pools[i]->layer_target[size_t(layer_id)] += uint32_t(signalled);
+    pools[i]->layer_signal[size_t(layer_id)] = 1;
+  }
+  if (rc != HICACHE_OK) return rc;
+  if (layer_id + 1 == L) {
+    for (int32_t i = 0; i < np; ++i)
+      for (int64_t l = 0; l < L; ++l) {
+        const cudaError_t e = cudaEventRecord(pools[i]->events[size_t(l)], static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+      }
   }
   return HICACHE_OK;
 }

@@ -108,10 +108,13 @@ void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, XferPara
 // Enqueue validated runs (see hicache_api.cpp).  A call split over several
 // launches has each launch after the first start programmatically behind the
 // one before it.  pdl_first: the first launch too, behind the kernel before it
-// on the stream, which must be a one-layer load of another layer.
+// on the stream, which must be a one-layer load of another layer.  signal (one
+// direction only): every CTA of every launch adds one to *signal once its
+// last tile has landed; *signalled grows by the CTAs launched.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
-            void *stream, bool pdl_first = false);
+            void *stream, bool pdl_first = false, unsigned int *signal = nullptr,
+            int64_t *signalled = nullptr);
 // Enqueue validated load runs as pipelined launches (every layer, layer by
 // layer, per-layer counters) and update the pool's per-layer signals
 // (hicache_pipeline.cpp).

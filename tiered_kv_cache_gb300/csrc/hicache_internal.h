@@ -121,6 +121,8 @@ struct XferHeader {
                               // before it touches memory
   int32_t Dp;                 // device pages per buffer (bounds-checked builds)
   int64_t host_vecs;          // vectors of the whole host pool (bounds-checked builds)
+  unsigned int *signal;       // if not null, every CTA of a one-direction launch adds
+                              // one here once its last tile has landed
 };
 
 // ---- bounds-checked builds (HICACHE_CHECKED) -------------------------------
@@ -181,6 +183,9 @@ struct GroupHeader {
   // scheduler words (as launch_pipelined_load)
   unsigned int *layer_done[kMaxGroup];
   unsigned int *sched;
+  // one-layer group loads only: if signal[0] is not null, every CTA adds one to
+  // signal[j] for each job j once its last tile has landed
+  unsigned int *signal[kMaxGroup];
 };
 template <int WORDS>
 struct GroupParamsT {

@@ -302,6 +302,15 @@ __global__ void __launch_bounds__(kThreads) xfer_kernel(const __grid_constant__ 
     if (g + int32_t(gridDim.x) >= job.total_tiles) allow_next_launch();
     move_tile<LAYOUT, ALL, TO_HOST>(p.h, job, runs, s_bufs, g, p.h.layer);
   }
+  if (p.h.signal != nullptr) {
+    // The barrier orders the CTA's stores before thread 0's fence, which is
+    // cumulative: one fence covers the whole CTA before it counts itself done.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(p.h.signal, 1u);
+    }
+  }
   finish_after_previous_launch();
 }
 
@@ -358,6 +367,13 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const __grid_constant__
     const Run *runs = reinterpret_cast<const Run *>(&p.blob[h.job[0].runs_word]);
     move_tile<LAYOUT, ALL, TO_HOST>(h, h.job[0], runs, s_bufs + p.g.bufs_word[j], g - p.g.tile_start[j],
                                     h.layer);
+  }
+  if (p.g.signal[0] != nullptr) {
+    __syncthreads();                                    // as in xfer_kernel: one cumulative fence
+    if (threadIdx.x == 0) {
+      __threadfence();
+      for (int j = 0; j < p.g.njobs; ++j) atomicAdd(p.g.signal[j], 1u);
+    }
   }
   finish_after_previous_launch();
 }

@@ -32,6 +32,13 @@ struct hicache_plan {
   int64_t graph_pages = 0;
   int32_t graph_layout = -1;
   int64_t graph_launches = 0;         // kernel launches one replay makes
+  // hicache_plan_load_layer_chained: the stream and layer of the last chained
+  // call, and the device KV whose buffers were found disjoint
+  std::mutex chain_mu;
+  void *chain_stream = nullptr;
+  int32_t chain_layer = -1;
+  std::vector<void *> chain_bufs;
+  int64_t chain_pages = 0;
 };
 
 namespace hicache {
@@ -179,6 +186,64 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
   clear_error();
   if (layer_id < 0) return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d is negative", layer_id);
   return hicache_plan_execute(plan, kv, layout, layer_id, stream);
+}
+
+int hicache_plan_load_layer_chained(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
+                                    int32_t layer_id, void *stream) {
+  clear_error();
+  if (!plan) return set_error(HICACHE_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->direction != HICACHE_DIR_LOAD)
+    return set_error(HICACHE_ERR_INVALID_ARG, "a per-layer transfer must be a load");
+  hicache_pool *pool = plan->pool;
+  const Shape &s = pool->shape;
+  if (layer_id < 0 || layer_id >= s.L)
+    return set_error(HICACHE_ERR_INVALID_ARG, "layer_id %d outside [0, %lld)", layer_id, (long long)s.L);
+  int32_t lay = 0;
+  int rc = resolve_layout(layout, s.layout, &lay);
+  if (rc) return rc;
+  if ((rc = check_kv(pool, kv, plan->device_num_pages))) return rc;
+  if ((rc = check_device(pool))) return rc;
+  if ((rc = refuse_capture(stream))) return rc;
+  if (!wait_value32())
+    return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no chained loads");
+  std::lock_guard<std::mutex> g(plan->chain_mu);
+  // consecutive layers' kernels overlap, so no two buffers may share bytes
+  // (checked once per set of buffers)
+  const std::vector<void *> bufs(kv->buf_ptrs, kv->buf_ptrs + s.B * s.L);
+  if (plan->chain_bufs != bufs || plan->chain_pages != kv->device_num_pages) {
+    std::vector<std::pair<uintptr_t, uint64_t>> spans;
+    const uint64_t buf_bytes = uint64_t(kv->device_num_pages) * uint64_t(s.PV) * 16u;
+    for (void *b : bufs) spans.emplace_back(reinterpret_cast<uintptr_t>(b), buf_bytes);
+    if ((rc = check_disjoint(spans))) return rc;
+    plan->chain_bufs = bufs;
+    plan->chain_pages = kv->device_num_pages;
+    plan->chain_layer = -1;
+  }
+  // the call continues a chain when it loads the layer after the plan's
+  // previous chained call, on the same stream: its kernel then starts as that
+  // layer's kernel drains, with nothing in between on the stream
+  const bool chained = plan->chain_layer >= 0 && plan->chain_stream == stream &&
+                       layer_id == plan->chain_layer + 1;
+  int64_t signalled = 0;
+  rc = enqueue(pool, kv, plan->runs, nullptr, lay, layer_id, false, stream, chained,
+               pool->layer_done + layer_id, &signalled);
+  plan->chain_stream = stream;
+  plan->chain_layer = rc == HICACHE_OK && layer_id + 1 < s.L ? layer_id : -1;
+  {
+    // the launches that went out count towards the layer, even if a later one failed
+    std::lock_guard<std::mutex> gs(pool->signal_mu);
+    pool->layer_target[size_t(layer_id)] += uint32_t(signalled);
+    pool->layer_signal[size_t(layer_id)] = 1;
+  }
+  if (rc != HICACHE_OK) return rc;
+  if (layer_id + 1 == s.L) {
+    // the layer events fire once the last layer's kernel is done
+    for (int64_t l = 0; l < s.L; ++l) {
+      const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+    }
+  }
+  return HICACHE_OK;
 }
 
 int hicache_plan_load_pipelined(const hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
