@@ -96,8 +96,10 @@ int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int
                   int64_t launch_factor) {
   int64_t vecs = 0;
   int32_t count = 0;
+  bool uniform = true;
   while (next + size_t(count) < runs.size() && count < max_runs) {
     const RunRec &r = runs[next + size_t(count)];
+    if (r.len != runs[next].len) uniform = false;
     const int64_t nv = vecs + r.len * upp;
     const int64_t tiles = (nv + hicache::kTileVecs - 1) / hicache::kTileVecs;
     if (nv > kMaxOuterVecs || tiles * outers * launch_factor > kMaxTiles) {
@@ -111,7 +113,9 @@ int32_t fill_runs(const std::vector<RunRec> &runs, size_t next, int64_t upp, int
   job.n_runs = count;
   job.runs_word = word;
   job.vecs_per_outer = uint32_t(vecs);
-  job.pad = 0;
+  // runs of one length: the kernel finds a vector's run by one division
+  job.run_vecs = uniform && count > 0 ? uint32_t(runs[next].len * upp) : 0u;
+  job.fd_run = hicache::make_fastdiv(job.run_vecs ? job.run_vecs : 1u);
   job.tiles_per_outer = int32_t((vecs + hicache::kTileVecs - 1) / hicache::kTileVecs);
   job.total_tiles = int32_t(job.tiles_per_outer * outers);
   return count;
@@ -147,7 +151,7 @@ void fill_shape(const hicache_pool *pool, int64_t upp, int32_t layer, int64_t de
   h.fd_PV = hicache::make_fastdiv(uint32_t(s.PV));
   h.fd_LV = hicache::make_fastdiv(uint32_t(s.L * s.V));
   h.fd_LPV = hicache::make_fastdiv(uint32_t(s.LPV));
-  h.job[1] = hicache::Job{0, nb, 0, 0, 0u, 0u};
+  h.job[1] = hicache::Job{0, nb, 0, 0, 0u, 0u, hicache::make_fastdiv(1u)};
   h.wait_previous = 0;
   h.Dp = int32_t(device_pages);
   h.host_vecs = s.B * s.Hp * s.LPV;
@@ -177,10 +181,11 @@ int check_device(const hicache_pool *pool) {
 // per chunk so the two directions share every CTA.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
-            void *stream, bool pdl_first, unsigned int *signal, int64_t *signalled) {
+            void *stream, bool pdl_first, unsigned int *signal, int64_t *signalled,
+            const std::function<bool()> *more) {
   const bool bidir = load_runs != nullptr;
-  if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
-  if (int rc = check_device(pool)) return rc;
+  bool produced = more == nullptr;        // every run is already in `runs`
+  if (!produced && bidir) return set_error(HICACHE_ERR_INVALID_ARG, "runs produced during a fused call");
   const Shape &s = pool->shape;
   const bool all = layer < 0;
   const int32_t nb = int32_t(s.B * s.L);
@@ -192,12 +197,21 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
   const int64_t upp = !all || layout == HICACHE_LAYER_FIRST ? s.PV : (kv_all ? s.BLPV : s.LPV);
   const int64_t capacity = (hicache::kBlobWords - nb) / 2;  // runs per launch
 
+  size_t next0 = 0, next1 = 0;
+  // runs still coming in: launch a chunk only once more runs than one launch
+  // takes are in, so that the last run, which may still grow, stays behind
+  const auto top_up = [&]() {
+    while (!produced && runs.size() - next0 <= size_t(capacity)) produced = (*more)();
+  };
+  top_up();
+  if (runs.empty() && (!bidir || load_runs->empty())) return HICACHE_OK;
+  if (int rc = check_device(pool)) return rc;
+
   thread_local hicache::XferParams params;
   hicache::XferHeader &h = params.h;
   fill_header(pool, kv, params, upp, all ? 0 : layer);
   if (!bidir) h.signal = signal;
 
-  size_t next0 = 0, next1 = 0;
   const size_t n1 = bidir ? load_runs->size() : 0;
   while (next0 < runs.size() || next1 < n1) {
     const bool more0 = next0 < runs.size(), more1 = next1 < n1;
@@ -240,6 +254,7 @@ int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::ve
     if (signalled && h.signal) *signalled += x.grid;
     next0 += size_t(c0);
     next1 += size_t(c1);
+    top_up();
   }
   return HICACHE_OK;
 }
@@ -257,11 +272,30 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
                      (long long)pool->shape.L);
   if ((rc = check_kv(pool, kv, 0))) return rc;
   thread_local std::vector<RunRec> runs;
-  if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction,
-                    max_run_pages(pool->shape), &runs)))
-    return rc;
-  if ((rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream)))
-    return rc;
+  const int64_t max_run = max_run_pages(pool->shape);
+  bool sorted = true;
+  if ((rc = validate_pairs(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction, &sorted))) return rc;
+  if (sorted && n > kStreamPairs) {
+    // Pairs already in host order (the usual case: a request's host pages
+    // come from the allocator in order): the whole call is validated, so the
+    // runs are built a chunk at a time and each launch goes out as soon as its
+    // runs are final, while the host works on the next chunk.
+    runs.clear();
+    int64_t done = 0;
+    const std::function<bool()> more = [&]() {
+      const int64_t stop = std::min(n, done + kStreamPairs);
+      append_runs(dev, host, done, stop, max_run, &runs);
+      done = stop;
+      return done == n;
+    };
+    rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream, false, nullptr,
+                 nullptr, &more);
+  } else {
+    if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction, max_run, &runs)))
+      return rc;
+    rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream);
+  }
+  if (rc) return rc;
   if (layer >= 0) {
     const cudaError_t e = cudaEventRecord(pool->events[size_t(layer)], static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");

@@ -46,6 +46,13 @@ int resolve_layout(int32_t layout, int32_t pool_layout, int32_t *out);
 int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
             int32_t direction, int64_t max_run, std::vector<RunRec> *runs);
 int64_t max_run_pages(const Shape &s);
+// The checks of prepass alone (ranges, repeated destinations), and whether the
+// pairs already come sorted by (host page, device page).
+int validate_pairs(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+                   int32_t direction, bool *sorted);
+// Append the runs of sorted pairs [begin, end) to *runs, continuing its last run.
+void append_runs(const int64_t *dev, const int64_t *host, int64_t begin, int64_t end, int64_t max_run,
+                 std::vector<RunRec> *runs);
 bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common);
 
 // cuStreamWaitValue32 from the driver (hicache_pipeline.cpp); nullptr if the
@@ -111,10 +118,16 @@ void fill_header(const hicache_pool *pool, const hicache_device_kv *kv, XferPara
 // on the stream, which must be a one-layer load of another layer.  signal (one
 // direction only): every CTA of every launch adds one to *signal once its
 // last tile has landed; *signalled grows by the CTAs launched.
+// more (one direction only): runs still coming in; each call appends the next
+// ones to `runs` (the same vector) and returns true once all are in.  Chunks
+// go out as their runs become final, so the host's work on later runs
+// overlaps the launches of the earlier ones.
 int enqueue(const hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
             const std::vector<RunRec> *load_runs, int32_t layout, int32_t layer, bool to_host,
             void *stream, bool pdl_first = false, unsigned int *signal = nullptr,
-            int64_t *signalled = nullptr);
+            int64_t *signalled = nullptr, const std::function<bool()> *more = nullptr);
+// Pairs a call must have before its runs are built in chunks during the launches.
+constexpr int64_t kStreamPairs = 4096;
 // Enqueue validated load runs as pipelined launches (every layer, layer by
 // layer, per-layer counters) and update the pool's per-layer signals
 // (hicache_pipeline.cpp).

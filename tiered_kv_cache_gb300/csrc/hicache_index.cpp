@@ -155,56 +155,131 @@ bool first_repeated(const int64_t *dev, int64_t n, int64_t Dp, int64_t *repeated
   return false;
 }
 
-// Validate n index pairs and reduce them to runs: pairs sorted by (host page,
-// device page), merged while both pages step by one (at most max_run pages per
-// run).  On error the last-error text is set and *runs holds no usable table.
-int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
-            int32_t direction, int64_t max_run, std::vector<RunRec> *runs) {
+// Check n index pairs without reducing them: both pages in range, no
+// destination named twice (host pages of a backup, device pages of a load),
+// and whether the pairs already come in (host page, device page) order.
+int validate_pairs(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+                   int32_t direction, bool *sorted) {
   if (n < 0) return set_error(HICACHE_ERR_INVALID_ARG, "n = %lld is negative", (long long)n);
   if (direction != HICACHE_DIR_BACKUP && direction != HICACHE_DIR_LOAD)
     return set_error(HICACHE_ERR_INVALID_ARG, "unknown direction %d", direction);
   if (Dp < 1 || Dp >= INT32_MAX)
     return set_error(HICACHE_ERR_INVALID_ARG, "device_num_pages = %lld must be in [1, 2^31)",
                      (long long)Dp);
-  runs->clear();
+  *sorted = true;
   if (n == 0) return HICACHE_OK;
   if (!dev || !host) return set_error(HICACHE_ERR_INVALID_ARG, "index array is NULL");
+  const bool backup = direction == HICACHE_DIR_BACKUP;
+  const int64_t *dst = backup ? host : dev;
+  const int64_t bound = backup ? Hp : Dp;
+  // One pass over the pairs that only notes whether anything is wrong:
+  // ranges, order, and repeated destinations in a per-thread bitmap of one bit
+  // per page (pools of up to 2^27 pages).  It is all a large call costs the
+  // host before its first launch, so it has no early exit; the exact first
+  // error is looked for only when something was wrong.
+  const bool bitmap = n > 32 && bound <= (int64_t(1) << 27);
+  uint64_t *bits = nullptr;
+  const size_t words = size_t((bound + 63) / 64);
+  if (bitmap) {
+    thread_local std::vector<uint64_t> tls_bits;
+    std::vector<uint64_t> &vbits = tls_bits;
+    if (vbits.size() < words) vbits.resize(words, 0);
+    bits = vbits.data();
+  }
+  bool bad = false, in_order = true;
+  uint64_t dup = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t d = dev[i], h = host[i];
+    bad |= uint64_t(d) >= uint64_t(Dp) || uint64_t(h) >= uint64_t(Hp);
+    if (i > 0) in_order &= !(h < host[i - 1] || (h == host[i - 1] && d < dev[i - 1]));
+    if (bitmap) {
+      const uint64_t x = uint64_t(backup ? h : d);
+      if (x < uint64_t(bound)) {
+        uint64_t &w = bits[x >> 6];
+        const uint64_t bit = uint64_t(1) << (x & 63);
+        dup |= w & bit;
+        w |= bit;
+      }
+    }
+  }
+  if (bitmap) {
+    if (words <= size_t(2 * n)) {
+      std::fill(bits, bits + words, uint64_t(0));
+    } else {
+      for (int64_t k = 0; k < n; ++k)
+        if (uint64_t(dst[k]) < uint64_t(bound)) bits[size_t(dst[k] >> 6)] = 0;
+    }
+  }
+  if (bad) {
+    for (int64_t i = 0; i < n; ++i) {
+      if (dev[i] < 0 || dev[i] >= Dp)
+        return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] = %lld outside [0, %lld)", (long long)i,
+                         (long long)dev[i], (long long)Dp);
+      if (host[i] < 0 || host[i] >= Hp)
+        return set_error(HICACHE_ERR_INDEX_RANGE, "host_pages[%lld] = %lld outside [0, %lld)", (long long)i,
+                         (long long)host[i], (long long)Hp);
+    }
+  }
+  *sorted = in_order;
+  int64_t page = 0;
+  bool repeated = false;
+  if (bitmap) {
+    if (dup) repeated = first_repeated(dst, n, bound, &page);
+  } else if (n <= 32) {
+    for (int64_t a = 0; a < n && !repeated; ++a)
+      for (int64_t b = a + 1; b < n; ++b)
+        if (dst[a] == dst[b]) {
+          repeated = true;
+          page = dst[a];
+          break;
+        }
+  } else {
+    repeated = first_repeated(dst, n, bound, &page);
+  }
+  if (repeated)
+    return set_error(HICACHE_ERR_DUPLICATE_INDEX, "%s page %lld is a %s destination twice",
+                     backup ? "host" : "device", (long long)page, backup ? "backup" : "load");
+  return HICACHE_OK;
+}
+
+// Append the runs of pairs [begin, end) of a sequence sorted by (host page,
+// device page) to *runs, continuing its last run where both pages step by one
+// (at most max_run pages per run).
+void append_runs(const int64_t *dev, const int64_t *host, int64_t begin, int64_t end, int64_t max_run,
+                 std::vector<RunRec> *runs) {
+  for (int64_t i = begin; i < end; ++i) {
+    const int64_t h = host[i], d = dev[i];
+    if (!runs->empty()) {
+      RunRec &r = runs->back();
+      if (h == r.h0 + r.len && d == r.d0 + r.len && r.len < max_run) {
+        ++r.len;
+        continue;
+      }
+    }
+    runs->push_back(RunRec{h, d, 1});
+  }
+}
+
+// Validate n index pairs and reduce them to runs: pairs sorted by (host page,
+// device page), merged while both pages step by one (at most max_run pages per
+// run).  On error the last-error text is set and *runs holds no usable table.
+int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
+            int32_t direction, int64_t max_run, std::vector<RunRec> *runs) {
+  runs->clear();
+  bool sorted = true;
+  if (int rc = validate_pairs(Hp, Dp, dev, host, n, direction, &sorted)) return rc;
+  if (n == 0) return HICACHE_OK;
+  if (sorted) {
+    append_runs(dev, host, 0, n, max_run, runs);
+    return HICACHE_OK;
+  }
   // one lookup of the per-thread buffer: in a shared library every access to
   // a thread_local can be a call, too slow inside a per-page loop
   thread_local std::vector<Pair> tls_pairs;
   std::vector<Pair> &pairs = tls_pairs;
   pairs.resize(size_t(n));
-  bool sorted = true;
-  for (int64_t i = 0; i < n; ++i) {
-    const int64_t d = dev[i], h = host[i];
-    if (d < 0 || d >= Dp)
-      return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] = %lld outside [0, %lld)",
-                       (long long)i, (long long)d, (long long)Dp);
-    if (h < 0 || h >= Hp)
-      return set_error(HICACHE_ERR_INDEX_RANGE, "host_pages[%lld] = %lld outside [0, %lld)",
-                       (long long)i, (long long)h, (long long)Hp);
-    pairs[size_t(i)] = Pair{h, d};
-    if (i > 0 && pair_less(pairs[size_t(i)], pairs[size_t(i - 1)])) sorted = false;
-  }
-  if (!sorted) sort_pairs(pairs, Dp);
-  if (direction == HICACHE_DIR_BACKUP) {
-    for (int64_t i = 1; i < n; ++i)
-      if (pairs[size_t(i)].h == pairs[size_t(i - 1)].h)
-        return set_error(HICACHE_ERR_DUPLICATE_INDEX,
-                         "host page %lld is a backup destination twice",
-                         (long long)pairs[size_t(i)].h);
-  } else if (n <= 32) {
-    for (int64_t i = 0; i < n; ++i)
-      for (int64_t k = i + 1; k < n; ++k)
-        if (dev[i] == dev[k])
-          return set_error(HICACHE_ERR_DUPLICATE_INDEX,
-                           "device page %lld is a load destination twice", (long long)dev[i]);
-  } else {
-    int64_t page = 0;
-    if (first_repeated(dev, n, Dp, &page))
-      return set_error(HICACHE_ERR_DUPLICATE_INDEX, "device page %lld is a load destination twice",
-                       (long long)page);
-  }
+  for (int64_t i = 0; i < n; ++i) pairs[size_t(i)] = Pair{host[i], dev[i]};
+  sort_pairs(pairs, Dp);
   for (int64_t i = 0; i < n; ++i) {
     const Pair &p = pairs[size_t(i)];
     if (!runs->empty()) {

@@ -101,7 +101,10 @@ struct Job {
   int32_t tiles_per_outer;    // tiles of one outer unit (a buffer, or a buffer-layer)
   int32_t total_tiles;
   uint32_t vecs_per_outer;    // vectors of one outer unit: every run end to end (< 2^31)
-  uint32_t pad;
+  uint32_t run_vecs;          // nonzero when every run of the job has the same length:
+                              // the vectors of one run, so that vector w of an outer
+                              // unit is in run w / run_vecs (fd_run) without a search
+  FastDiv fd_run;
 };
 
 // Everything a transfer launch needs, in vectors of 16 bytes.

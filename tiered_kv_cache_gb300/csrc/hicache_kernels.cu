@@ -224,7 +224,30 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
     const uint32_t base = warp0 + k * kThreads;
     const uint32_t w = base + lane;
     dst[k] = nullptr;
-    if (base < job.vecs_per_outer) {                       // warp-uniform
+    if (job.run_vecs != 0) {                               // runs of one length: no search
+      if (w < job.vecs_per_outer) {
+        const uint32_t r = fast_div(w, job.fd_run);
+#if HICACHE_CHECKED
+        if (r >= uint32_t(job.n_runs)) {
+          report_check(kCheckRun, r);
+          continue;
+        }
+#endif
+        const Run cur = runs[r];
+        uint4 *dev, *host;
+        map_vector<LAYOUT, ALL>(h, bufs, b, l, cur, w - r * job.run_vecs, dev, host);
+#if HICACHE_CHECKED
+        if (dev == nullptr) continue;
+#endif
+        if (TO_HOST) {
+          v[k] = ld_stream(dev);
+          dst[k] = host;
+        } else {
+          v[k] = ld_stream(host);
+          dst[k] = dev;
+        }
+      }
+    } else if (base < job.vecs_per_outer) {                // warp-uniform
       if (k == 0 || base >= rb_end) {
         rb = find_run(runs, job.n_runs, base);
         rb_end = uint32_t(runs[rb].vec0) + uint32_t(runs[rb].len) * h.unit_per_page;
