@@ -3,8 +3,8 @@ transfer kernel checks each decoded vector against the device buffers, the
 host pool and the run table before touching it, and records a failure in a
 device word instead of the access.  The randomised corpora -- 300 transfer
 cases, 150 buffer groups, 100 call sequences of every kind -- and the
-tensor-parallel and pipelined tests run against the checked library in a
-child process (valid inputs only), and every test must leave the check words
+tensor-parallel, pipelined, chained and large-call tests run against the
+checked library in a child process (valid inputs only), and every test must leave the check words
 at zero (tests/conftest.py); their oracle comparisons run as usual."""
 import os
 import subprocess
@@ -18,7 +18,8 @@ from tiered_kv_cache_gb300 import build as hc_build
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CORPORA = ["tests/test_gpu_fuzz.py", "tests/test_gpu_group_fuzz.py", "tests/test_gpu_sequence.py",
-           "tests/test_gpu_tp.py", "tests/test_gpu_pipelined.py", "tests/test_gpu_group.py"]
+           "tests/test_gpu_tp.py", "tests/test_gpu_pipelined.py", "tests/test_gpu_group.py",
+           "tests/test_gpu_chained.py", "tests/test_gpu_large_calls.py"]
 
 
 def test_corpora_under_the_bounds_checked_build():

@@ -327,3 +327,32 @@ def test_index_marshalling_fast_paths():
     ro.flags.writeable = False
     assert hc._ptr(ro) == ro.ctypes.data
     assert hc._ptr(a[:0]) is None
+
+
+def test_large_sorted_calls_are_refused_whole():
+    """A large call whose pairs come in host order is validated in full before
+    any run is built (so before any launch): a bad index or a repeated
+    destination at its very end is refused, and the same pairs minus the bad
+    one reduce to the runs of a plain merge."""
+    n = 50_000
+    rng = np.random.default_rng(1700)
+    dp = rng.permutation(n).astype(np.int64)
+    hp = np.arange(n, dtype=np.int64)
+    runs = hc.prepass(n, n, dp, hp, hc.LOAD)
+    assert len(runs) == n - int(np.count_nonzero(np.diff(dp) == 1))
+    assert runs[:, 2].sum() == n
+    for fix, status in [(lambda d, h: d.__setitem__(-1, n), "INDEX_RANGE"),
+                        (lambda d, h: d.__setitem__(-1, -1), "INDEX_RANGE"),
+                        (lambda d, h: h.__setitem__(-1, n), "INDEX_RANGE"),
+                        (lambda d, h: d.__setitem__(-1, d[0]), "DUPLICATE_INDEX")]:
+        d, h = dp.copy(), hp.copy()
+        fix(d, h)
+        with pytest.raises(hc.HiCacheError) as e:
+            hc.prepass(n, n, d, h, hc.LOAD)
+        assert e.value.status == status
+    # a backup naming the last host page twice
+    h = hp.copy()
+    h[-1] = h[-2]
+    with pytest.raises(hc.HiCacheError) as e:
+        hc.prepass(n, n, dp, h, hc.BACKUP)
+    assert e.value.status == "DUPLICATE_INDEX"
