@@ -278,7 +278,8 @@ def binding_resource(link):
         "host_dram_copy_gbs": (link.get("host_dram") or {}).get("copy_gbs_read_plus_write"),
         "sm_kernel_grids": "38-608 CTAs x 4 or 8 16-byte vectors in flight per thread",
         "ncu_c2c_fraction": "65.8% RX at 210.9 GB/s, 60.3% TX at 192.9 GB/s of ncu's nominal C2C peak "
-                            "(about 320 GB/s per direction; profiles/xfer_kernel_counters_llama3_8b_64pages.md)",
+                            "(about 320 GB/s per direction; an ncu C2CLink-section capture of the transfer "
+                            "kernels)",
         "nominal": "900 GB/s two-way NVLink-C2C per Grace, which serves two GPUs: 450 two-way, 225 per "
                    "direction per GPU (a reading of the superchip figure)",
     }
