@@ -1,7 +1,8 @@
 """Seeded random sequences of every kind of call -- backup, load, per-layer
-load, pipelined (plain and allocation-free), fused backup + load, plans, group
-calls and group plans -- on two pools that share the page numbering, all on one
-stream.
+load, pipelined (plain and allocation-free), fused backup + load, plans
+(per-layer, chained per-layer, graph replay), group calls and group plans
+(graph replay, chained per-layer), a one-rank tensor-parallel load -- on two
+pools that share the page numbering, all on one stream.
 A shadow copy of the device buffers and host pools is updated by the oracle in
 the same order; at the end every byte must agree (GB300)."""
 import ctypes
@@ -18,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 TEN_S = 10_000_000
 OPS = ["backup", "load", "load_layer", "pipelined", "noalloc", "fused", "plan_layers", "plan_graph",
-       "group_backup", "group_load", "group_layer", "group_pipelined", "group_plan_graph"]
+       "plan_chained", "tp1", "group_backup", "group_load", "group_layer", "group_pipelined",
+       "group_plan_graph", "group_plan_chained"]
 
 
 def _noalloc(pool, kv, dp, hp, stream):
@@ -101,6 +103,20 @@ def test_random_call_sequence(seed):
                 plan.load_layers(kv, stream=st)
                 shadow(i, "load", dp, hp)
             plans.append(plan)                 # kept until the stream is done
+        elif op == "plan_chained":
+            # layers first..last in order, one chained call each: a chain from
+            # layer 0, or calls that start mid-way (each a new chain)
+            plan = pool.plan(dp, hp, Dp, hc.LOAD)
+            first = 0 if rng.random() < 0.7 else int(rng.integers(0, L))
+            last = int(rng.integers(first, L))
+            for l in range(first, last + 1):
+                plan.load_layer_chained(kv, l, stream=st)
+                shadow(i, "load", dp, hp, l)
+            plans.append(plan)                 # kept until the stream is done
+        elif op == "tp1":
+            # a tensor-parallel load with this pool as the group's only rank
+            hc.tp_load_pipelined(pool, [kv], [pool.layer_counters()], 0, dp, hp, stream=st)
+            shadow(i, "load", dp, hp)
         elif op == "group_backup":
             hc.group_transfer(pools, kvs, dp, hp, hc.BACKUP, stream=st)
             shadow(0, "backup", dp, hp)
@@ -117,6 +133,13 @@ def test_random_call_sequence(seed):
             hc.group_load_pipelined(pools, kvs, dp, hp, stream=st)
             shadow(0, "load", dp, hp)
             shadow(1, "load", dp, hp)
+        elif op == "group_plan_chained":
+            gplan = hc.group_plan(pools, dp, hp, Dp)
+            for l in range(0, int(rng.integers(0, L)) + 1):
+                gplan.load_layer_chained(kvs, l, stream=st)
+                shadow(0, "load", dp, hp, l)
+                shadow(1, "load", dp, hp, l)
+            plans.append(gplan)                # kept until the stream is done
         else:
             gplan = hc.group_plan(pools, dp, hp, Dp)
             gplan.load_layers(kvs, stream=st)
