@@ -170,8 +170,12 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
                         hicache_pool **out);
 /* Destroys the pool's events and the pool.  Transfers already enqueued still
  * run; the host buffer must stay allocated until they finish.  The pool's
- * pipelined loads count into device words the pool owns, so this first waits
- * on the host for the last of them to finish.  Plans and engines of the pool
+ * pipelined, tensor-parallel and chained per-layer loads count into device
+ * words the pool owns, so this first waits on the host for the last of them to
+ * finish (for a chain of per-layer calls left before its last layer, for the
+ * whole device).  In a tensor-parallel group the other ranks' loads count into
+ * this pool too: every rank's pool must outlive the group's loads.  Plans and
+ * engines of the pool
  * must be destroyed first, and no other thread may be inside a call on the
  * pool meanwhile. */
 int hicache_pool_destroy(hicache_pool *pool);
@@ -236,8 +240,9 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
  * 최적화", without a launch and an event per layer.  The layer events are
  * recorded too, once the whole load is in.  Checks as hicache_load.  A
  * pipelined load may only go on another stream than the pool's previous one
- * once that one's pipelined loads have finished (INVALID_ARG otherwise): the
- * per-layer counts must rise in load order.  A stream that is being captured
+ * once that one's counted loads (pipelined, tensor-parallel, chained per-layer)
+ * have finished (INVALID_ARG otherwise): the per-layer counts must rise in
+ * load order.  A stream that is being captured
  * into a CUDA graph is refused (INVALID_ARG, nothing enqueued): the value each
  * layer's counter must reach is raised on the host when the call is enqueued,
  * so a graph replayed twice, or never, would leave hicache_wait_layer passing
@@ -298,9 +303,16 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
  *   - A capturing stream is refused (INVALID_ARG): the count each layer must
  *     reach is raised on the host when the call is enqueued.
  *   - Calls of one plan's chain come from one thread, in layer order.
+ *   - The pool's counters are shared with its pipelined and tensor-parallel
+ *     loads, and counts from two loads cannot be told apart: all of them go
+ *     on one stream, or on another only once the earlier ones have finished.
+ *     A chain stopped before its last layer counts as unfinished (it has no
+ *     event behind it): a counted load on another stream is then refused
+ *     (INVALID_ARG) until a counted load on the chain's stream closes it.
  * Errors: INVALID_ARG (NULL plan, backup plan, layer_id outside [0,
- * num_layers), bad layout or kv, overlapping buffers, capturing stream),
- * CUDA; on a refused call nothing is enqueued. */
+ * num_layers), bad layout or kv, overlapping buffers, capturing stream,
+ * another stream while a counted load is unfinished), CUDA; on a refused
+ * call nothing is enqueued. */
 int hicache_plan_load_layer_chained(hicache_plan *plan, const hicache_device_kv *kv, int32_t layout,
                                     int32_t layer_id, void *stream);
 /* hicache_load_pipelined without any allocation.  The pages have no

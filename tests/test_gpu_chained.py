@@ -86,8 +86,8 @@ def test_chained_layers_equal_the_oracle(layout, shape):
 
 
 def test_chain_breaks_and_restarts_stay_correct():
-    """Layers out of order, a switch of stream and a restart from layer 0 each
-    start a new chain (a plain wait for earlier work); the result is the
+    """Layers out of order start a new chain (a plain wait for earlier work);
+    another stream is refused while the chain is open; the result is the
     oracle's load whatever the order."""
     B, L, P, R, Dp, Hp, n = 2, 5, 16, 64, 40, 40, 17
     rng = np.random.default_rng(1300)
@@ -103,9 +103,14 @@ def test_chain_breaks_and_restarts_stay_correct():
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         gh.sentinel_fill(bufs)
         torch.cuda.synchronize()
-        for layer, st in [(0, s1), (1, s1), (3, s1), (2, s1), (4, s2)]:
-            plan.load_layer_chained(kv, layer, stream=st)
+        for layer in (0, 1, 3, 2):
+            plan.load_layer_chained(kv, layer, stream=s1)
+        with pytest.raises(hc.HiCacheError) as e:            # the chain on s1 is still open
+            plan.load_layer_chained(kv, 4, stream=s2)
+        assert e.value.status == "INVALID_ARG"
+        plan.load_layer_chained(kv, 4, stream=s1)             # the last layer closes it
         hc.wait(s1, TEN_S)
+        plan.load_layer_chained(kv, 0, stream=s2)             # and another stream may follow
         hc.wait(s2, TEN_S)
         got = gh.to_np(bufs, 2)
         for k in range(B * L):
@@ -207,3 +212,54 @@ def test_chained_group_layers_equal_the_oracle(layout):
     for pool in pools:
         pool.close()
     mem.free()
+
+
+def test_counted_loads_share_one_stream_at_a_time():
+    """Chained per-layer calls count into the same per-layer counters as
+    pipelined loads, and counts from two loads cannot be told apart: a counted
+    load on another stream is refused while a chain is open or a pipelined load
+    is still running, and accepted once they are done."""
+    B, L, P, R, Dp, Hp, n = 1, 4, 16, 64, 32, 32, 9
+    rng = np.random.default_rng(1800)
+    dp = rng.choice(Dp, n, replace=False)
+    hp = rng.choice(Hp, n, replace=False)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=1800)
+    kv = hc.DeviceKV(bufs, Dp)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        plan = pool.plan(dp, hp, Dp, hc.LOAD)
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        for layer in range(2):                            # a chain left open on s1
+            plan.load_layer_chained(kv, layer, stream=s1)
+        hc.wait(s1, TEN_S)
+        with pytest.raises(hc.HiCacheError) as e:
+            pool.load_pipelined(kv, dp, hp, stream=s2)
+        assert e.value.status == "INVALID_ARG" and "chained" in str(e.value)
+        for layer in range(2, L):                         # closing the chain
+            plan.load_layer_chained(kv, layer, stream=s1)
+        hc.wait(s1, TEN_S)
+        pool.load_pipelined(kv, dp, hp, stream=s2)        # now accepted
+        hc.wait(s2, TEN_S)
+        # a pipelined load still queued on s2 (behind a sleep) refuses a chain on s1
+        with torch.cuda.stream(s2):
+            torch.cuda._sleep(int(2e8))
+        pool.load_pipelined(kv, dp, hp, stream=s2)
+        with pytest.raises(hc.HiCacheError) as e:
+            plan.load_layer_chained(kv, 0, stream=s1)
+        assert e.value.status == "INVALID_ARG"
+        hc.wait(s2, 60_000_000)
+        for layer in range(L):
+            plan.load_layer_chained(kv, layer, stream=s1)
+        hc.wait(s1, TEN_S)
+        for layer in range(L):
+            done, target = pool.pipeline_status(layer)
+            assert done == target, layer
+        # every load moved the same pages from the same host pool: the moved rows
+        # must be what the oracle's load puts there (the others are unchanged)
+        got = gh.to_np(bufs, 2)
+        want = [g.copy() for g in got]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, hc.PAGE_FIRST)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k]), k
+        plan.close()

@@ -454,8 +454,11 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
 int hicache_pool_destroy(hicache_pool *pool) {
   if (!pool) return HICACHE_OK;
   // pipelined loads count into the pool's device words: let the last one end
-  // (they all follow one another on one stream) before the words are freed
-  if (pool->pipeline_stream_set && pool->pipeline_last) (void)cudaEventSynchronize(pool->pipeline_last);
+  // (they all follow one another on one stream) before the words are freed.
+  // A chain of per-layer calls left open has no event behind its last kernel,
+  // so then the whole device is waited for.
+  if (pool->chain_open) (void)cudaDeviceSynchronize();
+  else if (pool->pipeline_stream_set && pool->pipeline_last) (void)cudaEventSynchronize(pool->pipeline_last);
   for (auto ev : pool->events)
     if (ev) cudaEventDestroy(ev);
   if (pool->layer_done) cudaFree(pool->layer_done);

@@ -267,19 +267,9 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
   std::sort(order.begin(), order.end());
   std::vector<std::unique_lock<std::mutex>> locks;
   for (hicache_pool *p : order) locks.emplace_back(p->signal_mu);
-  for (int32_t i = 0; i < npools; ++i) {
-    hicache_pool *p = pools[i];
-    if (p->pipeline_stream_set && p->pipeline_stream != stream &&
-        cudaEventQuery(p->pipeline_last) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return set_error(HICACHE_ERR_INVALID_ARG,
-                       "a pipelined load of pool %d is still running on another stream", i);
-    }
-  }
-  for (int32_t i = 0; i < npools; ++i) {
-    pools[i]->pipeline_stream_set = true;
-    pools[i]->pipeline_stream = stream;
-  }
+  for (int32_t i = 0; i < npools; ++i)
+    if ((rc = check_counted_stream(pools[i], stream))) return rc;
+  for (int32_t i = 0; i < npools; ++i) claim_counted_stream(pools[i], stream);
   if ((rc = enqueue_group_pipelined(pools, kvs, npools, runs, lay, stream))) return rc;
   for (int32_t i = 0; i < npools; ++i) {
     hicache_pool *p = pools[i];
@@ -289,6 +279,7 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
     }
     const cudaError_t e = cudaEventRecord(p->pipeline_last, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
+    p->chain_open = false;
   }
   return HICACHE_OK;
 }
@@ -425,22 +416,35 @@ int hicache_group_plan_load_layer_chained(hicache_group_plan *plan, const hicach
   }
   const bool chained = plan->chain_layer >= 0 && plan->chain_stream == stream &&
                        layer_id == plan->chain_layer + 1;
+  // every pool's signal lock, in address order (the pools are distinct); the
+  // pools' counted loads share their counters: one stream at a time
+  std::vector<hicache_pool *> order(pools, pools + np);
+  std::sort(order.begin(), order.end());
+  std::vector<std::unique_lock<std::mutex>> locks;
+  for (hicache_pool *p : order) locks.emplace_back(p->signal_mu);
+  for (int32_t i = 0; i < np; ++i)
+    if ((rc = check_counted_stream(pools[i], stream))) return rc;
+  for (int32_t i = 0; i < np; ++i) claim_counted_stream(pools[i], stream);
   int64_t signalled = 0;
   rc = enqueue_group(pools, kvs, np, plan->runs, lay, layer_id, false, stream, chained, true, &signalled);
   plan->chain_stream = stream;
   plan->chain_layer = rc == HICACHE_OK && layer_id + 1 < L ? layer_id : -1;
   for (int32_t i = 0; i < np; ++i) {
-    std::lock_guard<std::mutex> gs(pools[i]->signal_mu);
     pools[i]->layer_target[size_t(layer_id)] += uint32_t(signalled);
     pools[i]->layer_signal[size_t(layer_id)] = 1;
+    pools[i]->chain_open = true;
   }
   if (rc != HICACHE_OK) return rc;
   if (layer_id + 1 == L) {
-    for (int32_t i = 0; i < np; ++i)
+    for (int32_t i = 0; i < np; ++i) {
       for (int64_t l = 0; l < L; ++l) {
         const cudaError_t e = cudaEventRecord(pools[i]->events[size_t(l)], static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
       }
+      const cudaError_t e = cudaEventRecord(pools[i]->pipeline_last, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(chained load)");
+      pools[i]->chain_open = false;
+    }
   }
   return HICACHE_OK;
 }

@@ -87,6 +87,9 @@ struct hicache_pool {
   bool pipeline_stream_set = false;
   void *pipeline_stream = nullptr;
   cudaEvent_t pipeline_last = nullptr;  // recorded after each pipelined load
+  // a chained per-layer load on pipeline_stream has not reached its last
+  // layer (no pipeline_last recorded behind it yet)
+  bool chain_open = false;
   // Allocation-free pipelined loads (signal 2): the library's static counters
   // on this device and, per layer, the value the last such load brings them to.
   unsigned int *noalloc_done = nullptr;
@@ -136,6 +139,15 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
 // INVALID_ARG if `stream` is capturing (pipelined loads keep their per-layer
 // targets on the host, raised at enqueue time), CUDA if that cannot be told.
 int refuse_capture(void *stream);
+// Counted loads of a pool -- pipelined, tensor-parallel, chained per-layer --
+// add into the same per-layer counters, which cannot tell two loads apart, so
+// they go on one stream, or on another only once the earlier ones have
+// finished: the pool's last counted-load event has fired and no chain is
+// left open.  check_counted_stream: INVALID_ARG otherwise (no side effect);
+// claim_counted_stream: make `stream` the pool's counted-load stream.  Both
+// with pool->signal_mu held.
+int check_counted_stream(hicache_pool *pool, void *stream);
+void claim_counted_stream(hicache_pool *pool, void *stream);
 
 // hicache_plan.cpp: per-layer graphs.
 // INVALID_ARG unless the (address, bytes) spans are pairwise disjoint.

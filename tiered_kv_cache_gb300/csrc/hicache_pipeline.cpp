@@ -47,6 +47,24 @@ int refuse_capture(void *stream) {
   return HICACHE_OK;
 }
 
+int check_counted_stream(hicache_pool *pool, void *stream) {
+  if (!pool->pipeline_stream_set || pool->pipeline_stream == stream) return HICACHE_OK;
+  if (pool->chain_open)
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "a chained per-layer load of this pool on another stream has not reached its last layer");
+  if (cudaEventQuery(pool->pipeline_last) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return set_error(HICACHE_ERR_INVALID_ARG,
+                     "a pipelined load of this pool is still running on another stream");
+  }
+  return HICACHE_OK;
+}
+
+void claim_counted_stream(hicache_pool *pool, void *stream) {
+  pool->pipeline_stream_set = true;
+  pool->pipeline_stream = stream;
+}
+
 int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std::vector<RunRec> &runs,
                       int32_t layout, void *stream) {
   if (int rc = check_device(pool)) return rc;
@@ -54,16 +72,10 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
   if (!wait_value32())
     return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
   std::lock_guard<std::mutex> g(pool->signal_mu);
-  // the counts stay in order while pipelined loads follow one another on one
+  // the counts stay in order while counted loads follow one another on one
   // stream; another stream is fine once the earlier ones have finished
-  if (pool->pipeline_stream_set && pool->pipeline_stream != stream &&
-      cudaEventQuery(pool->pipeline_last) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return set_error(HICACHE_ERR_INVALID_ARG,
-                     "a pipelined load of this pool is still running on another stream");
-  }
-  pool->pipeline_stream_set = true;
-  pool->pipeline_stream = stream;
+  if (int rc = check_counted_stream(pool, stream)) return rc;
+  claim_counted_stream(pool, stream);
   const Shape &s = pool->shape;
   const int32_t nb = int32_t(s.B * s.L);
   thread_local hicache::XferParams params;
@@ -98,6 +110,7 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
   }
   const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
+  pool->chain_open = false;            // the event covers any chain before it on this stream
   return HICACHE_OK;
 }
 

@@ -224,24 +224,30 @@ int hicache_plan_load_layer_chained(hicache_plan *plan, const hicache_device_kv 
   // layer's kernel drains, with nothing in between on the stream
   const bool chained = plan->chain_layer >= 0 && plan->chain_stream == stream &&
                        layer_id == plan->chain_layer + 1;
+  // the pool's counted loads share its counters: one stream at a time
+  std::lock_guard<std::mutex> gs(pool->signal_mu);
+  if ((rc = check_counted_stream(pool, stream))) return rc;
+  claim_counted_stream(pool, stream);
   int64_t signalled = 0;
   rc = enqueue(pool, kv, plan->runs, nullptr, lay, layer_id, false, stream, chained,
                pool->layer_done + layer_id, &signalled);
   plan->chain_stream = stream;
   plan->chain_layer = rc == HICACHE_OK && layer_id + 1 < s.L ? layer_id : -1;
-  {
-    // the launches that went out count towards the layer, even if a later one failed
-    std::lock_guard<std::mutex> gs(pool->signal_mu);
-    pool->layer_target[size_t(layer_id)] += uint32_t(signalled);
-    pool->layer_signal[size_t(layer_id)] = 1;
-  }
+  // the launches that went out count towards the layer, even if a later one failed
+  pool->layer_target[size_t(layer_id)] += uint32_t(signalled);
+  pool->layer_signal[size_t(layer_id)] = 1;
+  pool->chain_open = true;
   if (rc != HICACHE_OK) return rc;
   if (layer_id + 1 == s.L) {
-    // the layer events fire once the last layer's kernel is done
+    // the layer events fire once the last layer's kernel is done, and so does
+    // the pool's counted-load event, which closes the chain
     for (int64_t l = 0; l < s.L; ++l) {
       const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
       if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
     }
+    const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(chained load)");
+    pool->chain_open = false;
   }
   return HICACHE_OK;
 }

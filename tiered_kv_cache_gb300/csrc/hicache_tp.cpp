@@ -129,14 +129,8 @@ int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_
   if (!wait_value32())
     return set_error(HICACHE_ERR_CUDA, "the driver offers no cuStreamWaitValue32: no pipelined loads");
   std::lock_guard<std::mutex> g(pool->signal_mu);
-  if (pool->pipeline_stream_set && pool->pipeline_stream != stream &&
-      cudaEventQuery(pool->pipeline_last) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return set_error(HICACHE_ERR_INVALID_ARG,
-                     "a pipelined load of this pool is still running on another stream");
-  }
-  pool->pipeline_stream_set = true;
-  pool->pipeline_stream = stream;
+  if ((rc = check_counted_stream(pool, stream))) return rc;
+  claim_counted_stream(pool, stream);
   // this rank waits for every other rank's tiles, whatever happens to its own launches
   const int64_t others = all_tiles - share_tiles(pool, own, words0);
   for (int64_t l = 0; l < s.L; ++l) {
@@ -176,6 +170,7 @@ int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_
   }
   const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
+  pool->chain_open = false;
   return HICACHE_OK;
 }
 
