@@ -291,8 +291,7 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
     rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream, false, nullptr,
                  nullptr, &more);
   } else {
-    if ((rc = prepass(pool->shape.Hp, kv->device_num_pages, dev, host, n, direction, max_run, &runs)))
-      return rc;
+    build_runs(kv->device_num_pages, dev, host, n, sorted, max_run, &runs);
     rc = enqueue(pool, kv, runs, nullptr, lay, layer, direction == HICACHE_DIR_BACKUP, stream);
   }
   if (rc) return rc;

@@ -50,6 +50,9 @@ int64_t max_run_pages(const Shape &s);
 // pairs already come sorted by (host page, device page).
 int validate_pairs(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n,
                    int32_t direction, bool *sorted);
+// The runs of n pairs that validate_pairs accepted (sorted: as it reported).
+void build_runs(int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n, bool sorted, int64_t max_run,
+                std::vector<RunRec> *runs);
 // Append the runs of sorted pairs [begin, end) to *runs, continuing its last run.
 void append_runs(const int64_t *dev, const int64_t *host, int64_t begin, int64_t end, int64_t max_run,
                  std::vector<RunRec> *runs);

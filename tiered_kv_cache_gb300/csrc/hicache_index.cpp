@@ -268,10 +268,18 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
   runs->clear();
   bool sorted = true;
   if (int rc = validate_pairs(Hp, Dp, dev, host, n, direction, &sorted)) return rc;
-  if (n == 0) return HICACHE_OK;
+  build_runs(Dp, dev, host, n, sorted, max_run, runs);
+  return HICACHE_OK;
+}
+
+// The runs of n validated pairs (sorted: they already come in host order).
+void build_runs(int64_t Dp, const int64_t *dev, const int64_t *host, int64_t n, bool sorted, int64_t max_run,
+                std::vector<RunRec> *runs) {
+  runs->clear();
+  if (n == 0) return;
   if (sorted) {
     append_runs(dev, host, 0, n, max_run, runs);
-    return HICACHE_OK;
+    return;
   }
   // one lookup of the per-thread buffer: in a shared library every access to
   // a thread_local can be a call, too slow inside a per-page loop
@@ -291,7 +299,6 @@ int prepass(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *host, int
     }
     runs->push_back(RunRec{p.h, p.d, 1});
   }
-  return HICACHE_OK;
 }
 
 // Runs are capped so that a unit (at most every buffer and layer of a run)
