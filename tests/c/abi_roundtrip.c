@@ -171,6 +171,52 @@ int main(void) {
   for (int l = 0; l < L; ++l) cudaFree(bufs2[l]);
   free(h2);
 
+  /* the same host pages once more, one chained per-layer call per layer
+   * (each layer waited for on the device), then as a one-rank tensor-parallel
+   * load, each into other device pages */
+  const int64_t dst5[N] = {29, 30, 31, 32, 33, 34, 35, 36};
+  const int64_t dst6[N] = {37, 38, 39, 40, 44, 45, 46, 3};
+  hicache_plan *plan = NULL;
+  CHECK(hicache_plan_create(pool, dst5, hp, N, Dp, HICACHE_DIR_LOAD, &plan));
+  for (int l = 0; l < L; ++l) {
+    CHECK(hicache_plan_load_layer_chained(plan, &kv, HICACHE_LAYOUT_POOL, l, xfer));
+    CHECK(hicache_wait_layer(pool, l, comp));
+  }
+  int64_t first = -1, count = -1;
+  CHECK(hicache_tp_share(N, 1, 0, &first, &count));
+  if (first != 0 || count != N) return 8;
+  void *counters = NULL;
+  CHECK(hicache_pool_layer_counters(pool, &counters));
+  CHECK(hicache_tp_load_pipelined(pool, &kv, (void *const *)&counters, 1, 0, dst6, hp, N, HICACHE_LAYOUT_POOL,
+                                  xfer));
+  for (int l = 0; l < L; ++l) CHECK(hicache_wait_layer(pool, l, comp));
+  CHECK(hicache_wait(comp, -1));
+  CHECK(hicache_wait(xfer, -1));
+  CHECK(hicache_plan_destroy(plan));
+  const int64_t *dsts2[2] = {dst5, dst6};
+  for (int v = 0; v < 2; ++v)
+    for (int k = 0; k < NB; ++k) {
+      if (cudaMemcpy(h, bufs[k], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+      for (int i = 0; i < N; ++i)
+        for (int64_t t = 0; t < P; ++t)
+          for (int64_t e = 0; e < R; ++e)
+            if (h[(dsts2[v][i] * P + t) * R + e] != pattern(k, src[i] * P + t, e)) return 9;
+    }
+
+  /* the roofline probe's streaming copy: one device buffer into another */
+  CHECK(hicache_stream_copy(bufs[1], bufs[0], buf_bytes, 0, 4, xfer));
+  CHECK(hicache_wait(xfer, -1));
+  if (cudaMemcpy(h, bufs[1], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+  uint16_t *h0 = (uint16_t *)malloc(buf_bytes);
+  if (cudaMemcpy(h0, bufs[0], buf_bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return 2;
+  if (memcmp(h, h0, buf_bytes) != 0) return 10;
+  free(h0);
+
+  /* the plain build reports no failed bounds check (and says it is plain) */
+  uint64_t cfirst = 1, ccount = 1;
+  CHECK(hicache_check_status(&cfirst, &ccount, 0));
+  if (cfirst != 0 || ccount != 0) return 11;
+
   /* errors enqueue nothing and explain themselves */
   const int64_t bad[1] = {Dp};
   const int64_t okh[1] = {0};
