@@ -650,6 +650,28 @@ def bench_extras(torch, hc, args, link):
     out["small_mix"] = bench_small_mix(torch, hc, args)
     out["small_mix"]["wall_s"] = round(time.perf_counter() - t0, 1)
     torch.cuda.empty_cache()
+    # the row-size x page-size stress (fully scattered pages, about 1 GiB per call)
+    t0 = time.perf_counter()
+    rows = bench_shapes(torch, hc, args)
+    for r in rows:
+        for k in [k for k in r if k.endswith("_gbs")]:
+            peak = link["d2h_gbs"] if k.startswith("backup") else link["h2d_gbs"]
+            r[k.replace("_gbs", "_frac_of_link")] = frac(r[k], peak)
+    out["shapes"] = {"rows": rows, "wall_s": round(time.perf_counter() - t0, 1)}
+    torch.cuda.empty_cache()
+    # the buffer group (MLA latent + indexer key + scales) and the tensor-parallel
+    # load with stand-in ranks
+    small_args = types.SimpleNamespace(ctas=args.ctas, steps=min(args.steps, 5), warmup=3)
+    t0 = time.perf_counter()
+    res, launches = bench_nsa_group(torch, hc, small_args)
+    out["nsa_group"] = {"results": res, "gpu_launches": launches, "wall_s": round(time.perf_counter() - t0, 1)}
+    torch.cuda.empty_cache()
+    t0 = time.perf_counter()
+    out["tp_mla61"] = {"results": bench_tp_mla(torch, hc, small_args),
+                       "how": "tp stand-in ranks on one GPU (pools over one host memory); host_read_gbs is "
+                              "the group's, over the one host link",
+                       "wall_s": round(time.perf_counter() - t0, 1)}
+    torch.cuda.empty_cache()
     return out
 
 
