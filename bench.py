@@ -277,9 +277,10 @@ def binding_resource(link):
                     "sm_kernel_max": max(d2h.values())},
         "host_dram_copy_gbs": (link.get("host_dram") or {}).get("copy_gbs_read_plus_write"),
         "sm_kernel_grids": "38-608 CTAs x 4 or 8 16-byte vectors in flight per thread",
-        "ncu_c2c_fraction": "65.8% RX at 210.9 GB/s, 60.3% TX at 192.9 GB/s of ncu's nominal C2C peak "
-                            "(about 320 GB/s per direction; an ncu C2CLink-section capture of the transfer "
-                            "kernels)",
+        "ncu_c2c_fraction": "of ncu's nominal C2C capacity (about 320 GB/s per direction), protocol bytes "
+                            "included: a load fills 66.0% of RX, a backup 75.5% of TX, the fused pair 79.5% "
+                            "each way; one direction alone leaves raw capacity unused, so for loads the host "
+                            "side's read-return rate binds",
         "nominal": "900 GB/s two-way NVLink-C2C per Grace, which serves two GPUs: 450 two-way, 225 per "
                    "direction per GPU (a reading of the superchip figure)",
     }
