@@ -1418,7 +1418,9 @@ def main():
     w["pool"].close()
     del w
     torch.cuda.empty_cache()
-    if not args.no_extras and args.workload == "llama3_8b_32k" and args.pages == 512:
+    # the other workload shapes, on the single-GPU run only (under torchrun every
+    # rank would pin its own copy of the larger pools at the same time)
+    if not args.no_extras and world == 1 and args.workload == "llama3_8b_32k" and args.pages == 512:
         out["workloads"] = bench_extras(torch, hc, args, link)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline()
