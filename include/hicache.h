@@ -303,6 +303,11 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
  *   - A capturing stream is refused (INVALID_ARG): the count each layer must
  *     reach is raised on the host when the call is enqueued.
  *   - Calls of one plan's chain come from one thread, in layer order.
+ *   - Consecutive layers overlap only if the call for layer l + 1 arrives
+ *     before layer l's kernel has ended; a caller that does per-layer host
+ *     work between the calls (e.g. enqueueing attention) may lose that, and
+ *     is better served by hicache_plan_load_layers or
+ *     hicache_plan_load_pipelined, which enqueue every layer at once.
  *   - The pool's counters are shared with its pipelined and tensor-parallel
  *     loads, and counts from two loads cannot be told apart: all of them go
  *     on one stream, or on another only once the earlier ones have finished.
