@@ -178,3 +178,40 @@ def test_mla61_64k_eight_ranks_full_size():
     del host, bufs, kvs
     mem.free()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("tp", [2, 3])
+def test_parts_split_over_several_launches(tp):
+    """8,000 scattered one-token pages: each rank's part needs several
+    launches (the run table of one launch holds under 1,800 runs), and each
+    rank's targets must add up every rank's launches exactly as those ranks
+    split them -- the counts reach the targets, and every rank ends with the
+    oracle's load."""
+    B, L, P, R, Dp, Hp, n = 1, 3, 1, 64, 9000, 9000, 8000
+    rng = np.random.default_rng(1900 + tp)
+    dp = rng.permutation(Dp)[:n]
+    hp = np.sort(rng.choice(Hp, n, replace=False))
+    mem = hc.PinnedHost(B * L * Hp * P * R * 2)
+    pools, bufs, kvs, counters = group(tp, L, B, P, R, Hp, Dp, "layer_first", mem)
+    host = pools[0].host_array(np.uint16)
+    host[:] = rng.integers(0, 1 << 16, host.size, dtype=np.uint16)
+    for b in bufs:
+        gh.sentinel_fill(b, 0xC3)
+    torch.cuda.synchronize()
+    launches = run_group(pools, kvs, counters, dp, hp, [torch.cuda.Stream() for _ in range(tp)])
+    assert launches >= 2 * tp
+    torch.cuda.synchronize()
+    for p in pools:
+        for layer in range(L):
+            done, target = p.pipeline_status(layer)
+            assert done == target and target > 0, (layer, done, target)
+    want = [np.full((Dp * P, R), 0xC3C3, np.uint16) for _ in range(B * L)]
+    gh.orc().load(want, host, B, L, P, R, Hp, dp, hp, hc.LAYER_FIRST)
+    for r in range(tp):
+        got = gh.to_np(bufs[r], 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k]), (r, k)
+    for p in pools:
+        p.close()
+    del host
+    mem.free()
