@@ -534,18 +534,20 @@ def _elapsed(torch, e0, e1):
     return e0.elapsed_time(e1) / 1e3
 
 
-def breakdown_from_events(ev, bpx, link):
-    """Per-layout, per-operation GB/s (from the mean launch time) and their
-    fraction of the in-run link peak, from (name, start, end) event triples."""
+def breakdown_from_events(ev, bpx, link, stat="mean"):
+    """Per-layout, per-operation GB/s (from the mean launch time, or the
+    median with stat="median") and their fraction of the in-run link peak,
+    from (name, start, end) event triples."""
     per = {}
     for name, a, b in ev:
         per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
+    avg = statistics.median if stat == "median" else statistics.mean
     breakdown = {}
     for lay in LAYOUT_NAMES:
-        bk = bpx / statistics.mean(per[f"{lay}/backup"]) / GB
-        ld = bpx / statistics.mean(per[f"{lay}/load"]) / GB
-        bi = 2 * bpx / statistics.mean(per[f"{lay}/bidir"]) / GB
-        bf = 2 * bpx / statistics.mean(per[f"{lay}/bidir_fused"]) / GB
+        bk = bpx / avg(per[f"{lay}/backup"]) / GB
+        ld = bpx / avg(per[f"{lay}/load"]) / GB
+        bi = 2 * bpx / avg(per[f"{lay}/bidir"]) / GB
+        bf = 2 * bpx / avg(per[f"{lay}/bidir_fused"]) / GB
         breakdown[lay] = {
             "backup_gbs": round(bk, 1), "load_gbs": round(ld, 1),
             "bidir_streams_gbs": round(bi, 1), "bidir_fused_gbs": round(bf, 1),
@@ -553,19 +555,24 @@ def breakdown_from_events(ev, bpx, link):
             "load_frac_of_link": frac(ld, link["h2d_gbs"]),
             "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
             "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
-            # per-op launch times (GB/s above are from the mean)
-            "ms": {op: {"median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
+            # per-op launch times (GB/s above are from the `stat` of these)
+            "ms": {op: {"mean": round(statistics.mean(per[f"{lay}/{op}"]) * 1e3, 3),
+                        "median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
                         "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"])}
                    for op in ("backup", "load", "bidir", "bidir_fused")},
         }
     return per, breakdown
 
 
-def bench_deep78(torch, hc, args, link, steps=3):
+def bench_deep78(torch, hc, args, link, steps=5):
     """The deep-model segment-count stress: 78 layers, K+V, 512 fully scattered
     device pages per request (39,936 page x layer segments per buffer under
     page_first_direct), the same four operations per layout as the headline
-    step, timed with events over `steps` steps after one warm-up step."""
+    step, timed with events over `steps` steps after one warm-up step.  GB/s
+    come from the median launch time: on the shared host an occasional window
+    of a few hundred ms slows every transfer in it, and with a handful of steps
+    one such window would move the mean by up to a tenth (the mean and the
+    minimum stay in `ms`)."""
     w = build_workload("cuda", 512, args.ctas, "deep78_32k")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     run_step(torch, w, s1, s2)
@@ -578,12 +585,12 @@ def bench_deep78(torch, hc, args, link, steps=3):
     seg = {lay: hc.segment_count(s.num_layers, s.num_buffers, s.page_size, s.row_elems, s.host_pages,
                                  LAYOUT_IDS[lay], w["a_dev"], w["a_host"]) // s.num_buffers
            for lay in LAYOUT_NAMES}
-    _, br = breakdown_from_events(ev, w["bytes_per_xfer"], link)
+    _, br = breakdown_from_events(ev, w["bytes_per_xfer"], link, stat="median")
     w["pool"].close()
     del w
     torch.cuda.empty_cache()
     return {"bytes_per_transfer": 512 * s.page_bytes, "segments_per_buffer": seg, "steps": steps,
-            "breakdown": br}
+            "gbs_from": "median launch time", "breakdown": br}
 
 
 def bench_host_shuffled(torch, hc, args, link, reps=5):
