@@ -48,6 +48,15 @@
  *     launching the second or later launch of a call split over several
  *     launches leaves the earlier ones enqueued.)  n == 0 is valid and launches
  *     no kernel (hicache_load_layer still records its layer event).
+ *   - The validation of a call of 49,152 pairs or more is split over up to
+ *     four host threads: the caller's and up to three worker threads of the
+ *     library, started on its first such call in each process, asleep between
+ *     calls and never ended before the process ends (the library is therefore
+ *     never unloaded: dlclose leaves it mapped).  A call made while another
+ *     thread's call holds them validates on the calling thread alone.  The
+ *     environment variable HICACHE_VALIDATE_THREADS, read once, caps the
+ *     threads (1: the calling thread only).  Results and error reports are
+ *     the same either way.
  *   - Transfers must be called with the pool's device current.
  *   - Return value: HICACHE_OK (0) or a negative hicache_status; the text of
  *     the last error of the calling thread is in hicache_last_error().

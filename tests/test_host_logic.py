@@ -22,7 +22,8 @@ def built():
 
 
 def declared_functions():
-    src = open(HEADER, encoding="utf-8").read()
+    with open(HEADER, encoding="utf-8") as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(hicache_[a-z_]+)\s*\(", src)))
 
@@ -235,7 +236,8 @@ def test_page_span_is_exactly_the_page(shape):
 def test_group_calls_reject_bad_arguments_before_any_cuda_call():
     """A group call with no pools, too many, NULL arrays or a NULL pool is
     refused on the host; the Python group size matches the header's."""
-    hdr = open(os.path.join(ROOT, "include", "hicache.h")).read()
+    with open(os.path.join(ROOT, "include", "hicache.h")) as f:
+        hdr = f.read()
     assert int(re.search(r"#define HICACHE_MAX_GROUP (\d+)", hdr).group(1)) == hc.MAX_GROUP
     lib = hc.library()
     kvs = (hc._DeviceKVStruct * 1)()

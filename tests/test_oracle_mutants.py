@@ -39,7 +39,8 @@ MUTANTS = [
 
 @pytest.mark.parametrize("name,orig,bad", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, orig, bad):
-    src = open(SRC, encoding="utf-8").read()
+    with open(SRC, encoding="utf-8") as f:
+        src = f.read()
     assert src.count(orig) == 1, f"mutant {name} no longer matches the oracle source"
     mutated = src.replace(orig, bad)
     csrc = tmp_path / "mutant.c"

@@ -103,7 +103,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 def _link(nvcc, lib, objs, force):
     if force or _stale(lib, objs):
         tmp = lib + f".tmp{os.getpid()}"
-        cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
+        # nodelete: dlclose() leaves the library mapped, since the worker threads
+        # of its host-side validation live until the process exits
+        cmd = ([nvcc] + ARCH + ["-shared", "-cudart", "static", "-Xlinker", "-z,nodelete", "-o", tmp] + objs
+               + ["-lpthread", "-ldl", "-lrt"])
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("libhicache link failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)

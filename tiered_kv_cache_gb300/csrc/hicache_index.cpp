@@ -3,9 +3,17 @@
 // their merge into runs, and the host-only calls built on them (the pre-pass
 // itself, segment counts and page spans).  Nothing here touches a GPU.
 
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
 #include <climits>
+#include <condition_variable>
 #include <cstdint>
+#include <cstdlib>
+#include <functional>
+#include <mutex>
+#include <thread>
 #include <vector>
 
 #include "hicache.h"
@@ -155,6 +163,217 @@ bool first_repeated(const int64_t *dev, int64_t n, int64_t Dp, int64_t *repeated
   return false;
 }
 
+// ---- validation ----------------------------------------------------------------
+//
+// One pass over the pairs that only notes whether anything is wrong: ranges,
+// order, and repeated destinations.  It is all a large call costs the host
+// before its first launch, so it has no early exit; the exact first error is
+// looked for only when something was wrong.
+
+struct Scan {
+  bool bad = false;       // a page out of range
+  bool in_order = true;   // (host page, device page) never decreases
+  bool strict = true;     // the destination page always increases
+  uint64_t dup = 0;       // nonzero: a destination page met twice in the bitmap
+};
+
+// Pairs [lo, hi).  BACKUP: the destination is the host page.  BITS: note each
+// destination page below `bound` in `bits`, one bit per page.
+template <bool BACKUP, bool BITS>
+Scan scan_pairs(const int64_t *dev, const int64_t *host, int64_t lo, int64_t hi, int64_t Hp, int64_t Dp,
+                uint64_t bound, uint64_t *bits) {
+  Scan r;
+  bool bad = false, in_order = true, strict = true;
+  uint64_t dup = 0;
+  for (int64_t i = lo; i < hi; ++i) {
+    const int64_t d = dev[i], h = host[i];
+    bad |= uint64_t(d) >= uint64_t(Dp) || uint64_t(h) >= uint64_t(Hp);
+    if (i > lo) {
+      in_order &= !(h < host[i - 1] || (h == host[i - 1] && d < dev[i - 1]));
+      strict &= BACKUP ? h > host[i - 1] : d > dev[i - 1];
+    }
+    if (BITS) {
+      const uint64_t x = uint64_t(BACKUP ? h : d);
+      if (x < bound) {
+        uint64_t &w = bits[x >> 6];
+        const uint64_t bit = uint64_t(1) << (x & 63);
+        dup |= w & bit;
+        w |= bit;
+      }
+    }
+  }
+  r.bad = bad;
+  r.in_order = in_order;
+  r.strict = strict;
+  r.dup = dup;
+  return r;
+}
+
+// Worker threads for the validation of large calls.  A call of at least
+// kParallelPairs pairs splits its pass over up to kValidateParts threads: the
+// calling thread and the workers scan chunks of the pairs, each thread into a
+// bitmap of its own, and the caller then merges the bitmaps (a page set in
+// two of them is a repeated destination).  The pool is made on first
+// use in each process (threads do not survive fork(), so a child makes its
+// own) and is never destroyed: its workers sleep on it between calls until
+// the process exits, and the library is linked so that it is never unloaded.
+// One call at a time uses it; a call that finds it busy scans on its own.
+// HICACHE_VALIDATE_THREADS=1 (read once) keeps every pass on the calling
+// thread; 2 to 4 sets the number of parts.
+constexpr int64_t kParallelPairs = 49152;
+constexpr int kValidateParts = 4;
+constexpr int64_t kValidateChunks = 32;
+
+class Workers {
+ public:
+  static Workers *get() {
+    static std::mutex mu;
+    static Workers *pool = nullptr;
+    static pid_t owner = 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (pool && owner == getpid()) return pool->workers_ ? pool : nullptr;
+    pool = new Workers;  // never deleted (see above); an old pool of a parent process is left alone
+    owner = getpid();
+    int parts = kValidateParts;
+    const unsigned hw = std::thread::hardware_concurrency();
+    if (hw < 2 * kValidateParts) parts = hw >= 4 ? 2 : 1;
+    if (const char *env = std::getenv("HICACHE_VALIDATE_THREADS"))
+      parts = std::max(1, std::min(kValidateParts, std::atoi(env)));
+    for (int k = 1; k < parts; ++k) {
+      try {
+        std::thread(&Workers::loop, pool, k).detach();
+      } catch (...) {
+        break;
+      }
+      ++pool->workers_;
+    }
+    return pool->workers_ ? pool : nullptr;
+  }
+
+  int parts() const { return workers_ + 1; }
+  std::mutex &job() { return job_; }
+  // the bitmap of part k >= 1 (guarded by job())
+  std::vector<uint64_t> &bits(int k) { return bits_[k]; }
+
+  // Run fn(0) on the calling thread and fn(k) for 0 < k < n on the workers;
+  // return once all have returned.  The caller holds job().
+  void run(int n, const std::function<void(int)> &fn) {
+    {
+      std::lock_guard<std::mutex> g(m_);
+      fn_ = &fn;
+      n_ = n;
+      pending_ = n - 1;
+      ++gen_;
+    }
+    wake_.notify_all();
+    fn(0);
+    std::unique_lock<std::mutex> g(m_);
+    done_.wait(g, [&] { return pending_ == 0; });
+  }
+
+ private:
+  void loop(int k) {
+    uint64_t seen = 0;
+    std::unique_lock<std::mutex> g(m_);
+    for (;;) {
+      wake_.wait(g, [&] { return gen_ != seen; });
+      seen = gen_;
+      if (k >= n_) continue;
+      const std::function<void(int)> *fn = fn_;
+      g.unlock();
+      (*fn)(k);
+      g.lock();
+      if (--pending_ == 0) done_.notify_one();
+    }
+  }
+
+  std::mutex job_, m_;
+  std::condition_variable wake_, done_;
+  uint64_t gen_ = 0;
+  int n_ = 0, pending_ = 0, workers_ = 0;
+  const std::function<void(int)> *fn_ = nullptr;
+  std::vector<uint64_t> bits_[kValidateParts];
+};
+
+// Scan pairs [0, n) in parts on the workers when the call is large enough and
+// the pool is free; otherwise in one part here.  `bits0` is the calling
+// thread's bitmap (BITS); every bitmap is left cleared.
+template <bool BACKUP, bool BITS>
+Scan scan_all(const int64_t *dev, const int64_t *host, int64_t n, int64_t Hp, int64_t Dp, uint64_t bound,
+              uint64_t *bits0, size_t words) {
+  Workers *w = n >= kParallelPairs ? Workers::get() : nullptr;
+  std::unique_lock<std::mutex> j;
+  int parts = 1;
+  if (w) {
+    parts = w->parts();
+    // merging the bitmaps costs words x parts; keep that below one step per pair
+    while (BITS && parts > 1 && uint64_t(words) * uint64_t(parts) > uint64_t(n)) --parts;
+    if (parts > 1) j = std::unique_lock<std::mutex>(w->job(), std::try_to_lock);
+    if (!j.owns_lock()) parts = 1;
+  }
+  if (parts == 1) {
+    Scan r = scan_pairs<BACKUP, BITS>(dev, host, 0, n, Hp, Dp, bound, bits0);
+    if (BITS) {
+      if (words <= size_t(2 * n)) {
+        std::fill(bits0, bits0 + words, uint64_t(0));
+      } else {
+        const int64_t *dst = BACKUP ? host : dev;
+        for (int64_t k = 0; k < n; ++k)
+          if (uint64_t(dst[k]) < bound) bits0[size_t(dst[k] >> 6)] = 0;
+      }
+    }
+    return r;
+  }
+  uint64_t *bits[kValidateParts] = {bits0};
+  for (int k = 1; k < parts; ++k) {
+    std::vector<uint64_t> &v = w->bits(k);
+    if (BITS && v.size() < words) v.resize(words, 0);
+    bits[k] = v.data();
+  }
+  // The pairs go out in kValidateChunks contiguous chunks, each thread taking
+  // the next free one: the caller starts at once, the workers as they wake.
+  Scan rs[kValidateParts];
+  std::atomic<int64_t> next{0};
+  const std::function<void(int)> part = [&](int k) {
+    Scan acc;
+    for (int64_t c; (c = next.fetch_add(1, std::memory_order_relaxed)) < kValidateChunks;) {
+      const Scan t = scan_pairs<BACKUP, BITS>(dev, host, n * c / kValidateChunks, n * (c + 1) / kValidateChunks,
+                                              Hp, Dp, bound, bits[k]);
+      acc.bad |= t.bad;
+      acc.in_order &= t.in_order;
+      acc.strict &= t.strict;
+      acc.dup |= t.dup;
+    }
+    rs[k] = acc;
+  };
+  w->run(parts, part);
+  Scan r;
+  for (int k = 0; k < parts; ++k) {
+    r.bad |= rs[k].bad;
+    r.in_order &= rs[k].in_order;
+    r.strict &= rs[k].strict;
+    r.dup |= rs[k].dup;
+  }
+  for (int64_t c = 1; c < kValidateChunks; ++c) {  // the pair before each chunk's first
+    const int64_t i = n * c / kValidateChunks;
+    r.in_order &= !(host[i] < host[i - 1] || (host[i] == host[i - 1] && dev[i] < dev[i - 1]));
+    r.strict &= BACKUP ? host[i] > host[i - 1] : dev[i] > dev[i - 1];
+  }
+  if (BITS) {
+    uint64_t dup = 0;
+    for (size_t x = 0; x < words; ++x) {
+      uint64_t acc = 0;
+      for (int k = 0; k < parts; ++k) {
+        dup |= acc & bits[k][x];
+        acc |= bits[k][x];
+        bits[k][x] = 0;
+      }
+    }
+    r.dup |= dup;
+  }
+  return r;
+}
+
 // Check n index pairs without reducing them: both pages in range, no
 // destination named twice (host pages of a backup, device pages of a load),
 // and whether the pairs already come in (host page, device page) order.
@@ -172,45 +391,24 @@ int validate_pairs(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *ho
   const bool backup = direction == HICACHE_DIR_BACKUP;
   const int64_t *dst = backup ? host : dev;
   const int64_t bound = backup ? Hp : Dp;
-  // One pass over the pairs that only notes whether anything is wrong:
-  // ranges, order, and repeated destinations in a per-thread bitmap of one bit
-  // per page (pools of up to 2^27 pages).  It is all a large call costs the
-  // host before its first launch, so it has no early exit; the exact first
-  // error is looked for only when something was wrong.
-  const bool bitmap = n > 32 && bound <= (int64_t(1) << 27);
-  uint64_t *bits = nullptr;
-  const size_t words = size_t((bound + 63) / 64);
-  if (bitmap) {
+  // A backup whose host pages strictly increase (the usual order) names no
+  // host page twice, so it needs no bitmap; other backups are checked
+  // afterwards.  A load notes its device pages in a bitmap of one bit per
+  // page (pools of up to 2^27 pages).
+  const bool bitmap = !backup && n > 32 && bound <= (int64_t(1) << 27);
+  Scan r;
+  if (backup) {
+    r = scan_all<true, false>(dev, host, n, Hp, Dp, uint64_t(bound), nullptr, 0);
+  } else if (bitmap) {
     thread_local std::vector<uint64_t> tls_bits;
     std::vector<uint64_t> &vbits = tls_bits;
+    const size_t words = size_t((bound + 63) / 64);
     if (vbits.size() < words) vbits.resize(words, 0);
-    bits = vbits.data();
+    r = scan_all<false, true>(dev, host, n, Hp, Dp, uint64_t(bound), vbits.data(), words);
+  } else {
+    r = scan_all<false, false>(dev, host, n, Hp, Dp, uint64_t(bound), nullptr, 0);
   }
-  bool bad = false, in_order = true;
-  uint64_t dup = 0;
-  for (int64_t i = 0; i < n; ++i) {
-    const int64_t d = dev[i], h = host[i];
-    bad |= uint64_t(d) >= uint64_t(Dp) || uint64_t(h) >= uint64_t(Hp);
-    if (i > 0) in_order &= !(h < host[i - 1] || (h == host[i - 1] && d < dev[i - 1]));
-    if (bitmap) {
-      const uint64_t x = uint64_t(backup ? h : d);
-      if (x < uint64_t(bound)) {
-        uint64_t &w = bits[x >> 6];
-        const uint64_t bit = uint64_t(1) << (x & 63);
-        dup |= w & bit;
-        w |= bit;
-      }
-    }
-  }
-  if (bitmap) {
-    if (words <= size_t(2 * n)) {
-      std::fill(bits, bits + words, uint64_t(0));
-    } else {
-      for (int64_t k = 0; k < n; ++k)
-        if (uint64_t(dst[k]) < uint64_t(bound)) bits[size_t(dst[k] >> 6)] = 0;
-    }
-  }
-  if (bad) {
+  if (r.bad) {
     for (int64_t i = 0; i < n; ++i) {
       if (dev[i] < 0 || dev[i] >= Dp)
         return set_error(HICACHE_ERR_INDEX_RANGE, "device_pages[%lld] = %lld outside [0, %lld)", (long long)i,
@@ -220,11 +418,13 @@ int validate_pairs(int64_t Hp, int64_t Dp, const int64_t *dev, const int64_t *ho
                          (long long)host[i], (long long)Hp);
     }
   }
-  *sorted = in_order;
+  *sorted = r.in_order;
   int64_t page = 0;
   bool repeated = false;
-  if (bitmap) {
-    if (dup) repeated = first_repeated(dst, n, bound, &page);
+  if (r.strict) {
+    // strictly increasing destinations: none repeats
+  } else if (bitmap) {
+    if (r.dup) repeated = first_repeated(dst, n, bound, &page);
   } else if (n <= 32) {
     for (int64_t a = 0; a < n && !repeated; ++a)
       for (int64_t b = a + 1; b < n; ++b)
