@@ -604,7 +604,11 @@ int hicache_layer_checksum(const hicache_device_kv *kv, const hicache_pool_desc 
  * hicache_tp_share: the pairs [*first, *first + *count) of rank `rank` when n
  * pairs are split into tp contiguous parts in the caller's order:
  * [floor(n*rank/tp), floor(n*(rank+1)/tp)).  1 <= tp <= 16, 0 <= rank < tp,
- * 0 <= n < 2^40.  Host-only.  Errors: INVALID_ARG. */
+ * 0 <= n < 2^40.  Host-only.  Errors: INVALID_ARG.
+ * The backup of a replicated latent splits the same way and needs no
+ * exchange: rank r calls hicache_backup for its own pairs, from its own
+ * replica into the host memory the ranks share (or one rank backs up them
+ * all), so each rank's host link carries 1/tp of the bytes. */
 int hicache_tp_share(int64_t n, int32_t tp, int32_t rank, int64_t *first, int64_t *count);
 /* The device address of the pool's num_layers per-layer counters (uint32, in
  * device memory the pool owns), which hicache_tp_load_pipelined of any rank

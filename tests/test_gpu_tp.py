@@ -106,6 +106,42 @@ def test_every_rank_ends_with_the_full_load(layout, tp, n):
     mem.free()
 
 
+@pytest.mark.parametrize("layout", list(hc.LAYOUTS))
+@pytest.mark.parametrize("tp,n", [(2, 23), (3, 23), (8, 23), (8, 5)])
+def test_partitioned_backup_of_a_replicated_latent(layout, tp, n):
+    """A replicated latent's backup needs no exchange: rank r backs up the
+    pairs of hicache_tp_share(n, tp, r) from its own replica into the host
+    memory the ranks share, each on its own stream.  The host pool then equals
+    the oracle's backup of all n pairs, and so does rank 0 backing up alone."""
+    B, L, P, R, Dp, Hp = 1, 5, 16, 72, 48, 40
+    lay = hc.LAYOUTS[layout]
+    rng = np.random.default_rng(1500 + 7 * tp + n + lay)
+    dp = wl.fragmented_pages(rng, Dp, n)
+    hp = rng.choice(Hp, n, replace=False).astype(np.int64)
+    mem = hc.PinnedHost(B * L * Hp * P * R * 2)
+    pools, bufs, kvs, _ = group(tp, L, B, P, R, Hp, Dp, layout, mem)
+    src = gh.random_device_bufs(B, L, P, R, Dp, 2, seed=tp * 31 + n)
+    for r in range(tp):                                  # identical replicas
+        for k in range(B * L):
+            bufs[r][k].copy_(src[k])
+    host = pools[0].host_array(np.uint16)
+    want = np.full(host.size, 0x5A5A, np.uint16)
+    gh.orc().backup(gh.to_np(src, 2), want, B, L, P, R, Hp, dp, hp, lay)
+    for ranks in (range(tp), [0]):
+        host[:] = 0x5A5A
+        streams = [torch.cuda.Stream() for _ in range(tp)]
+        for r in ranks:
+            first, count = hc.tp_share(n, tp, r) if len(ranks) > 1 else (0, n)
+            pools[r].backup(kvs[r], dp[first:first + count], hp[first:first + count], stream=streams[r])
+        for st in streams:
+            hc.wait(st, TEN_S)
+        assert np.array_equal(host, want), (len(ranks), tp, n)
+    for p in pools:
+        p.close()
+    del host
+    mem.free()
+
+
 def test_refusals_enqueue_nothing_and_keep_the_targets():
     B, L, P, R, Dp, Hp, tp = 1, 4, 16, 64, 32, 32, 2
     mem = hc.PinnedHost(B * L * Hp * P * R * 2)
