@@ -564,15 +564,16 @@ def breakdown_from_events(ev, bpx, link, stat="mean"):
     return per, breakdown
 
 
-def bench_deep78(torch, hc, args, link, steps=5):
+def bench_deep78(torch, hc, args, link, steps=20):
     """The deep-model segment-count stress: 78 layers, K+V, 512 fully scattered
     device pages per request (39,936 page x layer segments per buffer under
     page_first_direct), the same four operations per layout as the headline
     step, timed with events over `steps` steps after one warm-up step.  GB/s
-    come from the median launch time: on the shared host an occasional window
-    of a few hundred ms slows every transfer in it, and with a handful of steps
-    one such window would move the mean by up to a tenth (the mean and the
-    minimum stay in `ms`)."""
+    come from the median launch time, with the mean and the minimum beside it
+    in `ms`: on some shared hosts a disturbance every ~0.5 s halves both
+    directions of a two-direction transfer for a few tens of ms (one-direction
+    transfers are untouched), and it can fall on the same operation of
+    several steps in a row."""
     w = build_workload("cuda", 512, args.ctas, "deep78_32k")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     run_step(torch, w, s1, s2)
