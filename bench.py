@@ -656,7 +656,7 @@ def bench_extras(torch, hc, args, link):
                            "efficiency = (load + compute - overlapped) / min(load, compute)"}
     torch.cuda.empty_cache()
     t0 = time.perf_counter()
-    out["small_mix"] = bench_small_mix(torch, hc, args)
+    out["small_mix"] = bench_small_mix(torch, hc, args, link)
     out["small_mix"]["wall_s"] = round(time.perf_counter() - t0, 1)
     torch.cuda.empty_cache()
     # the row-size x page-size stress (fully scattered pages, about 1 GiB per call)
@@ -1026,11 +1026,13 @@ def bench_shapes(torch, hc, args):
     return res
 
 
-def bench_small_mix(torch, hc, args):
+def bench_small_mix(torch, hc, args, link=None):
     """10,000 seeded requests, 1-256 pages log-uniform, 30% backup / 70% load,
     random pages, layer_first.  Per-call latency = host wall clock from the API
     call until the stream is idle; aggregate GB/s without per-call waits, on one
-    stream and through the submission engine."""
+    stream and through the submission engine.  With the link peaks given, the
+    one-stream ceiling is each direction's bytes at its own peak, one after the
+    other: total / (backup bytes / D2H peak + load bytes / H2D peak)."""
     from tiered_kv_cache_gb300 import workloads as wl
     s = wl.SMALL_MIX
     vals = [v.view(torch.int16) for v in wl.kv_values(s, device="cuda")]
@@ -1105,6 +1107,11 @@ def bench_small_mix(torch, hc, args):
            "aggregate_gbs_wall": round(total / wall / GB, 1),
            "aggregate_gbs_engine_wall": round(total / wall_engine / GB, 1),
            "engine_launches": l1 - l0, "engine_fused_launches": f1 - f0}
+    if link and link.get("h2d_gbs") and link.get("d2h_gbs"):
+        back = sum(len(r.device_pages) for r in reqs if r.direction == "backup") * s.page_bytes
+        ceiling = total / (back / (link["d2h_gbs"] * GB) + (total - back) / (link["h2d_gbs"] * GB)) / GB
+        out["one_stream_ceiling_gbs"] = round(ceiling, 1)
+        out["aggregate_device_frac_of_ceiling"] = frac(total / dev / GB, ceiling)
     pool.close()
     return out
 
@@ -1320,7 +1327,7 @@ def main():
                                 "event per layer and a stand-in attention kernel on a second stream",
                     "value": "GB/s of the 61 per-layer loads at 64K tokens"}
         else:
-            res = bench_small_mix(torch, hc, args)
+            res = bench_small_mix(torch, hc, args, link)
             launches = int(res["launches_per_call"] * res["requests"])
             value = res["aggregate_gbs_device"]
             what = {"workload": "small_mix: 32 layers, K+V, 8 kv heads x 128, page 16, 10,000 requests "
