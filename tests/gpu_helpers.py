@@ -4,11 +4,17 @@ Expected values always come from the oracle (``oracle/``) run on host copies of
 the same inputs; nothing here computes a layout offset itself."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
 import oracle
 import tiered_kv_cache_gb300 as hc
+
+# HICACHE_SOAK=k runs the randomised corpora over k times their seeds (a soak;
+# the default, 1, is the committed corpus)
+SOAK = max(1, int(os.environ.get("HICACHE_SOAK", "1")))
 
 NP_DT = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
 TORCH_DT = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}

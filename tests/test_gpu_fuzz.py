@@ -46,7 +46,7 @@ def draw(seed):
                 layer=int(rng.integers(0, L)), seed=seed)
 
 
-@pytest.mark.parametrize("seed", range(300))
+@pytest.mark.parametrize("seed", range(300 * gh.SOAK))
 def test_random_case(seed):
     c = draw(seed)
     B, L, P, R, Dp, Hp, es, layout = (c[k] for k in ("B", "L", "P", "R", "Dp", "Hp", "es", "layout"))

@@ -40,7 +40,7 @@ def draw(seed):
                 layer=int(rng.integers(0, L)))
 
 
-@pytest.mark.parametrize("seed", range(150))
+@pytest.mark.parametrize("seed", range(150 * gh.SOAK))
 def test_random_group(seed):
     c = draw(seed)
     L, P, Dp, layout, dp, hp = c["L"], c["P"], c["Dp"], c["layout"], c["dp"], c["hp"]

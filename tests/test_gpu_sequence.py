@@ -30,7 +30,7 @@ def _noalloc(pool, kv, dp, hp, stream):
     hc._check(rc)
 
 
-@pytest.mark.parametrize("seed", range(100))
+@pytest.mark.parametrize("seed", range(100 * gh.SOAK))
 def test_random_call_sequence(seed):
     rng = np.random.default_rng(9000 + seed)
     L, P, Dp, Hp = int(rng.integers(1, 5)), int(rng.choice([1, 4, 16])), 24, 24
