@@ -13,7 +13,7 @@ import tiered_kv_cache_gb300 as hc
 
 from test_host_logic import py_runs
 
-N = 200_003                      # above the split threshold, not a multiple of the part count
+N = 100_003                      # above the split threshold, not a multiple of the part count
 DP, HP = 3 * N, 2 * N + 7
 
 
