@@ -278,7 +278,7 @@ def binding_resource(link):
         "host_dram_copy_gbs": (link.get("host_dram") or {}).get("copy_gbs_read_plus_write"),
         "sm_kernel_grids": "38-608 CTAs x 4 or 8 16-byte vectors in flight per thread",
         "ncu_c2c_fraction": "of ncu's nominal C2C capacity (about 320 GB/s per direction), protocol bytes "
-                            "included: a load fills 66.0% of RX, a backup 75.5% of TX, the fused pair 79.5% "
+                            "included: a load fills 66% of RX, a backup 75% of TX, the fused pair 79% "
                             "each way; one direction alone leaves raw capacity unused, so for loads the host "
                             "side's read-return rate binds",
         "nominal": "900 GB/s two-way NVLink-C2C per Grace, which serves two GPUs: 450 two-way, 225 per "
@@ -863,7 +863,7 @@ def bench_tp_mla(torch, hc, args):
             t = wl.mla_transfer(s, tokens)
             nbytes = len(t.device_pages) * s.page_bytes
 
-            def once():
+            def once(plain=False):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 torch.cuda.synchronize()
@@ -872,7 +872,11 @@ def bench_tp_mla(torch, hc, args):
                 for st in streams:
                     st.wait_event(e0)
                 for r, pool in enumerate(pools):
-                    hc.tp_load_pipelined(pool, kvs, counters, r, t.device_pages, t.host_pages, stream=streams[r])
+                    if plain:                              # the same bytes as one plain pipelined load
+                        pool.load_pipelined(kvs[r], t.device_pages, t.host_pages, stream=streams[r])
+                    else:
+                        hc.tp_load_pipelined(pool, kvs, counters, r, t.device_pages, t.host_pages,
+                                             stream=streams[r])
                 for st in streams:
                     j = torch.cuda.Event()
                     j.record(st)
@@ -888,6 +892,14 @@ def bench_tp_mla(torch, hc, args):
                 "ms": round(el * 1e3, 3), "host_read_gbs": round(nbytes / el / GB, 1),
                 "device_write_gbs": round(tp * nbytes / el / GB, 1),
                 "host_bytes_per_rank": nbytes // tp}
+            if tp == 1:
+                # the plain pipelined load of the same pages, timed the same way (two
+                # cross-stream hops around the launch), for comparison with tp = 1
+                for _ in range(3):
+                    once(plain=True)
+                el = statistics.median([once(plain=True) for _ in range(max(3, min(args.steps, 10)))])
+                out[f"pipelined/{tokens // 1024}k"] = {"ms": round(el * 1e3, 3),
+                                                       "host_read_gbs": round(nbytes / el / GB, 1)}
         for p in pools:
             p.close()
         del bufs, kvs

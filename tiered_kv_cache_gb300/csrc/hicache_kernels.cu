@@ -198,10 +198,18 @@ __device__ __forceinline__ int find_run(const Run *runs, int n_runs, uint32_t w)
 // in `fan` sets of device buffers, bufs[r * nb + i] for r < fan -- the ranks of
 // a tensor-parallel group that each hold the whole replicated latent.  One
 // layer's tile lies in one buffer, so only that buffer's base changes per rank.
+// With pub.count > 0, thread 0 also publishes the CTA's previous layer between
+// this tile's loads and its stores (see tp_pipelined_load_kernel).
+struct TpPublish {
+  unsigned int *const *counters;   // each rank's per-layer counters
+  int32_t layer;
+  uint32_t count;                  // 0: nothing to publish
+};
+
 template <int LAYOUT, bool ALL, bool TO_HOST, bool FANOUT = false>
 __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, const Run *runs,
                                           uint4 *const *bufs, int32_t g, int layer, int fan = 1,
-                                          int nb = 0) {
+                                          int nb = 0, TpPublish pub = {nullptr, 0, 0}) {
   const int32_t outer = g / job.tiles_per_outer;
   const int32_t inner = g - outer * job.tiles_per_outer;
   int b, l;
@@ -286,6 +294,15 @@ __device__ __forceinline__ void move_tile(const XferHeader &h, const Job &job, c
   }
   if constexpr (FANOUT) {
     static_assert(!ALL && !TO_HOST, "fan-out is for loads of one layer");
+    if (pub.count != 0 && threadIdx.x == 0) {
+      // Every thread's stores of the published layer came before the barrier
+      // that ended the CTA's previous tile, and that barrier comes before this
+      // point, so thread 0's system-wide fence (cumulative) makes the whole
+      // CTA's stores of that layer visible to every GPU before the counts.
+      // Here the fence waits while this tile's loads are in flight anyway.
+      __threadfence_system();
+      for (int r = 0; r < fan; ++r) atomicAdd_system(&pub.counters[r][pub.layer], pub.count);
+    }
     const int idx = b * h.L + l;
     uint4 *const base0 = bufs[idx];
     for (int r = 0; r < fan; ++r) {
@@ -487,25 +504,33 @@ __global__ void __launch_bounds__(kThreads)
   // count of its finished tiles of one layer and fences and counts them once,
   // when its next tile is in another layer or it has none left.  Tiles come
   // in layer order, so that is as soon as its last tile of the layer is done.
+  // All CTAs cross a layer at about the same time; a fence between tiles
+  // would stall them all at once and leave the link idle at every layer (a
+  // fixed ~2.5 us a layer), so it is taken inside the next tile, after that
+  // tile's loads are issued (move_tile's `pub`), and only the CTA's last
+  // layer is published after its last tile.  Both follow a barrier that
+  // every thread reached after its stores of the published layer (the pattern
+  // of a cooperative grid barrier: one cumulative fence by thread 0).
   int32_t held_layer = 0;                               // CTA-uniform, as g is
   uint32_t held = 0;
   for (int32_t g = s_next;; g = s_next) {
     const bool done = g >= total;
     const int32_t layer = done ? -1 : g / per_layer;
+    TpPublish pub{f.counters, held_layer, 0};
     if (held != 0 && layer != held_layer) {
-      // The barrier orders every thread's stores before thread 0's fence, and
-      // the fence is cumulative: one system-wide fence by thread 0 makes the
-      // whole CTA's stores visible to every GPU before the counts (the
-      // pattern of a cooperative grid barrier).
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        __threadfence_system();
-        for (int r = 0; r < f.tp; ++r) atomicAdd_system(&f.counters[r][held_layer], held);
+      if (done) {
+        if (threadIdx.x == 0) {
+          __threadfence_system();
+          for (int r = 0; r < f.tp; ++r) atomicAdd_system(&f.counters[r][held_layer], held);
+        }
+      } else {
+        pub.count = held;
       }
       held = 0;
     }
     if (done) break;
-    move_tile<LAYOUT, false, false, true>(p.h, job, runs, s_bufs, g - layer * per_layer, layer, f.tp, nb);
+    move_tile<LAYOUT, false, false, true>(p.h, job, runs, s_bufs, g - layer * per_layer, layer, f.tp, nb,
+                                          pub);
     held_layer = layer;
     ++held;
     __syncthreads();                                    // every thread has read s_next
