@@ -307,8 +307,8 @@ int hicache_plan_load_layer(const hicache_plan *plan, const hicache_device_kv *k
  *   - Each layer is signalled on the device, not by an event recorded between
  *     kernels (which would stop them overlapping): every CTA counts itself into
  *     the layer's pool counter once its tiles have landed, and
- *     hicache_wait_layer(pool, l, stream) waits for that count.  The layer
- *     events are recorded after the call for the last layer.
+ *     hicache_wait_layer(pool, l, stream) waits for that count, and
+ *     hicache_layer_event(pool, l) gives an event that fires once it is in.
  *   - A capturing stream is refused (INVALID_ARG): the count each layer must
  *     reach is raised on the host when the call is enqueued.
  *   - Calls of one plan's chain come from one thread, in layer order.
@@ -459,8 +459,8 @@ int hicache_group_plan_load_layers(hicache_group_plan *plan, const hicache_devic
  * when that loaded layer_id - 1 on the same stream (nothing else enqueued on
  * the stream in between), and every CTA counted into each pool's counter of
  * the layer, so hicache_wait_layer on any pool of the group waits for that
- * pool's layer on the device.  Every pool's layer events are recorded after
- * the call for the last layer.  No two device buffers of the group may
+ * pool's layer on the device (and hicache_layer_event gives an event that
+ * fires once that count is in).  No two device buffers of the group may
  * overlap; a capturing stream is refused.  Errors as
  * hicache_group_plan_execute, plus INVALID_ARG for layer_id outside [0,
  * num_layers), overlapping buffers or a capturing stream; on a refused call
@@ -471,9 +471,14 @@ int hicache_group_plan_destroy(hicache_group_plan *plan);
 
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
-/* The pool-owned event recorded by the last load of `layer` (*event_out is a
- * cudaEvent_t; do not destroy it).  After a pipelined load it fires when the
- * whole load is in; hicache_wait_layer waits for the layer alone. */
+/* The pool-owned event of the last load of `layer` enqueued before this call
+ * (*event_out is a cudaEvent_t; do not destroy it): it fires once that load
+ * has moved the layer.  Where that load is signalled on the device
+ * (pipelined, allocation-free pipelined, tensor-parallel and chained
+ * per-layer loads), this call records the event, on a stream of the pool's
+ * own that waits for the load's count of the layer; the pool's device must
+ * be current.  Otherwise it is the event the load recorded on its stream.
+ * Errors: INVALID_ARG, CUDA. */
 int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
 /* Make `compute_stream` wait (on the device; the host does not block) for the
  * last load of `layer` enqueued before this call: its layer event, or, if that

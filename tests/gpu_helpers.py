@@ -120,3 +120,19 @@ def sampled_host_check(host_words: np.ndarray, bufs, dp, hp, layout, B, L, P, R,
         t = torch.from_numpy(doff[sel]).to("cuda")
         dev_vals[sel] = flat[int(k)].index_select(0, t).cpu().numpy().view(host_words.dtype)
     return np.array_equal(got_host, dev_vals)
+
+
+_libcuda = None
+
+
+def stream_wait_event(stream, event_handle: int):
+    """Make `stream` wait for a raw cudaEvent_t (e.g. a pool's layer event)
+    through the driver API (a runtime event handle is a driver event)."""
+    import ctypes
+    global _libcuda
+    if _libcuda is None:
+        _libcuda = ctypes.CDLL("libcuda.so.1")
+        _libcuda.cuStreamWaitEvent.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        _libcuda.cuStreamWaitEvent.restype = ctypes.c_int
+    rc = _libcuda.cuStreamWaitEvent(ctypes.c_void_p(int(stream.cuda_stream)), ctypes.c_void_p(event_handle), 0)
+    assert rc == 0, f"cuStreamWaitEvent returned {rc}"

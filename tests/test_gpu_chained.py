@@ -82,6 +82,19 @@ def test_chained_layers_equal_the_oracle(layout, shape):
         got = gh.to_np(bufs, 2)
         for k in range(B * L):
             assert np.array_equal(got[k], want[k]), ("waited", k)
+        # and waited on each layer's CUDA event, taken right after its chained
+        # call (the event fires once the layer's count is in)
+        gh.sentinel_fill(bufs)
+        torch.cuda.synchronize()
+        sums.zero_()
+        for layer in range(L):
+            plan.load_layer_chained(kv, layer, stream=xfer)
+            gh.stream_wait_event(comp, pool.layer_event(layer))
+            hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+        hc.wait(comp, TEN_S)
+        hc.wait(xfer, TEN_S)
+        torch.cuda.synchronize()
+        assert torch.equal(sums, after), "a layer event fired before its layer landed"
         plan.close()
 
 
@@ -208,6 +221,21 @@ def test_chained_group_layers_equal_the_oracle(layout):
             hc.layer_checksum(kvs[i], pool, dp, layer, after[i].data_ptr() + 8 * layer)
     torch.cuda.synchronize()
     assert torch.equal(sums, after)
+    # and waited on each pool's layer event, from sentinel-filled buffers
+    for bufs in bufsets:
+        for b in bufs:
+            b.view(torch.uint8).fill_(0x77)
+    torch.cuda.synchronize()
+    ev_sums = torch.zeros_like(sums)
+    for layer in range(L):
+        plan.load_layer_chained(kvs, layer, stream=xfer)
+        for i, (pool, kv) in enumerate(zip(pools, kvs)):
+            gh.stream_wait_event(comp, pool.layer_event(layer))
+            hc.layer_checksum(kv, pool, dp, layer, ev_sums[i].data_ptr() + 8 * layer, stream=comp)
+    hc.wait(comp, TEN_S)
+    hc.wait(xfer, TEN_S)
+    torch.cuda.synchronize()
+    assert torch.equal(ev_sums, after), "a layer event fired before its layer landed"
     plan.close()
     for pool in pools:
         pool.close()

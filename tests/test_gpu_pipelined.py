@@ -90,6 +90,46 @@ def test_compute_waits_for_each_layer():
         plan.close()
 
 
+def test_layer_events_of_counted_loads():
+    """After a pipelined load (and an allocation-free one), each layer's event,
+    asked for right after the call, holds the stand-in attention until that
+    layer has landed; after a plain per-layer load it is that load's event."""
+    import ctypes
+    B, L, P, R, Dp, Hp, n = 1, 12, 64, 576, 128, 128, 100
+    rng = np.random.default_rng(330)
+    dp = wl.fragmented_pages(rng, Dp, n)
+    hp = np.arange(n)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=330)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        kv = hc.DeviceKV(bufs, Dp)
+        want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+        expect = [int(want[layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32).astype(np.uint64)
+                      .sum(dtype=np.uint64)) for layer in range(L)]
+        xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def noalloc():
+            hc._check(hc.library().hicache_load_pipelined_noalloc(
+                pool.handle, ctypes.byref(kv.struct), hc._ptr(hc._idx(dp)), hc._ptr(hc._idx(hp)), len(dp),
+                hc.LAYOUT_POOL, hc._stream(xfer)))
+
+        for load in (lambda: pool.load_pipelined(kv, dp, hp, stream=xfer), noalloc,
+                     lambda: [pool.load_layer(kv, dp, hp, layer, stream=xfer) for layer in range(L)]):
+            gh.sentinel_fill(bufs, 0)
+            torch.cuda.synchronize()
+            sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+            load()
+            for layer in range(L):
+                gh.stream_wait_event(comp, pool.layer_event(layer))
+                hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+            hc.wait(comp, TEN_S)
+            hc.wait(xfer, TEN_S)
+            got = sums.cpu().numpy().view(np.uint64)
+            assert [int(x) for x in got] == expect
+
+
 def test_wait_layer_follows_the_last_load_kind_and_stream_rule():
     B, L, P, R, Dp, Hp = 1, 3, 4, 64, 8, 8
     bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]

@@ -458,6 +458,12 @@ int hicache_pool_destroy(hicache_pool *pool) {
   // so then the whole device is waited for.
   if (pool->chain_open) (void)cudaDeviceSynchronize();
   else if (pool->pipeline_stream_set && pool->pipeline_last) (void)cudaEventSynchronize(pool->pipeline_last);
+  if (pool->event_stream) {
+    // its waits read the counters freed below; every one is met once the
+    // loads above are done
+    (void)cudaStreamSynchronize(pool->event_stream);
+    (void)cudaStreamDestroy(pool->event_stream);
+  }
   for (auto ev : pool->events)
     if (ev) cudaEventDestroy(ev);
   if (pool->layer_done) cudaFree(pool->layer_done);
@@ -529,6 +535,14 @@ int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out) {
   if (layer < 0 || layer >= pool->shape.L)
     return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
                      (long long)pool->shape.L);
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  if (pool->layer_signal[size_t(layer)] != 0) {
+    // the layer's last load is signalled on the device: record its event now,
+    // behind a wait for that load's count of the layer
+    int rc = check_device(pool);
+    if (rc) return rc;
+    if ((rc = record_counted_layer_event(pool, layer))) return rc;
+  }
   *event_out = pool->events[size_t(layer)];
   return HICACHE_OK;
 }

@@ -437,10 +437,6 @@ int hicache_group_plan_load_layer_chained(hicache_group_plan *plan, const hicach
   if (rc != HICACHE_OK) return rc;
   if (layer_id + 1 == L) {
     for (int32_t i = 0; i < np; ++i) {
-      for (int64_t l = 0; l < L; ++l) {
-        const cudaError_t e = cudaEventRecord(pools[i]->events[size_t(l)], static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
-      }
       const cudaError_t e = cudaEventRecord(pools[i]->pipeline_last, static_cast<cudaStream_t>(stream));
       if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(chained load)");
       pools[i]->chain_open = false;

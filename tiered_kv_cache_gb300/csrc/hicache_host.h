@@ -62,6 +62,10 @@ bool intersects(std::vector<int64_t> a, std::vector<int64_t> b, int64_t *common)
 // driver does not offer it.
 using WaitValue32Fn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 WaitValue32Fn wait_value32();
+// Record `layer`'s event on the pool's event stream behind a wait for the
+// counter of the layer's last load (signal 1 or 2) to reach its current
+// target.  The caller holds pool->signal_mu, on the pool's device.
+int record_counted_layer_event(hicache_pool *pool, int64_t layer);
 
 }  // namespace hicache
 
@@ -93,6 +97,11 @@ struct hicache_pool {
   // a chained per-layer load on pipeline_stream has not reached its last
   // layer (no pipeline_last recorded behind it yet)
   bool chain_open = false;
+  // Where hicache_layer_event records the event of a load signalled on the
+  // device: a stream of the pool's own that first waits for the layer's
+  // counter to reach its target (made on first use, drained and destroyed
+  // with the pool).
+  cudaStream_t event_stream = nullptr;
   // Allocation-free pipelined loads (signal 2): the library's static counters
   // on this device and, per layer, the value the last such load brings them to.
   unsigned int *noalloc_done = nullptr;

@@ -123,6 +123,25 @@ uint32_t g_noalloc_target[hicache::kNoAllocMaxDevices][hicache::kNoAllocMaxLayer
 uint32_t g_noalloc_slot[hicache::kNoAllocMaxDevices];  // next scheduler pair, per device
 }  // namespace
 
+int record_counted_layer_event(hicache_pool *pool, int64_t layer) {
+  if (!pool->event_stream) {
+    const cudaError_t e = cudaStreamCreateWithFlags(&pool->event_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      pool->event_stream = nullptr;
+      return cuda_error(e, "cudaStreamCreateWithFlags(event stream)");
+    }
+  }
+  const bool noalloc = pool->layer_signal[size_t(layer)] == 2;
+  unsigned int *counter = (noalloc ? pool->noalloc_done : pool->layer_done) + layer;
+  const uint32_t target = noalloc ? pool->noalloc_target[size_t(layer)] : pool->layer_target[size_t(layer)];
+  const CUresult r = wait_value32()(static_cast<CUstream>(pool->event_stream),
+                                    reinterpret_cast<CUdeviceptr>(counter), target, CU_STREAM_WAIT_VALUE_GEQ);
+  if (r != CUDA_SUCCESS) return set_error(HICACHE_ERR_CUDA, "cuStreamWaitValue32 failed (%d)", int(r));
+  const cudaError_t e = cudaEventRecord(pool->events[size_t(layer)], pool->event_stream);
+  if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
+  return HICACHE_OK;
+}
+
 }  // namespace hicache
 
 using namespace hicache;

@@ -239,12 +239,7 @@ int hicache_plan_load_layer_chained(hicache_plan *plan, const hicache_device_kv 
   pool->chain_open = true;
   if (rc != HICACHE_OK) return rc;
   if (layer_id + 1 == s.L) {
-    // the layer events fire once the last layer's kernel is done, and so does
-    // the pool's counted-load event, which closes the chain
-    for (int64_t l = 0; l < s.L; ++l) {
-      const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
-      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
-    }
+    // the pool's counted-load event, behind the last layer's kernel, closes the chain
     const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(chained load)");
     pool->chain_open = false;
