@@ -246,8 +246,8 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
  * (a stream memory wait on a per-layer counter, cuStreamWaitValue32), so
  * attention on layer l can start while later layers still load -- the
  * per-layer overlap of "HiCache 시스템 설계와 최적화", section "CPU→GPU 전송
- * 최적화", without a launch and an event per layer.  The layer events are
- * recorded too, once the whole load is in.  Checks as hicache_load.  A
+ * 최적화", without a launch and an event per layer (hicache_layer_event
+ * gives a layer's event when asked for).  Checks as hicache_load.  A
  * pipelined load may only go on another stream than the pool's previous one
  * once that one's counted loads (pipelined, tensor-parallel, chained per-layer)
  * have finished (INVALID_ARG otherwise): the per-layer counts must rise in
@@ -482,7 +482,8 @@ int hicache_group_plan_destroy(hicache_group_plan *plan);
 int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
 /* Make `compute_stream` wait (on the device; the host does not block) for the
  * last load of `layer` enqueued before this call: its layer event, or, if that
- * load was pipelined, that layer's counter. */
+ * load is signalled on the device (pipelined, allocation-free pipelined,
+ * tensor-parallel, chained per-layer), that layer's counter. */
 int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
 
 /* Block the calling host thread until all work on `stream` is done, for at

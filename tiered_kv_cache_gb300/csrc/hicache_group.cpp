@@ -273,10 +273,7 @@ int hicache_group_load_pipelined(hicache_pool *const *pools, const hicache_devic
   if ((rc = enqueue_group_pipelined(pools, kvs, npools, runs, lay, stream))) return rc;
   for (int32_t i = 0; i < npools; ++i) {
     hicache_pool *p = pools[i];
-    for (int64_t l = 0; l < p->shape.L; ++l) {
-      const cudaError_t e = cudaEventRecord(p->events[size_t(l)], static_cast<cudaStream_t>(stream));
-      if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
-    }
+    // (the layer events are recorded when asked for: hicache_layer_event)
     const cudaError_t e = cudaEventRecord(p->pipeline_last, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
     p->chain_open = false;

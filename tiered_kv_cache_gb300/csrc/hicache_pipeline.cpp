@@ -103,11 +103,7 @@ int enqueue_pipelined(hicache_pool *pool, const hicache_device_kv *kv, const std
     }
     next += size_t(c);
   }
-  // the layer events also fire, once the whole load is in
-  for (int64_t l = 0; l < s.L; ++l) {
-    const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
-  }
+  // (the layer events are recorded when asked for: hicache_layer_event)
   const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
   pool->chain_open = false;            // the event covers any chain before it on this stream

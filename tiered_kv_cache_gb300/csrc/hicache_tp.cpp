@@ -164,10 +164,7 @@ int hicache_tp_load_pipelined(hicache_pool *pool, const hicache_device_kv *rank_
     for (int64_t l = 0; l < s.L; ++l) pool->layer_target[size_t(l)] += uint32_t(params.h.job[0].total_tiles);
     next += size_t(c);
   }
-  for (int64_t l = 0; l < s.L; ++l) {
-    const cudaError_t e = cudaEventRecord(pool->events[size_t(l)], static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
-  }
+  // (the layer events are recorded when asked for: hicache_layer_event)
   const cudaError_t e = cudaEventRecord(pool->pipeline_last, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(pipelined load)");
   pool->chain_open = false;
