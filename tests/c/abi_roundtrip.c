@@ -181,6 +181,9 @@ int main(void) {
   for (int l = 0; l < L; ++l) {
     CHECK(hicache_plan_load_layer_chained(plan, &kv, HICACHE_LAYOUT_POOL, l, xfer));
     CHECK(hicache_wait_layer(pool, l, comp));
+    void *ev = NULL;                       /* or its CUDA event, recorded on request */
+    CHECK(hicache_layer_event(pool, l, &ev));
+    if (!ev || cudaStreamWaitEvent(comp, (cudaEvent_t)ev, 0) != cudaSuccess) return 12;
   }
   int64_t first = -1, count = -1;
   CHECK(hicache_tp_share(N, 1, 0, &first, &count));
