@@ -471,19 +471,27 @@ int hicache_group_plan_destroy(hicache_group_plan *plan);
 
 /* ---- per-layer events (KV_READY) ---------------------------------------------- */
 
-/* The pool-owned event of the last load of `layer` enqueued before this call
- * (*event_out is a cudaEvent_t; do not destroy it): it fires once that load
- * has moved the layer.  Where that load is signalled on the device
- * (pipelined, allocation-free pipelined, tensor-parallel and chained
- * per-layer loads), this call records the event, on a stream of the pool's
- * own that waits for the load's count of the layer; the pool's device must
- * be current.  Otherwise it is the event the load recorded on its stream.
+/* The last load of a layer, for this call and hicache_wait_layer, is the last
+ * call enqueued before it that loaded the layer: one layer or every layer
+ * (hicache_load, hicache_backup_load, a plan's or a group's load of every
+ * layer), n > 0.  Loads queued through the submission engine are not among
+ * them: wait for those through the engine.
+ *
+ * The pool-owned event of the last load of `layer` (*event_out is a
+ * cudaEvent_t; do not destroy it): it fires once that load has moved the
+ * layer.  Where that load is signalled on the device (pipelined,
+ * allocation-free pipelined, tensor-parallel and chained per-layer loads),
+ * this call records the event, on a stream of the pool's own that waits for
+ * the load's count of the layer; the pool's device must be current.  After a
+ * load of every layer it is the pool's event recorded behind that load (one
+ * event for all layers); otherwise the event the load recorded on its stream.
  * Errors: INVALID_ARG, CUDA. */
 int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
 /* Make `compute_stream` wait (on the device; the host does not block) for the
- * last load of `layer` enqueued before this call: its layer event, or, if that
- * load is signalled on the device (pipelined, allocation-free pipelined,
- * tensor-parallel, chained per-layer), that layer's counter. */
+ * last load of `layer` enqueued before this call: its layer event (the whole
+ * load's, for a load of every layer), or, if that load is signalled on the
+ * device (pipelined, allocation-free pipelined, tensor-parallel, chained
+ * per-layer), that layer's counter. */
 int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
 
 /* Block the calling host thread until all work on `stream` is done, for at
@@ -551,7 +559,9 @@ int hicache_engine_destroy(hicache_engine *engine);
  * backup reads); the dependency is recorded on after_stream during this call.
  * kv's buffer table is copied.  *ticket receives the request's id (a request
  * paired ahead of earlier ones may finish before them).  After a launch failure
- * the engine refuses new requests (CUDA). */
+ * the engine refuses new requests (CUDA).  hicache_wait_layer and
+ * hicache_layer_event do not see queued loads: wait for them through the
+ * engine. */
 int hicache_engine_submit(hicache_engine *engine, const hicache_device_kv *kv,
                           const int64_t *device_pages, const int64_t *host_pages, int64_t n,
                           int32_t direction, int32_t layout, int32_t after_stream_valid,

@@ -130,6 +130,61 @@ def test_layer_events_of_counted_loads():
             assert [int(x) for x in got] == expect
 
 
+def test_waits_follow_a_load_of_every_layer():
+    """A load of every layer -- hicache_load, a fused backup + load, a plan's
+    or a group's load of every layer -- is the last load of each layer: after
+    an earlier pipelined load (whose counts are all in), hicache_wait_layer and
+    the layer event both hold the stand-in attention until the new load is in."""
+    B, L, P, R, Dp, Hp, n = 1, 12, 64, 576, 256, 256, 100
+    rng = np.random.default_rng(350)
+    dp = wl.fragmented_pages(rng, Dp // 2, n)             # loads: device pages below Dp / 2
+    hp = np.arange(n)
+    bdp, bhp = np.arange(Dp // 2, Dp // 2 + 8), np.arange(Hp - 8, Hp)   # the fused call's backup
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=350)
+    mem = hc.PinnedHost(B * L * Hp * P * R * 2)
+    pool = hc.Pool(L, B, P, R, Hp, "page_first", host_ptr=mem.ptr, host_bytes=mem.nbytes)
+    host = pool.host_array(np.uint8)
+    host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+    kv = hc.DeviceKV(bufs, Dp)
+    want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+    gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+    expect = [int(want[layer].reshape(Dp, -1)[dp].reshape(-1).view(np.uint32).astype(np.uint64)
+                  .sum(dtype=np.uint64)) for layer in range(L)]
+    plan = pool.plan(dp, hp, Dp, hc.LOAD)
+    gplan = hc.group_plan([pool], dp, hp, Dp)
+    xfer, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    loads = {
+        "load": lambda: pool.load(kv, dp, hp, stream=xfer),
+        "backup_load": lambda: pool.backup_load(kv, bdp, bhp, dp, hp, stream=xfer),
+        "plan": lambda: plan.execute(kv, stream=xfer),
+        "group": lambda: hc.group_transfer([pool], [kv], dp, hp, hc.LOAD, stream=xfer),
+        "group_plan": lambda: gplan.execute([kv], stream=xfer),
+    }
+    for name, load in loads.items():
+        for by_event in (False, True):
+            pool.load_pipelined(kv, dp, hp, stream=xfer)       # counts met: a stale wait passes at once
+            hc.wait(xfer, TEN_S)
+            gh.sentinel_fill(bufs, 0)
+            torch.cuda.synchronize()
+            sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+            load()
+            for layer in range(L):
+                if by_event:
+                    gh.stream_wait_event(comp, pool.layer_event(layer))
+                else:
+                    pool.wait_layer(layer, comp)
+                hc.layer_checksum(kv, pool, dp, layer, sums.data_ptr() + 8 * layer, stream=comp)
+            hc.wait(comp, TEN_S)
+            hc.wait(xfer, TEN_S)
+            got = sums.cpu().numpy().view(np.uint64)
+            assert [int(x) for x in got] == expect, (name, by_event)
+    plan.close()
+    gplan.close()
+    pool.close()
+    del host
+    mem.free()
+
+
 def test_wait_layer_follows_the_last_load_kind_and_stream_rule():
     B, L, P, R, Dp, Hp = 1, 3, 4, 64, 8, 8
     bufs = [torch.zeros((Dp * P, R), dtype=torch.int16, device="cuda") for _ in range(B * L)]

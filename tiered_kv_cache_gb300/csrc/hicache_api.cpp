@@ -300,7 +300,17 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
     std::lock_guard<std::mutex> g(pool->signal_mu);
     pool->layer_signal[size_t(layer)] = 0;
+  } else if (direction == HICACHE_DIR_LOAD && n > 0) {
+    return mark_all_layer_load(pool, stream);
   }
+  return HICACHE_OK;
+}
+
+int mark_all_layer_load(hicache_pool *pool, void *stream) {
+  const cudaError_t e = cudaEventRecord(pool->load_all, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(load of every layer)");
+  std::lock_guard<std::mutex> g(pool->signal_mu);
+  for (auto &sig : pool->layer_signal) sig = 3;
   return HICACHE_OK;
 }
 
@@ -433,6 +443,7 @@ int hicache_pool_create(const hicache_pool_desc *desc, void *host_pool, size_t h
     }
   }
   e = cudaEventCreateWithFlags(&p->pipeline_last, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->load_all, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     hicache_pool_destroy(p);
     return cuda_error(e, "cudaEventCreateWithFlags");
@@ -468,6 +479,7 @@ int hicache_pool_destroy(hicache_pool *pool) {
     if (ev) cudaEventDestroy(ev);
   if (pool->layer_done) cudaFree(pool->layer_done);
   if (pool->pipeline_last) cudaEventDestroy(pool->pipeline_last);
+  if (pool->load_all) cudaEventDestroy(pool->load_all);
   delete pool;
   return HICACHE_OK;
 }
@@ -525,8 +537,10 @@ int hicache_backup_load(hicache_pool *pool, const hicache_device_kv *kv,
                        (long long)page);
   }
   if (lrun.empty()) return enqueue(pool, kv, brun, nullptr, lay, -1, true, stream);
-  if (brun.empty()) return enqueue(pool, kv, lrun, nullptr, lay, -1, false, stream);
-  return enqueue(pool, kv, brun, &lrun, lay, -1, true, stream);
+  rc = brun.empty() ? enqueue(pool, kv, lrun, nullptr, lay, -1, false, stream)
+                    : enqueue(pool, kv, brun, &lrun, lay, -1, true, stream);
+  if (rc) return rc;
+  return mark_all_layer_load(pool, stream);
 }
 
 int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out) {
@@ -536,14 +550,15 @@ int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out) {
     return set_error(HICACHE_ERR_INVALID_ARG, "layer %d outside [0, %lld)", layer,
                      (long long)pool->shape.L);
   std::lock_guard<std::mutex> g(pool->signal_mu);
-  if (pool->layer_signal[size_t(layer)] != 0) {
+  const uint8_t sig = pool->layer_signal[size_t(layer)];
+  if (sig == 1 || sig == 2) {
     // the layer's last load is signalled on the device: record its event now,
     // behind a wait for that load's count of the layer
     int rc = check_device(pool);
     if (rc) return rc;
     if ((rc = record_counted_layer_event(pool, layer))) return rc;
   }
-  *event_out = pool->events[size_t(layer)];
+  *event_out = sig == 3 ? pool->load_all : pool->events[size_t(layer)];
   return HICACHE_OK;
 }
 

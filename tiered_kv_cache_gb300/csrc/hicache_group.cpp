@@ -244,6 +244,9 @@ int hicache_group_transfer(hicache_pool *const *pools, const hicache_device_kv *
       std::lock_guard<std::mutex> g(p->signal_mu);
       p->layer_signal[size_t(layer_id)] = 0;
     }
+  } else if (direction == HICACHE_DIR_LOAD && n > 0) {
+    for (int32_t i = 0; i < npools; ++i)
+      if ((rc = mark_all_layer_load(pools[i], stream))) return rc;
   }
   return HICACHE_OK;
 }
@@ -372,6 +375,9 @@ int hicache_group_plan_execute(const hicache_group_plan *plan, const hicache_dev
       std::lock_guard<std::mutex> g(p->signal_mu);
       p->layer_signal[size_t(layer_id)] = 0;
     }
+  } else if (!plan->runs.empty()) {
+    for (int32_t i = 0; i < np; ++i)
+      if ((rc = mark_all_layer_load(pools[i], stream))) return rc;
   }
   return HICACHE_OK;
 }

@@ -66,6 +66,9 @@ WaitValue32Fn wait_value32();
 // counter of the layer's last load (signal 1 or 2) to reach its current
 // target.  The caller holds pool->signal_mu, on the pool's device.
 int record_counted_layer_event(hicache_pool *pool, int64_t layer);
+// After a load of every layer was enqueued on `stream`: record the pool's
+// load_all event there and make it every layer's last load (signal 3).
+int mark_all_layer_load(hicache_pool *pool, void *stream);
 
 }  // namespace hicache
 
@@ -102,6 +105,10 @@ struct hicache_pool {
   // counter to reach its target (made on first use, drained and destroyed
   // with the pool).
   cudaStream_t event_stream = nullptr;
+  // Recorded behind every load of every layer (hicache_load, a fused backup
+  // and load, a plan's or group's load of every layer, an engine load); signal
+  // 3 sends hicache_wait_layer and hicache_layer_event of every layer to it.
+  cudaEvent_t load_all = nullptr;
   // Allocation-free pipelined loads (signal 2): the library's static counters
   // on this device and, per layer, the value the last such load brings them to.
   unsigned int *noalloc_done = nullptr;

@@ -265,8 +265,9 @@ int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream) 
       return set_error(HICACHE_ERR_CUDA, "cuStreamWaitValue32 failed (%d)", int(r));
     return HICACHE_OK;
   }
-  const cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream),
-                                            pool->events[size_t(layer)], 0);
+  // signal 3: the last load of this layer loaded every layer
+  const cudaEvent_t ev = pool->layer_signal[size_t(layer)] == 3 ? pool->load_all : pool->events[size_t(layer)];
+  const cudaError_t e = cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream), ev, 0);
   if (e != cudaSuccess) return cuda_error(e, "cudaStreamWaitEvent");
   return HICACHE_OK;
 }

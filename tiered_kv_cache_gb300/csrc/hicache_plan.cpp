@@ -177,6 +177,8 @@ int hicache_plan_execute(const hicache_plan *plan, const hicache_device_kv *kv, 
     if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(layer event)");
     std::lock_guard<std::mutex> g(pool->signal_mu);
     pool->layer_signal[size_t(layer_id)] = 0;
+  } else if (plan->direction == HICACHE_DIR_LOAD && plan->n > 0) {
+    return mark_all_layer_load(pool, stream);
   }
   return HICACHE_OK;
 }
