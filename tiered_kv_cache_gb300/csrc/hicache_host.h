@@ -88,8 +88,10 @@ struct hicache_pool {
   // Per-layer completion of pipelined loads (hicache_load_pipelined): device
   // counters that the kernel raises as layers land, the value each must reach
   // for the last pipelined load, which signal hicache_wait_layer should use
-  // for each layer (0: the layer event, 1: the counter), and the one stream
-  // all pipelined loads of the pool go on (which keeps the counts in order).
+  // for each layer (0: the layer event, 1: the counter, 2: the allocation-free
+  // load's counter, 3: load_all, after a load of every layer), and the one
+  // stream all pipelined loads of the pool go on (which keeps the counts in
+  // order).
   unsigned int *layer_done = nullptr;
   std::mutex signal_mu;
   std::vector<uint32_t> layer_target;
