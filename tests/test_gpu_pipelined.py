@@ -120,6 +120,8 @@ def test_layer_events_of_counted_loads():
             gh.sentinel_fill(bufs, 0)
             torch.cuda.synchronize()
             sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+            with torch.cuda.stream(xfer):
+                torch.cuda._sleep(1_000_000)     # the load starts late: an early wait reads the sentinel
             load()
             for layer in range(L):
                 gh.stream_wait_event(comp, pool.layer_event(layer))
@@ -167,6 +169,8 @@ def test_waits_follow_a_load_of_every_layer():
             gh.sentinel_fill(bufs, 0)
             torch.cuda.synchronize()
             sums = torch.zeros(L, dtype=torch.int64, device="cuda")
+            with torch.cuda.stream(xfer):
+                torch.cuda._sleep(1_000_000)     # the load starts late: an early wait reads the sentinel
             load()
             for layer in range(L):
                 if by_event:
