@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CORPORA = ["tests/test_gpu_fuzz.py", "tests/test_gpu_group_fuzz.py", "tests/test_gpu_sequence.py",
            "tests/test_gpu_tp.py", "tests/test_gpu_pipelined.py", "tests/test_gpu_group.py",
-           "tests/test_gpu_chained.py", "tests/test_gpu_large_calls.py"]
+           "tests/test_gpu_chained.py", "tests/test_gpu_large_calls.py", "tests/test_gpu_wait_fuzz.py"]
 
 
 def test_corpora_under_the_bounds_checked_build():
