@@ -475,7 +475,8 @@ int hicache_group_plan_destroy(hicache_group_plan *plan);
  * call enqueued before it that loaded the layer: one layer or every layer
  * (hicache_load, hicache_backup_load, a plan's or a group's load of every
  * layer), n > 0.  Loads queued through the submission engine are not among
- * them: wait for those through the engine.
+ * them (wait for those through the engine), nor is a load of every layer
+ * captured into a CUDA graph.
  *
  * The pool-owned event of the last load of `layer` (*event_out is a
  * cudaEvent_t; do not destroy it): it fires once that load has moved the

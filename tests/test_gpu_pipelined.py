@@ -327,3 +327,37 @@ def test_pipelined_loads_refuse_a_capturing_stream():
         assert int(marker.item()) == 1
         assert [pool.pipeline_status(layer) for layer in range(L)] == before
         plan.close()
+
+
+def test_a_captured_load_of_every_layer_leaves_the_waits():
+    """hicache_load captured into a CUDA graph: the replay moves the pages,
+    and the per-layer waits still refer to the last load enqueued outside the
+    capture (they neither fail nor wait on the graph)."""
+    B, L, P, R, Dp, Hp, n = 1, 4, 16, 64, 48, 48, 10
+    rng = np.random.default_rng(360)
+    dp = rng.permutation(Dp)[:n]
+    hp = np.arange(n)
+    bufs = gh.random_device_bufs(B, L, P, R, Dp, seed=360)
+    with hc.Pool(L, B, P, R, Hp, "page_first") as pool:
+        host = pool.host_array(np.uint8)
+        host[:] = rng.integers(0, 256, host.size, dtype=np.uint8)
+        kv = hc.DeviceKV(bufs, Dp)
+        s, comp = torch.cuda.Stream(), torch.cuda.Stream()
+        pool.load_layer(kv, dp, hp, 0, stream=s)
+        torch.cuda.synchronize()
+        gh.sentinel_fill(bufs, 0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            pool.load(kv, dp, hp, stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+        for layer in range(L):
+            pool.wait_layer(layer, comp)
+            gh.stream_wait_event(comp, pool.layer_event(layer))
+        comp.synchronize()
+        want = [np.zeros((Dp * P, R), np.uint16) for _ in range(B * L)]
+        gh.orc().load(want, host.view(np.uint16), B, L, P, R, Hp, dp, hp, 1)
+        got = gh.to_np(bufs, 2)
+        for k in range(B * L):
+            assert np.array_equal(got[k], want[k]), k

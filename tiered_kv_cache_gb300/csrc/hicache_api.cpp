@@ -307,6 +307,11 @@ int transfer(hicache_pool *pool, const hicache_device_kv *kv, const int64_t *dev
 }
 
 int mark_all_layer_load(hicache_pool *pool, void *stream) {
+  // a load captured into a CUDA graph is not enqueued until the graph runs
+  cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
+  const cudaError_t ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &status);
+  if (ce != cudaSuccess) return cuda_error(ce, "cudaStreamIsCapturing");
+  if (status != cudaStreamCaptureStatusNone) return HICACHE_OK;
   const cudaError_t e = cudaEventRecord(pool->load_all, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_error(e, "cudaEventRecord(load of every layer)");
   std::lock_guard<std::mutex> g(pool->signal_mu);
