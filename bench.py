@@ -555,10 +555,13 @@ def breakdown_from_events(ev, bpx, link, stat="mean"):
             "load_frac_of_link": frac(ld, link["h2d_gbs"]),
             "bidir_streams_frac_of_link": frac(bi, link["bidir_gbs"]),
             "bidir_fused_frac_of_link": frac(bf, link["bidir_gbs"]),
-            # per-op launch times (GB/s above are from the `stat` of these)
+            # per-op launch times (GB/s above are from the `stat` of these); `slow`
+            # counts the steps more than 15% above the fastest (on a shared host,
+            # windows of host-memory contention slow the two-direction steps)
             "ms": {op: {"mean": round(statistics.mean(per[f"{lay}/{op}"]) * 1e3, 3),
                         "median": round(statistics.median(per[f"{lay}/{op}"]) * 1e3, 3),
-                        "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"])}
+                        "min": round(min(per[f"{lay}/{op}"]) * 1e3, 3), "n": len(per[f"{lay}/{op}"]),
+                        "slow": sum(1 for t in per[f"{lay}/{op}"] if t > 1.15 * min(per[f"{lay}/{op}"]))}
                    for op in ("backup", "load", "bidir", "bidir_fused")},
         }
     return per, breakdown
