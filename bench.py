@@ -654,9 +654,11 @@ def bench_extras(torch, hc, args, link):
     res, launches = bench_mla_overlap(torch, hc, mla_args)
     out["mla61"] = {"results": res, "gpu_launches": launches, "wall_s": round(time.perf_counter() - t0, 1),
                     "how": "61 per-layer loads with an event each (per_layer), the same replayed from a "
-                           "plan's graph (graph), one pipelined launch (pipelined), one all-layer launch; "
-                           "alone and overlapped with a stand-in attention on a second stream; overlap "
-                           "efficiency = (load + compute - overlapped) / min(load, compute)"}
+                           "plan's graph (graph), one chained call per layer (chained: attention behind "
+                           "the layer's counter; chained_events: behind the layer's CUDA event), one "
+                           "pipelined launch (pipelined), one all-layer launch; alone and overlapped with "
+                           "a stand-in attention on a second stream; overlap efficiency = (load + compute "
+                           "- overlapped) / min(load, compute)"}
     torch.cuda.empty_cache()
     t0 = time.perf_counter()
     out["small_mix"] = bench_small_mix(torch, hc, args, link)
@@ -785,6 +787,14 @@ def bench_mla_overlap(torch, hc, args):
                 hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
                                   stream=comp)
 
+        def overlapped_chained_events(reps):
+            # the pages' own form: one call per layer, attention behind that layer's CUDA event
+            for layer in range(L):
+                plan.load_layer_chained(kv, layer, stream=xfer)
+                _stream_wait_raw_event(comp, pool.layer_event(layer))
+                hc.layer_checksum(kv, pool, t.device_pages, layer, sums.data_ptr() + 8 * layer, reps=reps,
+                                  stream=comp)
+
         def overlapped_graph(reps):
             plan.load_layers(kv, stream=xfer)
             for layer in range(L):
@@ -813,6 +823,7 @@ def bench_mla_overlap(torch, hc, args):
         cg = timed(lambda: overlapped_graph(reps))
         ach = timed(loads_chained)
         cch = timed(lambda: overlapped_chained(reps))
+        cce = timed(lambda: overlapped_chained_events(reps))
         out[f"{tokens // 1024}k" + ("_xfer_high_priority" if prio else "")] = {
             "pages": n, "bytes": nbytes,
             "per_layer_loads_ms": round(a * 1e3, 3), "per_layer_load_gbs": round(nbytes / a / GB, 1),
@@ -834,11 +845,30 @@ def bench_mla_overlap(torch, hc, args):
             "per_layer_chained_gbs": round(nbytes / ach / GB, 1),
             "overlapped_chained_ms": round(cch * 1e3, 3),
             "overlap_efficiency_chained": round((ach + b - cch) / min(ach, b), 3),
+            "overlapped_chained_events_ms": round(cce * 1e3, 3),
+            "overlap_efficiency_chained_events": round((ach + b - cce) / min(ach, b), 3),
         }
         plan.close()
     launches = hc.launch_count() - launches0
     pool.close()
     return out, launches
+
+
+_libcuda = None
+
+
+def _stream_wait_raw_event(stream, event_handle: int):
+    """Make a torch stream wait for a raw cudaEvent_t (a pool's layer event)
+    through the driver API (a runtime event handle is a driver event)."""
+    import ctypes
+    global _libcuda
+    if _libcuda is None:
+        _libcuda = ctypes.CDLL("libcuda.so.1")
+        _libcuda.cuStreamWaitEvent.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        _libcuda.cuStreamWaitEvent.restype = ctypes.c_int
+    rc = _libcuda.cuStreamWaitEvent(ctypes.c_void_p(int(stream.cuda_stream)), ctypes.c_void_p(event_handle), 0)
+    if rc != 0:
+        raise RuntimeError(f"cuStreamWaitEvent returned {rc}")
 
 
 def bench_tp_mla(torch, hc, args):
