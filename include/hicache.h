@@ -492,7 +492,12 @@ int hicache_layer_event(hicache_pool *pool, int32_t layer, void **event_out);
  * last load of `layer` enqueued before this call: its layer event (the whole
  * load's, for a load of every layer), or, if that load is signalled on the
  * device (pipelined, allocation-free pipelined, tensor-parallel, chained
- * per-layer), that layer's counter. */
+ * per-layer), that layer's count: the wait for the count goes on the pool's
+ * own stream, and compute_stream waits for the event recorded behind it (as
+ * hicache_layer_event), so that the kernel enqueued next on compute_stream
+ * does not start late behind a stream memory wait.  A compute stream that is
+ * being captured waits for the count itself (cuStreamWaitValue32).  For a
+ * load signalled on the device the pool's device must be current. */
 int hicache_wait_layer(hicache_pool *pool, int32_t layer, void *compute_stream);
 
 /* Block the calling host thread until all work on `stream` is done, for at
